@@ -1,0 +1,248 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+* fp16 / bf16 conversions against numpy's and torch's own conversions;
+* the block-layout reading against hand-derived single-field probes
+  (tests/golden/*_probes.txt);
+* the dot product against unit-vector probes, all-zero and constant-block
+  closed forms, exact integer arithmetic and a BLAS matmul;
+* the encoders against their error bounds and nearest-value property;
+* the bf16 GEMM reference against torch's bf16 rounding and against the
+  exact reference on bf16-exact inputs.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from quantised_gguf_weight_gb300 import synth
+from tests import golden_probes
+
+FMTS = ["q8_0", "q4_k"]
+
+
+# ------------------------------------------------------------ scalar codecs
+
+def test_fp16_decode_every_pattern(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.fp16_to_f64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_fp16_encode_matches_numpy(orc):
+    rng = np.random.default_rng(0)
+    mags = np.ldexp(rng.uniform(1.0, 2.0, 4000), rng.integers(-30, 18, 4000))
+    vals = mags * rng.choice([-1.0, 1.0], 4000)
+    # exact ties: midpoints between adjacent fp16 values (normal and subnormal)
+    h = rng.integers(1, 0x7BFF, 2000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    vals = np.concatenate([vals, (lo + hi) / 2, [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e9,
+                                                 2.0 ** -25, 2.0 ** -26, 3 * 2.0 ** -26]])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([orc.f64_to_fp16(v) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_round_matches_torch(orc):
+    rng = np.random.default_rng(1)
+    u = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    u[:3000] = (u[:3000] & 0xFFFF0000) | 0x8000          # exact ties
+    u[3000:4000] = (u[3000:4000] & 0xFFFF0000) | 0x7FFF
+    f = u.view(np.float32)
+    keep = ~np.isnan(f)
+    f = f[keep]
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.f32_to_bf16(v) for v in f], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    back = np.array([orc.bf16_to_f64(int(b)) for b in got[:500]])
+    ref_back = torch.from_numpy(ref[:500].view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(back, ref_back)
+
+
+# ------------------------------------------------------------ layout probes
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_layout_probes(orc, fmt):
+    probes = golden_probes.load(fmt)
+    assert len(probes) >= 6
+    for name, K, raw, exp in probes:
+        got = orc.decode(fmt, raw, K)[0]
+        assert np.array_equal(got, exp), (name, np.nonzero(got != exp)[0][:8])
+
+
+# ------------------------------------------------------------ dot product
+
+@pytest.mark.parametrize("fmt,rows,K", [("q8_0", 3, 96), ("q4_k", 3, 512), ("q4_k", 2, 300),
+                                        ("q8_0", 2, 40)])
+def test_unit_vectors_recover_matrix(orc, fmt, rows, K):
+    """x = e_c gives y[r] = W[r][c]: the dot indexes W row-major, column fastest."""
+    wq = synth.weights(fmt, rows, K, seed=11)
+    W = orc.decode(fmt, wq, K)
+    eye = np.eye(K, dtype=np.float32)
+    y, s = orc.gemv(fmt, wq, K, eye)
+    assert np.array_equal(y, W.T)
+    assert np.array_equal(s, np.abs(W.T))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_all_zero_blocks(orc, fmt):
+    K = 512
+    wq = np.zeros(4 * synth.row_bytes(fmt, K), np.uint8)
+    y, s = orc.gemv(fmt, wq, K, synth.activations(3, K, seed=2))
+    assert np.all(y == 0.0) and np.all(s == 0.0)
+
+
+@pytest.mark.parametrize("fmt,w_const,n_blocks", [("q8_0", 3.0, 7), ("q4_k", 2.5, 3)])
+def test_constant_block_closed_form(orc, fmt, w_const, n_blocks):
+    """A row of identical constant blocks and x = v gives y = K * w * v exactly."""
+    name, K0, raw, exp = [p for p in golden_probes.load(fmt) if p[0] == "constant_block"][0]
+    assert np.all(exp == w_const)
+    K = K0 * n_blocks
+    wq = np.tile(raw, 2 * n_blocks)                      # 2 rows
+    for v in (1.0, -0.75, 3.0):
+        x = np.full((1, K), v, np.float32)
+        y, s = orc.gemv(fmt, wq, K, x)
+        assert np.all(y == K * w_const * v)
+        assert np.all(s == K * abs(w_const * v))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_exact_integer_dot(orc, fmt):
+    """Power-of-two scales and small-integer x: every product and partial sum
+    is exact in f64, so the oracle equals the exact rational dot."""
+    rows, K, B = 3, 512, 2
+    wq = synth.pow2_scaled_blocks(synth.weights(fmt, rows, K, seed=5), fmt, (-4, -3, -2, -1, 0), 5)
+    x = synth.small_int_activations(B, K, seed=5)
+    W = orc.decode(fmt, wq, K)
+    y, _ = orc.gemv(fmt, wq, K, x)
+    for b in range(B):
+        for r in range(rows):
+            exact = sum(Fraction(float(W[r, c])) * Fraction(float(x[b, c])) for c in range(K))
+            assert Fraction(float(y[b, r])) == exact
+
+
+@pytest.mark.parametrize("fmt,rows,K,B", [("q8_0", 17, 576, 3), ("q4_k", 9, 896, 2),
+                                          ("q4_k", 5, 4096, 1)])
+def test_dot_matches_blas(orc, fmt, rows, K, B):
+    wq = synth.weights(fmt, rows, K, seed=3)
+    x = synth.activations(B, K, seed=3)
+    W = orc.decode(fmt, wq, K)
+    y, s = orc.gemv(fmt, wq, K, x)
+    ref = x.astype(np.float64) @ W.T
+    sref = np.abs(x.astype(np.float64)) @ np.abs(W.T)
+    assert np.all(np.abs(y - ref) <= 1e-13 * sref)
+    assert np.allclose(s, sref, rtol=1e-13, atol=0)
+
+
+def test_row_subset_equals_slice(orc):
+    fmt, K = "q4_k", 512
+    wq = synth.weights(fmt, 40, K, seed=9)
+    x = synth.activations(2, K, seed=9)
+    yall, _ = orc.gemv(fmt, wq, K, x)
+    rows = [39, 0, 17, 17, 5]
+    ysub, _ = orc.gemv(fmt, wq, K, x, rows=rows)
+    assert np.array_equal(ysub, yall[:, rows])
+
+
+def test_threaded_equals_serial(orc):
+    fmt, K = "q8_0", 896
+    wq = synth.weights(fmt, 301, K, seed=4)
+    x = synth.activations(2, K, seed=4)
+    y1, s1 = orc.gemv(fmt, wq, K, x)
+    y2, s2 = orc.gemv_threaded(fmt, wq, K, x, np.arange(301), threads=4)
+    assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
+
+
+# ------------------------------------------------------------ encoders
+
+def test_q8_0_roundtrip_nearest(orc):
+    rng = np.random.default_rng(7)
+    K = 96
+    w = rng.normal(0, 0.02, (6, K)) * rng.choice([1, 10, 0.01], (6, 1))
+    w[5, :32] = 0.0                                       # all-zero block
+    # tiny weights: d rounds to the fp16 subnormal 2^-24 and |w/d| > 127 clamps
+    w[4] = rng.uniform(-1.0, 1.0, K) * 127 * 1.3 * 2.0 ** -24
+    raw = orc.quantise("q8_0", w)
+    wh = orc.decode("q8_0", raw, K)
+    rec = raw.view(synth.Q8_0_DTYPE)
+    d = rec["d"].astype(np.float64).reshape(6, -1)
+    assert np.all(d[5, 0] == 0.0) and np.all(wh[5, :32] == 0.0)
+    for r in range(6):
+        for c in range(K):
+            dd = d[r, c // 32]
+            cands = dd * np.arange(-127, 128)
+            best = np.min(np.abs(cands - w[r, c]))
+            assert abs(wh[r, c] - w[r, c]) == best      # nearest representable value
+    # error bound |w - w_hat| <= d/2 wherever no clamping happened
+    dd = np.repeat(d, 32, axis=1)[:, :K]
+    unclamped = np.abs(w) <= 127.5 * dd
+    assert np.all((np.abs(wh - w) <= 0.5 * dd)[unclamped])
+    assert not unclamped[4].all() and np.all(np.abs(wh[4]) <= 127 * dd[4])
+
+
+def test_q4_k_roundtrip_bound(orc):
+    rng = np.random.default_rng(8)
+    K = 512
+    w = rng.normal(0, 0.03, (5, K)) + rng.normal(0, 0.01, (5, 1))
+    raw = orc.quantise("q4_k", w)
+    wh = orc.decode("q4_k", raw, K)
+    rec = raw.view(synth.Q4_K_DTYPE).reshape(5, -1)
+    d = rec["d"].astype(np.float64)
+    dmin = rec["dmin"].astype(np.float64)
+    # grid step d*sc_j <= 63 d (half-step error 31.5 d); the grid's ends miss
+    # [lo, hi] by at most 15 d/2 (rounding sc_j) plus dmin/2 (rounding m_j)
+    bound = np.repeat(39.0 * d + 0.5 * dmin, 256, axis=1)
+    assert np.all(np.abs(wh - w) <= bound)
+    # 4-bit steps of about (6 sigma)/15 give an rms error near step/sqrt(12)
+    assert np.sqrt(np.mean((wh - w) ** 2)) < 0.15 * np.std(w)
+
+
+def test_q4_k_requantise_is_fixed_point_for_probes(orc):
+    """Decoding the hand-derived constant block, re-encoding and decoding again
+    gives the same weights (the encoder reproduces exactly representable rows)."""
+    name, K, raw, exp = [p for p in golden_probes.load("q4_k") if p[0] == "constant_block"][0]
+    wh = orc.decode("q4_k", orc.quantise("q4_k", exp[None, :]), K)
+    assert np.allclose(wh[0], exp, rtol=2e-3)
+
+
+# ------------------------------------------------------------ bf16 GEMM reference
+
+def test_gemm_bf16_reference_matches_torch_rounding(orc):
+    fmt, rows, K, M = "q4_k", 6, 512, 5
+    wq = synth.weights(fmt, rows, K, seed=12)
+    x = synth.activations(M, K, seed=12)
+    W = orc.decode(fmt, wq, K)
+    y2, s2 = orc.gemm_bf16(fmt, wq, K, x)
+    Wb = torch.from_numpy(W).float().bfloat16().double()
+    xb = torch.from_numpy(x).bfloat16().double()
+    ref = (xb @ Wb.T).numpy()
+    sref = (xb.abs() @ Wb.abs().T).numpy()
+    assert np.all(np.abs(y2 - ref) <= 1e-13 * sref)
+    # and it differs from the exact reference by at most two bf16 roundings
+    y1, s1 = orc.gemv(fmt, wq, K, x)
+    assert np.all(np.abs(y2 - y1) <= 2 * 2.0 ** -8 * s1)
+
+
+def test_gemm_bf16_reference_exact_on_bf16_inputs(orc):
+    """Weights and activations already representable in bf16: both references agree."""
+    names = ("constant_block", "chunk2_low_nibble_scale_high_bits", "min_subblock7_high_bits",
+             "full_formula_subblock6")
+    probes = {p[0]: p for p in golden_probes.load("q4_k")}
+    K = 256
+    wq = np.concatenate([probes[n][2] for n in names])
+    W = np.stack([probes[n][3] for n in names])
+    exact_bf16 = torch.from_numpy(W).float().bfloat16().double().numpy() == W
+    x = synth.small_int_activations(4, K, seed=1, lo=-3, hi=3)
+    y1, _ = orc.gemv("q4_k", wq, K, x)
+    y2, _ = orc.gemm_bf16("q4_k", wq, K, x)
+    rows_exact = exact_bf16.all(axis=1)
+    assert rows_exact[:3].all() and not rows_exact[3]     # 981 needs 10 significant bits
+    assert np.array_equal(y1[:, :3], y2[:, :3])
+    assert not np.array_equal(y1[:, 3], y2[:, 3])
