@@ -1,0 +1,127 @@
+/*
+ * qk.h -- C ABI of the GB300 (sm_103a) quantised-weight GEMV / GEMM library.
+ *
+ * The library multiplies GGUF block-quantised weights by fp32 activations,
+ * decoding every block inside the multiply.  That is the operation behind
+ * "Weights stay QUANTISED on the device: a matvec whose weight type has a
+ * device kernel ... uploads the GGUF bytes verbatim and decodes each block
+ * inside the matmul" (nurllama 0.18.1 API reference, model.nu) and behind the
+ * quantised matvec dispatch `lk_matvec_q ks gt wd xd yd rows cols batch`
+ * (same page, kernels.nu).  One entry point per weight format; there is no
+ * type dispatch and no host fallback.
+ *
+ * Operation (every entry point):
+ *   y[b][r] = sum_{c < K} W[row_offset + r][c] * x[b][c]
+ * with W row-major, the column index fastest ("weight W[out,in] -> W[r*in + c],
+ * matvec y[r] = sum_c W[r*in+c] x[c]", kernels.nu layout contract).
+ *
+ * Block formats (the pages name them, the bytes follow the GGUF layouts):
+ *   Q8_0 : 34-byte blocks of 32 weights: fp16 d, then 32 int8 q;  w = d*q.
+ *   Q4_K : 144-byte super-blocks of 256 weights: fp16 d, fp16 dmin, 12 bytes
+ *          of packed 6-bit sub-block scales sc and mins m (8 sub-blocks of
+ *          32), 128 bytes of 4-bit quants q;  w = d*sc*q - dmin*m.
+ *   A row holds ceil(K / 32) (Q8_0) or ceil(K / 256) (Q4_K) whole blocks;
+ *   columns >= K inside a row's last block are ignored.
+ *
+ * Row addressing: `w` points at the first byte of the whole tensor, and a call
+ * uses rows [row_offset, row_offset + rows).  Row r starts at byte
+ * r * row_bytes with row_bytes = blocks_per_row * block_bytes.  This is how
+ * the parts of a fused tensor are addressed ("a weight here is a device
+ * pointer plus a row count, so the parts are row ranges inside the uploaded
+ * tensor", nurllama README, "What it runs", phi3), and how one expert of a
+ * 3-D expert tensor [E][rows_e][K] is addressed: row_offset = e*rows_e + r0.
+ *
+ * Ownership and execution: every pointer is a device pointer owned by the
+ * caller; the library allocates and frees nothing per call and keeps no
+ * per-call state.  Calls are asynchronous on `stream` (NULL = the legacy
+ * default stream) and never synchronise.
+ *
+ * Errors: argument errors are detected on the host before any launch and
+ * leave every output untouched; a failed launch returns QK_ERR_CUDA.  Device
+ * waits are bounded: a kernel whose wait runs out records the fact in a
+ * device error word and returns early (its outputs are then unspecified);
+ * qk_device_error() reads and clears that word.
+ */
+#ifndef QK_H
+#define QK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *qk_stream_t;
+
+typedef enum {
+    QK_OK = 0,
+    QK_ERR_NULL = 1,        /* a required pointer is NULL                              */
+    QK_ERR_BAD_DIM = 2,     /* rows/N/M <= 0, K <= 0, row_offset < 0, ldy too small     */
+    QK_ERR_ALIGN = 3,       /* w, x or y misaligned (see each call)                     */
+    QK_ERR_BATCH = 4,       /* GEMV batch outside [1, QK_MAX_BATCH]                     */
+    QK_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed                     */
+    QK_ERR_TIMEOUT = 6,     /* a bounded device wait ran out (from qk_device_error)     */
+    QK_ERR_WORKSPACE = 7,   /* workspace NULL, misaligned or smaller than required      */
+    QK_ERR_TOO_LARGE = 8    /* a size exceeds what the kernels support (see each call)  */
+} qk_status;
+
+#define QK_MAX_BATCH 8
+
+/*
+ * Q8_0 GEMV, batch 1..8: y[b*ldy + r] = sum_{c<K} W[row_offset + r][c] * x[b*K + c].
+ *   w      device, raw Q8_0 block bytes of the whole tensor; 2-byte aligned.
+ *   x      device fp32 [batch][K], row stride K; 4-byte aligned.
+ *   y      device fp32 [batch][ldy]; writes y[b*ldy + r] for r < rows only;
+ *          4-byte aligned.  ldy == 0 means ldy = rows.
+ *   K      columns, any K >= 1.  The kernel keeps the whole activation batch
+ *          (batch * K * 4 bytes, K rounded up to the block size) in shared
+ *          memory next to at least two staged tiles of rows; calls where that
+ *          does not fit in the device's shared memory per block (for example
+ *          batch * K above about 45000 on GB300) return QK_ERR_TOO_LARGE.
+ * Arithmetic is fp32; results differ from the exact dot by at most
+ * 1e-5 * sum|w*x| + 1e-6 per element (the tests check this bound).
+ */
+int qmatvec_q8_0(const void *w, int64_t row_offset, int64_t rows, int64_t K,
+                 const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
+
+/*
+ * Q4_K GEMV, batch 1..8.  Same contract as qmatvec_q8_0, with w 16-byte
+ * aligned (144-byte super-blocks keep every row 16-byte aligned).
+ */
+int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
+                 const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
+
+/*
+ * Bytes of one row of a tensor with K columns: ceil(K/32)*34 (Q8_0) or
+ * ceil(K/256)*144 (Q4_K).
+ */
+int64_t qk_row_bytes_q8_0(int64_t K);
+int64_t qk_row_bytes_q4_k(int64_t K);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qk_status_string(int status);
+
+/*
+ * Reads and clears the device error word of the current device after
+ * synchronising `stream`: QK_OK, QK_ERR_TIMEOUT (a bounded wait ran out) or
+ * QK_ERR_CUDA (the synchronisation itself failed).  Meant for tests and
+ * debugging; the compute calls never synchronise.
+ */
+int qk_device_error(qk_stream_t stream);
+
+/*
+ * Upper bound, in nanoseconds, of every device-side wait of later launches
+ * (default 2e9).  Returns the previous value.  Tests shorten it.
+ */
+uint64_t qk_set_wait_limit_ns(uint64_t ns);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int qk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QK_H */

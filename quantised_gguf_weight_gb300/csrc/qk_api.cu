@@ -1,0 +1,128 @@
+// qk_api.cu -- the extern "C" entry points declared in include/qk.h.
+//
+// Host side only: argument validation (before any launch, outputs untouched
+// on error), row-offset addressing, launch planning, the device error word
+// and its read-back.  The compute runs entirely in the kernels of
+// qk_gemv.cu and qk_gemm.cu; there is no host fallback of any kind.
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qk.h"
+#include "qk_internal.h"
+
+namespace {
+
+// Device error word: bit kErrTimeout is set by a kernel whose bounded wait ran
+// out.  One per device (a __device__ variable lives in every context).
+__device__ int g_qk_error_word;
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int64_t> g_skip_tile{-1};
+
+int *error_word_ptr()
+{
+    static int *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_qk_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t K,
+               const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream)
+{
+    if (!w || !x || !y) return QK_ERR_NULL;
+    if (rows <= 0 || K <= 0 || row_offset < 0) return QK_ERR_BAD_DIM;
+    if (batch < 1 || batch > QK_MAX_BATCH) return QK_ERR_BATCH;
+    if (ldy == 0) ldy = rows;
+    if (ldy < rows) return QK_ERR_BAD_DIM;
+    if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4))
+        return QK_ERR_ALIGN;
+    qk::GemvPlan plan;
+    if (!qk::gemv_plan(fmt, rows, K, batch, &plan)) {
+        // either no usable device or the activations do not fit in shared memory
+        int dev_count = 0;
+        if (cudaGetDeviceCount(&dev_count) != cudaSuccess || dev_count == 0) return QK_ERR_CUDA;
+        return QK_ERR_TOO_LARGE;
+    }
+    if (row_offset > (INT64_MAX / plan.row_bytes) - rows) return QK_ERR_BAD_DIM;
+    int *err = error_word_ptr();
+    if (!err) return QK_ERR_CUDA;
+    const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * plan.row_bytes;
+    cudaError_t e = qk::gemv_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
+                                    reinterpret_cast<cudaStream_t>(stream), plan, err,
+                                    g_wait_limit_ns.load(), g_skip_tile.load());
+    return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmatvec_q8_0(const void *w, int64_t row_offset, int64_t rows, int64_t K, const float *x,
+                 int batch, float *y, int64_t ldy, qk_stream_t stream)
+{
+    return gemv_entry(qk::kFmtQ80, w, row_offset, rows, K, x, batch, y, ldy, stream);
+}
+
+int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K, const float *x,
+                 int batch, float *y, int64_t ldy, qk_stream_t stream)
+{
+    return gemv_entry(qk::kFmtQ4K, w, row_offset, rows, K, x, batch, y, ldy, stream);
+}
+
+int64_t qk_row_bytes_q8_0(int64_t K) { return K <= 0 ? 0 : ((K + 31) / 32) * 34; }
+int64_t qk_row_bytes_q4_k(int64_t K) { return K <= 0 ? 0 : ((K + 255) / 256) * 144; }
+
+const char *qk_status_string(int status)
+{
+    switch (status) {
+    case QK_OK: return "ok";
+    case QK_ERR_NULL: return "null pointer argument";
+    case QK_ERR_BAD_DIM: return "bad dimension (rows/N/M/K <= 0, negative row_offset, or ldy too small)";
+    case QK_ERR_ALIGN: return "misaligned pointer";
+    case QK_ERR_BATCH: return "batch outside [1, 8]";
+    case QK_ERR_CUDA: return "CUDA error";
+    case QK_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case QK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case QK_ERR_TOO_LARGE: return "size beyond what the kernels support";
+    default: return "unknown status";
+    }
+}
+
+int qk_device_error(qk_stream_t stream)
+{
+    int *err = error_word_ptr();
+    if (!err) return QK_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QK_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QK_ERR_CUDA;
+    if (v) {
+        const int zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QK_ERR_CUDA;
+        return QK_ERR_TIMEOUT;
+    }
+    return QK_OK;
+}
+
+uint64_t qk_set_wait_limit_ns(uint64_t ns)
+{
+    if (ns == 0) ns = 1;
+    return g_wait_limit_ns.exchange(ns);
+}
+
+int qk_version(void) { return 100; }
+
+// Test hook, not part of the public header: CTA 0 of every later GEMV launch
+// skips the bulk copy of its tile `tile` (-1 restores normal operation), so
+// its consumers' bounded wait runs out and the launch records QK_ERR_TIMEOUT.
+int64_t qk_debug_skip_tile(int64_t tile) { return g_skip_tile.exchange(tile); }
+
+}  // extern "C"

@@ -1,0 +1,140 @@
+// qk_gemv.cu -- launch planning and dispatch of the GEMV kernel
+// (qk_gemv_kernel.cuh): team shape, tile size, shared-memory layout, grid.
+#include <algorithm>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qk_gemv_kernel.cuh"
+#include "qk_internal.h"
+
+namespace qk {
+
+namespace {
+
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+DevInfo dev_info()
+{
+    static DevInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo{};
+    DevInfo &di = cache[dev];
+    if (di.sms == 0) {
+        int sms = 0, smem = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        di.smem_optin = smem;
+        di.sms = sms;
+    }
+    return di;
+}
+
+int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
+
+// Layout for a given activation unit stride XU; false if it cannot fit.
+bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int64_t row_bytes, const DevInfo &di,
+               GemvPlan *p)
+{
+    const int UC = fmt == kFmtQ4K ? 128 : 32;
+    const int max_c = max_consumers(fmt, batch);
+    const int SW = U < max_c ? U : max_c;
+    const int R = rows_per_thread(fmt, batch);
+    int64_t grid = di.sms;
+    if (grid > rows) grid = rows;
+    const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
+    const int64_t xsum_bytes = fmt == kFmtQ4K ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128) : 0;
+    const int64_t off_x = 256;
+    const int64_t off_xsum = off_x + x_bytes;
+    const int64_t off_red = off_xsum + xsum_bytes;
+    const int64_t budget = di.smem_optin;
+    // teams: no more than the threads allow, than the CTA has rows for, and
+    // than fit with two stages next to the activations and the partials
+    const int64_t rows_per_cta = (rows + grid - 1) / grid;
+    int64_t slots = max_c / SW;
+    slots = std::min<int64_t>(slots, (rows_per_cta + R - 1) / R);
+    for (; slots >= 1; --slots) {
+        const int64_t red_bytes = round_up(2 * slots * R * batch * SW * 4, 128);
+        const int64_t stage = round_up(slots * R * row_bytes + 32, 128);
+        if (off_red + red_bytes + 2 * stage <= budget) break;
+    }
+    if (slots < 1) return false;
+    const int64_t red_bytes = round_up(2 * slots * R * batch * SW * 4, 128);
+    const int64_t off_stage = off_red + red_bytes;
+    const int64_t stage = round_up(slots * R * row_bytes + 32, 128);
+    int64_t stages = (budget - off_stage) / stage;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2 || stage > (1 << 20)) return false;
+    p->U = U;
+    p->XU = XU;
+    p->SW = SW;
+    p->slots = static_cast<int>(slots);
+    p->NTC = static_cast<int>(round_up(slots * SW, 32));
+    p->R = R;
+    p->tile_rows = static_cast<int>(slots * R);
+    p->stages = static_cast<int>(stages);
+    p->stage_bytes = static_cast<int>(stage);
+    p->off_x = static_cast<int>(off_x);
+    p->off_xsum = static_cast<int>(off_xsum);
+    p->off_red = static_cast<int>(off_red);
+    p->off_stage = static_cast<int>(off_stage);
+    p->smem = static_cast<int>(off_stage + stages * stage);
+    p->row_bytes = row_bytes;
+    p->grid = static_cast<int>(grid);
+    return true;
+}
+
+}  // namespace
+
+// Launch plan of a GEMV call; returns false if it cannot fit in shared memory.
+bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p)
+{
+    const DevInfo di = dev_info();
+    if (di.sms <= 0) return false;
+    const int UC = fmt == kFmtQ4K ? 128 : 32;
+    const int64_t row_bytes = fmt == kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
+    const int64_t U64 = (K + UC - 1) / UC;
+    if (U64 > (1 << 20)) return false;
+    const int U = static_cast<int>(U64);
+    // a compile-time activation unit stride (32 or 128) where it fits
+    if (U <= 32 && plan_with(fmt, rows, batch, U, 32, row_bytes, di, p)) return true;
+    if (U > 32 && U <= 128 && plan_with(fmt, rows, batch, U, 128, row_bytes, di, p)) return true;
+    return plan_with(fmt, rows, batch, U, U, row_bytes, di, p);
+}
+
+cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
+                        int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
+                        int *err, uint64_t wait_ns, int64_t skip_tile)
+{
+    GemvArgs a;
+    a.w = w_rows;
+    a.x = x;
+    a.y = y;
+    a.rows = rows;
+    a.K = K;
+    a.ldy = ldy;
+    a.row_bytes = p.row_bytes;
+    a.U = p.U;
+    a.XU = p.XU;
+    a.SW = p.SW;
+    a.slots = p.slots;
+    a.NTC = p.NTC;
+    a.tile_rows = p.tile_rows;
+    a.stages = p.stages;
+    a.stage_bytes = p.stage_bytes;
+    a.off_x = p.off_x;
+    a.off_xsum = p.off_xsum;
+    a.off_red = p.off_red;
+    a.off_stage = p.off_stage;
+    a.skip_tile = skip_tile;
+    a.wait_ns = wait_ns;
+    a.err = err;
+    if (p.R != rows_per_thread(fmt, batch)) return cudaErrorInvalidValue;
+    const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
+    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, a, p.grid, p.smem, st);
+    return gemv_launch_q80(batch, us, a, p.grid, p.smem, st);
+}
+
+}  // namespace qk

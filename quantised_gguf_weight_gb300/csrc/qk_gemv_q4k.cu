@@ -1,0 +1,22 @@
+// qk_gemv_q4k.cu -- instantiations of the GEMV kernel for one weight format
+// (compiled as their own translation unit so the formats build in parallel).
+#include "qk_gemv_kernel.cuh"
+
+namespace qk {
+
+cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st)
+{
+    switch (batch) {
+    case 1: QK_GEMV_DISPATCH_US(kFmtQ4K, 1, us)
+    case 2: QK_GEMV_DISPATCH_US(kFmtQ4K, 2, us)
+    case 3: QK_GEMV_DISPATCH_US(kFmtQ4K, 3, us)
+    case 4: QK_GEMV_DISPATCH_US(kFmtQ4K, 4, us)
+    case 5: QK_GEMV_DISPATCH_US(kFmtQ4K, 5, us)
+    case 6: QK_GEMV_DISPATCH_US(kFmtQ4K, 6, us)
+    case 7: QK_GEMV_DISPATCH_US(kFmtQ4K, 7, us)
+    case 8: QK_GEMV_DISPATCH_US(kFmtQ4K, 8, us)
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qk

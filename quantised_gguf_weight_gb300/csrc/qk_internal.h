@@ -1,0 +1,26 @@
+// qk_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qk {
+
+constexpr int kFmtQ80 = 0;
+constexpr int kFmtQ4K = 1;
+constexpr int kMaxConsumers = 512;   // consumer threads per GEMV CTA
+constexpr int kMaxStages = 8;        // shared-memory ring depth
+
+// Launch plan of one GEMV call (shared-memory layout, grid, team shape).
+struct GemvPlan {
+    int U, XU, SW, slots, NTC, R, tile_rows, stages, stage_bytes;
+    int off_x, off_xsum, off_red, off_stage, smem, grid;
+    int64_t row_bytes;
+};
+
+bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p);
+cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
+                        int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
+                        int *err, uint64_t wait_ns, int64_t skip_tile);
+
+}  // namespace qk

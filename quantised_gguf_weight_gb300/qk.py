@@ -1,0 +1,127 @@
+"""Python binding of libqk (include/qk.h): argument marshalling only.
+
+Every call forwards device pointers, sizes and the current torch CUDA stream
+to the C ABI; all the work runs in the library's CUDA kernels.  There is no
+fallback: if the library is missing or fails to load, every call raises.
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+QK_OK = 0
+STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 4: "QK_ERR_BATCH",
+          5: "QK_ERR_CUDA", 6: "QK_ERR_TIMEOUT", 7: "QK_ERR_WORKSPACE", 8: "QK_ERR_TOO_LARGE"}
+MAX_BATCH = 8
+
+EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
+           "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_version"]
+
+
+class QKError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = load().qk_status_string(status).decode()
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({msg})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load the in-tree libqk.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"libqk.so not built ({p}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for name in ("qmatvec_q8_0", "qmatvec_q4_k"):
+            fn = getattr(lib, name)
+            fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P]
+            fn.restype = I
+        for name in ("qk_row_bytes_q8_0", "qk_row_bytes_q4_k"):
+            getattr(lib, name).argtypes = [I64]
+            getattr(lib, name).restype = I64
+        lib.qk_status_string.argtypes = [I]
+        lib.qk_status_string.restype = ctypes.c_char_p
+        lib.qk_device_error.argtypes = [P]
+        lib.qk_device_error.restype = I
+        lib.qk_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.qk_set_wait_limit_ns.restype = ctypes.c_uint64
+        lib.qk_version.restype = I
+        lib.qk_debug_skip_tile.argtypes = [I64]
+        lib.qk_debug_skip_tile.restype = I64
+        _lib = lib
+        return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def row_bytes(fmt: str, K: int) -> int:
+    lib = load()
+    return int(lib.qk_row_bytes_q8_0(K) if fmt == "q8_0" else lib.qk_row_bytes_q4_k(K))
+
+
+def _check(status: int, what: str):
+    if status != QK_OK:
+        raise QKError(status, what)
+
+
+def _qmatvec(name: str, w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.Tensor,
+             y: torch.Tensor | None, ldy: int, stream) -> torch.Tensor:
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    batch = x.shape[0]
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+        ldy = rows
+    st = getattr(load(), name)(w.data_ptr(), row_offset, rows, K, x.data_ptr(), batch, y.data_ptr(),
+                               ldy, _stream(stream))
+    _check(st, name)
+    return y
+
+
+def qmatvec_q8_0(w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.Tensor,
+                 y: torch.Tensor | None = None, ldy: int = 0, stream=None) -> torch.Tensor:
+    """y[b][r] = sum_c W[row_offset + r][c] x[b][c] for Q8_0 block bytes `w` (uint8, device)."""
+    return _qmatvec("qmatvec_q8_0", w, row_offset, rows, K, x, y, ldy, stream)
+
+
+def qmatvec_q4_k(w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.Tensor,
+                 y: torch.Tensor | None = None, ldy: int = 0, stream=None) -> torch.Tensor:
+    """y[b][r] = sum_c W[row_offset + r][c] x[b][c] for Q4_K block bytes `w` (uint8, device)."""
+    return _qmatvec("qmatvec_q4_k", w, row_offset, rows, K, x, y, ldy, stream)
+
+
+def device_error(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device error word."""
+    return int(load().qk_device_error(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(load().qk_set_wait_limit_ns(int(ns)))
+
+
+def debug_skip_tile(tile: int) -> int:
+    """Test hook: CTA 0 of later GEMV launches skips copying tile `tile` (-1: off)."""
+    return int(load().qk_debug_skip_tile(int(tile)))

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load on a machine without a GPU, export every function
+include/*.h declares, and reject bad arguments before touching the device.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from quantised_gguf_weight_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    from quantised_gguf_weight_gb300 import qk
+    return qk.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qk_status_string", "qk_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(9):
+        assert lib.qk_status_string(s)
+    assert lib.qk_status_string(99) == b"unknown status"
+
+
+def test_row_bytes(lib):
+    assert lib.qk_row_bytes_q8_0(576) == 18 * 34
+    assert lib.qk_row_bytes_q8_0(40) == 2 * 34
+    assert lib.qk_row_bytes_q4_k(896) == 4 * 144
+    assert lib.qk_row_bytes_q4_k(4096) == 16 * 144
+    assert lib.qk_row_bytes_q4_k(0) == 0
+
+
+FAKE = 0x10000  # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("name", ["qmatvec_q8_0", "qmatvec_q4_k"])
+def test_argument_validation_without_gpu(lib, name):
+    f = getattr(lib, name)
+    ok_args = dict(w=FAKE, off=0, rows=16, K=256, x=FAKE, batch=1, y=FAKE, ldy=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return f(a["w"], a["off"], a["rows"], a["K"], a["x"], a["batch"], a["y"], a["ldy"], None)
+
+    assert call(w=None) == 1
+    assert call(x=None) == 1
+    assert call(y=None) == 1
+    assert call(rows=0) == 2
+    assert call(K=0) == 2
+    assert call(K=-5) == 2
+    assert call(off=-1) == 2
+    assert call(ldy=8) == 2          # ldy < rows
+    assert call(batch=0) == 4
+    assert call(batch=9) == 4
+    assert call(x=FAKE + 2) == 3     # x not 4-byte aligned
+    assert call(y=FAKE + 1) == 3
+    assert call(w=FAKE + 1) == 3     # odd w
+    if name == "qmatvec_q4_k":
+        assert call(w=FAKE + 8) == 3  # Q4_K needs 16-byte aligned super-blocks
+
+
+def test_wait_limit_roundtrip(lib):
+    old = lib.qk_set_wait_limit_ns(12345)
+    assert lib.qk_set_wait_limit_ns(old) == 12345
+
+
+def test_product_path_does_not_import_the_oracle():
+    """Nothing in the package imports, loads or builds anything under oracle/."""
+    pkg = os.path.join(ROOT, "quantised_gguf_weight_gb300")
+    pat = re.compile(r"^\s*(from\s+oracle\b|import\s+oracle\b)|qk_oracle|libqk_oracle", re.M)
+    for path in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True) + \
+            glob.glob(os.path.join(pkg, "csrc", "*")):
+        assert not pat.search(open(path, errors="replace").read()), path

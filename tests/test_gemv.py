@@ -1,0 +1,205 @@
+"""GPU parity of the Q8_0 / Q4_K GEMV against the CPU oracle.
+
+Tolerance (fp32 GEMV): |y - y_ref| <= 1e-5 * sum|w*x| + 1e-6 per element,
+y_ref and sum|w*x| from the f64 oracle.  Where every partial sum is exact in
+fp32 (power-of-two scales, small-integer activations) the GPU must be
+bit-identical to the oracle whatever its summation order.
+"""
+import numpy as np
+import pytest
+import torch
+
+from quantised_gguf_weight_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-5, 1e-6
+
+
+def gpu_gemv(qk, fmt, wq, row_offset, rows, K, x, y=None, ldy=0):
+    wd = torch.from_numpy(np.ascontiguousarray(wq)).cuda()
+    xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    fn = qk.qmatvec_q8_0 if fmt == "q8_0" else qk.qmatvec_q4_k
+    out = fn(wd, row_offset, rows, K, xd, y=y, ldy=ldy)
+    torch.cuda.synchronize()
+    return out
+
+
+def assert_close(y, yr, s, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    bad = ~(np.abs(y - yr) <= REL * s + ABS)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first at {tuple(i)}: "
+                             f"gpu {y[tuple(i)]!r} oracle {yr[tuple(i)]!r} S {s[tuple(i)]!r}")
+
+
+SMALL = [
+    # fmt, rows, K, batch, seed
+    ("q8_0", 576, 576, 1, 0),        # SmolLM-135M q-proj shape, seed 0
+    ("q8_0", 1000, 896, 1, 5), ("q8_0", 1000, 896, 2, 5), ("q8_0", 1000, 896, 3, 5),
+    ("q8_0", 1000, 896, 4, 5), ("q8_0", 1000, 896, 5, 5), ("q8_0", 1000, 896, 6, 5),
+    ("q8_0", 1000, 896, 7, 5), ("q8_0", 1000, 896, 8, 5),
+    ("q8_0", 333, 40, 3, 6),          # ragged K (partial block)
+    ("q8_0", 1, 32, 1, 7), ("q8_0", 7, 1, 2, 7), ("q8_0", 2, 33, 8, 7),
+    ("q8_0", 2000, 4096, 2, 8), ("q8_0", 150, 14336, 1, 8), ("q8_0", 61, 2080, 5, 8),
+    ("q4_k", 4864, 896, 1, 1),        # Qwen2.5-0.5B ffn_up shape (K = 3.5 super-blocks)
+    ("q4_k", 896, 4864, 1, 1),        # its ffn_down transpose (19 super-blocks)
+    ("q4_k", 1000, 4096, 1, 9), ("q4_k", 1000, 4096, 2, 9), ("q4_k", 1000, 4096, 3, 9),
+    ("q4_k", 1000, 4096, 4, 9), ("q4_k", 600, 4096, 5, 9), ("q4_k", 600, 4096, 6, 9),
+    ("q4_k", 600, 4096, 7, 9), ("q4_k", 600, 4096, 8, 9),
+    ("q4_k", 333, 300, 5, 10),        # ragged K inside a super-block
+    ("q4_k", 1, 256, 1, 11), ("q4_k", 3, 1, 1, 11), ("q4_k", 5, 65, 8, 11),
+    ("q4_k", 900, 14336, 1, 12), ("q4_k", 123, 14336, 2, 12), ("q4_k", 40, 20480, 1, 12),
+]
+
+
+@pytest.mark.parametrize("fmt,rows,K,batch,seed", SMALL)
+def test_gemv_matches_oracle(qk, orc, fmt, rows, K, batch, seed):
+    wq = synth.weights(fmt, rows, K, seed=seed)
+    x = synth.activations(batch, K, seed=seed)
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert_close(y, yr, s, f"{fmt} {rows}x{K} b{batch}")
+
+
+@pytest.mark.parametrize("fmt,K", [("q8_0", 4096), ("q4_k", 512), ("q4_k", 4096)])
+@pytest.mark.parametrize("batch", [1, 2, 3])
+def test_gemv_bit_exact_when_sums_are_exact(qk, orc, fmt, K, batch):
+    """Power-of-two d/dmin and |x| <= 2: every product and partial sum is a
+    multiple of 2^-4 below 2^20, so fp32 sums are exact in any order."""
+    rows = 300
+    if fmt == "q4_k" and K > 512:
+        K = 512
+    wq = synth.pow2_scaled_blocks(synth.weights(fmt, rows, K, seed=21), fmt, (-4, -3, -2, -1), 21)
+    x = synth.small_int_activations(batch, K, seed=21, lo=-2, hi=2)
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert np.all(s < 2.0 ** 20)
+    assert np.array_equal(y, yr.astype(np.float32))
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_row_ranges_equal_fused_call(qk, fmt):
+    """Row ranges 4096/1024/1024 of a fused qkv tensor give the same bits as one call."""
+    K = 4096 if fmt == "q4_k" else 896
+    wq = synth.weights(fmt, 6144, K, seed=3)
+    x = synth.activations(1, K, seed=3)
+    wd = torch.from_numpy(wq).cuda()
+    xd = torch.from_numpy(x).cuda()
+    fn = qk.qmatvec_q8_0 if fmt == "q8_0" else qk.qmatvec_q4_k
+    fused = fn(wd, 0, 6144, K, xd)
+    parts = torch.full((1, 6144), float("nan"), device="cuda")
+    for off, n in ((0, 4096), (4096, 1024), (5120, 1024)):
+        fn(wd, off, n, K, xd, y=parts[:, off:], ldy=6144)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, parts)
+
+
+def test_expert_row_offsets(qk, orc):
+    """3-D expert tensor [E][rows_e][K]: expert e is row_offset = e*rows_e."""
+    E, rows_e, K = 6, 200, 1024
+    wq = synth.weights("q4_k", E * rows_e, K, seed=4)
+    x = synth.activations(2, K, seed=4)
+    wd = torch.from_numpy(wq).cuda()
+    xd = torch.from_numpy(x).cuda()
+    for e in (0, 3, 5):
+        y = qk.qmatvec_q4_k(wd, e * rows_e, rows_e, K, xd).cpu().numpy()
+        yr, s = orc.gemv("q4_k", wq, K, x, rows=np.arange(e * rows_e, (e + 1) * rows_e))
+        assert_close(y, yr, s, f"expert {e}")
+
+
+def test_ldy_writes_only_the_range(qk, orc):
+    fmt, rows, K, B, ldy = "q8_0", 500, 576, 3, 777
+    wq = synth.weights(fmt, rows, K, seed=13)
+    x = synth.activations(B, K, seed=13)
+    y = torch.full((B, ldy), -7.0, device="cuda")
+    gpu_gemv(qk, fmt, wq, 0, rows, K, x, y=y, ldy=ldy)
+    yh = y.cpu().numpy()
+    assert np.all(yh[:, rows:] == -7.0)
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert_close(yh[:, :rows], yr, s, "ldy")
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_nonfinite_scales_propagate(qk, orc, fmt):
+    rows, K = 64, 512
+    wq = synth.weights(fmt, rows, K, seed=14)
+    rec = wq.view(synth.BLOCK[fmt][2]).reshape(rows, -1)
+    rec["d"][5, 0] = np.float16(np.nan)
+    rec["d"][9, 1] = np.float16(np.inf)
+    x = synth.activations(1, K, seed=14)
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert np.isnan(y[0, 5]) and np.isnan(yr[0, 5])
+    assert not np.isfinite(y[0, 9]) and not np.isfinite(yr[0, 9])
+    keep = np.isfinite(yr[0])
+    assert_close(y[:, keep], yr[:, keep], s[:, keep], "finite rows")
+
+
+def test_too_large_is_rejected_before_launch(qk):
+    K, B = 14336 * 3, 8
+    w = torch.zeros(qk.row_bytes("q4_k", K), dtype=torch.uint8, device="cuda")
+    x = torch.zeros((B, K), device="cuda")
+    y = torch.full((B, 1), 5.0, device="cuda")
+    with pytest.raises(qk.QKError) as ei:
+        qk.qmatvec_q4_k(w, 0, 1, K, x, y=y, ldy=1)
+    assert ei.value.status == 8
+    assert torch.all(y == 5.0)
+
+
+def test_bounded_wait_times_out_and_context_survives(qk, orc):
+    """A tile whose copy is never issued makes the consumers' wait run out:
+    the launch records QK_ERR_TIMEOUT and later launches work normally."""
+    fmt, rows, K = "q4_k", 2000, 4096
+    wq = synth.weights(fmt, rows, K, seed=15)
+    x = synth.activations(1, K, seed=15)
+    assert qk.device_error() == 0
+    old = qk.set_wait_limit_ns(20_000_000)
+    qk.debug_skip_tile(0)
+    try:
+        gpu_gemv(qk, fmt, wq, 0, rows, K, x)
+        assert qk.device_error() == 6
+    finally:
+        qk.debug_skip_tile(-1)
+        qk.set_wait_limit_ns(old)
+    assert qk.device_error() == 0
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert_close(y, yr, s, "after timeout")
+
+
+# ---------------------------------------------------------------- full-size configurations
+
+def _sample_rows(rows, n, seed):
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(rows, size=min(n, rows), replace=False)
+    return np.unique(np.concatenate([pick, [0, rows - 1]]))
+
+
+LLAMA8B = [("attn_qkv", 6144, 4096), ("attn_output", 4096, 4096), ("ffn_gate_up", 28672, 4096),
+           ("ffn_down", 4096, 14336)]
+
+
+@pytest.mark.parametrize("name,rows,K", LLAMA8B)
+def test_llama8b_layer_set_sampled(qk, orc, name, rows, K):
+    """Full-size Llama-8B-shaped Q4_K tensors, batch 1, checked on sampled rows."""
+    seed = 2
+    wq = synth.weights("q4_k", rows, K, seed=seed, stream0=10 * LLAMA8B.index((name, rows, K)))
+    x = synth.activations(1, K, seed=seed)
+    y = gpu_gemv(qk, "q4_k", wq, 0, rows, K, x).cpu().numpy()
+    idx = _sample_rows(rows, 384, seed)
+    yr, s = orc.gemv("q4_k", wq, K, x, rows=idx)
+    assert_close(y[:, idx], yr, s, name)
+
+
+@pytest.mark.parametrize("batch", [1, 8])
+def test_lm_head_q8_0_sampled(qk, orc, batch):
+    """Q8_0 lm_head 151936 x 896 (Qwen2.5-0.5B vocab), batch 1 and 8, sampled rows."""
+    rows, K, seed = 151936, 896, 3
+    wq = synth.weights("q8_0", rows, K, seed=seed)
+    x = synth.activations(batch, K, seed=seed)
+    y = gpu_gemv(qk, "q8_0", wq, 0, rows, K, x).cpu().numpy()
+    idx = _sample_rows(rows, 512, seed)
+    yr, s = orc.gemv("q8_0", wq, K, x, rows=idx)
+    assert_close(y[:, idx], yr, s, f"lm_head b{batch}")
