@@ -3,9 +3,11 @@
 
 Headline workload (the GEMV HBM-bandwidth metric): the batch-1 Q4_K decode
 GEMVs of a Llama-8B-shaped model, one step = one token through 32 layers.
-Per layer: fused attn_qkv 6144x4096 addressed as three row ranges
-(4096/1024/1024), attn_output 4096x4096, the fused ffn gate+up 28672x4096
-(one call), ffn_down 4096x14336 -- six launches.  Eight distinct layer weight
+Per layer: the fused attn_qkv 6144x4096 (one call; q, k and v are the row
+ranges 4096/1024/1024 of its output), attn_output 4096x4096, the fused ffn
+gate+up 28672x4096 (one call), ffn_down 4096x14336 -- four launches, with
+programmatic dependent launch on (weights are loaded once, so a call may
+stream its weights while the previous call drains).  Eight distinct layer weight
 sets (983 MB, far larger than L2) are rotated, so every weight byte comes
 from HBM.  Activations are fixed synthetic N(0,1) vectors (the ops between
 the GEMVs are not part of this library).  The step is captured once as a
@@ -39,7 +41,7 @@ LAYERS_PER_TOKEN = 32
 DISTINCT_LAYER_SETS = 8
 # (name, rows, K, row-range calls as (row_offset, rows))
 LAYER = [
-    ("attn_qkv", 6144, 4096, [(0, 4096), (4096, 1024), (5120, 1024)]),
+    ("attn_qkv", 6144, 4096, [(0, 6144)]),
     ("attn_output", 4096, 4096, [(0, 4096)]),
     ("ffn_gate_up", 28672, 4096, [(0, 28672)]),
     ("ffn_down", 4096, 14336, [(0, 4096)]),
@@ -354,7 +356,7 @@ def read_traffic(kernel_key: str, avg_launch_bytes: float):
 
 def measure_e2e(args, torch, wl, stream, step_bytes, world):
     """The step end to end through the public API: the host->device copies
-    of the step's activations from pinned memory, the 192 qmatvec_q4_k
+    of the step's activations from pinned memory, the 128 qmatvec_q4_k
     calls and the device->host copy of the last layer's output, captured
     once as a CUDA graph and replayed with a host synchronisation per step.
     The same step issued eagerly from Python is reported beside it."""
@@ -396,7 +398,7 @@ def measure_e2e(args, torch, wl, stream, step_bytes, world):
         s_eager = (time.perf_counter() - t0) / ne
     return {"value": round(world * step_bytes / s_graph / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * s_graph, 4),
-            "path": "pinned H2D + 192 qmatvec_q4_k calls + D2H captured as one CUDA graph, host sync per step",
+            "path": "pinned H2D + 128 qmatvec_q4_k calls + D2H captured as one CUDA graph, host sync per step",
             "eager_python_ms_per_step": round(1e3 * s_eager, 4),
             "eager_python_GB/s": round(world * step_bytes / s_eager / 1e9, 1)}
 
@@ -536,14 +538,15 @@ def run_reference(args):
 
 def workload_config():
     return {"workload": "llama8b_q4_k_decode_token_gemvs",
-            "description": "batch-1 Q4_K GEMVs of 32 Llama-8B-shaped layers per step: attn_qkv "
-                           "6144x4096 as row ranges 4096/1024/1024, attn_output 4096x4096, fused ffn "
-                           "gate+up 28672x4096, ffn_down 4096x14336",
+            "description": "batch-1 Q4_K GEMVs of 32 Llama-8B-shaped layers per step: fused attn_qkv "
+                           "6144x4096 (q/k/v = output row ranges 4096/1024/1024), attn_output 4096x4096, "
+                           "fused ffn gate+up 28672x4096, ffn_down 4096x14336",
             "weights": "Q4_K (144-byte super-blocks)", "activations": "fp32 N(0,1)", "batch": 1,
             "layers_per_step": LAYERS_PER_TOKEN, "distinct_layer_weight_sets": DISTINCT_LAYER_SETS,
             "bytes_per_step": layer_bytes() * LAYERS_PER_TOKEN,
             "l2": "inputs larger than L2: 8 distinct layer weight sets (983 MB) rotated",
-            "launch": "one CUDA graph per step (192 GEMV launches)", "parallelism": "replicas"}
+            "launch": "one CUDA graph per step (128 GEMV launches, programmatic dependent launch)",
+            "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------------- single-call mode (profiling)
@@ -591,6 +594,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the other GEMV configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--only", default=None, help="FMT:ROWS:K:BATCH -- time one GEMV call only")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -609,6 +613,7 @@ def main():
     qbuild.build()
     from quantised_gguf_weight_gb300 import qk, synth
     qk.load()
+    qk.set_programmatic_launch(not args.no_pdl)
     if args.only:
         return run_only(args, torch, qk, synth, device)
     r = measure_ours(args, torch, qk, synth, device, rank, ws)

@@ -117,6 +117,17 @@ int qk_device_error(qk_stream_t stream);
  */
 uint64_t qk_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Programmatic dependent launch for later calls (default off; returns the
+ * previous setting).  When on, a call may be scheduled while the kernel just
+ * before it in the stream is still running: it starts streaming its weights
+ * at once and waits for that kernel (griddepcontrol.wait) only before it
+ * reads x and writes y.  So the weights of a call must not be written by
+ * the kernel directly before it in the stream; x and y keep full stream
+ * order.  Meant for decode loops whose weights are loaded once.
+ */
+int qk_set_programmatic_launch(int enable);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int qk_version(void);
 

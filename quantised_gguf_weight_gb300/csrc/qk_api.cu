@@ -19,6 +19,7 @@ __device__ int g_qk_error_word;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int64_t> g_skip_tile{-1};
+std::atomic<int> g_programmatic{0};
 
 int *error_word_ptr()
 {
@@ -58,7 +59,7 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * plan.row_bytes;
     cudaError_t e = qk::gemv_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
                                     reinterpret_cast<cudaStream_t>(stream), plan, err,
-                                    g_wait_limit_ns.load(), g_skip_tile.load());
+                                    g_wait_limit_ns.load(), g_skip_tile.load(), g_programmatic.load() != 0);
     return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
 }
 
@@ -117,6 +118,8 @@ uint64_t qk_set_wait_limit_ns(uint64_t ns)
     if (ns == 0) ns = 1;
     return g_wait_limit_ns.exchange(ns);
 }
+
+int qk_set_programmatic_launch(int enable) { return g_programmatic.exchange(enable ? 1 : 0); }
 
 int qk_version(void) { return 100; }
 

@@ -40,7 +40,13 @@ bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int64_t row_byte
 {
     const int UC = fmt == kFmtQ4K ? 128 : 32;
     const int max_c = max_consumers(fmt, batch);
-    const int SW = U < max_c ? U : max_c;
+    // teams of up to 32 lanes are a power of two so that a team never
+    // straddles a warp (warp-shuffle reduction); longer rows use exactly U
+    int SW = U < max_c ? U : max_c;
+    if (U <= 32) {
+        SW = 1;
+        while (SW < U) SW <<= 1;
+    }
     const int R = rows_per_thread(fmt, batch);
     int64_t grid = di.sms;
     if (grid > rows) grid = rows;
@@ -106,7 +112,7 @@ bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p)
 
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_tile)
+                        int *err, uint64_t wait_ns, int64_t skip_tile, bool pdl)
 {
     GemvArgs a;
     a.w = w_rows;
@@ -133,8 +139,8 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     a.err = err;
     if (p.R != rows_per_thread(fmt, batch)) return cudaErrorInvalidValue;
     const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
-    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, a, p.grid, p.smem, st);
-    return gemv_launch_q80(batch, us, a, p.grid, p.smem, st);
+    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, a, p.grid, p.smem, st, pdl);
+    return gemv_launch_q80(batch, us, a, p.grid, p.smem, st, pdl);
 }
 
 }  // namespace qk

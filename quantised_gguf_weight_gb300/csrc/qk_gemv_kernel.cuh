@@ -275,6 +275,9 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
     const int64_t r_end = (a.rows * (blockIdx.x + 1)) / nG;
     const int64_t n_tiles = (r_end - r_begin + a.tile_rows - 1) / a.tile_rows;
 
+    // Programmatic dependent launch: the next grid in the stream may be
+    // scheduled now.  (No effect when launched without that attribute.)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar0 + 8u * s, 1);                    // full[s]
@@ -336,62 +339,60 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
     const uint32_t xs_addr = smem_u32(smem + a.off_x);
     float *xsum = reinterpret_cast<float *>(smem + a.off_xsum);
 
-    // Activations -> shared memory.  Pass 1 issues every copy asynchronously
-    // (float4 group f of batch row b holds columns 4f..4f+3; columns >= K are
-    // zero).  Pass 2 has each thread revisit only the groups it copied: for
-    // Q4_K it sums each 32-column sub-block (8 consecutive lanes) and applies
-    // the per-column 2^-s pre-scaling.  Loops are warp-uniform.
+    // Activations -> shared memory, in one warp-uniform pass: each lane loads
+    // float4 group f of batch row b (columns 4f..4f+3; columns >= K are zero)
+    // and stores it at its permuted place.  For Q4_K the 8 lanes holding a
+    // 32-column sub-block also sum it (unscaled) and the values are
+    // pre-multiplied by 2^-s for their nibble position.  The weights do not
+    // depend on earlier kernels, x may: with programmatic dependent launch
+    // only this part waits for the previous grid (no effect otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     {
         const int K = static_cast<int>(a.K);
         const int g_total = U * G;                 // float4 groups per batch row incl. padding
         const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15u) == 0);
+        constexpr int UNR = 4;
         for (int b = 0; b < B; ++b) {
             const float *xb = a.x + static_cast<int64_t>(b) * K;
-            for (int base = cwarp * 32; base < g_total; base += a.NTC) {
-                const int f = base + lane;
-                if (f < g_total) {
-                    const int u = f / G, g = f % G;
-                    const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>((b * G + g) * XU + u);
-                    const int c0 = 4 * f;
-                    if (vec && c0 + 3 < K) {
-                        cp_async_16(dst, xb + c0);
-                    } else {
+            for (int base = cwarp * 32; base < g_total; base += UNR * a.NTC) {
+                float4 v[UNR];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (c0 + e < K)
-                                cp_async_4(dst + 4u * e, xb + c0 + e);
-                            else
-                                asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + 4u * e), "f"(0.0f) : "memory");
+                for (int i = 0; i < UNR; ++i) {
+                    const int f = base + i * a.NTC + lane;
+                    const int c0 = 4 * f;
+                    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (f < g_total) {
+                        if (vec && c0 + 3 < K) {
+                            v[i] = __ldg(reinterpret_cast<const float4 *>(xb + c0));
+                        } else {
+                            if (c0 < K) v[i].x = __ldg(xb + c0);
+                            if (c0 + 1 < K) v[i].y = __ldg(xb + c0 + 1);
+                            if (c0 + 2 < K) v[i].z = __ldg(xb + c0 + 2);
+                            if (c0 + 3 < K) v[i].w = __ldg(xb + c0 + 3);
                         }
                     }
                 }
-            }
-        }
-        cp_async_wait_all();
-        if constexpr (FMT == kFmtQ4K) {
-            for (int b = 0; b < B; ++b) {
-                for (int base = cwarp * 32; base < g_total; base += a.NTC) {
-                    const int f = base + lane;
-                    const bool have = f < g_total;
+#pragma unroll
+                for (int i = 0; i < UNR; ++i) {
+                    const int f = base + i * a.NTC + lane;
+                    if (base + i * a.NTC >= g_total) break;            // warp-uniform
                     const int u = f / G, g = f % G;
-                    const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>((b * G + g) * XU + u);
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (have)
-                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(dst));
-                    float sum = (v.x + v.y) + (v.z + v.w);
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-                    if (have) {
-                        if ((lane & 7) == 0) xsum[(b * 4 + (g >> 3)) * XU + u] = sum;
+                    if constexpr (FMT == kFmtQ4K) {
+                        float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+                        if (f < g_total && (lane & 7) == 0) xsum[(b * 4 + (g >> 3)) * XU + u] = sum;
                         const int c = 4 * g;
-                        v.x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
-                        v.y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
-                        v.z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
-                        v.w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
+                        v[i].x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
+                        v[i].y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
+                        v[i].z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
+                        v[i].w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
+                    }
+                    if (f < g_total) {
+                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>((b * G + g) * XU + u);
                         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                                     ::"r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+                                     ::"r"(dst), "f"(v[i].x), "f"(v[i].y), "f"(v[i].z), "f"(v[i].w) : "memory");
                     }
                 }
             }
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
     float *red = reinterpret_cast<float *>(smem + a.off_red);
     const int n_out = a.slots * R * B;
     const int red_half = n_out * a.SW;
+    const bool warp_team = a.SW <= 32 && (32 % a.SW) == 0;
     const uint32_t gs_rt = 16u * static_cast<uint32_t>(XU);
     for (int64_t j = 0; j < n_tiles; ++j) {
         const int s = static_cast<int>(j % S);
@@ -434,6 +436,25 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
         __syncwarp();
         if (lane == 0) mbar_arrive(bar0 + 8u * (S + s));   // stage s may be refilled
 
+        if (warp_team) {
+            // teams of SW lanes (SW divides 32): butterfly inside the team,
+            // no barrier; a warp whose wait ran out leaves on its own
+            if (!ok) {
+                if (lane == 0) record_error(a.err, kErrTimeout);
+                break;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    float v = acc[r][b];
+                    for (int off = a.SW >> 1; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+                    const int rt = r * a.slots + slot;
+                    if (active && sl == ((r * B + b) % a.SW) && rt < n) a.y[b * a.ldy + row0 + rt] = v;
+                }
+            continue;
+        }
+
         // team reduction through shared memory: the partial of (slot, r, b)
         // from team member sl sits at red[((slot*R + r)*B + b)*SW + sl]
         float *rb = red + (j & 1) * red_half;
@@ -463,11 +484,11 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
 }
 
 // Launch one instantiation (defined per format in qk_gemv_q4k.cu / qk_gemv_q80.cu).
-cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st);
-cudaError_t gemv_launch_q80(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st);
+cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q80(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
 template <int FMT, int B, int R, int US>
-cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st)
+cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
     auto kern = gemv_kernel<FMT, B, R, US>;
     // raise the dynamic shared-memory limit once per device and size
@@ -481,7 +502,18 @@ cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t 
         if (e != cudaSuccess) return e;
         __atomic_store_n(&granted[dev], smem, __ATOMIC_RELEASE);
     }
-    kern<<<grid, 32 + a.NTC, smem, st>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 + a.NTC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -489,9 +521,9 @@ cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t 
 // compile-time 32 or 128 where it fits, else a runtime value.
 #define QK_GEMV_DISPATCH_US(FMT, B, US_RT)                                                  \
     switch (US_RT) {                                                                        \
-    case 32: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 32>(a, grid, smem, st);   \
-    case 128: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 128>(a, grid, smem, st); \
-    default: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 0>(a, grid, smem, st);    \
+    case 32: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 32>(a, grid, smem, st, pdl);   \
+    case 128: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 128>(a, grid, smem, st, pdl); \
+    default: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 0>(a, grid, smem, st, pdl);    \
     }
 
 }  // namespace qk

@@ -4,7 +4,7 @@
 
 namespace qk {
 
-cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st)
+cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
     switch (batch) {
     case 1: QK_GEMV_DISPATCH_US(kFmtQ4K, 1, us)

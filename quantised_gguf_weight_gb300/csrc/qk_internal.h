@@ -21,6 +21,6 @@ struct GemvPlan {
 bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p);
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_tile);
+                        int *err, uint64_t wait_ns, int64_t skip_tile, bool pdl);
 
 }  // namespace qk

@@ -24,7 +24,8 @@ STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 
 MAX_BATCH = 8
 
 EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
-           "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_version"]
+           "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
+           "qk_version"]
 
 
 class QKError(RuntimeError):
@@ -63,6 +64,8 @@ def load(path: str | None = None):
         lib.qk_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.qk_set_wait_limit_ns.restype = ctypes.c_uint64
         lib.qk_version.restype = I
+        lib.qk_set_programmatic_launch.argtypes = [I]
+        lib.qk_set_programmatic_launch.restype = I
         lib.qk_debug_skip_tile.argtypes = [I64]
         lib.qk_debug_skip_tile.restype = I64
         _lib = lib
@@ -120,6 +123,11 @@ def device_error(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> int:
     return int(load().qk_set_wait_limit_ns(int(ns)))
+
+
+def set_programmatic_launch(enable: bool) -> bool:
+    """Programmatic dependent launch for later calls (see include/qk.h)."""
+    return bool(load().qk_set_programmatic_launch(1 if enable else 0))
 
 
 def debug_skip_tile(tile: int) -> int:

@@ -148,10 +148,12 @@ def test_too_large_is_rejected_before_launch(qk):
     assert torch.all(y == 5.0)
 
 
-def test_bounded_wait_times_out_and_context_survives(qk, orc):
+@pytest.mark.parametrize("fmt,rows,K", [("q4_k", 2000, 4096), ("q4_k", 700, 14336), ("q8_0", 900, 896)])
+def test_bounded_wait_times_out_and_context_survives(qk, orc, fmt, rows, K):
     """A tile whose copy is never issued makes the consumers' wait run out:
-    the launch records QK_ERR_TIMEOUT and later launches work normally."""
-    fmt, rows, K = "q4_k", 2000, 4096
+    the launch records QK_ERR_TIMEOUT and later launches work normally.
+    (K = 4096 and 896 use warp-sized row teams, K = 14336 the shared-memory
+    team reduction.)"""
     wq = synth.weights(fmt, rows, K, seed=15)
     x = synth.activations(1, K, seed=15)
     assert qk.device_error() == 0
@@ -203,3 +205,27 @@ def test_lm_head_q8_0_sampled(qk, orc, batch):
     idx = _sample_rows(rows, 512, seed)
     yr, s = orc.gemv("q8_0", wq, K, x, rows=idx)
     assert_close(y[:, idx], yr, s, f"lm_head b{batch}")
+
+
+def test_programmatic_launch_chain(qk, orc):
+    """With programmatic dependent launch on, a chain whose every input is the
+    previous call's output still sees each output complete."""
+    K = 4096
+    ws = [synth.weights("q4_k", K, K, seed=30 + i) for i in range(4)]
+    x0 = synth.activations(1, K, seed=30)
+    wd = [torch.from_numpy(w).cuda() for w in ws]
+    old = qk.set_programmatic_launch(True)
+    try:
+        xs = [torch.from_numpy(x0).cuda()]
+        for i in range(4):
+            xs.append(qk.qmatvec_q4_k(wd[i], 0, K, K, xs[-1]))
+        torch.cuda.synchronize()
+    finally:
+        qk.set_programmatic_launch(old)
+    x = x0
+    for i in range(4):
+        got = xs[i + 1].cpu().numpy()
+        yr, s = orc.gemv("q4_k", ws[i], K, x.astype(np.float32))
+        # each stage is checked against the oracle fed with the GPU's own input
+        assert_close(got, yr, s, f"stage {i}")
+        x = xs[i + 1].cpu().numpy()
