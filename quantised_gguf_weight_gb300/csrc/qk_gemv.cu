@@ -34,40 +34,42 @@ DevInfo dev_info()
 
 int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
 
-// Layout for a given activation unit stride XU; false if it cannot fit.
-bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int64_t row_bytes, const DevInfo &di,
+// Layout for a given activation unit stride XU and team width SW; false if
+// it cannot fit.
+bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int SW, int64_t row_bytes, const DevInfo &di,
                GemvPlan *p)
 {
     const int UC = fmt == kFmtQ4K ? 128 : 32;
     const int max_c = max_consumers(fmt, batch);
-    // teams of up to 32 lanes are a power of two so that a team never
-    // straddles a warp (warp-shuffle reduction); longer rows use exactly U
-    int SW = U < max_c ? U : max_c;
-    if (U <= 32) {
-        SW = 1;
-        while (SW < U) SW <<= 1;
-    }
     const int R = rows_per_thread(fmt, batch);
     int64_t grid = di.sms;
     if (grid > rows) grid = rows;
     const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
     const int64_t xsum_bytes = fmt == kFmtQ4K ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128) : 0;
+    // batch 1 keeps a block-floating-point scale per 32-column group
+    const int64_t xscale_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 4, 128) : 0;
     const int64_t off_x = 256;
     const int64_t off_xsum = off_x + x_bytes;
-    const int64_t off_red = off_xsum + xsum_bytes;
+    const int64_t off_xscale = off_xsum + xsum_bytes;
+    const int64_t off_red = off_xscale + xscale_bytes;
     const int64_t budget = di.smem_optin;
+    const bool warp_team = SW <= 32 && (32 % SW) == 0;
     // teams: no more than the threads allow, than the CTA has rows for, and
     // than fit with two stages next to the activations and the partials
     const int64_t rows_per_cta = (rows + grid - 1) / grid;
     int64_t slots = max_c / SW;
     slots = std::min<int64_t>(slots, (rows_per_cta + R - 1) / R);
     for (; slots >= 1; --slots) {
-        const int64_t red_bytes = round_up(2 * slots * R * batch * SW * 4, 128);
+        const int64_t red_bytes = warp_team ? 0 : round_up(2 * slots * R * batch * SW * 4, 128);
         const int64_t stage = round_up(slots * R * row_bytes + 32, 128);
         if (off_red + red_bytes + 2 * stage <= budget) break;
     }
     if (slots < 1) return false;
-    const int64_t red_bytes = round_up(2 * slots * R * batch * SW * 4, 128);
+    if (warp_team && SW < 32) {
+        const int g = 32 / SW;                 // whole warps of consumers
+        slots = std::max<int64_t>(g, (slots / g) * g);
+    }
+    const int64_t red_bytes = warp_team ? 0 : round_up(2 * slots * R * batch * SW * 4, 128);
     const int64_t off_stage = off_red + red_bytes;
     const int64_t stage = round_up(slots * R * row_bytes + 32, 128);
     int64_t stages = (budget - off_stage) / stage;
@@ -84,12 +86,33 @@ bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int64_t row_byte
     p->stage_bytes = static_cast<int>(stage);
     p->off_x = static_cast<int>(off_x);
     p->off_xsum = static_cast<int>(off_xsum);
+    p->off_xscale = static_cast<int>(off_xscale);
     p->off_red = static_cast<int>(off_red);
     p->off_stage = static_cast<int>(off_stage);
     p->smem = static_cast<int>(off_stage + stages * stage);
     p->row_bytes = row_bytes;
     p->grid = static_cast<int>(grid);
     return true;
+}
+
+// Row-team width for warp-sized teams: a power of two up to 32 that gives
+// each lane at least `min_units` units where the row has them, with the
+// units spread evenly (the busiest lane at most 15% above the average).
+int warp_team_width(int U, int min_units)
+{
+    int best = 1;
+    double best_cost = 1e30;
+    for (int sw = 32; sw >= 1; sw >>= 1) {
+        if (sw > 1 && U / sw < min_units) continue;
+        const int per = (U + sw - 1) / sw;
+        const double cost = static_cast<double>(per) * sw / U;   // >= 1: load imbalance
+        if (cost <= 1.15) return sw;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = sw;
+        }
+    }
+    return best;
 }
 
 }  // namespace
@@ -104,10 +127,30 @@ bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p)
     const int64_t U64 = (K + UC - 1) / UC;
     if (U64 > (1 << 20)) return false;
     const int U = static_cast<int>(U64);
-    // a compile-time activation unit stride (32 or 128) where it fits
-    if (U <= 32 && plan_with(fmt, rows, batch, U, 32, row_bytes, di, p)) return true;
-    if (U > 32 && U <= 128 && plan_with(fmt, rows, batch, U, 128, row_bytes, di, p)) return true;
-    return plan_with(fmt, rows, batch, U, U, row_bytes, di, p);
+    // team width: warp-sized teams (shuffle reduction, no barrier) unless
+    // they would leave fewer than 256 consumers, then one team of U threads
+    // per row with the shared-memory reduction
+    const int min_units = fmt == kFmtQ80 ? 4 : 1;
+    const int sw_warp = warp_team_width(U, min_units);
+    const int XU_c = U <= 32 ? 32 : (U <= 128 ? 128 : U);   // compile-time strides where they fit
+    GemvPlan a_plan, b_plan;
+    bool a_ok = plan_with(fmt, rows, batch, U, XU_c, sw_warp, row_bytes, di, &a_plan);
+    if (!a_ok && XU_c != U) a_ok = plan_with(fmt, rows, batch, U, U, sw_warp, row_bytes, di, &a_plan);
+    const int max_c = max_consumers(fmt, batch);
+    bool b_ok = false;
+    if (U > 32 && U <= max_c && (!a_ok || a_plan.NTC < 256)) {
+        b_ok = plan_with(fmt, rows, batch, U, XU_c, U, row_bytes, di, &b_plan);
+        if (!b_ok && XU_c != U) b_ok = plan_with(fmt, rows, batch, U, U, U, row_bytes, di, &b_plan);
+    }
+    if (b_ok && (!a_ok || b_plan.NTC > a_plan.NTC)) {
+        *p = b_plan;
+        return true;
+    }
+    if (a_ok) {
+        *p = a_plan;
+        return true;
+    }
+    return false;
 }
 
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
@@ -132,6 +175,7 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     a.stage_bytes = p.stage_bytes;
     a.off_x = p.off_x;
     a.off_xsum = p.off_xsum;
+    a.off_xscale = p.off_xscale;
     a.off_red = p.off_red;
     a.off_stage = p.off_stage;
     a.skip_tile = skip_tile;

@@ -64,7 +64,7 @@ struct GemvArgs {
     int tile_rows;      // rows per stage = slots * R
     int stages;
     int stage_bytes;
-    int off_x, off_xsum, off_red, off_stage;   // shared-memory byte offsets
+    int off_x, off_xsum, off_xscale, off_red, off_stage;   // shared-memory byte offsets
     int64_t skip_tile;  // test hook: CTA 0 never copies this tile (-1: none)
     uint64_t wait_ns;
     int *err;
@@ -256,6 +256,150 @@ __device__ __forceinline__ void q8_unit(const uint8_t *const (&rowp)[R], int u, 
         }
 }
 
+// -------------------------------------------------------------------------- batch-1 integer units
+//
+// For batch 1 the activations are held as block floating point: each
+// 32-column group has one exponent E and every value becomes the 32-bit
+// integer m = rint(x * 2^(30-E)) (|m| < 2^31), stored as four byte planes
+// (plane 3 signed, planes 0..2 unsigned).  A weight group then costs one
+// 4-way byte dot product per plane, sum_i q_i m_i is assembled exactly in
+// integers per plane and x-group scale 2^(E-30) turns it back into a float.
+// Values within 2^7 of their group's largest magnitude are represented
+// exactly; the error of any other value is below 2^-31 of that magnitude.
+
+// sum(q*m) of one group from its four plane sums, as a float.
+__device__ __forceinline__ float planes_to_float(int s0, int s1, int s2, int s3)
+{
+    const int hi = s3 * 256 + s2;     // exact in int32 for 32-weight groups
+    const int lo = s1 * 256 + s0;
+    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
+}
+
+// One 128-weight Q4_K unit for R rows, batch 1.
+template <int R, int US>
+__device__ __forceinline__ void q4k_unit_dig(const uint8_t *const (&rowp)[R], int u, uint32_t xa, uint32_t gs_rt,
+                                             const float *__restrict__ xsum_u, const float *__restrict__ xscale_u,
+                                             int xstride, float (&acc)[R][1])
+{
+    const uint32_t gs = US ? 16u * US : gs_rt;
+    const int xstr = US ? US : xstride;
+    const int blk = u >> 1;
+    const int h = u & 1;
+    float ds[R][4], dm[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint4 hd = *reinterpret_cast<const uint4 *>(rowp[r] + blk * 144);
+        const float d = half_bits_to_float(hd.x);
+        const float dmin = half_bits_to_float(hd.x >> 16);
+        const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu;
+        const uint32_t m_lo = hd.z & 0x3F3F3F3Fu;
+        const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+        const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+        const uint32_t scw = h ? sc_hi : sc_lo;
+        const uint32_t mw = h ? m_hi : m_lo;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float sc = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j)) - kTwo23;
+            const float m = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j)) - kTwo23;
+            ds[r][j] = d * sc;
+            dm[r][j] = dmin * m;
+        }
+    }
+    const uint8_t *qoff[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) qoff[r] = rowp[r] + blk * 144 + 16 + 64 * h;
+#pragma unroll
+    for (int lc = 0; lc < 2; ++lc) {
+        int sl[R][4], sh[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sl[r][k] = sh[r][k] = 0;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint4 q[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) q[r] = *reinterpret_cast<const uint4 *>(qoff[r] + 32 * lc + 16 * p);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int g_lo = 16 * lc + 4 * p + k;
+                const uint4 xl = lds128u(xa + static_cast<uint32_t>(g_lo) * gs);
+                const uint4 xh = lds128u(xa + static_cast<uint32_t>(g_lo + 8) * gs);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t wd = k == 0 ? q[r].x : (k == 1 ? q[r].y : (k == 2 ? q[r].z : q[r].w));
+                    const uint32_t L = wd & 0x0F0F0F0Fu;          // low nibbles: 4 columns of sub-block 2lc
+                    const uint32_t H = (wd >> 4) & 0x0F0F0F0Fu;   // high nibbles: same columns of 2lc+1
+                    sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
+                    sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
+                    sl[r][2] = dp4a_uu(L, xl.z, sl[r][2]);
+                    sl[r][3] = dp4a_us(L, xl.w, sl[r][3]);
+                    sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
+                    sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
+                    sh[r][2] = dp4a_uu(H, xh.z, sh[r][2]);
+                    sh[r][3] = dp4a_us(H, xh.w, sh[r][3]);
+                }
+            }
+        }
+        const float X0 = xsum_u[(2 * lc) * xstr], X1 = xsum_u[(2 * lc + 1) * xstr];
+        const float S0 = xscale_u[(2 * lc) * xstr], S1 = xscale_u[(2 * lc + 1) * xstr];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2], sl[r][3]);
+            const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2], sh[r][3]);
+            float t = acc[r][0];
+            t = fmaf(ds[r][2 * lc] * S0, F0, t);
+            t = fmaf(-dm[r][2 * lc], X0, t);
+            t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
+            t = fmaf(-dm[r][2 * lc + 1], X1, t);
+            acc[r][0] = t;
+        }
+    }
+}
+
+// One 32-weight Q8_0 block for R rows, batch 1.
+template <int R, int US>
+__device__ __forceinline__ void q8_unit_dig(const uint8_t *const (&rowp)[R], int u, uint32_t xa, uint32_t gs_rt,
+                                            float xscale, float (&acc)[R][1])
+{
+    const uint32_t gs = US ? 16u * US : gs_rt;
+    uint32_t qw[R][8];
+    float d[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(rowp[r] + 34 * u);
+        const uint32_t off = static_cast<uint32_t>(a & 3u);           // 0 or 2
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(a - off);
+        uint32_t wv[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) wv[i] = wp[i];
+        d[r] = half_bits_to_float(wv[0] >> (8 * off));
+        const uint32_t sel = off ? 0x7654u : 0x5432u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qw[r][k] = __byte_perm(wv[k], wv[k + 1], sel);
+    }
+    int sp[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sp[r][k] = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint4 xv = lds128u(xa + static_cast<uint32_t>(k) * gs);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t v = qw[r][k];
+            sp[r][0] = dp4a_su(v, xv.x, sp[r][0]);
+            sp[r][1] = dp4a_su(v, xv.y, sp[r][1]);
+            sp[r][2] = dp4a_su(v, xv.z, sp[r][2]);
+            sp[r][3] = dp4a_ss(v, xv.w, sp[r][3]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2], sp[r][3]), acc[r][0]);
+}
+
 // -------------------------------------------------------------------------- kernel
 
 template <int FMT, int B, int R, int US>
@@ -338,6 +482,7 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
     const int XU = US ? US : a.XU;
     const uint32_t xs_addr = smem_u32(smem + a.off_x);
     float *xsum = reinterpret_cast<float *>(smem + a.off_xsum);
+    float *xscale = reinterpret_cast<float *>(smem + a.off_xscale);
 
     // Activations -> shared memory, in one warp-uniform pass: each lane loads
     // float4 group f of batch row b (columns 4f..4f+3; columns >= K are zero)
@@ -377,6 +522,47 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
                     const int f = base + i * a.NTC + lane;
                     if (base + i * a.NTC >= g_total) break;            // warp-uniform
                     const int u = f / G, g = f % G;
+                    if constexpr (B == 1) {
+                        // block floating point per 32-column group (8 lanes), as four byte planes
+                        float amax = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+                        float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                        if constexpr (FMT == kFmtQ4K) {
+                            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+                        }
+                        const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 255u);
+                        const bool finite = ebits != 255;
+                        const int E = max(ebits - 127, -96);
+                        const float up = __int_as_float((157 - E) << 23);     // 2^(30-E)
+                        const float down = __int_as_float((97 + E) << 23);    // 2^(E-30)
+                        uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+                        if (finite) {
+                            m0 = static_cast<uint32_t>(__float2int_rn(v[i].x * up));
+                            m1 = static_cast<uint32_t>(__float2int_rn(v[i].y * up));
+                            m2 = static_cast<uint32_t>(__float2int_rn(v[i].z * up));
+                            m3 = static_cast<uint32_t>(__float2int_rn(v[i].w * up));
+                        }
+                        // byte-plane transpose: plane k holds byte k of the four columns
+                        const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
+                        const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
+                        const uint32_t p0 = __byte_perm(t0, t1, 0x5410u), p1 = __byte_perm(t0, t1, 0x7632u);
+                        const uint32_t p2 = __byte_perm(t2, t3, 0x5410u), p3 = __byte_perm(t2, t3, 0x7632u);
+                        if (f < g_total) {
+                            const int grp = FMT == kFmtQ4K ? (g >> 3) : 0;
+                            if ((lane & 7) == 0) {
+                                xscale[grp * XU + u] = finite ? down : __int_as_float(0x7FC00000);
+                                if constexpr (FMT == kFmtQ4K) xsum[grp * XU + u] = sum;
+                            }
+                            const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(g * XU + u);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                         ::"r"(dst), "r"(p0), "r"(p1), "r"(p2), "r"(p3) : "memory");
+                        }
+                        continue;
+                    }
                     if constexpr (FMT == kFmtQ4K) {
                         float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
                         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
@@ -427,7 +613,11 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
             }
             for (int u = sl; u < U; u += a.SW) {
                 const uint32_t xa = xs_addr + 16u * static_cast<uint32_t>(u);
-                if constexpr (FMT == kFmtQ4K)
+                if constexpr (B == 1 && FMT == kFmtQ4K)
+                    q4k_unit_dig<R, US>(rowp, u, xa, gs_rt, xsum + u, xscale + u, XU, acc);
+                else if constexpr (B == 1)
+                    q8_unit_dig<R, US>(rowp, u, xa, gs_rt, xscale[u], acc);
+                else if constexpr (FMT == kFmtQ4K)
                     q4k_unit<B, R, US>(rowp, u, xa, gs_rt, xsum + u, XU, acc);
                 else
                     q8_unit<B, R, US>(rowp, u, xa, gs_rt, acc);

@@ -14,7 +14,7 @@ constexpr int kMaxStages = 8;        // shared-memory ring depth
 // Launch plan of one GEMV call (shared-memory layout, grid, team shape).
 struct GemvPlan {
     int U, XU, SW, slots, NTC, R, tile_rows, stages, stage_bytes;
-    int off_x, off_xsum, off_red, off_stage, smem, grid;
+    int off_x, off_xsum, off_xscale, off_red, off_stage, smem, grid;
     int64_t row_bytes;
 };
 
