@@ -94,6 +94,31 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
                  const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
 
 /*
+ * Q4_K prefill GEMM on the tensor cores:
+ *   y[m*ldy + n] = sum_{c<K} bf16(W[row_offset + n][c]) * bf16(x[m*K + c])
+ * for m < M tokens and n < N weight rows, accumulated in fp32.  Each weight
+ * is decoded to fp32 (w = d*sc*q - dmin*m) and rounded to bf16, each
+ * activation is rounded to bf16 (round to nearest even).  This is the
+ * batched (prefill) form of the matvec: the "matmuls run over up to
+ * LM_CHUNK positions at once ... each weight is read once per chunk"
+ * (nurllama 0.18.1 API reference, model.nu).
+ *   w          device Q4_K block bytes of the whole tensor; 16-byte aligned.
+ *   x          device fp32 [M][K], row stride K; 4-byte aligned.
+ *   y          device fp32 [M][ldy]; writes y[m*ldy + n] for n < N only.
+ *              ldy == 0 means ldy = N.
+ *   workspace  device scratch of at least qgemm_q4_k_workspace_bytes(M, N, K)
+ *              bytes, 256-byte aligned, owned by the caller (it receives the
+ *              bf16 copy of x; its contents on return are unspecified).
+ * Error bound: |y - exact| <= 1e-2 * sum|w*x| + 1e-6 per element (two bf16
+ * roundings); the tests also check it against the bf16-rounded product.
+ */
+int qgemm_q4_k(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+               float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream);
+
+/* Workspace bytes qgemm_q4_k needs for M tokens and K columns (N unused). */
+size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
  * Bytes of one row of a tensor with K columns: ceil(K/32)*34 (Q8_0) or
  * ceil(K/256)*144 (Q4_K).
  */

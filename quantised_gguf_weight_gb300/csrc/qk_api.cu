@@ -20,6 +20,7 @@ __device__ int g_qk_error_word;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int64_t> g_skip_tile{-1};
 std::atomic<int> g_programmatic{0};
+std::atomic<int> g_gemm_skip_chunk{-1};
 
 int *error_word_ptr()
 {
@@ -66,6 +67,38 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
 }  // namespace
 
 extern "C" {
+
+size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    (void)N;
+    if (M <= 0 || K <= 0) return 0;
+    return qk::gemm_workspace_bytes(M, K);
+}
+
+int qgemm_q4_k(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+               int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream)
+{
+    if (!w || !x || !y) return QK_ERR_NULL;
+    if (N <= 0 || K <= 0 || M <= 0 || row_offset < 0) return QK_ERR_BAD_DIM;
+    if (ldy == 0) ldy = N;
+    if (ldy < N) return QK_ERR_BAD_DIM;
+    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < qk::gemm_workspace_bytes(M, K))
+        return QK_ERR_WORKSPACE;
+    // tensor-map limits: at most 2^31 tokens and rows per call
+    if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1) return QK_ERR_TOO_LARGE;
+    const int64_t row_bytes = ((K + 255) / 256) * 144;
+    if (row_offset > (INT64_MAX / row_bytes) - N) return QK_ERR_BAD_DIM;
+    int *err = error_word_ptr();
+    if (!err) return QK_ERR_CUDA;
+    const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * row_bytes;
+    bool encode_failed = false;
+    cudaError_t e = qk::gemm_q4k_launch(w_rows, N, K, x, M, y, ldy, workspace,
+                                        reinterpret_cast<cudaStream_t>(stream), err, g_wait_limit_ns.load(),
+                                        g_gemm_skip_chunk.load(), &encode_failed);
+    if (encode_failed) return QK_ERR_CUDA;
+    return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
+}
 
 int qmatvec_q8_0(const void *w, int64_t row_offset, int64_t rows, int64_t K, const float *x,
                  int batch, float *y, int64_t ldy, qk_stream_t stream)
@@ -127,5 +160,10 @@ int qk_version(void) { return 100; }
 // skips the bulk copy of its tile `tile` (-1 restores normal operation), so
 // its consumers' bounded wait runs out and the launch records QK_ERR_TIMEOUT.
 int64_t qk_debug_skip_tile(int64_t tile) { return g_skip_tile.exchange(tile); }
+
+// Test hook, not part of the public header: CTA 0 of every later GEMM launch
+// never loads the activations of K chunk `chunk` (-1 restores normal
+// operation), so the MMA issuer's bounded wait runs out (QK_ERR_TIMEOUT).
+int qk_debug_gemm_skip_chunk(int chunk) { return g_gemm_skip_chunk.exchange(chunk); }
 
 }  // extern "C"

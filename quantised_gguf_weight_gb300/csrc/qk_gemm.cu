@@ -1,0 +1,399 @@
+// qk_gemm.cu -- prefill GEMM with GGUF Q4_K weights on the tcgen05 tensor
+// cores (sm_103a):  Y[m][n] = sum_k bf16(x[m][k]) * bf16(w[n][k]),
+// f32 accumulation, where w = d*sc*q - dmin*m is computed in fp32 and rounded
+// to bf16 (round to nearest even) in shared memory, once per weight.
+//
+// This is the prefill counterpart of the decode matvec: the chunked prefill
+// runs the matmuls over many positions at once so that "each weight is read
+// once per chunk" (nurllama 0.18.1 API reference, model.nu), and the loom
+// port runs prefill through GEMMs that dequantise the weight format in the
+// kernel ("loom-port-llm" SKILL.md, "What the starter generates", gen_gemm.py).
+//
+// Kernel shape (one CTA per 128 weight rows x up to 512 tokens):
+//  * warp 0 issues the TMA copies: the raw Q4_K bytes of 128 rows x one
+//    super-block (a 2-D tensor map over the rows, 144 x 128 bytes) and the
+//    bf16 activations of each 64-column K chunk (a 2-D tensor map with the
+//    128-byte swizzle, two boxes of 256 tokens);
+//  * warp 1 owns the tensor memory (512 f32 columns = 128 lanes x 512 tokens)
+//    and one of its threads issues tcgen05.mma (M = 128 weight rows, N = 256
+//    tokens, K = 16) and tcgen05.commit;
+//  * warps 2-5 dequantise each 64-column chunk of the 128 rows into the
+//    K-major 128-byte-swizzled bf16 layout the MMA reads, then run the
+//    epilogue: tcgen05.ld of 32 lanes x 32 columns -> coalesced stores of Y.
+// Double-buffered stages synchronise through mbarriers; every wait is bounded
+// and a wait that runs out aborts the CTA cleanly (copies drained, MMAs
+// completed, tensor memory freed) and records the device error word.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qk_device.cuh"
+#include "qk_internal.h"
+#include "qk_tc.cuh"
+
+namespace qk {
+
+namespace gemm {
+
+constexpr int kBM = 128;                 // weight rows per CTA (MMA M)
+constexpr int kBN = 256;                 // tokens per MMA (MMA N)
+constexpr int kHalves = 2;               // tokens per CTA pass = kBN * kHalves
+constexpr int kBK = 64;                  // K columns per stage (one 128-byte swizzle row)
+constexpr int kStages = 2;
+constexpr int kRawStages = 2;
+constexpr int kRawBytes = kBM * 144;     // one Q4_K super-block column of 128 rows
+constexpr int kBStage = kHalves * kBN * kBK * 2;   // 64 KB
+constexpr int kAStage = kBM * kBK * 2;             // 16 KB
+constexpr int kOffB = 0;
+constexpr int kOffA = kOffB + kStages * kBStage;
+constexpr int kOffRaw = kOffA + kStages * kAStage;
+constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+
+// barrier slots (8 bytes each) after kOffBar
+constexpr int kBarXFull = 0, kBarAFull = 2, kBarEmpty = 4, kBarRawFull = 6, kBarRawEmpty = 8, kBarAcc = 10,
+              kBarDone = 11;
+constexpr int kOffTmemSlot = 96, kOffAbort = 100;
+
+struct Args {
+    float *y;
+    int64_t N, K, M, ldy;
+    int n_tiles;
+    int nk;            // number of 64-column K chunks
+    int skip_chunk;    // test hook: CTA 0 never loads the activations of this chunk (-1: none)
+    uint64_t wait_ns;
+    int *err;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit, volatile int *abort_flag,
+                                              int *err)
+{
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, limit)) return true;
+    *abort_flag = 1;
+    record_error(err, kErrTimeout);
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
+    const uint32_t bar0 = base_u32 + kOffBar;
+    auto bar = [&](int i) { return bar0 + 8u * i; };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kOffBar + kOffAbort);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(base + kOffBar + kOffTmemSlot);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int n_tile = blockIdx.x % a.n_tiles;
+    const int m_block = blockIdx.x / a.n_tiles;
+    const int n0 = n_tile * kBM;
+    const int m0 = m_block * (kBN * kHalves);
+    const int nh = (a.M - m0) > kBN ? 2 : 1;          // token halves used in this pass
+    const int nk = a.nk;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kBarXFull + s), 1);
+            mbar_init(bar(kBarAFull + s), 128);
+            mbar_init(bar(kBarEmpty + s), 1);
+        }
+        for (int r = 0; r < kRawStages; ++r) {
+            mbar_init(bar(kBarRawFull + r), 1);
+            mbar_init(bar(kBarRawEmpty + r), 128);
+        }
+        mbar_init(bar(kBarAcc), 1);
+        mbar_init(bar(kBarDone), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(base_u32 + kOffBar + kOffTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_evict_first_policy();
+            const uint64_t pol_x = l2_evict_last_policy();
+            int issued_x = 0, issued_raw = 0;
+            for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
+                if ((kc & 3) == 0) {
+                    const int kb = kc >> 2, r = kb % kRawStages;
+                    if (kb >= kRawStages &&
+                        !wait_or_abort(bar(kBarRawEmpty + r), ((kb / kRawStages) - 1) & 1, a.wait_ns, abort_flag,
+                                       a.err))
+                        break;
+                    mbar_arrive_expect_tx(bar(kBarRawFull + r), kRawBytes);
+                    tma_load_2d(base_u32 + kOffRaw + r * kRawBytes, &tm_w, kb * 144, n0, bar(kBarRawFull + r), pol_w);
+                    ++issued_raw;
+                }
+                const int s = kc % kStages;
+                if (kc >= kStages &&
+                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
+                    break;
+                if (!(kc == a.skip_chunk && blockIdx.x == 0)) {
+                    mbar_arrive_expect_tx(bar(kBarXFull + s), static_cast<uint32_t>(nh * kBN * kBK * 2));
+                    for (int h = 0; h < nh; ++h)
+                        tma_load_2d(base_u32 + kOffB + s * kBStage + h * (kBN * kBK * 2), &tm_x, kc * kBK,
+                                    m0 + h * kBN, bar(kBarXFull + s), pol_x);
+                }
+                ++issued_x;
+            }
+            // let every copy issued land before the CTA can exit
+            for (int t = issued_x - kStages; t < issued_x; ++t) {
+                if (t < 0 || (t == a.skip_chunk && blockIdx.x == 0)) continue;
+                mbar_wait(bar(kBarXFull + t % kStages), (t / kStages) & 1, a.wait_ns);
+            }
+            for (int t = issued_raw - kRawStages; t < issued_raw; ++t) {
+                if (t < 0) continue;
+                mbar_wait(bar(kBarRawFull + t % kRawStages), (t / kRawStages) & 1, a.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+            bool any = false;
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kStages;
+                const uint32_t par = (kc / kStages) & 1;
+                if (!wait_or_abort(bar(kBarAFull + s), par, a.wait_ns, abort_flag, a.err)) break;
+                if (!wait_or_abort(bar(kBarXFull + s), par, a.wait_ns, abort_flag, a.err)) break;
+                tc_fence_after();
+                const uint32_t a_base = base_u32 + kOffA + s * kAStage;
+                const uint32_t b_base = base_u32 + kOffB + s * kBStage;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128_kmajor(a_base + 32u * kk);
+                    for (int h = 0; h < nh; ++h) {
+                        const uint64_t bd = smem_desc_sw128_kmajor(b_base + h * (kBN * kBK * 2) + 32u * kk);
+                        tc_mma_bf16(taddr + static_cast<uint32_t>(h * kBN), ad, bd, idesc, (kc | kk) != 0);
+                    }
+                }
+                any = true;
+                tc_commit(bar(kBarEmpty + s));   // stage s reusable once these MMAs complete
+            }
+            if (!*abort_flag) tc_commit(bar(kBarAcc));
+            if (any) {
+                // no MMA may still read shared memory or write tensor memory
+                // when the tensor memory is freed below
+                tc_commit(bar(kBarDone));
+                mbar_wait(bar(kBarDone), 0, a.wait_ns);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ dequantise + epilogue
+        const int t = tid - 64;          // 0..127: the weight row of this thread inside the tile
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % kStages;
+            const int kb = kc >> 2, c = kc & 3, r = kb % kRawStages;
+            if (c == 0 && !wait_or_abort(bar(kBarRawFull + r), (kb / kRawStages) & 1, a.wait_ns, abort_flag, a.err))
+                break;
+            if (kc >= kStages &&
+                !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
+                break;
+            const uint8_t *row = base + kOffRaw + r * kRawBytes + t * 144;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(row);
+            const float d = half_bits_to_float(hd.x);
+            const float dmin = half_bits_to_float(hd.x >> 16);
+            // 6-bit scale and min of sub-blocks 2c (low nibbles) and 2c+1 (high)
+            const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
+            const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+            const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+            const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
+            const int j0 = 2 * (c & 1);   // byte of the packed words for sub-block 2c
+            const float sc0 = static_cast<float>((scw >> (8 * j0)) & 0xFFu);
+            const float sc1 = static_cast<float>((scw >> (8 * j0 + 8)) & 0xFFu);
+            const float mm0 = static_cast<float>((mw >> (8 * j0)) & 0xFFu);
+            const float mm1 = static_cast<float>((mw >> (8 * j0 + 8)) & 0xFFu);
+            const float ds0 = d * sc0, ds1 = d * sc1, dm0 = dmin * mm0, dm1 = dmin * mm1;
+            const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
+            const uint32_t a_row = base_u32 + kOffA + s * kAStage + t * 128;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {            // bytes 16*half .. 16*half+15 of the chunk
+                const uint4 qv = qs[half];
+                const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int sel = 0; sel < 2; ++sel) {           // 0: low nibbles (cols i), 1: high (cols 32+i)
+                    const float ds = sel ? ds1 : ds0, dm = sel ? dm1 : dm0;
+                    // 16 weights: columns 32*sel + 16*half + [0, 16) of this chunk
+                    uint32_t packed[8];
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint32_t v = sel ? (w4[wi] >> 4) : w4[wi];
+                        const float q0 = static_cast<float>(v & 15u), q1 = static_cast<float>((v >> 8) & 15u);
+                        const float q2 = static_cast<float>((v >> 16) & 15u), q3 = static_cast<float>((v >> 24) & 15u);
+                        const __nv_bfloat162 p01 = __floats2bfloat162_rn(fmaf(q0, ds, -dm), fmaf(q1, ds, -dm));
+                        const __nv_bfloat162 p23 = __floats2bfloat162_rn(fmaf(q2, ds, -dm), fmaf(q3, ds, -dm));
+                        packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
+                        packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                    }
+                    // two 16-byte chunks (8 columns each) of the swizzled row
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        const int chunk = 4 * sel + 2 * half + h8;          // logical 16-byte chunk 0..7
+                        const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
+                                     "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
+                                     : "memory");
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarAFull + s));
+            if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
+        }
+        // epilogue: tensor memory -> registers -> Y
+        if (wait_or_abort(bar(kBarAcc), 0, a.wait_ns, abort_flag, a.err)) {
+            tc_fence_after();
+            const int q = warp & 3;                         // lane quarter this warp may access
+            const int n = n0 + 32 * q + lane;
+            const int cols = nh * kBN;
+            for (int j0 = 0; j0 < cols; j0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(j0), v);
+                tmem_ld_wait();
+                if (n < a.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t m = m0 + j0 + i;
+                        if (m < a.M) a.y[m * a.ldy + n] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(taddr, kTmemCols);
+    }
+}
+
+// X fp32 [M][K] -> Xb bf16 [M][K8], round to nearest even; columns K..K8-1 zero.
+__global__ void x_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ xb, int64_t M, int64_t K,
+                                 int64_t K8)
+{
+    const int64_t total = M * K8;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / K8, k = i - m * K8;
+        xb[i] = k < K ? __float2bfloat16_rn(x[m * K + k]) : __float2bfloat16_rn(0.0f);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace gemm
+
+int64_t gemm_k8(int64_t K) { return (K + 7) / 8 * 8; }
+
+size_t gemm_workspace_bytes(int64_t M, int64_t K) { return static_cast<size_t>(M * gemm_k8(K) * 2 + 256); }
+
+cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                            int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
+                            bool *encode_failed)
+{
+    using namespace gemm;
+    *encode_failed = false;
+    const int64_t K8 = gemm_k8(K);
+    const int64_t row_bytes = ((K + 255) / 256) * 144;
+    __nv_bfloat16 *xb = static_cast<__nv_bfloat16 *>(workspace);
+    {
+        const int64_t total = M * K8;
+        int64_t blocks = (total + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        x_to_bf16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(x, xb, M, K, K8);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) {
+        *encode_failed = true;
+        return cudaErrorNotSupported;
+    }
+    CUtensorMap tm_x, tm_w;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K8), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K8 * 2)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBN)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *encode_failed = true;
+            return cudaErrorInvalidValue;
+        }
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t box[2] = {144u, static_cast<cuuint32_t>(kBM)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *encode_failed = true;
+            return cudaErrorInvalidValue;
+        }
+    }
+    Args a;
+    a.y = y;
+    a.N = N;
+    a.K = K;
+    a.M = M;
+    a.ldy = ldy;
+    a.n_tiles = static_cast<int>((N + kBM - 1) / kBM);
+    a.nk = static_cast<int>((K8 + kBK - 1) / kBK);
+    a.skip_chunk = skip_chunk;
+    a.wait_ns = wait_ns;
+    a.err = err;
+    const int64_t m_blocks = (M + kBN * kHalves - 1) / (kBN * kHalves);
+    const int64_t grid = a.n_tiles * m_blocks;
+    static int granted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && granted[dev] == 0) {
+        e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        granted[dev] = 1;
+    }
+    gemm_q4k_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(tm_x, tm_w, a);
+    return cudaGetLastError();
+}
+
+}  // namespace qk

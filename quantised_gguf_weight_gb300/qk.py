@@ -23,7 +23,8 @@ STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 
           5: "QK_ERR_CUDA", 6: "QK_ERR_TIMEOUT", 7: "QK_ERR_WORKSPACE", 8: "QK_ERR_TOO_LARGE"}
 MAX_BATCH = 8
 
-EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
+EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
+           "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
            "qk_version"]
 
@@ -54,6 +55,12 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P]
             fn.restype = I
+        lib.qgemm_q4_k.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
+        lib.qgemm_q4_k.restype = I
+        lib.qgemm_q4_k_workspace_bytes.argtypes = [I64, I64, I64]
+        lib.qgemm_q4_k_workspace_bytes.restype = ctypes.c_size_t
+        lib.qk_debug_gemm_skip_chunk.argtypes = [I]
+        lib.qk_debug_gemm_skip_chunk.restype = I
         for name in ("qk_row_bytes_q8_0", "qk_row_bytes_q4_k"):
             getattr(lib, name).argtypes = [I64]
             getattr(lib, name).restype = I64
@@ -114,6 +121,35 @@ def qmatvec_q4_k(w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.T
                  y: torch.Tensor | None = None, ldy: int = 0, stream=None) -> torch.Tensor:
     """y[b][r] = sum_c W[row_offset + r][c] x[b][c] for Q4_K block bytes `w` (uint8, device)."""
     return _qmatvec("qmatvec_q4_k", w, row_offset, rows, K, x, y, ldy, stream)
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().qgemm_q4_k_workspace_bytes(M, N, K))
+
+
+def qgemm_q4_k(w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor,
+               y: torch.Tensor | None = None, ldy: int = 0, workspace: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """y[m][n] = sum_c bf16(W[row_offset + n][c]) bf16(x[m][c]) on the tensor cores (Q4_K bytes `w`).
+
+    `workspace` is caller-owned device scratch (uint8) of gemm_workspace_bytes(M, N, K) bytes;
+    it is allocated here through torch when not given."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+        ldy = N
+    nbytes = gemm_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    st = load().qgemm_q4_k(w.data_ptr(), row_offset, N, K, x.data_ptr(), M, y.data_ptr(), ldy,
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "qgemm_q4_k")
+    return y
+
+
+def debug_gemm_skip_chunk(chunk: int) -> int:
+    """Test hook: CTA 0 of later GEMM launches never loads K chunk `chunk` (-1: off)."""
+    return int(load().qk_debug_gemm_skip_chunk(int(chunk)))
 
 
 def device_error(stream=None) -> int:

@@ -34,7 +34,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qk_status_string", "qk_device_error"):
+    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes", "qk_status_string",
+              "qk_device_error"):
         assert n in names
 
 
@@ -98,3 +99,24 @@ def test_product_path_does_not_import_the_oracle():
     for path in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True) + \
             glob.glob(os.path.join(pkg, "csrc", "*")):
         assert not pat.search(open(path, errors="replace").read()), path
+
+
+def test_gemm_argument_validation_without_gpu(lib):
+    f = lib.qgemm_q4_k
+    ok = dict(w=FAKE, off=0, N=128, K=256, x=FAKE, M=4, y=FAKE, ldy=0, ws=FAKE, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["w"], a["off"], a["N"], a["K"], a["x"], a["M"], a["y"], a["ldy"], a["ws"], a["wsb"], None)
+
+    assert call(w=None) == 1
+    assert call(y=None) == 1
+    assert call(N=0) == 2
+    assert call(M=0) == 2
+    assert call(K=-1) == 2
+    assert call(ldy=64) == 2
+    assert call(w=FAKE + 8) == 3
+    assert call(ws=None) == 7
+    assert call(ws=FAKE + 16) == 7
+    assert call(wsb=100) == 7
+    assert lib.qgemm_q4_k_workspace_bytes(512, 14336, 4096) >= 512 * 4096 * 2
