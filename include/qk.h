@@ -119,6 +119,27 @@ int qgemm_q4_k(const void *w, int64_t row_offset, int64_t N, int64_t K, const fl
 size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
+ * qgemm_q4_k for callers that cannot allocate device memory -- for example a
+ * plugin inside an inference engine that owns every device allocation, or
+ * code that must not allocate once running -- and so cannot pass the
+ * workspace qgemm_q4_k needs.  The pages have no counterpart of this call;
+ * it exists for such callers only.
+ * Same operation, arguments and results as qgemm_q4_k, without the
+ * workspace: the scratch is a fixed array of QK_NOALLOC_SCRATCH_BYTES inside
+ * the library, held by every GPU that loads the library until the process
+ * exits.  No call allocates or frees memory.
+ *   Sizes: M * round_up(K, 8) * 2 + 256 must not exceed
+ *   QK_NOALLOC_SCRATCH_BYTES, else QK_ERR_TOO_LARGE (before any launch).
+ *   The first call on a device looks up the array's device address; make
+ *   it before any stream capture.
+ *   All calls share the array: calls that overlap on the GPU (for example on
+ *   two streams at once) race on it and give undefined results.
+ */
+#define QK_NOALLOC_SCRATCH_BYTES (8u << 20)
+int qgemm_q4_k_noalloc(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+                       float *y, int64_t ldy, qk_stream_t stream);
+
+/*
  * Bytes of one row of a tensor with K columns: ceil(K/32)*34 (Q8_0) or
  * ceil(K/256)*144 (Q4_K).
  */

@@ -66,6 +66,11 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
 
 }  // namespace
 
+namespace qk {
+int *library_error_word() { return error_word_ptr(); }
+uint64_t library_wait_limit_ns() { return g_wait_limit_ns.load(); }
+}  // namespace qk
+
 extern "C" {
 
 size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K)

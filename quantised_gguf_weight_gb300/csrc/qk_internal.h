@@ -23,6 +23,10 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
                         int *err, uint64_t wait_ns, int64_t skip_tile, bool pdl);
 
+// The device error word of the current device and the bound of device waits.
+int *library_error_word();
+uint64_t library_wait_limit_ns();
+
 int64_t gemm_k8(int64_t K);
 size_t gemm_workspace_bytes(int64_t M, int64_t K);
 cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,

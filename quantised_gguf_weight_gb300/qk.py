@@ -24,7 +24,7 @@ STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 
 MAX_BATCH = 8
 
 EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
-           "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
+           "qgemm_q4_k_noalloc", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
            "qk_version"]
 
