@@ -452,6 +452,31 @@ def measure_extra_rows(torch, qk, synth, device, stream):
                       "cache": "cold (rotated copies > L2)" if copies * rows * rb > l2 else "hot (L2-resident)"}
         del ws
 
+    def gemm_row(label, M, N, K, seed, copies):
+        ws = [torch.from_numpy(synth.weights("q4_k", N, K, seed=seed, stream0=50 * c)).to(device)
+              for c in range(copies)]
+        x = torch.from_numpy(synth.activations(M, K, seed=seed)).to(device)
+        y = torch.empty((M, N), device=device)
+        nbytes = qk.gemm_workspace_bytes(M, N, K)
+        wsp = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+        def mk(w):
+            def f(sh):
+                st = lib.qgemm_q4_k(w.data_ptr(), 0, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(),
+                                    nbytes, sh)
+                assert st == 0
+            return f
+        avg_ms = time_calls(torch, stream, [mk(w) for w in ws] * max(1, 4 // copies), 20)
+        flops = 2.0 * M * N * K
+        tflops = flops / (avg_ms * 1e-3) / 1e12
+        peak, src = peak_bf16(read_peaks())
+        out[label] = {"avg_us": round(avg_ms * 1e3, 2), "TFLOP/s": round(tflops, 1), "flops": flops,
+                      "bound": "tensor", "frac_of_bf16_peak": round(tflops / peak, 4), "peak_TFLOP/s": peak,
+                      "peak_source": f"{src} bf16 dense (burst)",
+                      "includes": "x->bf16 pre-pass + tcgen05 GEMM"}
+        del ws
+
+    gemm_row("q4_k_gemm_512x4096x14336", 512, 14336, 4096, 4, 2)
     gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1)
     gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1)
     gemv_row("q8_0_lm_head_151936x896_b1", "q8_0", 151936, 896, 1, 3, 3)
@@ -595,6 +620,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other GEMV configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--only-gemm", default=None, help="M:N:K -- time the Q4_K prefill GEMM only")
     ap.add_argument("--only", default=None, help="FMT:ROWS:K:BATCH -- time one GEMV call only")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -616,6 +642,24 @@ def main():
     qk.set_programmatic_launch(not args.no_pdl)
     if args.only:
         return run_only(args, torch, qk, synth, device)
+    if args.only_gemm:
+        M, N, K = (int(v) for v in args.only_gemm.split(":"))
+        wq = torch.from_numpy(synth.weights("q4_k", N, K, seed=4)).to(device)
+        x = torch.from_numpy(synth.activations(M, K, seed=4)).to(device)
+        y = torch.empty((M, N), device=device)
+        wsp = torch.empty(qk.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=device)
+        stream = torch.cuda.Stream(device=device)
+        for _ in range(args.warmup):
+            qk.qgemm_q4_k(wq, 0, N, K, x, y=y, ldy=N, workspace=wsp, stream=stream)
+        lib = qk.load()
+
+        def f(sh):
+            assert lib.qgemm_q4_k(wq.data_ptr(), 0, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(),
+                                  wsp.numel(), sh) == 0
+        ms = time_calls(torch, stream, [f] * 4, max(1, args.steps))
+        print(json.dumps({"only_gemm": args.only_gemm, "avg_us": round(ms * 1e3, 2),
+                          "TFLOP/s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}), flush=True)
+        return 0
     r = measure_ours(args, torch, qk, synth, device, rank, ws)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
