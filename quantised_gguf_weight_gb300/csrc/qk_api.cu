@@ -166,6 +166,19 @@ int qk_version(void) { return 100; }
 // its consumers' bounded wait runs out and the launch records QK_ERR_TIMEOUT.
 int64_t qk_debug_skip_tile(int64_t tile) { return g_skip_tile.exchange(tile); }
 
+// Test hook: the launch plan a GEMV call of this shape would use, as
+// {kind, SW, R, nkc, rows_w, stages, stage_bytes, smem, grid, XU, cpl, nw, m}; returns the
+// number of values written, or -1 if no plan fits.
+int qk_debug_gemv_plan(int fmt, int64_t rows, int64_t K, int batch, int64_t *out, int n)
+{
+    qk::GemvPlan p;
+    if (!out || !qk::gemv_plan(fmt, rows, K, batch, &p)) return -1;
+    const int64_t v[13] = {p.kind, p.SW, p.R, p.nkc, p.rows_w, p.stages, p.stage_bytes, p.smem, p.grid, p.XU, p.cpl, p.nw, p.m};
+    int k = 0;
+    for (; k < n && k < 13; ++k) out[k] = v[k];
+    return k;
+}
+
 // Test hook, not part of the public header: CTA 0 of every later GEMM launch
 // never loads the activations of K chunk `chunk` (-1 restores normal
 // operation), so the MMA issuer's bounded wait runs out (QK_ERR_TIMEOUT).

@@ -75,6 +75,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// A 32-bit counter in shared memory, published with release and read with
+// acquire semantics (CTA scope).
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Wait until the counter at `addr` exceeds `target` or the word at
+// `abort_addr` becomes nonzero, for at most limit_ns.  Returns true only in
+// the first case.
+__device__ __forceinline__ bool wait_counter_above(uint32_t addr, uint32_t target, uint32_t abort_addr,
+                                                   uint64_t limit_ns)
+{
+    if (ld_acquire_shared(addr) > target) return true;
+    const uint64_t deadline = globaltimer_ns() + limit_ns;
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_shared(addr) > target) return true;
+        if (ld_acquire_shared(abort_addr) != 0 || globaltimer_ns() > deadline) return false;
+    }
+}
+
 // ---------------------------------------------------------------- bulk copy
 
 // L2 policy: the weights are streamed once, so they are marked evict-first

@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "qk_gemv_kernel.cuh"
+#include "qk_gemv_ring.cuh"
 #include "qk_internal.h"
 
 namespace qk {
@@ -75,6 +75,7 @@ bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int SW, int64_t 
     int64_t stages = (budget - off_stage) / stage;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2 || stage > (1 << 20)) return false;
+    p->kind = 0;
     p->U = U;
     p->XU = XU;
     p->SW = SW;
@@ -115,6 +116,112 @@ int warp_team_width(int U, int min_units)
     return best;
 }
 
+// Ring-kernel plan: team width SW, lane units per lane per item (cpl), K
+// chunks and ring depth.  Among the powers of two SW, the one that keeps the
+// most lanes busy (lane units per row over chunks of SW*cpl units, times the
+// share of the consumer warps that get a row group at all); among equals the
+// one giving a lane more units per item, then the wider team (fewer copies
+// per item).  A row group split into K chunks is copied one
+// row at a time, so at most 8 rows per item are allowed then.
+bool ring_plan(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, GemvPlan *p)
+{
+    const int UC = fmt == kFmtQ4K ? 128 : 32;
+    const int UB = fmt == kFmtQ4K ? 144 : 34;
+    const int64_t row_bytes = fmt == kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
+    const int64_t U64 = (K + UC - 1) / UC;
+    if (U64 > (1 << 20)) return false;
+    const int U = static_cast<int>(U64);
+    const int LU = fmt == kFmtQ4K ? (U + 1) / 2 : U;
+    const int R = ring_rows(fmt, batch);
+    const int CM = ring_cpl_max(fmt, batch);
+    // activation unit stride: Q4_K stores half super-blocks h-major, so it
+    // needs an even stride of at least two slots per super-block
+    const int need = fmt == kFmtQ4K ? 2 * LU : U;
+    const int XU = need <= 32 ? 32 : (need <= 128 ? 128 : static_cast<int>(round_up(need, 2)));
+    const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
+    const int64_t xsum_bytes = fmt == kFmtQ4K ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128) : 0;
+    const int64_t xscale_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 4, 128) : 0;
+    const int64_t off_x = kRingBarBytes;
+    const int64_t off_xsum = off_x + x_bytes;
+    const int64_t off_xscale = off_xsum + xsum_bytes;
+    const int64_t off_stage = off_xscale + xscale_bytes;
+    const int64_t budget = di.smem_optin;
+    if (off_stage >= budget) return false;
+
+    int64_t grid = di.sms;
+    if (grid > rows) grid = rows;
+    const int64_t rows_per_cta = rows / grid;
+    const int NW = ring_warps(fmt, batch);
+    int best_sw = 0, best_nkc = 0, best_cpl = 0;
+    double best_util = -1.0;
+    for (int sw = 32; sw >= 1; sw >>= 1) {
+        const int cpl = std::min(CM, (LU + sw - 1) / sw);
+        const int nkc = (LU + sw * cpl - 1) / (sw * cpl);
+        const int rows_w = (32 / sw) * R;
+        if (nkc > 1 && rows_w > 8) continue;
+        // busy lanes, times the share of warps that get a row group
+        const double groups = static_cast<double>((rows_per_cta + rows_w - 1) / rows_w);
+        const double util = static_cast<double>(LU) / (static_cast<double>(nkc) * sw * cpl) *
+                            std::min(1.0, groups / NW);
+        if (util > best_util + 1e-9 || (util > best_util - 1e-9 && cpl > best_cpl)) {
+            best_util = util;
+            best_sw = sw;
+            best_nkc = nkc;
+            best_cpl = cpl;
+        }
+    }
+    if (best_sw == 0) return false;
+    const int SW = best_sw, nkc = best_nkc, cpl = best_cpl;
+    const int rows_w = (32 / SW) * R;
+    int64_t chunk_bytes = 0, row_stride = 0, stage;
+    if (nkc == 1) {
+        stage = round_up(rows_w * row_bytes + 32, 128);
+    } else {
+        chunk_bytes = static_cast<int64_t>(SW) * cpl * UB;
+        // a Q8_0 chunk is widened to 16-byte boundaries and its last block
+        // read as nine whole words
+        row_stride = fmt == kFmtQ4K ? chunk_bytes : round_up(chunk_bytes + 30, 16) + 16;
+        stage = round_up(rows_w * row_stride, 128);
+    }
+    if (stage > (1 << 20)) return false;
+    int64_t stages = (budget - off_stage) / stage;
+    if (stages > kRingMaxStages) stages = kRingMaxStages;
+    if (stages < 1) return false;
+    // consumer warps that get row groups, and stages per warp
+    const int64_t rows_cta_max = (rows + grid - 1) / grid;
+    int64_t nw = std::min<int64_t>(NW, (rows_cta_max + rows_w - 1) / rows_w);
+    nw = std::min(nw, stages);
+    const int64_t m = stages / nw;
+    stages = nw * m;
+    p->kind = 1;
+    p->U = U;
+    p->XU = XU;
+    p->SW = SW;
+    p->slots = 32 / SW;
+    p->NTC = 32 * ring_warps(fmt, batch);
+    p->R = R;
+    p->tile_rows = rows_w;
+    p->stages = static_cast<int>(stages);
+    p->stage_bytes = static_cast<int>(stage);
+    p->off_x = static_cast<int>(off_x);
+    p->off_xsum = static_cast<int>(off_xsum);
+    p->off_xscale = static_cast<int>(off_xscale);
+    p->off_red = 0;
+    p->off_stage = static_cast<int>(off_stage);
+    p->smem = static_cast<int>(off_stage + stages * stage);
+    p->grid = static_cast<int>(grid);
+    p->nw = static_cast<int>(nw);
+    p->m = static_cast<int>(m);
+    p->LU = LU;
+    p->cpl = cpl;
+    p->nkc = nkc;
+    p->rows_w = rows_w;
+    p->chunk_bytes = static_cast<int>(chunk_bytes);
+    p->row_stride = static_cast<int>(row_stride);
+    p->row_bytes = row_bytes;
+    return true;
+}
+
 }  // namespace
 
 // Launch plan of a GEMV call; returns false if it cannot fit in shared memory.
@@ -122,6 +229,7 @@ bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p)
 {
     const DevInfo di = dev_info();
     if (di.sms <= 0) return false;
+    if (ring_plan(fmt, rows, K, batch, di, p)) return true;
     const int UC = fmt == kFmtQ4K ? 128 : 32;
     const int64_t row_bytes = fmt == kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
     const int64_t U64 = (K + UC - 1) / UC;
@@ -157,6 +265,41 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
                         int *err, uint64_t wait_ns, int64_t skip_tile, bool pdl)
 {
+    if (p.kind == 1) {
+        RingArgs r;
+        r.w = w_rows;
+        r.x = x;
+        r.y = y;
+        r.rows = rows;
+        r.K = K;
+        r.ldy = ldy;
+        r.row_bytes = p.row_bytes;
+        r.U = p.U;
+        r.LU = p.LU;
+        r.XU = p.XU;
+        r.SW = p.SW;
+        r.lsw = 0;
+        while ((1 << r.lsw) < p.SW) ++r.lsw;
+        r.cpl = p.cpl;
+        r.nkc = p.nkc;
+        r.rows_w = p.rows_w;
+        r.chunk_bytes = p.chunk_bytes;
+        r.row_stride = p.row_stride;
+        r.nw = p.nw;
+        r.m = p.m;
+        r.stage_bytes = p.stage_bytes;
+        r.off_x = p.off_x;
+        r.off_xsum = p.off_xsum;
+        r.off_xscale = p.off_xscale;
+        r.off_stage = p.off_stage;
+        r.skip_item = skip_tile;
+        r.wait_ns = wait_ns;
+        r.err = err;
+        if (p.R != ring_rows(fmt, batch)) return cudaErrorInvalidValue;
+        const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
+        if (fmt == kFmtQ4K) return gemv_ring_launch_q4k(batch, us, r, p.grid, p.smem, st, pdl);
+        return gemv_ring_launch_q80(batch, us, r, p.grid, p.smem, st, pdl);
+    }
     GemvArgs a;
     a.w = w_rows;
     a.x = x;

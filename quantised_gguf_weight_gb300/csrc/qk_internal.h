@@ -12,9 +12,14 @@ constexpr int kMaxConsumers = 512;   // consumer threads per GEMV CTA
 constexpr int kMaxStages = 8;        // shared-memory ring depth
 
 // Launch plan of one GEMV call (shared-memory layout, grid, team shape).
+// kind 0: the tile kernel (qk_gemv_kernel.cuh); kind 1: the ring kernel
+// (qk_gemv_ring.cuh), which also uses LU, cpl, nkc, rows_w, chunk_bytes,
+// row_stride, nw, m.
 struct GemvPlan {
+    int kind;
     int U, XU, SW, slots, NTC, R, tile_rows, stages, stage_bytes;
     int off_x, off_xsum, off_xscale, off_red, off_stage, smem, grid;
+    int LU, cpl, nkc, rows_w, chunk_bytes, row_stride, nw, m;
     int64_t row_bytes;
 };
 

@@ -75,6 +75,8 @@ def load(path: str | None = None):
         lib.qk_set_programmatic_launch.restype = I
         lib.qk_debug_skip_tile.argtypes = [I64]
         lib.qk_debug_skip_tile.restype = I64
+        lib.qk_debug_gemv_plan.argtypes = [I, I64, I64, I, ctypes.POINTER(ctypes.c_int64), I]
+        lib.qk_debug_gemv_plan.restype = I
         _lib = lib
         return lib
 
@@ -167,5 +169,17 @@ def set_programmatic_launch(enable: bool) -> bool:
 
 
 def debug_skip_tile(tile: int) -> int:
-    """Test hook: CTA 0 of later GEMV launches skips copying tile `tile` (-1: off)."""
+    """Test hook: CTA 0 of later GEMV launches skips copying tile (ring item) `tile` (-1: off)."""
     return int(load().qk_debug_skip_tile(int(tile)))
+
+
+PLAN_FIELDS = ("kind", "SW", "R", "nkc", "rows_w", "stages", "stage_bytes", "smem", "grid", "XU", "cpl", "nw", "m")
+
+
+def debug_gemv_plan(fmt: str, rows: int, K: int, batch: int) -> dict:
+    """Test hook: the launch plan a GEMV call of this shape uses (needs a GPU)."""
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    n = load().qk_debug_gemv_plan({"q8_0": 0, "q4_k": 1}[fmt], int(rows), int(K), int(batch), out, len(PLAN_FIELDS))
+    if n < 0:
+        raise QKError(8, "no GEMV plan fits")
+    return dict(zip(PLAN_FIELDS, list(out)[:n]))
