@@ -314,7 +314,7 @@ def measure_ours(args, torch, qk, synth, device, rank, world):
     traffic = read_traffic("gemv_q4_k_b1", avg_launch_bytes=tot_b / launches_per_layer())
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic,
-                "kernel": "gemv_kernel<Q4_K, batch 1>: the six launches of a layer, each timed as "
+                "kernel": "gemv_kernel<Q4_K, batch 1>: the four launches of a layer, each timed as "
                           "back-to-back graph replays",
                 "peak_source": f"{hbm_src} HBM copy bandwidth",
                 "frac_of_8TBs_nominal": round(achieved / 8000.0, 4),

@@ -18,7 +18,7 @@ namespace {
 __device__ int g_qk_error_word;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
-std::atomic<int64_t> g_skip_tile{-1};
+std::atomic<int64_t> g_skip_item{-1};
 std::atomic<int> g_programmatic{0};
 std::atomic<int> g_gemm_skip_chunk{-1};
 
@@ -60,7 +60,7 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * plan.row_bytes;
     cudaError_t e = qk::gemv_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
                                     reinterpret_cast<cudaStream_t>(stream), plan, err,
-                                    g_wait_limit_ns.load(), g_skip_tile.load(), g_programmatic.load() != 0);
+                                    g_wait_limit_ns.load(), g_skip_item.load(), g_programmatic.load() != 0);
     return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
 }
 
@@ -161,21 +161,22 @@ int qk_set_programmatic_launch(int enable) { return g_programmatic.exchange(enab
 
 int qk_version(void) { return 100; }
 
-// Test hook, not part of the public header: CTA 0 of every later GEMV launch
-// skips the bulk copy of its tile `tile` (-1 restores normal operation), so
-// its consumers' bounded wait runs out and the launch records QK_ERR_TIMEOUT.
-int64_t qk_debug_skip_tile(int64_t tile) { return g_skip_tile.exchange(tile); }
+// Test hook, not part of the public header: in CTA 0 of every later GEMV
+// launch, consumer warp 0's item number `item` is never copied (-1 restores
+// normal operation), so that warp's bounded wait runs out and the launch
+// records QK_ERR_TIMEOUT.
+int64_t qk_debug_skip_item(int64_t item) { return g_skip_item.exchange(item); }
 
 // Test hook: the launch plan a GEMV call of this shape would use, as
-// {kind, SW, R, nkc, rows_w, stages, stage_bytes, smem, grid, XU, cpl, nw, m}; returns the
+// {SW, R, nkc, rows_w, stages, stage_bytes, smem, grid, XU, cpl, nw, m}; returns the
 // number of values written, or -1 if no plan fits.
 int qk_debug_gemv_plan(int fmt, int64_t rows, int64_t K, int batch, int64_t *out, int n)
 {
     qk::GemvPlan p;
     if (!out || !qk::gemv_plan(fmt, rows, K, batch, &p)) return -1;
-    const int64_t v[13] = {p.kind, p.SW, p.R, p.nkc, p.rows_w, p.stages, p.stage_bytes, p.smem, p.grid, p.XU, p.cpl, p.nw, p.m};
+    const int64_t v[12] = {p.SW, p.R, p.nkc, p.rows_w, p.stages, p.stage_bytes, p.smem, p.grid, p.XU, p.cpl, p.nw, p.m};
     int k = 0;
-    for (; k < n && k < 13; ++k) out[k] = v[k];
+    for (; k < n && k < 12; ++k) out[k] = v[k];
     return k;
 }
 

@@ -75,35 +75,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
-// A 32-bit counter in shared memory, published with release and read with
-// acquire semantics (CTA scope).
-__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-// Wait until the counter at `addr` exceeds `target` or the word at
-// `abort_addr` becomes nonzero, for at most limit_ns.  Returns true only in
-// the first case.
-__device__ __forceinline__ bool wait_counter_above(uint32_t addr, uint32_t target, uint32_t abort_addr,
-                                                   uint64_t limit_ns)
-{
-    if (ld_acquire_shared(addr) > target) return true;
-    const uint64_t deadline = globaltimer_ns() + limit_ns;
-    for (;;) {
-        __nanosleep(64);
-        if (ld_acquire_shared(addr) > target) return true;
-        if (ld_acquire_shared(abort_addr) != 0 || globaltimer_ns() > deadline) return false;
-    }
-}
-
 // ---------------------------------------------------------------- bulk copy
 
 // L2 policy: the weights are streamed once, so they are marked evict-first
@@ -128,43 +99,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-// ---------------------------------------------------------------- cp.async (LDGSTS)
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- named barriers
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Barrier among `nthreads` threads that also ORs a per-thread predicate.
-__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred)
-{
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(out)
-        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-        : "memory");
-    return out != 0;
 }
 
 // ---------------------------------------------------------------- numerics helpers
@@ -223,12 +162,6 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     return r;
 }
 
-// 16-byte shared-memory load as two 64-bit pairs.
-__device__ __forceinline__ void lds128(uint32_t addr, uint64_t &a, uint64_t &b)
-{
-    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
-}
-
 // ---------------------------------------------------------------- 4-way byte dot products
 // d = c + sum_{i<4} a.byte[i] * b.byte[i]; U/S = unsigned/signed bytes of a, b.
 __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c)
@@ -254,14 +187,6 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
     int d;
     asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
-}
-
-// 16-byte shared-memory load as four 32-bit words.
-__device__ __forceinline__ uint4 lds128u(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
 }
 
 __device__ __forceinline__ void record_error(int *err, int bit)

@@ -1,10 +1,11 @@
 // qk_gemv.cu -- launch planning and dispatch of the GEMV kernel
-// (qk_gemv_kernel.cuh): team shape, tile size, shared-memory layout, grid.
+// (qk_gemv_kernel.cuh): team shape, K chunks, stage ring, shared-memory
+// layout, grid.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "qk_gemv_ring.cuh"
+#include "qk_gemv_kernel.cuh"
 #include "qk_internal.h"
 
 namespace qk {
@@ -34,88 +35,6 @@ DevInfo dev_info()
 
 int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
 
-// Layout for a given activation unit stride XU and team width SW; false if
-// it cannot fit.
-bool plan_with(int fmt, int64_t rows, int batch, int U, int XU, int SW, int64_t row_bytes, const DevInfo &di,
-               GemvPlan *p)
-{
-    const int UC = fmt == kFmtQ4K ? 128 : 32;
-    const int max_c = max_consumers(fmt, batch);
-    const int R = rows_per_thread(fmt, batch);
-    int64_t grid = di.sms;
-    if (grid > rows) grid = rows;
-    const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
-    const int64_t xsum_bytes = fmt == kFmtQ4K ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128) : 0;
-    // batch 1 keeps a block-floating-point scale per 32-column group
-    const int64_t xscale_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 4, 128) : 0;
-    const int64_t off_x = 256;
-    const int64_t off_xsum = off_x + x_bytes;
-    const int64_t off_xscale = off_xsum + xsum_bytes;
-    const int64_t off_red = off_xscale + xscale_bytes;
-    const int64_t budget = di.smem_optin;
-    const bool warp_team = SW <= 32 && (32 % SW) == 0;
-    // teams: no more than the threads allow, than the CTA has rows for, and
-    // than fit with two stages next to the activations and the partials
-    const int64_t rows_per_cta = (rows + grid - 1) / grid;
-    int64_t slots = max_c / SW;
-    slots = std::min<int64_t>(slots, (rows_per_cta + R - 1) / R);
-    for (; slots >= 1; --slots) {
-        const int64_t red_bytes = warp_team ? 0 : round_up(2 * slots * R * batch * SW * 4, 128);
-        const int64_t stage = round_up(slots * R * row_bytes + 32, 128);
-        if (off_red + red_bytes + 2 * stage <= budget) break;
-    }
-    if (slots < 1) return false;
-    if (warp_team && SW < 32) {
-        const int g = 32 / SW;                 // whole warps of consumers
-        slots = std::max<int64_t>(g, (slots / g) * g);
-    }
-    const int64_t red_bytes = warp_team ? 0 : round_up(2 * slots * R * batch * SW * 4, 128);
-    const int64_t off_stage = off_red + red_bytes;
-    const int64_t stage = round_up(slots * R * row_bytes + 32, 128);
-    int64_t stages = (budget - off_stage) / stage;
-    if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2 || stage > (1 << 20)) return false;
-    p->kind = 0;
-    p->U = U;
-    p->XU = XU;
-    p->SW = SW;
-    p->slots = static_cast<int>(slots);
-    p->NTC = static_cast<int>(round_up(slots * SW, 32));
-    p->R = R;
-    p->tile_rows = static_cast<int>(slots * R);
-    p->stages = static_cast<int>(stages);
-    p->stage_bytes = static_cast<int>(stage);
-    p->off_x = static_cast<int>(off_x);
-    p->off_xsum = static_cast<int>(off_xsum);
-    p->off_xscale = static_cast<int>(off_xscale);
-    p->off_red = static_cast<int>(off_red);
-    p->off_stage = static_cast<int>(off_stage);
-    p->smem = static_cast<int>(off_stage + stages * stage);
-    p->row_bytes = row_bytes;
-    p->grid = static_cast<int>(grid);
-    return true;
-}
-
-// Row-team width for warp-sized teams: a power of two up to 32 that gives
-// each lane at least `min_units` units where the row has them, with the
-// units spread evenly (the busiest lane at most 15% above the average).
-int warp_team_width(int U, int min_units)
-{
-    int best = 1;
-    double best_cost = 1e30;
-    for (int sw = 32; sw >= 1; sw >>= 1) {
-        if (sw > 1 && U / sw < min_units) continue;
-        const int per = (U + sw - 1) / sw;
-        const double cost = static_cast<double>(per) * sw / U;   // >= 1: load imbalance
-        if (cost <= 1.15) return sw;
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = sw;
-        }
-    }
-    return best;
-}
-
 // Ring-kernel plan: team width SW, lane units per lane per item (cpl), K
 // chunks and ring depth.  Among the powers of two SW, the one that keeps the
 // most lanes busy (lane units per row over chunks of SW*cpl units, times the
@@ -123,7 +42,7 @@ int warp_team_width(int U, int min_units)
 // one giving a lane more units per item, then the wider team (fewer copies
 // per item).  A row group split into K chunks is copied one
 // row at a time, so at most 8 rows per item are allowed then.
-bool ring_plan(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, GemvPlan *p)
+bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, GemvPlan *p)
 {
     const int UC = fmt == kFmtQ4K ? 128 : 32;
     const int UB = fmt == kFmtQ4K ? 144 : 34;
@@ -132,8 +51,8 @@ bool ring_plan(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, G
     if (U64 > (1 << 20)) return false;
     const int U = static_cast<int>(U64);
     const int LU = fmt == kFmtQ4K ? (U + 1) / 2 : U;
-    const int R = ring_rows(fmt, batch);
-    const int CM = ring_cpl_max(fmt, batch);
+    const int R = gemv_rows(fmt, batch);
+    const int CM = gemv_cpl_max(fmt, batch);
     // activation unit stride: Q4_K stores half super-blocks h-major, so it
     // needs an even stride of at least two slots per super-block
     const int need = fmt == kFmtQ4K ? 2 * LU : U;
@@ -141,7 +60,7 @@ bool ring_plan(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, G
     const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
     const int64_t xsum_bytes = fmt == kFmtQ4K ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128) : 0;
     const int64_t xscale_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 4, 128) : 0;
-    const int64_t off_x = kRingBarBytes;
+    const int64_t off_x = kGemvBarBytes;
     const int64_t off_xsum = off_x + x_bytes;
     const int64_t off_xscale = off_xsum + xsum_bytes;
     const int64_t off_stage = off_xscale + xscale_bytes;
@@ -151,7 +70,7 @@ bool ring_plan(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, G
     int64_t grid = di.sms;
     if (grid > rows) grid = rows;
     const int64_t rows_per_cta = rows / grid;
-    const int NW = ring_warps(fmt, batch);
+    const int NW = gemv_warps(fmt, batch);
     int best_sw = 0, best_nkc = 0, best_cpl = 0;
     double best_util = -1.0;
     for (int sw = 32; sw >= 1; sw >>= 1) {
@@ -185,28 +104,26 @@ bool ring_plan(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, G
     }
     if (stage > (1 << 20)) return false;
     int64_t stages = (budget - off_stage) / stage;
-    if (stages > kRingMaxStages) stages = kRingMaxStages;
+    if (stages > kGemvMaxStages) stages = kGemvMaxStages;
     if (stages < 1) return false;
-    // consumer warps that get row groups, and stages per warp
+    // consumer warps that get row groups, and stages per warp: two or more
+    // stages a warp where the ring holds that many (a warp then has an item
+    // in flight while it works on another), else one
     const int64_t rows_cta_max = (rows + grid - 1) / grid;
     int64_t nw = std::min<int64_t>(NW, (rows_cta_max + rows_w - 1) / rows_w);
     nw = std::min(nw, stages);
+    if (stages / nw < 2 && stages >= 2 * std::min<int64_t>(nw, 8)) nw = std::min<int64_t>(nw, stages / 2);
     const int64_t m = stages / nw;
     stages = nw * m;
-    p->kind = 1;
     p->U = U;
     p->XU = XU;
     p->SW = SW;
-    p->slots = 32 / SW;
-    p->NTC = 32 * ring_warps(fmt, batch);
     p->R = R;
-    p->tile_rows = rows_w;
     p->stages = static_cast<int>(stages);
     p->stage_bytes = static_cast<int>(stage);
     p->off_x = static_cast<int>(off_x);
     p->off_xsum = static_cast<int>(off_xsum);
     p->off_xscale = static_cast<int>(off_xscale);
-    p->off_red = 0;
     p->off_stage = static_cast<int>(off_stage);
     p->smem = static_cast<int>(off_stage + stages * stage);
     p->grid = static_cast<int>(grid);
@@ -229,105 +146,46 @@ bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p)
 {
     const DevInfo di = dev_info();
     if (di.sms <= 0) return false;
-    if (ring_plan(fmt, rows, K, batch, di, p)) return true;
-    const int UC = fmt == kFmtQ4K ? 128 : 32;
-    const int64_t row_bytes = fmt == kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
-    const int64_t U64 = (K + UC - 1) / UC;
-    if (U64 > (1 << 20)) return false;
-    const int U = static_cast<int>(U64);
-    // team width: warp-sized teams (shuffle reduction, no barrier) unless
-    // they would leave fewer than 256 consumers, then one team of U threads
-    // per row with the shared-memory reduction
-    const int min_units = fmt == kFmtQ80 ? 4 : 1;
-    const int sw_warp = warp_team_width(U, min_units);
-    const int XU_c = U <= 32 ? 32 : (U <= 128 ? 128 : U);   // compile-time strides where they fit
-    GemvPlan a_plan, b_plan;
-    bool a_ok = plan_with(fmt, rows, batch, U, XU_c, sw_warp, row_bytes, di, &a_plan);
-    if (!a_ok && XU_c != U) a_ok = plan_with(fmt, rows, batch, U, U, sw_warp, row_bytes, di, &a_plan);
-    const int max_c = max_consumers(fmt, batch);
-    bool b_ok = false;
-    if (U > 32 && U <= max_c && (!a_ok || a_plan.NTC < 256)) {
-        b_ok = plan_with(fmt, rows, batch, U, XU_c, U, row_bytes, di, &b_plan);
-        if (!b_ok && XU_c != U) b_ok = plan_with(fmt, rows, batch, U, U, U, row_bytes, di, &b_plan);
-    }
-    if (b_ok && (!a_ok || b_plan.NTC > a_plan.NTC)) {
-        *p = b_plan;
-        return true;
-    }
-    if (a_ok) {
-        *p = a_plan;
-        return true;
-    }
-    return false;
+    return gemv_plan_for(fmt, rows, K, batch, di, p);
 }
 
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_tile, bool pdl)
+                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl)
 {
-    if (p.kind == 1) {
-        RingArgs r;
-        r.w = w_rows;
-        r.x = x;
-        r.y = y;
-        r.rows = rows;
-        r.K = K;
-        r.ldy = ldy;
-        r.row_bytes = p.row_bytes;
-        r.U = p.U;
-        r.LU = p.LU;
-        r.XU = p.XU;
-        r.SW = p.SW;
-        r.lsw = 0;
-        while ((1 << r.lsw) < p.SW) ++r.lsw;
-        r.cpl = p.cpl;
-        r.nkc = p.nkc;
-        r.rows_w = p.rows_w;
-        r.chunk_bytes = p.chunk_bytes;
-        r.row_stride = p.row_stride;
-        r.nw = p.nw;
-        r.m = p.m;
-        r.stage_bytes = p.stage_bytes;
-        r.off_x = p.off_x;
-        r.off_xsum = p.off_xsum;
-        r.off_xscale = p.off_xscale;
-        r.off_stage = p.off_stage;
-        r.skip_item = skip_tile;
-        r.wait_ns = wait_ns;
-        r.err = err;
-        if (p.R != ring_rows(fmt, batch)) return cudaErrorInvalidValue;
-        const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
-        if (fmt == kFmtQ4K) return gemv_ring_launch_q4k(batch, us, r, p.grid, p.smem, st, pdl);
-        return gemv_ring_launch_q80(batch, us, r, p.grid, p.smem, st, pdl);
-    }
-    GemvArgs a;
-    a.w = w_rows;
-    a.x = x;
-    a.y = y;
-    a.rows = rows;
-    a.K = K;
-    a.ldy = ldy;
-    a.row_bytes = p.row_bytes;
-    a.U = p.U;
-    a.XU = p.XU;
-    a.SW = p.SW;
-    a.slots = p.slots;
-    a.NTC = p.NTC;
-    a.tile_rows = p.tile_rows;
-    a.stages = p.stages;
-    a.stage_bytes = p.stage_bytes;
-    a.off_x = p.off_x;
-    a.off_xsum = p.off_xsum;
-    a.off_xscale = p.off_xscale;
-    a.off_red = p.off_red;
-    a.off_stage = p.off_stage;
-    a.skip_tile = skip_tile;
-    a.wait_ns = wait_ns;
-    a.err = err;
-    if (p.R != rows_per_thread(fmt, batch)) return cudaErrorInvalidValue;
+    if (p.R != gemv_rows(fmt, batch)) return cudaErrorInvalidValue;
+    GemvArgs r;
+    r.w = w_rows;
+    r.x = x;
+    r.y = y;
+    r.rows = rows;
+    r.K = K;
+    r.ldy = ldy;
+    r.row_bytes = p.row_bytes;
+    r.U = p.U;
+    r.LU = p.LU;
+    r.XU = p.XU;
+    r.SW = p.SW;
+    r.lsw = 0;
+    while ((1 << r.lsw) < p.SW) ++r.lsw;
+    r.cpl = p.cpl;
+    r.nkc = p.nkc;
+    r.rows_w = p.rows_w;
+    r.chunk_bytes = p.chunk_bytes;
+    r.row_stride = p.row_stride;
+    r.nw = p.nw;
+    r.m = p.m;
+    r.stage_bytes = p.stage_bytes;
+    r.off_x = p.off_x;
+    r.off_xsum = p.off_xsum;
+    r.off_xscale = p.off_xscale;
+    r.off_stage = p.off_stage;
+    r.skip_item = skip_item;
+    r.wait_ns = wait_ns;
+    r.err = err;
     const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
-    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, a, p.grid, p.smem, st, pdl);
-    return gemv_launch_q80(batch, us, a, p.grid, p.smem, st, pdl);
+    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, r, p.grid, p.smem, st, pdl);
+    return gemv_launch_q80(batch, us, r, p.grid, p.smem, st, pdl);
 }
 
 }  // namespace qk

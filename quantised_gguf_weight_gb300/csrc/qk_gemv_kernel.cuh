@@ -1,43 +1,37 @@
-// qk_gemv_kernel.cuh -- the fused dequantise-and-multiply GEMV kernel for
-// GGUF Q8_0 / Q4_K weights against fp32 activations, batch 1..8 (sm_103a).
+// qk_gemv_kernel.cuh -- the GEMV kernel (sm_103a):
+// fused dequantise-and-multiply of GGUF Q8_0 / Q4_K rows against fp32
+// activations, y[b][r] = sum_c W[r][c] x[b][c], batch 1..8.
 //
 // The operation is the quantised matvec of "nurllama 0.18.1 API reference",
-// kernels.nu (`lk_matvec_q`, the batched `mv_*_b` forms): every block is
-// decoded inside the dot product, y[b][r] = sum_c W[r][c] x[b][c].
-//
-// Design (one GPU, memory-bound):
-//  * Persistent grid, one CTA per SM.  CTA i owns the contiguous row range
-//    [rows*i/G, rows*(i+1)/G), i.e. one contiguous byte span of the tensor.
-//  * Warp 0 is the producer: one lane streams tiles of whole rows into a ring
-//    of shared-memory stages with 1-D bulk copies (cp.async.bulk, completion
-//    on an mbarrier, L2 evict-first).  A tile's byte span is widened to
-//    16-byte boundaries (Q8_0 rows are 34*nb bytes, not 16-byte multiples);
-//    a 16-byte granule that holds a byte of the tensor never crosses a page,
-//    so the widened copy stays inside mapped memory.
-//  * The other warps are consumers.  A row is cut into units -- 128 weights
-//    of Q4_K (half a super-block: four 32-weight sub-blocks) or one 32-weight
-//    Q8_0 block -- and a team of SW = units-per-row threads covers one row
-//    (the "one warp per output row, the lanes split each block" shape of the
-//    nurllama README, "What it runs", generalised to teams of any width).
-//    Each thread handles its unit for R rows at once, so each activation
-//    value read from shared memory serves R rows.
-//  * Activations live in shared memory as float4 groups: group g of unit u
-//    of batch row b at float4 index (b*G + g)*XU + u, so threads holding
-//    consecutive units read consecutive 16-byte words.  XU (the unit stride)
-//    is a compile-time constant US where the kernel is specialised for it,
-//    which turns every activation load into a fixed-offset shared load.
-//  * Q4_K decoding: a 4-bit field at bit position s of a 32-bit word becomes
-//    the exact float 2^23 + q*2^s with one LOP3 (mask | 0x4B000000), and
-//    subtracting 2^23 leaves q*2^s exactly.  The activations in shared memory
-//    are pre-multiplied by 2^-s for the position their column's nibble has,
-//    so (q*2^s)*(x*2^-s) = q*x exactly.  Per 32-weight sub-block j the row
-//    contributes d*sc_j * sum(q*x) - dmin*m_j * sum(x) (the identical
-//    factorisation of w = d*sc*q - dmin*m); the sub-block sums of x are
-//    computed once per CTA.  Int8 Q8_0 quants use the same trick on bytes
-//    (bias 128) and contribute d * sum(q*x) per block.  Pairs of weights go
-//    through packed f32x2 FADD/FFMA.
-//  * Each thread's partial sums go to shared memory; after one named barrier
-//    per tile the partials of a row are summed by a warp and written to y.
+// kernels.nu (`lk_matvec_q`, the batched `mv_*_b` forms).  Shape of the
+// kernel:
+//  * Persistent grid, one CTA per SM, CTA i owning the contiguous row range
+//    [rows*i/G, rows*(i+1)/G).
+//  * The rows of a CTA are cut into row groups of rows_w = (32/SW)*R rows and
+//    each row into nkc K-chunks of SW*cpl lane units (a lane unit is one Q4_K
+//    super-block of 256 weights or one 32-weight Q8_0 block).  An item is one
+//    row group x one K-chunk.
+//  * Consumer warp w owns row groups w, w+nw, ... and m shared-memory stages
+//    of its own; its t-th item goes to stage w*m + t%m.  Lane w of warp 0 is
+//    its producer: it streams the warp's items into its stages with 1-D bulk
+//    copies (one per item when the row group is a single chunk -- its rows
+//    are contiguous -- else one per row), completion on the stage's "full"
+//    mbarrier.  Every stage is filled and drained in order by one producer
+//    lane and one warp, so its phase parity is never ambiguous, and the
+//    warps' pipelines do not wait on one another.
+//  * For each item a lane copies its lane units of its team's R rows from
+//    shared memory into registers, the warp hands the stage back at once
+//    (its "empty" mbarrier) and the arithmetic runs from registers, so the
+//    stages stay in flight.  Partial sums stay in registers across the chunks
+//    of a row group and are summed over the SW lanes of a team with shuffles.
+//  * Activations are staged once per CTA in shared memory, in the layout of
+//    the unit functions: batch 1 as block floating point byte planes (four
+//    byte dot products per weight group), batch >= 2 as fp32 (packed f32x2
+//    arithmetic).  Q4_K half super-blocks are stored h-major (unit slot
+//    h*XH + super-block), so lanes holding consecutive super-blocks read
+//    consecutive 16-byte words.
+// Every wait is bounded; a wait that runs out records QK_ERR_TIMEOUT in the
+// device error word and the kernel leaves without touching the rest of y.
 #pragma once
 
 #include <cstdint>
@@ -51,44 +45,10 @@ namespace qk {
 constexpr uint32_t kMagic = 0x4B000000u;   // 2^23 as an fp32 bit pattern
 constexpr float kTwo23 = 8388608.0f;
 
-struct GemvArgs {
-    const uint8_t *w;   // first byte of row 0 of this call's row range
-    const float *x;     // [B][K], row stride K
-    float *y;           // [B][ldy]
-    int64_t rows, K, ldy, row_bytes;
-    int U;              // units per row
-    int XU;             // unit stride of the shared-memory activation layout (>= U)
-    int SW;             // threads per row team
-    int slots;          // row teams per CTA
-    int NTC;            // consumer threads (multiple of 32, >= slots * SW)
-    int tile_rows;      // rows per stage = slots * R
-    int stages;
-    int stage_bytes;
-    int off_x, off_xsum, off_xscale, off_red, off_stage;   // shared-memory byte offsets
-    int64_t skip_tile;  // test hook: CTA 0 never copies this tile (-1: none)
-    uint64_t wait_ns;
-    int *err;
-};
-
-// Consumer threads per CTA, at most: 512 for batch 1, 256 otherwise (the
-// register budget of a thread).
-__host__ __device__ constexpr int max_consumers(int /*fmt*/, int batch)
-{
-    return batch <= 1 ? kMaxConsumers : kMaxConsumers / 2;
-}
-
-// Rows each thread handles at once.
-__host__ __device__ constexpr int rows_per_thread(int fmt, int batch)
-{
-    return fmt == kFmtQ4K ? (batch <= 4 ? 2 : 1) : (batch <= 2 ? 4 : 2);
-}
-
-// -------------------------------------------------------------------------- Q4_K unit
-
 // Bit position of the nibble that carries local column c (0..127) of a
-// 128-weight unit inside its 32-bit qs word, after the (word >> 12) used for
-// the upper nibbles.  Low nibbles (first 32 columns of a 64-column chunk) sit
-// at 0, 8, 16 and 12; high nibbles at 4, 12, 8 and 16.
+// 128-weight half super-block inside its 32-bit qs word, after the
+// (word >> 12) used for the upper nibbles.  Low nibbles (first 32 columns of
+// a 64-column chunk) sit at 0, 8, 16 and 12; high nibbles at 4, 12, 8 and 16.
 __device__ __forceinline__ int q4k_nibble_shift(int c)
 {
     const int e = c & 3;
@@ -98,129 +58,324 @@ __device__ __forceinline__ int q4k_nibble_shift(int c)
     return hi ? hi_s : lo_s;
 }
 
-// One 128-weight unit (half h of super-block blk) for R rows; adds each
-// row's contribution to acc[r][b].  xa: shared address of float4 group 0 of
-// unit u (batch row 0); gs: byte stride between groups (16*XU).
-template <int B, int R, int US>
-__device__ __forceinline__ void q4k_unit(const uint8_t *const (&rowp)[R], int u, uint32_t xa, uint32_t gs_rt,
-                                         const float *__restrict__ xsum_u, int xsum_stride,
-                                         float (&acc)[R][B])
+// Batch 1 holds the activations as block floating point: each 32-column
+// group has one exponent E and every value becomes the 32-bit integer
+// m = rint(x * 2^(30-E)) (|m| < 2^31), stored as four byte planes (plane 3
+// signed, planes 0..2 unsigned).  A weight group then costs one 4-way byte
+// dot product per plane, sum_i q_i m_i is assembled in integers per plane and
+// the group scale 2^(E-30) turns it back into a float.  Values within 2^7 of
+// their group's largest magnitude are represented exactly; the error of any
+// other value is below 2^-31 of that magnitude.
+
+// sum(q*m) of one group from its four plane sums, as a float.
+__device__ __forceinline__ float planes_to_float(int s0, int s1, int s2, int s3)
+{
+    const int hi = s3 * 256 + s2;     // exact in int32 for 32-weight groups
+    const int lo = s1 * 256 + s0;
+    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
+}
+
+constexpr int kGemvMaxStages = 32;
+constexpr int kGemvBarBytes = 768;   // full[32] at 0, empty[32] at 256, abort flag at 512, issued_use[32] at 528
+
+struct GemvArgs {
+    const uint8_t *w;   // first byte of row 0 of this call's row range
+    const float *x;     // [B][K], row stride K
+    float *y;           // [B][ldy]
+    int64_t rows, K, ldy, row_bytes;
+    int U;              // activation units per row (Q4_K: 128-column halves, Q8_0: blocks)
+    int LU;             // lane units per row (Q4_K: super-blocks, Q8_0: blocks)
+    int XU;             // unit stride of the shared-memory activation layout
+    int SW;             // lanes per row team (power of two, <= 32)
+    int lsw;            // log2(SW)
+    int cpl;            // lane units per lane per item
+    int nkc;            // K chunks per row group (chunk = SW * cpl lane units)
+    int rows_w;         // rows per item = (32/SW) * R
+    int chunk_bytes;    // bytes of one row's full chunk (nkc > 1)
+    int row_stride;     // bytes between rows of a stage (nkc > 1)
+    int nw;             // consumer warps that get row groups (<= the launched ones)
+    int m;              // stages per consumer warp (stage w*m + t%m holds warp w's item t)
+    int stage_bytes;
+    int off_x, off_xsum, off_xscale, off_stage;
+    int64_t skip_item;  // test hook: in CTA 0 warp 0's item with this number is never copied (-1: none)
+    uint64_t wait_ns;
+    int *err;
+};
+
+// Consumer warps per CTA and rows per thread of the ring kernel.
+// (B = 1: 12 warps in all, three per scheduler, which leaves 168 registers a
+// thread; B >= 2: 9 warps.)
+__host__ __device__ constexpr int gemv_warps(int /*fmt*/, int batch) { return batch == 1 ? 11 : 8; }
+__host__ __device__ constexpr int gemv_rows(int fmt, int batch)
+{
+    return fmt == kFmtQ4K ? (batch <= 4 ? 2 : 1) : (batch == 1 ? 2 : (batch == 2 ? 4 : 2));
+}
+// Lane units a lane may hold in registers per item (Q4_K: one super-block of
+// R rows; Q8_0: up to 72 words of blocks).
+__host__ __device__ constexpr int gemv_cpl_max(int fmt, int batch)
+{
+    return fmt == kFmtQ4K ? 1 : (batch == 1 ? 4 : (batch <= 4 ? 2 : 1));
+}
+
+// -------------------------------------------------------------------------- Q4_K, batch 1
+//
+// One super-block of R rows from registers: hd = bytes 0..15 (d, dmin,
+// scales[12]), qs = bytes 16..143.  x: block-floating-point byte planes of
+// the two 128-column halves at xa[h]; per 32-column group j of half h the
+// plain sum is xsum_h[j*XU] and the plane scale 2^(E-30) is xsc_h[j*XU].
+// The high nibbles are used in place (byte & 0xF0 = 16 q), which is folded
+// into their sub-block scale as d/16 (exact: a power of two).
+template <int R, int US>
+__device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
+                                             const uint8_t *xa0, const uint8_t *xa1, uint32_t gs_rt, const float *xsum0,
+                                             const float *xsum1, const float *xsc0, const float *xsc1,
+                                             int xstride, float (&acc)[R][1])
 {
     const uint32_t gs = US ? 16u * US : gs_rt;
-    const int blk = u >> 1;
-    const int h = u & 1;
-    float ds[R][4], dm[R][4];
+    const int xstr = US ? US : xstride;
+    float d[R], dmin[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const uint4 hd = *reinterpret_cast<const uint4 *>(rowp[r] + blk * 144);
-        const float d = half_bits_to_float(hd.x);
-        const float dmin = half_bits_to_float(hd.x >> 16);
-        // 6-bit scales and mins of the four sub-blocks 4h..4h+3, one per byte
-        const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu;
-        const uint32_t m_lo = hd.z & 0x3F3F3F3Fu;
-        const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-        const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-        const uint32_t scw = h ? sc_hi : sc_lo;
-        const uint32_t mw = h ? m_hi : m_lo;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float sc = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j)) - kTwo23;
-            const float m = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j)) - kTwo23;
-            ds[r][j] = d * sc;
-            dm[r][j] = dmin * m;
-        }
+        d[r] = half_bits_to_float(hd[r].x);
+        dmin[r] = half_bits_to_float(hd[r].x >> 16);
     }
-    const uint64_t neg_magic = pack2f(-kTwo23, -kTwo23);
-    const uint8_t *qoff[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) qoff[r] = rowp[r] + blk * 144 + 16 + 64 * h;
+    for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !has_hi) break;
+        const uint8_t *xa = h ? xa1 : xa0;
+        const float *xsum_u = h ? xsum1 : xsum0;
+        const float *xsc_u = h ? xsc1 : xsc0;
+        // d*sc and -dmin*m of the four sub-blocks 4h..4h+3: the 6-bit field
+        // placed in a float's mantissa is 2^23 + v, and one FMA against the
+        // matching offset gives the exact product
+        float ds[R][4], dmn[R][4];
 #pragma unroll
-    for (int lc = 0; lc < 2; ++lc) {
-        uint64_t A[R][B][2];
+        for (int r = 0; r < R; ++r) {
+            uint32_t scw, mw;
+            if (h == 0) {
+                scw = hd[r].y & 0x3F3F3F3Fu;
+                mw = hd[r].z & 0x3F3F3F3Fu;
+            } else {
+                scw = (hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u);
+                mw = ((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u);
+            }
+            const float dlo = d[r], dhi = d[r] * 0.0625f;
+            const float clo = dlo * -kTwo23, chi = dhi * -kTwo23, cm = dmin[r] * kTwo23;
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+            for (int j = 0; j < 4; ++j) {
+                const float fs = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j));
+                const float fm = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j));
+                ds[r][j] = (j & 1) ? fmaf(dhi, fs, chi) : fmaf(dlo, fs, clo);
+                dmn[r][j] = fmaf(-dmin[r], fm, cm);
+            }
+        }
 #pragma unroll
-            for (int b = 0; b < B; ++b) A[r][b][0] = A[r][b][1] = 0ull;
+        for (int lc = 0; lc < 2; ++lc) {
+            int sl[R][4], sh[R][4];
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            uint4 q[R];
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int r = 0; r < R; ++r) q[r] = *reinterpret_cast<const uint4 *>(qoff[r] + 32 * lc + 16 * p);
+                for (int k = 0; k < 4; ++k) sl[r][k] = sh[r][k] = 0;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int g_lo = 16 * lc + 4 * p + k;
-                const int g_hi = g_lo + 8;
-                uint64_t qp[R][4];
+            for (int p = 0; p < 2; ++p) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t wd = k == 0 ? q[r].x : (k == 1 ? q[r].y : (k == 2 ? q[r].z : q[r].w));
-                    const uint32_t wd2 = wd >> 12;
-                    qp[r][0] = add_f32x2(pack2(magic_field<0xFu>(wd), magic_field<0xF00u>(wd)), neg_magic);
-                    qp[r][1] = add_f32x2(pack2(magic_field<0xF0000u>(wd), magic_field<0xF000u>(wd2)), neg_magic);
-                    qp[r][2] = add_f32x2(pack2(magic_field<0xF0u>(wd), magic_field<0xF000u>(wd)), neg_magic);
-                    qp[r][3] = add_f32x2(pack2(magic_field<0xF00u>(wd2), magic_field<0xF0000u>(wd2)), neg_magic);
-                }
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    uint64_t xl0, xl1, xh0, xh1;
-                    lds128(xa + static_cast<uint32_t>(b * 32 + g_lo) * gs, xl0, xl1);
-                    lds128(xa + static_cast<uint32_t>(b * 32 + g_hi) * gs, xh0, xh1);
+                for (int k = 0; k < 4; ++k) {
+                    const int g_lo = 16 * lc + 4 * p + k;
+                    const uint4 xl = *reinterpret_cast<const uint4 *>(xa + g_lo * gs);
+                    const uint4 xh = *reinterpret_cast<const uint4 *>(xa + (g_lo + 8) * gs);
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        A[r][b][0] = fma_f32x2(qp[r][0], xl0, A[r][b][0]);
-                        A[r][b][0] = fma_f32x2(qp[r][1], xl1, A[r][b][0]);
-                        A[r][b][1] = fma_f32x2(qp[r][2], xh0, A[r][b][1]);
-                        A[r][b][1] = fma_f32x2(qp[r][3], xh1, A[r][b][1]);
+                        const uint4 q = qs[r][4 * h + 2 * lc + p];
+                        const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+                        const uint32_t L = wd & 0x0F0F0F0Fu;   // q of sub-block 2lc
+                        const uint32_t H = wd & 0xF0F0F0F0u;   // 16 q of sub-block 2lc+1
+                        sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
+                        sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
+                        sl[r][2] = dp4a_uu(L, xl.z, sl[r][2]);
+                        sl[r][3] = dp4a_us(L, xl.w, sl[r][3]);
+                        sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
+                        sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
+                        sh[r][2] = dp4a_uu(H, xh.z, sh[r][2]);
+                        sh[r][3] = dp4a_us(H, xh.w, sh[r][3]);
                     }
                 }
             }
-        }
-        // scale this chunk's two sub-blocks (local 2lc = low nibbles, 2lc+1 = high)
-        const int xstr = US ? US : xsum_stride;
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const float X0 = xsum_u[(b * 4 + 2 * lc) * xstr];
-            const float X1 = xsum_u[(b * 4 + 2 * lc + 1) * xstr];
+            const float X0 = xsum_u[(2 * lc) * xstr], X1 = xsum_u[(2 * lc + 1) * xstr];
+            const float S0 = xsc_u[(2 * lc) * xstr], S1 = xsc_u[(2 * lc + 1) * xstr];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float2 a0 = unpack2f(A[r][b][0]);
-                const float2 a1 = unpack2f(A[r][b][1]);
-                float t = acc[r][b];
-                t = fmaf(ds[r][2 * lc], a0.x + a0.y, t);
-                t = fmaf(-dm[r][2 * lc], X0, t);
-                t = fmaf(ds[r][2 * lc + 1], a1.x + a1.y, t);
-                t = fmaf(-dm[r][2 * lc + 1], X1, t);
-                acc[r][b] = t;
+                const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2], sl[r][3]);
+                const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2], sh[r][3]);
+                float t = acc[r][0];
+                t = fmaf(ds[r][2 * lc] * S0, F0, t);
+                t = fmaf(dmn[r][2 * lc], X0, t);
+                t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
+                t = fmaf(dmn[r][2 * lc + 1], X1, t);
+                acc[r][0] = t;
             }
         }
     }
 }
 
-// -------------------------------------------------------------------------- Q8_0 unit
-
-// One 32-weight block (block u) for R rows.  Blocks are 34 bytes, so a
-// block starts 0 or 2 bytes past a 4-byte boundary; nine aligned words are
-// read and realigned with byte permutes.
+// -------------------------------------------------------------------------- Q4_K, batch >= 2
+//
+// One super-block of R rows from registers against fp32 activations that are
+// pre-multiplied by 2^-s for their nibble position (see q4k_nibble_shift):
+// a nibble at bit s of a word becomes the exact float 2^23 + q*2^s with one
+// LOP3, 2^23 is subtracted, and (q*2^s)*(x*2^-s) = q*x exactly.
 template <int B, int R, int US>
-__device__ __forceinline__ void q8_unit(const uint8_t *const (&rowp)[R], int u, uint32_t xa, uint32_t gs_rt,
-                                        float (&acc)[R][B])
+__device__ __forceinline__ void q4k_sb_fp(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
+                                            const uint8_t *xa0, const uint8_t *xa1, uint32_t gs_rt, const float *xsum0,
+                                            const float *xsum1, int xstride, float (&acc)[R][B])
 {
     const uint32_t gs = US ? 16u * US : gs_rt;
-    uint32_t qw[R][8];
-    float d[R];
+    const int xstr = US ? US : xstride;
+    const uint64_t neg_magic = pack2f(-kTwo23, -kTwo23);
+    float d[R], dmin[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(rowp[r] + 34 * u);
-        const uint32_t off = static_cast<uint32_t>(a & 3u);           // 0 or 2
-        const uint32_t *wp = reinterpret_cast<const uint32_t *>(a - off);
-        uint32_t wv[9];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) wv[i] = wp[i];
-        d[r] = half_bits_to_float(wv[0] >> (8 * off));
-        const uint32_t sel = off ? 0x7654u : 0x5432u;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) qw[r][k] = __byte_perm(wv[k], wv[k + 1], sel) ^ 0x80808080u;
+        d[r] = half_bits_to_float(hd[r].x);
+        dmin[r] = half_bits_to_float(hd[r].x >> 16);
     }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !has_hi) break;
+        const uint8_t *xa = h ? xa1 : xa0;
+        const float *xsum_u = h ? xsum1 : xsum0;
+        float ds[R][4], dmn[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            uint32_t scw, mw;
+            if (h == 0) {
+                scw = hd[r].y & 0x3F3F3F3Fu;
+                mw = hd[r].z & 0x3F3F3F3Fu;
+            } else {
+                scw = (hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u);
+                mw = ((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u);
+            }
+            const float cs = d[r] * -kTwo23, cm = dmin[r] * kTwo23;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ds[r][j] = fmaf(d[r], __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j)), cs);
+                dmn[r][j] = fmaf(-dmin[r], __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j)), cm);
+            }
+        }
+#pragma unroll
+        for (int lc = 0; lc < 2; ++lc) {
+            uint64_t A[R][B][2];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) A[r][b][0] = A[r][b][1] = 0ull;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int g_lo = 16 * lc + 4 * p + k;
+                    const int g_hi = g_lo + 8;
+                    uint64_t qp[R][4];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint4 q = qs[r][4 * h + 2 * lc + p];
+                        const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+                        const uint32_t wd2 = wd >> 12;
+                        qp[r][0] = add_f32x2(pack2(magic_field<0xFu>(wd), magic_field<0xF00u>(wd)), neg_magic);
+                        qp[r][1] = add_f32x2(pack2(magic_field<0xF0000u>(wd), magic_field<0xF000u>(wd2)), neg_magic);
+                        qp[r][2] = add_f32x2(pack2(magic_field<0xF0u>(wd), magic_field<0xF000u>(wd)), neg_magic);
+                        qp[r][3] = add_f32x2(pack2(magic_field<0xF00u>(wd2), magic_field<0xF0000u>(wd2)), neg_magic);
+                    }
+#pragma unroll
+                    for (int b = 0; b < B; ++b) {
+                        const ulonglong2 xl = *reinterpret_cast<const ulonglong2 *>(xa + (b * 32 + g_lo) * gs);
+                        const ulonglong2 xh = *reinterpret_cast<const ulonglong2 *>(xa + (b * 32 + g_hi) * gs);
+                        const uint64_t xl0 = xl.x, xl1 = xl.y, xh0 = xh.x, xh1 = xh.y;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            A[r][b][0] = fma_f32x2(qp[r][0], xl0, A[r][b][0]);
+                            A[r][b][0] = fma_f32x2(qp[r][1], xl1, A[r][b][0]);
+                            A[r][b][1] = fma_f32x2(qp[r][2], xh0, A[r][b][1]);
+                            A[r][b][1] = fma_f32x2(qp[r][3], xh1, A[r][b][1]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const float X0 = xsum_u[(b * 4 + 2 * lc) * xstr];
+                const float X1 = xsum_u[(b * 4 + 2 * lc + 1) * xstr];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 a0 = unpack2f(A[r][b][0]);
+                    const float2 a1 = unpack2f(A[r][b][1]);
+                    float t = acc[r][b];
+                    t = fmaf(ds[r][2 * lc], a0.x + a0.y, t);
+                    t = fmaf(dmn[r][2 * lc], X0, t);
+                    t = fmaf(ds[r][2 * lc + 1], a1.x + a1.y, t);
+                    t = fmaf(dmn[r][2 * lc + 1], X1, t);
+                    acc[r][b] = t;
+                }
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------------------- Q8_0
+//
+// A 34-byte block starts 0 or 2 bytes past a 4-byte boundary; the lane keeps
+// the nine aligned words that cover it and realigns them with byte permutes.
+template <int R>
+__device__ __forceinline__ void q8_realign(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], float (&d)[R],
+                                           uint32_t (&qw)[R][8])
+{
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        d[r] = half_bits_to_float(wv[r][0] >> (8 * off[r]));
+        const uint32_t sel = off[r] ? 0x7654u : 0x5432u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qw[r][k] = __byte_perm(wv[r][k], wv[r][k + 1], sel);
+    }
+}
+
+// Batch 1: block-floating-point planes of the block's 32 columns at xa.
+template <int R, int US>
+__device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], const uint8_t *xa,
+                                            uint32_t gs_rt, float xscale, float (&acc)[R][1])
+{
+    const uint32_t gs = US ? 16u * US : gs_rt;
+    float d[R];
+    uint32_t qw[R][8];
+    q8_realign<R>(wv, off, d, qw);
+    int sp[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sp[r][k] = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xa + k * gs);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t v = qw[r][k];
+            sp[r][0] = dp4a_su(v, xv.x, sp[r][0]);
+            sp[r][1] = dp4a_su(v, xv.y, sp[r][1]);
+            sp[r][2] = dp4a_su(v, xv.z, sp[r][2]);
+            sp[r][3] = dp4a_ss(v, xv.w, sp[r][3]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2], sp[r][3]), acc[r][0]);
+}
+
+// Batch >= 2: int8 quants through the magic-exponent trick (bias 128), fp32 x.
+template <int B, int R, int US>
+__device__ __forceinline__ void q8_blk_fp(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], const uint8_t *xa,
+                                           uint32_t gs_rt, float (&acc)[R][B])
+{
+    const uint32_t gs = US ? 16u * US : gs_rt;
+    float d[R];
+    uint32_t qw[R][8];
+    q8_realign<R>(wv, off, d, qw);
     const uint64_t neg_bias = pack2f(-(kTwo23 + 128.0f), -(kTwo23 + 128.0f));
     uint64_t part[R][B];
 #pragma unroll
@@ -232,14 +387,14 @@ __device__ __forceinline__ void q8_unit(const uint8_t *const (&rowp)[R], int u, 
         uint64_t q01[R], q23[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const uint32_t v = qw[r][k];
+            const uint32_t v = qw[r][k] ^ 0x80808080u;
             q01[r] = add_f32x2(pack2(__byte_perm(v, kMagic, 0x7440u), __byte_perm(v, kMagic, 0x7441u)), neg_bias);
             q23[r] = add_f32x2(pack2(__byte_perm(v, kMagic, 0x7442u), __byte_perm(v, kMagic, 0x7443u)), neg_bias);
         }
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-            uint64_t x01, x23;
-            lds128(xa + static_cast<uint32_t>(b * 8 + k) * gs, x01, x23);
+            const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xa + (b * 8 + k) * gs);
+            const uint64_t x01 = xv.x, x23 = xv.y;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 part[r][b] = fma_f32x2(q01[r], x01, part[r][b]);
@@ -256,176 +411,144 @@ __device__ __forceinline__ void q8_unit(const uint8_t *const (&rowp)[R], int u, 
         }
 }
 
-// -------------------------------------------------------------------------- batch-1 integer units
+// -------------------------------------------------------------------------- activations -> shared memory
 //
-// For batch 1 the activations are held as block floating point: each
-// 32-column group has one exponent E and every value becomes the 32-bit
-// integer m = rint(x * 2^(30-E)) (|m| < 2^31), stored as four byte planes
-// (plane 3 signed, planes 0..2 unsigned).  A weight group then costs one
-// 4-way byte dot product per plane, sum_i q_i m_i is assembled exactly in
-// integers per plane and x-group scale 2^(E-30) turns it back into a float.
-// Values within 2^7 of their group's largest magnitude are represented
-// exactly; the error of any other value is below 2^-31 of that magnitude.
-
-// sum(q*m) of one group from its four plane sums, as a float.
-__device__ __forceinline__ float planes_to_float(int s0, int s1, int s2, int s3)
+// One warp-uniform pass: each lane loads float4 group f of batch row b
+// (columns 4f..4f+3; columns >= K are zero) and stores it at its place.  For
+// Q4_K the 8 lanes holding a 32-column group also sum it (unscaled).  Batch 1
+// stores block-floating-point byte planes (one exponent per 32 columns),
+// batch >= 2 stores fp32 pre-multiplied by 2^-s for the Q4_K nibble position.
+template <int FMT, int B, int US>
+__device__ __forceinline__ void stage_x(const GemvArgs &a, int cwarp, int lane, int nthreads, uint32_t xs_addr,
+                                             float *xsum, float *xscale)
 {
-    const int hi = s3 * 256 + s2;     // exact in int32 for 32-weight groups
-    const int lo = s1 * 256 + s0;
-    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
-}
-
-// One 128-weight Q4_K unit for R rows, batch 1.
-template <int R, int US>
-__device__ __forceinline__ void q4k_unit_dig(const uint8_t *const (&rowp)[R], int u, uint32_t xa, uint32_t gs_rt,
-                                             const float *__restrict__ xsum_u, const float *__restrict__ xscale_u,
-                                             int xstride, float (&acc)[R][1])
-{
-    const uint32_t gs = US ? 16u * US : gs_rt;
-    const int xstr = US ? US : xstride;
-    const int blk = u >> 1;
-    const int h = u & 1;
-    float ds[R][4], dm[R][4];
+    constexpr int UC = FMT == kFmtQ4K ? 128 : 32;
+    constexpr int G = UC / 4;
+    const int XU = US ? US : a.XU;
+    const int XH = XU >> 1;
+    const int K = static_cast<int>(a.K);
+    const int g_total = a.U * G;
+    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15u) == 0);
+    constexpr int UNR = 4;
+    for (int b = 0; b < B; ++b) {
+        const float *xb = a.x + static_cast<int64_t>(b) * K;
+        for (int base = cwarp * 32; base < g_total; base += UNR * nthreads) {
+            float4 v[UNR];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const uint4 hd = *reinterpret_cast<const uint4 *>(rowp[r] + blk * 144);
-        const float d = half_bits_to_float(hd.x);
-        const float dmin = half_bits_to_float(hd.x >> 16);
-        const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu;
-        const uint32_t m_lo = hd.z & 0x3F3F3F3Fu;
-        const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-        const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-        const uint32_t scw = h ? sc_hi : sc_lo;
-        const uint32_t mw = h ? m_hi : m_lo;
+            for (int i = 0; i < UNR; ++i) {
+                const int f = base + i * nthreads + lane;
+                const int c0 = 4 * f;
+                v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (f < g_total) {
+                    if (vec && c0 + 3 < K) {
+                        v[i] = __ldg(reinterpret_cast<const float4 *>(xb + c0));
+                    } else {
+                        if (c0 < K) v[i].x = __ldg(xb + c0);
+                        if (c0 + 1 < K) v[i].y = __ldg(xb + c0 + 1);
+                        if (c0 + 2 < K) v[i].z = __ldg(xb + c0 + 2);
+                        if (c0 + 3 < K) v[i].w = __ldg(xb + c0 + 3);
+                    }
+                }
+            }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float sc = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j)) - kTwo23;
-            const float m = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j)) - kTwo23;
-            ds[r][j] = d * sc;
-            dm[r][j] = dmin * m;
-        }
-    }
-    const uint8_t *qoff[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) qoff[r] = rowp[r] + blk * 144 + 16 + 64 * h;
-#pragma unroll
-    for (int lc = 0; lc < 2; ++lc) {
-        int sl[R][4], sh[R][4];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sl[r][k] = sh[r][k] = 0;
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            uint4 q[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) q[r] = *reinterpret_cast<const uint4 *>(qoff[r] + 32 * lc + 16 * p);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int g_lo = 16 * lc + 4 * p + k;
-                const uint4 xl = lds128u(xa + static_cast<uint32_t>(g_lo) * gs);
-                const uint4 xh = lds128u(xa + static_cast<uint32_t>(g_lo + 8) * gs);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t wd = k == 0 ? q[r].x : (k == 1 ? q[r].y : (k == 2 ? q[r].z : q[r].w));
-                    const uint32_t L = wd & 0x0F0F0F0Fu;          // low nibbles: 4 columns of sub-block 2lc
-                    const uint32_t H = (wd >> 4) & 0x0F0F0F0Fu;   // high nibbles: same columns of 2lc+1
-                    sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
-                    sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
-                    sl[r][2] = dp4a_uu(L, xl.z, sl[r][2]);
-                    sl[r][3] = dp4a_us(L, xl.w, sl[r][3]);
-                    sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
-                    sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
-                    sh[r][2] = dp4a_uu(H, xh.z, sh[r][2]);
-                    sh[r][3] = dp4a_us(H, xh.w, sh[r][3]);
+            for (int i = 0; i < UNR; ++i) {
+                if (base + i * nthreads >= g_total) break;   // warp-uniform
+                const int f = base + i * nthreads + lane;
+                const int u = f / G, g = f % G;
+                const int us = FMT == kFmtQ4K ? ((u & 1) * XH + (u >> 1)) : u;   // unit slot
+                if constexpr (B == 1) {
+                    float amax = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+                    float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                    if constexpr (FMT == kFmtQ4K) {
+                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+                    }
+                    const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 255u);
+                    const bool finite = ebits != 255;
+                    const int E = max(ebits - 127, -96);
+                    const float up = __int_as_float((157 - E) << 23);     // 2^(30-E)
+                    const float down = __int_as_float((97 + E) << 23);    // 2^(E-30)
+                    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+                    if (finite) {
+                        m0 = static_cast<uint32_t>(__float2int_rn(v[i].x * up));
+                        m1 = static_cast<uint32_t>(__float2int_rn(v[i].y * up));
+                        m2 = static_cast<uint32_t>(__float2int_rn(v[i].z * up));
+                        m3 = static_cast<uint32_t>(__float2int_rn(v[i].w * up));
+                    }
+                    // byte-plane transpose: plane k holds byte k of the four columns
+                    const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
+                    const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
+                    const uint32_t p0 = __byte_perm(t0, t1, 0x5410u), p1 = __byte_perm(t0, t1, 0x7632u);
+                    const uint32_t p2 = __byte_perm(t2, t3, 0x5410u), p3 = __byte_perm(t2, t3, 0x7632u);
+                    if (f < g_total) {
+                        const int grp = FMT == kFmtQ4K ? (g >> 3) : 0;
+                        if ((lane & 7) == 0) {
+                            xscale[grp * XU + us] = finite ? down : __int_as_float(0x7FC00000);
+                            if constexpr (FMT == kFmtQ4K) xsum[grp * XU + us] = sum;
+                        }
+                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(g * XU + us);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                     ::"r"(dst), "r"(p0), "r"(p1), "r"(p2), "r"(p3) : "memory");
+                    }
+                    continue;
+                }
+                if constexpr (FMT == kFmtQ4K) {
+                    float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+                    if (f < g_total && (lane & 7) == 0) xsum[(b * 4 + (g >> 3)) * XU + us] = sum;
+                    const int c = 4 * g;
+                    v[i].x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
+                    v[i].y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
+                    v[i].z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
+                    v[i].w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
+                }
+                if (f < g_total) {
+                    const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>((b * G + g) * XU + us);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(dst), "f"(v[i].x), "f"(v[i].y), "f"(v[i].z), "f"(v[i].w) : "memory");
                 }
             }
         }
-        const float X0 = xsum_u[(2 * lc) * xstr], X1 = xsum_u[(2 * lc + 1) * xstr];
-        const float S0 = xscale_u[(2 * lc) * xstr], S1 = xscale_u[(2 * lc + 1) * xstr];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2], sl[r][3]);
-            const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2], sh[r][3]);
-            float t = acc[r][0];
-            t = fmaf(ds[r][2 * lc] * S0, F0, t);
-            t = fmaf(-dm[r][2 * lc], X0, t);
-            t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
-            t = fmaf(-dm[r][2 * lc + 1], X1, t);
-            acc[r][0] = t;
-        }
     }
-}
-
-// One 32-weight Q8_0 block for R rows, batch 1.
-template <int R, int US>
-__device__ __forceinline__ void q8_unit_dig(const uint8_t *const (&rowp)[R], int u, uint32_t xa, uint32_t gs_rt,
-                                            float xscale, float (&acc)[R][1])
-{
-    const uint32_t gs = US ? 16u * US : gs_rt;
-    uint32_t qw[R][8];
-    float d[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(rowp[r] + 34 * u);
-        const uint32_t off = static_cast<uint32_t>(a & 3u);           // 0 or 2
-        const uint32_t *wp = reinterpret_cast<const uint32_t *>(a - off);
-        uint32_t wv[9];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) wv[i] = wp[i];
-        d[r] = half_bits_to_float(wv[0] >> (8 * off));
-        const uint32_t sel = off ? 0x7654u : 0x5432u;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) qw[r][k] = __byte_perm(wv[k], wv[k + 1], sel);
-    }
-    int sp[R][4];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sp[r][k] = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint4 xv = lds128u(xa + static_cast<uint32_t>(k) * gs);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t v = qw[r][k];
-            sp[r][0] = dp4a_su(v, xv.x, sp[r][0]);
-            sp[r][1] = dp4a_su(v, xv.y, sp[r][1]);
-            sp[r][2] = dp4a_su(v, xv.z, sp[r][2]);
-            sp[r][3] = dp4a_ss(v, xv.w, sp[r][3]);
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2], sp[r][3]), acc[r][0]);
 }
 
 // -------------------------------------------------------------------------- kernel
 
-template <int FMT, int B, int R, int US>
-__global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(const GemvArgs a)
+template <int FMT, int B, int US>
+__global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int UC = FMT == kFmtQ4K ? 128 : 32;  // columns per unit
-    constexpr int G = UC / 4;                      // float4 groups per unit
+    constexpr int R = gemv_rows(FMT, B);
+    constexpr int NW = gemv_warps(FMT, B);
+    constexpr int CM = gemv_cpl_max(FMT, B);
+    constexpr int UB = FMT == kFmtQ4K ? 144 : 34;    // bytes per lane unit
     const int tid = threadIdx.x;
-    const int S = a.stages;
-    const uint32_t bar0 = smem_u32(smem);
-    const int n_cwarps = a.NTC / 32;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 16 * kMaxStages);
+    const uint32_t nw = static_cast<uint32_t>(a.nw);  // consumer warps with row groups
+    const uint32_t m = static_cast<uint32_t>(a.m);    // stages per consumer warp
+    const uint32_t bar_full = smem_u32(smem);
+    const uint32_t bar_empty = bar_full + 256u;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 512);
+    int *issued_use = reinterpret_cast<int *>(smem + 528);   // per stage: use of its last copy, -1 none
 
     const int64_t nG = gridDim.x;
     const int64_t r_begin = (a.rows * blockIdx.x) / nG;
     const int64_t r_end = (a.rows * (blockIdx.x + 1)) / nG;
-    const int64_t n_tiles = (r_end - r_begin + a.tile_rows - 1) / a.tile_rows;
+    const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + a.rows_w - 1) / a.rows_w);
+    const uint32_t nkc = static_cast<uint32_t>(a.nkc);
 
-    // Programmatic dependent launch: the next grid in the stream may be
-    // scheduled now.  (No effect when launched without that attribute.)
+    // programmatic dependent launch: the next grid in the stream may start
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar0 + 8u * s, 1);                    // full[s]
-            mbar_init(bar0 + 8u * (S + s), n_cwarps);       // empty[s]
+        for (uint32_t s = 0; s < nw * m; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 1);
+            issued_use[s] = -1;
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -435,36 +558,70 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
     const uint32_t stage0 = smem_u32(smem + a.off_stage);
 
     // ------------------------------------------------------------------ producer
+    // Lane w of warp 0 feeds consumer warp w: row groups w, w+nw, ..., each
+    // as nkc K-chunk items; item t of the warp goes to stage w*m + t%m.  The
+    // warps' pipelines are independent, so no warp waits behind another.
     if (tid < 32) {
-        if (tid == 0) {
+        const uint32_t w = static_cast<uint32_t>(tid);
+        if (w < nw) {
             const uint64_t pol = l2_evict_first_policy();
-            int64_t j = 0;
             bool ok = true;
-            for (; j < n_tiles; ++j) {
-                const int s = static_cast<int>(j % S);
-                const uint32_t use = static_cast<uint32_t>(j / S);
-                if (j >= S && !mbar_wait(bar0 + 8u * (S + s), (use - 1) & 1u, a.wait_ns)) {
-                    ok = false;
-                    break;
+            uint32_t t = 0, tm = 0, use = 0;                 // item number, its stage offset and use
+            for (uint32_t g = w; ok && g < n_groups; g += nw) {
+                const int64_t row0 = r_begin + static_cast<int64_t>(g) * a.rows_w;
+                const int n = static_cast<int>(min(static_cast<int64_t>(a.rows_w), r_end - row0));
+                const uint8_t *src0 = a.w + row0 * a.row_bytes;
+                for (uint32_t c = 0; c < nkc; ++c, ++t) {
+                    const uint32_t st = w * m + tm;
+                    const uint32_t bar = bar_full + 8u * st;
+                    if (*abort_flag || (use > 0 && !mbar_wait(bar_empty + 8u * st, (use - 1) & 1u, a.wait_ns))) {
+                        ok = false;
+                        break;
+                    }
+                    const bool skip = w == 0 && t == a.skip_item && blockIdx.x == 0;   // test hook
+                    if (!skip) {
+                        const uint32_t dst = stage0 + st * static_cast<uint32_t>(a.stage_bytes);
+                        if (nkc == 1) {
+                            const uintptr_t gs = reinterpret_cast<uintptr_t>(src0);
+                            const uintptr_t ge = gs + static_cast<uintptr_t>(n * a.row_bytes);
+                            const uintptr_t lo = gs & ~static_cast<uintptr_t>(15);
+                            const uint32_t bytes =
+                                static_cast<uint32_t>(((ge + 15) & ~static_cast<uintptr_t>(15)) - lo);
+                            mbar_arrive_expect_tx(bar, bytes);
+                            bulk_g2s(dst, reinterpret_cast<const void *>(lo), bytes, bar, pol);
+                        } else {
+                            const int64_t cb = static_cast<int64_t>(c) * a.chunk_bytes;
+                            const int64_t cl = min(static_cast<int64_t>(a.chunk_bytes), a.row_bytes - cb);
+                            uint32_t total = 0;
+                            for (int q = 0; q < n; ++q) {
+                                const uintptr_t gs = reinterpret_cast<uintptr_t>(src0 + q * a.row_bytes + cb);
+                                total += static_cast<uint32_t>(((gs + cl + 15) & ~static_cast<uintptr_t>(15)) -
+                                                               (gs & ~static_cast<uintptr_t>(15)));
+                            }
+                            mbar_arrive_expect_tx(bar, total);
+                            for (int q = 0; q < n; ++q) {
+                                const uintptr_t gs = reinterpret_cast<uintptr_t>(src0 + q * a.row_bytes + cb);
+                                const uintptr_t lo = gs & ~static_cast<uintptr_t>(15);
+                                const uintptr_t hi = (gs + cl + 15) & ~static_cast<uintptr_t>(15);
+                                bulk_g2s(dst + static_cast<uint32_t>(q * a.row_stride),
+                                         reinterpret_cast<const void *>(lo), static_cast<uint32_t>(hi - lo), bar, pol);
+                            }
+                        }
+                        issued_use[st] = static_cast<int>(use);
+                    }
+                    if (++tm == m) {
+                        tm = 0;
+                        ++use;
+                    }
                 }
-                if (j == a.skip_tile && blockIdx.x == 0) continue;   // test hook
-                const int64_t row0 = r_begin + j * a.tile_rows;
-                const int64_t n = min(static_cast<int64_t>(a.tile_rows), r_end - row0);
-                const uintptr_t gs = reinterpret_cast<uintptr_t>(a.w + row0 * a.row_bytes);
-                const uintptr_t ge = gs + static_cast<uintptr_t>(n * a.row_bytes);
-                const uintptr_t lo = gs & ~static_cast<uintptr_t>(15);
-                const uintptr_t hi = (ge + 15) & ~static_cast<uintptr_t>(15);
-                const uint32_t bytes = static_cast<uint32_t>(hi - lo);
-                mbar_arrive_expect_tx(bar0 + 8u * s, bytes);
-                bulk_g2s(stage0 + static_cast<uint32_t>(s) * a.stage_bytes,
-                         reinterpret_cast<const void *>(lo), bytes, bar0 + 8u * s, pol);
             }
             if (!ok) {
+                *abort_flag = 1;
                 record_error(a.err, kErrTimeout);
-                // let the copies already issued land before the CTA exits
-                for (int64_t t = j - S; t < j; ++t) {
-                    if (t < 0 || (t == a.skip_tile && blockIdx.x == 0)) continue;
-                    mbar_wait(bar0 + 8u * (t % S), static_cast<uint32_t>(t / S) & 1u, a.wait_ns);
+                // let this warp's copies already issued land before the CTA exits
+                for (uint32_t q = 0; q < m; ++q) {
+                    const int u = issued_use[w * m + q];
+                    if (u >= 0) mbar_wait(bar_full + 8u * (w * m + q), static_cast<uint32_t>(u) & 1u, a.wait_ns);
                 }
             }
         }
@@ -472,204 +629,147 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
     }
 
     // ------------------------------------------------------------------ consumers
-    const int ctid = tid - 32;
+    const uint32_t cwarp = static_cast<uint32_t>((tid >> 5) - 1);
     const int lane = tid & 31;
-    const int cwarp = ctid >> 5;
-    const bool active = ctid < a.slots * a.SW;
-    const int slot = active ? ctid / a.SW : 0;
-    const int sl = active ? ctid - slot * a.SW : 0;
-    const int U = a.U;
+    const int SW = a.SW;
+    const int team = lane >> a.lsw;
+    const int sl = lane & (SW - 1);
+    const int cpl = a.cpl;
     const int XU = US ? US : a.XU;
-    const uint32_t xs_addr = smem_u32(smem + a.off_x);
-    float *xsum = reinterpret_cast<float *>(smem + a.off_xsum);
-    float *xscale = reinterpret_cast<float *>(smem + a.off_xscale);
+    const int XH = XU >> 1;
+    const uint8_t *xs = smem + a.off_x;
+    const float *xsum = reinterpret_cast<const float *>(smem + a.off_xsum);
+    const float *xscale = reinterpret_cast<const float *>(smem + a.off_xscale);
 
-    // Activations -> shared memory, in one warp-uniform pass: each lane loads
-    // float4 group f of batch row b (columns 4f..4f+3; columns >= K are zero)
-    // and stores it at its permuted place.  For Q4_K the 8 lanes holding a
-    // 32-column sub-block also sum it (unscaled) and the values are
-    // pre-multiplied by 2^-s for their nibble position.  The weights do not
-    // depend on earlier kernels, x may: with programmatic dependent launch
-    // only this part waits for the previous grid (no effect otherwise).
+    // the weights do not depend on earlier kernels, x may: with programmatic
+    // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    {
-        const int K = static_cast<int>(a.K);
-        const int g_total = U * G;                 // float4 groups per batch row incl. padding
-        const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15u) == 0);
-        constexpr int UNR = 4;
-        for (int b = 0; b < B; ++b) {
-            const float *xb = a.x + static_cast<int64_t>(b) * K;
-            for (int base = cwarp * 32; base < g_total; base += UNR * a.NTC) {
-                float4 v[UNR];
-#pragma unroll
-                for (int i = 0; i < UNR; ++i) {
-                    const int f = base + i * a.NTC + lane;
-                    const int c0 = 4 * f;
-                    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (f < g_total) {
-                        if (vec && c0 + 3 < K) {
-                            v[i] = __ldg(reinterpret_cast<const float4 *>(xb + c0));
-                        } else {
-                            if (c0 < K) v[i].x = __ldg(xb + c0);
-                            if (c0 + 1 < K) v[i].y = __ldg(xb + c0 + 1);
-                            if (c0 + 2 < K) v[i].z = __ldg(xb + c0 + 2);
-                            if (c0 + 3 < K) v[i].w = __ldg(xb + c0 + 3);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < UNR; ++i) {
-                    const int f = base + i * a.NTC + lane;
-                    if (base + i * a.NTC >= g_total) break;            // warp-uniform
-                    const int u = f / G, g = f % G;
-                    if constexpr (B == 1) {
-                        // block floating point per 32-column group (8 lanes), as four byte planes
-                        float amax = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
-                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-                        float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                        if constexpr (FMT == kFmtQ4K) {
-                            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-                        }
-                        const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 255u);
-                        const bool finite = ebits != 255;
-                        const int E = max(ebits - 127, -96);
-                        const float up = __int_as_float((157 - E) << 23);     // 2^(30-E)
-                        const float down = __int_as_float((97 + E) << 23);    // 2^(E-30)
-                        uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-                        if (finite) {
-                            m0 = static_cast<uint32_t>(__float2int_rn(v[i].x * up));
-                            m1 = static_cast<uint32_t>(__float2int_rn(v[i].y * up));
-                            m2 = static_cast<uint32_t>(__float2int_rn(v[i].z * up));
-                            m3 = static_cast<uint32_t>(__float2int_rn(v[i].w * up));
-                        }
-                        // byte-plane transpose: plane k holds byte k of the four columns
-                        const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
-                        const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
-                        const uint32_t p0 = __byte_perm(t0, t1, 0x5410u), p1 = __byte_perm(t0, t1, 0x7632u);
-                        const uint32_t p2 = __byte_perm(t2, t3, 0x5410u), p3 = __byte_perm(t2, t3, 0x7632u);
-                        if (f < g_total) {
-                            const int grp = FMT == kFmtQ4K ? (g >> 3) : 0;
-                            if ((lane & 7) == 0) {
-                                xscale[grp * XU + u] = finite ? down : __int_as_float(0x7FC00000);
-                                if constexpr (FMT == kFmtQ4K) xsum[grp * XU + u] = sum;
-                            }
-                            const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(g * XU + u);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                         ::"r"(dst), "r"(p0), "r"(p1), "r"(p2), "r"(p3) : "memory");
-                        }
-                        continue;
-                    }
-                    if constexpr (FMT == kFmtQ4K) {
-                        float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-                        if (f < g_total && (lane & 7) == 0) xsum[(b * 4 + (g >> 3)) * XU + u] = sum;
-                        const int c = 4 * g;
-                        v[i].x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
-                        v[i].y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
-                        v[i].z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
-                        v[i].w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
-                    }
-                    if (f < g_total) {
-                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>((b * G + g) * XU + u);
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                                     ::"r"(dst), "f"(v[i].x), "f"(v[i].y), "f"(v[i].z), "f"(v[i].w) : "memory");
-                    }
-                }
-            }
-        }
-    }
-    named_bar_sync(1, a.NTC);
+    stage_x<FMT, B, US>(a, static_cast<int>(cwarp), lane, 32 * NW, smem_u32(xs),
+                             reinterpret_cast<float *>(smem + a.off_xsum),
+                             reinterpret_cast<float *>(smem + a.off_xscale));
+    named_bar_sync(1, 32 * NW);
+    if (cwarp >= nw) return;
 
-    float *red = reinterpret_cast<float *>(smem + a.off_red);
-    const int n_out = a.slots * R * B;
-    const int red_half = n_out * a.SW;
-    const bool warp_team = a.SW <= 32 && (32 % a.SW) == 0;
     const uint32_t gs_rt = 16u * static_cast<uint32_t>(XU);
-    for (int64_t j = 0; j < n_tiles; ++j) {
-        const int s = static_cast<int>(j % S);
-        const bool ok = mbar_wait(bar0 + 8u * s, static_cast<uint32_t>(j / S) & 1u, a.wait_ns);
-        if (!ok) *abort_flag = 1;
-        const int64_t row0 = r_begin + j * a.tile_rows;
-        const int n = static_cast<int>(min(static_cast<int64_t>(a.tile_rows), r_end - row0));
+    const uintptr_t wbase = reinterpret_cast<uintptr_t>(a.w);
+    const int chunk_lu = SW * cpl;                 // lane units per chunk
+    const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
+    uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
+    bool failed = false;
+    for (uint32_t g = cwarp; g < n_groups && !failed; g += nw) {
+        const int64_t row0 = r_begin + static_cast<int64_t>(g) * a.rows_w;
+        const int n = static_cast<int>(min(static_cast<int64_t>(a.rows_w), r_end - row0));
         float acc[R][B];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
-        if (ok && active) {
-            const uintptr_t gsrc = reinterpret_cast<uintptr_t>(a.w + row0 * a.row_bytes);
-            const uint8_t *sbase = smem + a.off_stage + static_cast<int64_t>(s) * a.stage_bytes + (gsrc & 15u);
+        for (uint32_t c = 0; c < nkc; ++c) {
+            const uint32_t st = st0 + tm;
+            bool ok = *abort_flag == 0 && mbar_wait(bar_full + 8u * st, par, a.wait_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok);   // the warp leaves together or not at all
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    record_error(a.err, kErrTimeout);
+                }
+                failed = true;
+                break;
+            }
+            const uint8_t *stage = smem + a.off_stage + st * static_cast<uint32_t>(a.stage_bytes);
+            // where this lane's rows start their chunk in the stage (rows past
+            // the group's end read its last row and are not stored)
             const uint8_t *rowp[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int rt = min(r * a.slots + slot, n - 1);
-                rowp[r] = sbase + static_cast<int64_t>(rt) * a.row_bytes;
-            }
-            for (int u = sl; u < U; u += a.SW) {
-                const uint32_t xa = xs_addr + 16u * static_cast<uint32_t>(u);
-                if constexpr (B == 1 && FMT == kFmtQ4K)
-                    q4k_unit_dig<R, US>(rowp, u, xa, gs_rt, xsum + u, xscale + u, XU, acc);
-                else if constexpr (B == 1)
-                    q8_unit_dig<R, US>(rowp, u, xa, gs_rt, xscale[u], acc);
-                else if constexpr (FMT == kFmtQ4K)
-                    q4k_unit<B, R, US>(rowp, u, xa, gs_rt, xsum + u, XU, acc);
-                else
-                    q8_unit<B, R, US>(rowp, u, xa, gs_rt, acc);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8u * (S + s));   // stage s may be refilled
-
-        if (warp_team) {
-            // teams of SW lanes (SW divides 32): butterfly inside the team,
-            // no barrier; a warp whose wait ran out leaves on its own
-            if (!ok) {
-                if (lane == 0) record_error(a.err, kErrTimeout);
-                break;
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    float v = acc[r][b];
-                    for (int off = a.SW >> 1; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-                    const int rt = r * a.slots + slot;
-                    if (active && sl == ((r * B + b) % a.SW) && rt < n) a.y[b * a.ldy + row0 + rt] = v;
+                const int lr = min(team * R + r, n - 1);
+                if (nkc == 1) {
+                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>(row0 * a.row_bytes);
+                    rowp[r] = stage + (gsrc & 15u) + static_cast<int64_t>(lr) * a.row_bytes;
+                } else {
+                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>((row0 + lr) * a.row_bytes) +
+                                           static_cast<uintptr_t>(c) * a.chunk_bytes;
+                    rowp[r] = stage + lr * a.row_stride + (gsrc & 15u);
                 }
-            continue;
-        }
-
-        // team reduction through shared memory: the partial of (slot, r, b)
-        // from team member sl sits at red[((slot*R + r)*B + b)*SW + sl]
-        float *rb = red + (j & 1) * red_half;
-        if (active) {
+            }
+            // lane units of this lane in this chunk: i*SW + sl (i < cpl) from
+            // the chunk's start, lane unit c*chunk_lu + i*SW + sl of the row
+            const int lu0 = static_cast<int>(c) * chunk_lu + sl;
+            if constexpr (FMT == kFmtQ4K) {
+                uint4 hd[R], qs[R][8];
+                const bool valid = lu0 < a.LU;
+                if (valid) {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+                    for (int r = 0; r < R; ++r) {
+                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + sl * UB);
+                        hd[r] = p[0];
 #pragma unroll
-                for (int b = 0; b < B; ++b) rb[((slot * R + r) * B + b) * a.SW + sl] = acc[r][b];
-        }
-        named_bar_sync(1, a.NTC);
-        if (*abort_flag) {
-            if (ctid == 0) record_error(a.err, kErrTimeout);
-            break;
-        }
-        for (int o = cwarp; o < n_out; o += n_cwarps) {
-            float v = 0.f;
-            for (int t = lane; t < a.SW; t += 32) v += rb[o * a.SW + t];
+                        for (int i = 0; i < 8; ++i) qs[r][i] = p[1 + i];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
+                if (valid) {
+                    const int lu = lu0;
+                    const bool has_hi = 2 * lu + 1 < a.U;
+                    const uint8_t *xa0 = xs + 16 * lu;
+                    const uint8_t *xa1 = xs + 16 * (XH + lu);
+                    if constexpr (B == 1)
+                        q4k_sb_dig<R, US>(hd, qs, has_hi, xa0, xa1, gs_rt, xsum + lu, xsum + XH + lu,
+                                            xscale + lu, xscale + XH + lu, XU, acc);
+                    else
+                        q4k_sb_fp<B, R, US>(hd, qs, has_hi, xa0, xa1, gs_rt, xsum + lu, xsum + XH + lu, XU, acc);
+                }
+            } else {
+                uint32_t wv[CM][R][9], off[CM][R];
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-            const int b = o % B;
-            const int r = (o / B) % R;
-            const int sidx = o / (B * R);
-            const int rt = r * a.slots + sidx;
-            if (lane == 0 && rt < n) a.y[b * a.ldy + row0 + rt] = v;
+                for (int i = 0; i < CM; ++i) {
+                    const int lu = lu0 + i * SW;
+                    if (i < cpl && lu < a.LU) {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uintptr_t ad = reinterpret_cast<uintptr_t>(rowp[r] + (i * SW + sl) * UB);
+                            off[i][r] = static_cast<uint32_t>(ad & 3u);          // 0 or 2
+                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - off[i][r]);
+#pragma unroll
+                            for (int k = 0; k < 9; ++k) wv[i][r][k] = wp[k];
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * st);
+#pragma unroll
+                for (int i = 0; i < CM; ++i) {
+                    const int lu = lu0 + i * SW;
+                    if (i < cpl && lu < a.LU) {
+                        const uint8_t *xa = xs + 16 * lu;
+                        if constexpr (B == 1)
+                            q8_blk_dig<R, US>(wv[i], off[i], xa, gs_rt, xscale[lu], acc);
+                        else
+                            q8_blk_fp<B, R, US>(wv[i], off[i], xa, gs_rt, acc);
+                    }
+                }
+            }
+            if (++tm == m) {
+                tm = 0;
+                par ^= 1u;
+            }
         }
+        if (failed) break;
+        // sum over the SW lanes of each team; lane 0 of the team writes
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                float v = acc[r][b];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const float t = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    if (o < SW) v += t;
+                }
+                const int lr = team * R + r;
+                if (sl == 0 && lr < n) a.y[b * a.ldy + row0 + lr] = v;
+            }
     }
 }
 
@@ -677,11 +777,10 @@ __global__ void __launch_bounds__(32 + max_consumers(FMT, B), 1) gemv_kernel(con
 cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q80(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
-template <int FMT, int B, int R, int US>
+template <int FMT, int B, int US>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
-    auto kern = gemv_kernel<FMT, B, R, US>;
-    // raise the dynamic shared-memory limit once per device and size
+    auto kern = gemv_kernel<FMT, B, US>;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -694,7 +793,7 @@ cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(32 + a.NTC);
+    cfg.blockDim = dim3(32 * (gemv_warps(FMT, B) + 1));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -707,13 +806,11 @@ cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t 
     return cudaGetLastError();
 }
 
-// Instantiations for one format and batch: the activation unit stride is a
-// compile-time 32 or 128 where it fits, else a runtime value.
-#define QK_GEMV_DISPATCH_US(FMT, B, US_RT)                                                  \
-    switch (US_RT) {                                                                        \
-    case 32: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 32>(a, grid, smem, st, pdl);   \
-    case 128: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 128>(a, grid, smem, st, pdl); \
-    default: return gemv_launch_one<FMT, B, rows_per_thread(FMT, B), 0>(a, grid, smem, st, pdl);    \
+#define QK_GEMV_DISPATCH_US(FMT, B, US_RT)                                       \
+    switch (US_RT) {                                                                  \
+    case 32: return gemv_launch_one<FMT, B, 32>(a, grid, smem, st, pdl);         \
+    case 128: return gemv_launch_one<FMT, B, 128>(a, grid, smem, st, pdl);       \
+    default: return gemv_launch_one<FMT, B, 0>(a, grid, smem, st, pdl);          \
     }
 
 }  // namespace qk

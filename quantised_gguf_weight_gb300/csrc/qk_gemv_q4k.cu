@@ -1,5 +1,5 @@
-// qk_gemv_q4k.cu -- instantiations of the GEMV kernel for one weight format
-// (compiled as their own translation unit so the formats build in parallel).
+// qk_gemv_q4k.cu -- instantiations of the GEMV kernel for one weight
+// format (its own translation unit so the kernels build in parallel).
 #include "qk_gemv_kernel.cuh"
 
 namespace qk {

@@ -8,25 +8,19 @@ namespace qk {
 
 constexpr int kFmtQ80 = 0;
 constexpr int kFmtQ4K = 1;
-constexpr int kMaxConsumers = 512;   // consumer threads per GEMV CTA
-constexpr int kMaxStages = 8;        // shared-memory ring depth
-
-// Launch plan of one GEMV call (shared-memory layout, grid, team shape).
-// kind 0: the tile kernel (qk_gemv_kernel.cuh); kind 1: the ring kernel
-// (qk_gemv_ring.cuh), which also uses LU, cpl, nkc, rows_w, chunk_bytes,
-// row_stride, nw, m.
+// Launch plan of one GEMV call (qk_gemv_kernel.cuh): team shape, K chunks,
+// stage ring, shared-memory layout and grid.
 struct GemvPlan {
-    int kind;
-    int U, XU, SW, slots, NTC, R, tile_rows, stages, stage_bytes;
-    int off_x, off_xsum, off_xscale, off_red, off_stage, smem, grid;
-    int LU, cpl, nkc, rows_w, chunk_bytes, row_stride, nw, m;
+    int U, LU, XU, SW, R, cpl, nkc, rows_w, chunk_bytes, row_stride;
+    int nw, m, stages, stage_bytes;
+    int off_x, off_xsum, off_xscale, off_stage, smem, grid;
     int64_t row_bytes;
 };
 
 bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p);
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_tile, bool pdl);
+                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl);
 
 // The device error word of the current device and the bound of device waits.
 int *library_error_word();

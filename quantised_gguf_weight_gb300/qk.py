@@ -73,8 +73,8 @@ def load(path: str | None = None):
         lib.qk_version.restype = I
         lib.qk_set_programmatic_launch.argtypes = [I]
         lib.qk_set_programmatic_launch.restype = I
-        lib.qk_debug_skip_tile.argtypes = [I64]
-        lib.qk_debug_skip_tile.restype = I64
+        lib.qk_debug_skip_item.argtypes = [I64]
+        lib.qk_debug_skip_item.restype = I64
         lib.qk_debug_gemv_plan.argtypes = [I, I64, I64, I, ctypes.POINTER(ctypes.c_int64), I]
         lib.qk_debug_gemv_plan.restype = I
         _lib = lib
@@ -168,12 +168,13 @@ def set_programmatic_launch(enable: bool) -> bool:
     return bool(load().qk_set_programmatic_launch(1 if enable else 0))
 
 
-def debug_skip_tile(tile: int) -> int:
-    """Test hook: CTA 0 of later GEMV launches skips copying tile (ring item) `tile` (-1: off)."""
-    return int(load().qk_debug_skip_tile(int(tile)))
+def debug_skip_item(item: int) -> int:
+    """Test hook: in CTA 0 of later GEMV launches, consumer warp 0's item number
+    `item` is never copied (-1: off)."""
+    return int(load().qk_debug_skip_item(int(item)))
 
 
-PLAN_FIELDS = ("kind", "SW", "R", "nkc", "rows_w", "stages", "stage_bytes", "smem", "grid", "XU", "cpl", "nw", "m")
+PLAN_FIELDS = ("SW", "R", "nkc", "rows_w", "stages", "stage_bytes", "smem", "grid", "XU", "cpl", "nw", "m")
 
 
 def debug_gemv_plan(fmt: str, rows: int, K: int, batch: int) -> dict:

@@ -148,22 +148,22 @@ def test_too_large_is_rejected_before_launch(qk):
     assert torch.all(y == 5.0)
 
 
-@pytest.mark.parametrize("fmt,rows,K", [("q4_k", 2000, 4096), ("q4_k", 700, 14336), ("q8_0", 900, 896)])
-def test_bounded_wait_times_out_and_context_survives(qk, orc, fmt, rows, K):
-    """A tile whose copy is never issued makes the consumers' wait run out:
-    the launch records QK_ERR_TIMEOUT and later launches work normally.
-    (K = 4096 and 896 use warp-sized row teams, K = 14336 the shared-memory
-    team reduction.)"""
+@pytest.mark.parametrize("fmt,rows,K,nkc", [("q4_k", 2000, 4096, 1), ("q4_k", 4096, 14336, 2), ("q8_0", 900, 896, 1)])
+def test_bounded_wait_times_out_and_context_survives(qk, orc, fmt, rows, K, nkc):
+    """An item whose copy is never issued makes its warp's wait run out: the
+    launch records QK_ERR_TIMEOUT and later launches work normally.  (The
+    K = 14336 case splits rows into K chunks, one copy per row.)"""
+    assert qk.debug_gemv_plan(fmt, rows, K, 1)["nkc"] == nkc
     wq = synth.weights(fmt, rows, K, seed=15)
     x = synth.activations(1, K, seed=15)
     assert qk.device_error() == 0
     old = qk.set_wait_limit_ns(20_000_000)
-    qk.debug_skip_tile(0)
+    qk.debug_skip_item(0)
     try:
         gpu_gemv(qk, fmt, wq, 0, rows, K, x)
         assert qk.device_error() == 6
     finally:
-        qk.debug_skip_tile(-1)
+        qk.debug_skip_item(-1)
         qk.set_wait_limit_ns(old)
     assert qk.device_error() == 0
     y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
