@@ -35,13 +35,8 @@ DevInfo dev_info()
 
 int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
 
-// Ring-kernel plan: team width SW, lane units per lane per item (cpl), K
-// chunks and ring depth.  Among the powers of two SW, the one that keeps the
-// most lanes busy (lane units per row over chunks of SW*cpl units, times the
-// share of the consumer warps that get a row group at all); among equals the
-// one giving a lane more units per item, then the wider team (fewer copies
-// per item).  A row group split into K chunks is copied one
-// row at a time, so at most 8 rows per item are allowed then.
+// GEMV plan: team width SW, lane units per lane per item (cpl), K chunks,
+// consumer warps, stages per warp and the shared-memory layout.
 bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, GemvPlan *p)
 {
     const int UC = fmt == kFmtQ4K ? 128 : 32;
@@ -69,8 +64,14 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
 
     int64_t grid = di.sms;
     if (grid > rows) grid = rows;
-    const int64_t rows_per_cta = rows / grid;
     const int NW = gemv_warps(fmt, batch);
+    // The way a row is cut into lanes and K chunks fixes the order of its
+    // additions, so it depends on K (and the format and batch) only: the
+    // rows of a call get the same bits as the same rows of a larger call.
+    // Most busy lanes first; among equals more units a lane, then the wider
+    // team (fewer copies).  A row group split into K chunks is copied one row
+    // at a time: at most 8 rows an item, and chunks of 2 KB or more are
+    // preferred.
     int best_sw = 0, best_nkc = 0, best_cpl = 0;
     double best_util = -1.0;
     for (int sw = 32; sw >= 1; sw >>= 1) {
@@ -78,10 +79,8 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
         const int nkc = (LU + sw * cpl - 1) / (sw * cpl);
         const int rows_w = (32 / sw) * R;
         if (nkc > 1 && rows_w > 8) continue;
-        // busy lanes, times the share of warps that get a row group
-        const double groups = static_cast<double>((rows_per_cta + rows_w - 1) / rows_w);
-        const double util = static_cast<double>(LU) / (static_cast<double>(nkc) * sw * cpl) *
-                            std::min(1.0, groups / NW);
+        double util = static_cast<double>(LU) / (static_cast<double>(nkc) * sw * cpl);
+        if (nkc > 1 && static_cast<int64_t>(sw) * cpl * UB < 2048) util *= 0.85;
         if (util > best_util + 1e-9 || (util > best_util - 1e-9 && cpl > best_cpl)) {
             best_util = util;
             best_sw = sw;

@@ -82,6 +82,9 @@ def test_gemv_bit_exact_when_sums_are_exact(qk, orc, fmt, K, batch):
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
 def test_row_ranges_equal_fused_call(qk, fmt):
     """Row ranges 4096/1024/1024 of a fused qkv tensor give the same bits as one call."""
+    K0 = 4096 if fmt == "q4_k" else 896
+    plans = [qk.debug_gemv_plan(fmt, n, K0, 1) for n in (6144, 4096, 1024)]
+    assert len({(p["SW"], p["nkc"], p["cpl"]) for p in plans}) == 1   # the row's cut depends on K only
     K = 4096 if fmt == "q4_k" else 896
     wq = synth.weights(fmt, 6144, K, seed=3)
     x = synth.activations(1, K, seed=3)
