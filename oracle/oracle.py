@@ -83,6 +83,8 @@ def _bind(lib):
     lib.qko_gemv.argtypes = [ctypes.c_int, P, I64, P, I64, P, I64, P, P]
     lib.qko_gemv.restype = ctypes.c_int
     lib.qko_gemm_bf16.argtypes = [ctypes.c_int, P, I64, P, I64, P, I64, P, P]
+    lib.qko_swiglu.argtypes = [ctypes.c_int, P, I64, P, P, I64, P, I64, P, P, P, P, P]
+    lib.qko_swiglu.restype = ctypes.c_int
     lib.qko_gemm_bf16.restype = ctypes.c_int
     lib.qko_quantise_q8_0_row.argtypes = [P, I64, P]
     lib.qko_quantise_q8_0_row.restype = None
@@ -150,6 +152,24 @@ def gemv(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, rows=None, lib=None):
                                     _ptr(y), _ptr(s))
     assert rc == 0
     return y, s
+
+
+def swiglu(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, gate_rows, up_rows, lib=None):
+    """(h, g, u, Sg, Su), all f64 [batch][n]: g and u the matvecs of the gate and
+    up rows, h = silu(g) * u with silu(z) = z / (1 + e^-z)."""
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    assert x.shape[1] == K
+    nr = wq.size // row_bytes(fmt, K)
+    gr = _rows_arg(gate_rows, nr)
+    ur = _rows_arg(up_rows, nr)
+    assert gr.size == ur.size
+    B, n = x.shape[0], gr.size
+    out = [np.empty((B, n), dtype=np.float64) for _ in range(5)]
+    rc = (lib or _load()).qko_swiglu(FMT[fmt], _ptr(wq), K, _ptr(gr), _ptr(ur), n, _ptr(x), B,
+                                     *[_ptr(o) for o in out])
+    assert rc == 0
+    return tuple(out)
 
 
 def gemm_bf16(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, rows=None, lib=None):

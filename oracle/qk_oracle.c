@@ -209,6 +209,31 @@ int qko_gemv(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows, int64_t
 }
 
 /*
+ * Fused gate/up matvec with the SwiGLU product -- the decode FFN of the llama
+ * shape, "RMSNorm -> GQA attention ... -> SwiGLU FFN" (nurllama README,
+ * "What it runs"); silumul computes g <- silu(g) * u (nurllama 0.18.1 API
+ * reference, kernels.nu `lk_silumul`, beside `lk_gelumul`), and the matvecs
+ * "with fused SwiGLU" (loom-port-llm SKILL.md, "Kernel inventory") fold it
+ * into the gate/up matvec; gate and up may be row ranges of one tensor (the
+ * phi3 ffn_up).  For p < n:
+ *   g[b][p] = sum_c W[gate_rows[p]][c] x[b][c]
+ *   u[b][p] = sum_c W[up_rows[p]][c]   x[b][c]
+ *   h[b][p] = silu(g) * u,   silu(z) = z / (1 + e^-z)   (all f64)
+ * g, u and their magnitude sums sg, su (layout [batch][n]) are returned for
+ * the error bound.
+ */
+int qko_swiglu(int fmt, const uint8_t *wq, int64_t K, const int64_t *gate_rows, const int64_t *up_rows,
+               int64_t n, const float *x, int64_t batch, double *h, double *g, double *u, double *sg, double *su)
+{
+    int rc = qko_gemv(fmt, wq, K, gate_rows, n, x, batch, g, sg);
+    if (rc) return rc;
+    rc = qko_gemv(fmt, wq, K, up_rows, n, x, batch, u, su);
+    if (rc) return rc;
+    for (int64_t i = 0; i < batch * n; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+    return 0;
+}
+
+/*
  * bf16 reference of the prefill GEMM: each weight is rounded to fp32 and then
  * to bf16, each activation to bf16 (both round-to-nearest-even), and the
  * products are summed in f64 in natural order.  Layout as qko_gemv with

@@ -7,7 +7,9 @@
   closed forms, exact integer arithmetic and a BLAS matmul;
 * the encoders against their error bounds and nearest-value property;
 * the bf16 GEMM reference against torch's bf16 rounding and against the
-  exact reference on bf16-exact inputs.
+  exact reference on bf16-exact inputs;
+* the SwiGLU product against known values of silu, its odd-part identity
+  silu(z) - silu(-z) = z, and its limits.
 """
 from fractions import Fraction
 
@@ -246,3 +248,49 @@ def test_gemm_bf16_reference_exact_on_bf16_inputs(orc):
     assert rows_exact[:3].all() and not rows_exact[3]     # 981 needs 10 significant bits
     assert np.array_equal(y1[:, :3], y2[:, :3])
     assert not np.array_equal(y1[:, 3], y2[:, 3])
+
+
+# ------------------------------------------------------------ SwiGLU
+
+def _unit_rows_q8_0(n_rows: int) -> np.ndarray:
+    """Q8_0 rows of one block (K = 32), row i = the unit vector e_i (d = 1, q_i = 1)."""
+    rec = np.zeros(n_rows, dtype=synth.Q8_0_DTYPE)
+    rec["d"] = np.float16(1.0)
+    for i in range(n_rows):
+        rec["qs"][i, i] = 1
+    return rec.view(np.uint8).copy()
+
+
+def _swiglu_of(orc, z: float, v: float) -> float:
+    """h for gate value z and up value v: gate row e_0, up row e_1, x = (z, v, 0...)."""
+    wq = _unit_rows_q8_0(2)
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 1] = z, v
+    h, g, u, sg, su = orc.swiglu("q8_0", wq, 32, x, [0], [1])
+    assert g[0, 0] == np.float32(z) and u[0, 0] == np.float32(v)
+    return float(h[0, 0])
+
+
+def test_swiglu_known_values(orc):
+    """silu(ln 3) = (3/4) ln 3; silu(0) = 0; silu(z) -> z for large z and -> 0 for very negative z."""
+    ln3 = float(np.float32(np.log(3.0)))
+    assert abs(_swiglu_of(orc, ln3, 2.0) - 2.0 * 0.75 * 1.0986122886681098) < 3e-7
+    assert _swiglu_of(orc, 0.0, 5.0) == 0.0
+    assert abs(_swiglu_of(orc, 40.0, 1.5) - 60.0) < 1e-12
+    assert abs(_swiglu_of(orc, -50.0, 3.0)) < 1e-18           # the gate, not the up value, goes through silu
+
+
+@pytest.mark.parametrize("z", [0.3, 1.75, 5.5, 12.0])
+def test_swiglu_odd_part_identity(orc, z):
+    """sigma(z) + sigma(-z) = 1 makes silu(z) - silu(-z) = z."""
+    assert abs((_swiglu_of(orc, z, 1.0) - _swiglu_of(orc, -z, 1.0)) - np.float32(z)) < 1e-14 * (1 + z)
+
+
+def test_swiglu_uses_the_given_rows(orc):
+    """h[b][p] pairs gate row gate_rows[p] with up row up_rows[p], for every batch row."""
+    wq = _unit_rows_q8_0(4)
+    x = synth.activations(3, 32, seed=9)
+    h, g, u, _, _ = orc.swiglu("q8_0", wq, 32, x, [2, 0], [1, 3])
+    assert np.array_equal(g, x[:, [2, 0]].astype(np.float64))
+    assert np.array_equal(u, x[:, [1, 3]].astype(np.float64))
+    assert np.all(np.abs(h) <= np.abs(g * u) + 1e-300)       # |silu(z)| <= |z|

@@ -34,6 +34,9 @@ MUTATIONS = {
     "gemm_skips_w_rounding": ("w[c] = qko_bf16_to_f64(qko_f32_to_bf16((float)w[c]));", "w[c] = (double)(float)w[c];"),
     "q8_encode_no_clamp_sign": ("if (q < -127.0) q = -127.0;", "if (q < -127.0) q = 127.0;"),
     "q4_encode_high_nibble": ("(uint8_t)(best << 4);", "(uint8_t)(best << 3);"),
+    "swiglu_gate_up_swapped": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = u[i] / (1.0 + exp(-u[i])) * g[i];"),
+    "silu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+    "silu_missing_z": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = 1.0 / (1.0 + exp(-g[i])) * u[i];"),
 }
 
 PINS = [
@@ -52,6 +55,8 @@ PINS = [
     (pins.test_q4_k_roundtrip_bound, {}),
     (pins.test_gemm_bf16_reference_matches_torch_rounding, {}),
     (pins.test_gemm_bf16_reference_exact_on_bf16_inputs, {}),
+    (pins.test_swiglu_known_values, {}),
+    (pins.test_swiglu_odd_part_identity, {"z": 1.75}),
 ]
 
 
