@@ -476,7 +476,31 @@ def measure_extra_rows(torch, qk, synth, device, stream):
                       "includes": "x->bf16 pre-pass + tcgen05 GEMM"}
         del ws
 
+    def swiglu_row(label, fmt, F, K, batch, seed, copies):
+        """Fused gate+up tensor [2F][K] (gate rows 0..F-1, up rows F..2F-1)."""
+        rb = qk.row_bytes(fmt, K)
+        ws = [torch.from_numpy(synth.weights(fmt, 2 * F, K, seed=seed, stream0=50 * c)).to(device)
+              for c in range(copies)]
+        x = torch.from_numpy(synth.activations(batch, K, seed=seed)).to(device)
+        h = torch.empty((batch, F), device=device)
+        fn = lib.qmatvec_swiglu_q8_0 if fmt == "q8_0" else lib.qmatvec_swiglu_q4_k
+
+        def mk(w):
+            def f(sh):
+                st = fn(w.data_ptr(), 0, F, F, K, x.data_ptr(), batch, h.data_ptr(), F, sh)
+                assert st == 0
+            return f
+        fns = [mk(w) for w in ws] * max(1, 8 // len(ws))
+        avg_ms = time_calls(torch, stream, fns, 20)
+        b = 2 * F * rb + batch * K * 4 + batch * F * 4
+        out[label] = {"bytes": b, "avg_us": round(avg_ms * 1e3, 2),
+                      "GB/s": round(b / (avg_ms * 1e-3) / 1e9, 1),
+                      "cache": "cold (rotated copies > L2)" if copies * 2 * F * rb > l2 else "hot (L2-resident)",
+                      "computes": "h = silu(W_gate x) * (W_up x), one launch"}
+        del ws
+
     gemm_row("q4_k_gemm_512x4096x14336", 512, 14336, 4096, 4, 2)
+    swiglu_row("q4_k_swiglu_llama8b_ffn_14336x4096_b1", "q4_k", 14336, 4096, 1, 2, 4)
     gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1)
     gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1)
     gemv_row("q8_0_lm_head_151936x896_b1", "q8_0", 151936, 896, 1, 3, 3)

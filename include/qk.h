@@ -94,6 +94,32 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
                  const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
 
 /*
+ * Fused gate/up GEMV with the SwiGLU product, batch 1..8:
+ *   g = sum_{c<K} W[gate_offset + p][c] * x[b*K + c]
+ *   u = sum_{c<K} W[up_offset + p][c]   * x[b*K + c]
+ *   h[b*ldh + p] = silu(g) * u,   silu(z) = z / (1 + e^-z),   for p < F.
+ * The llama FFN "SwiGLU" (nurllama README, "What it runs") as silumul
+ * g <- silu(g) * u (nurllama 0.18.1 API reference, kernels.nu `lk_silumul`),
+ * folded into the matvec as in loom's "matvecs ... with fused SwiGLU"
+ * (loom-port-llm SKILL.md, "Kernel inventory").  Gate and up rows may be row
+ * ranges of one fused tensor (phi3's ffn_up: gate_offset 0, up_offset F;
+ * nurllama README, "What it runs"), or of two tensors passed as one
+ * allocation with the offsets between them.
+ *   w            device block bytes holding both row ranges; alignment as the
+ *                plain GEMV of the format (Q8_0 2 bytes, Q4_K 16 bytes).
+ *   gate_offset, up_offset  first gate / up row (>= 0), in rows of K columns.
+ *   x            device fp32 [batch][K];  h  device fp32 [batch][ldh], ldh == 0
+ *                means ldh = F; only h[b*ldh + p] for p < F is written.
+ * g and u are computed exactly as the plain GEMV's rows (same error bound,
+ * 1e-5 * sum|w*x| + 1e-6 each); silu uses CUDA's expf.  Errors: as the plain
+ * GEMV; a negative up_offset is QK_ERR_BAD_DIM.
+ */
+int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
+                        const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
+int qmatvec_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
+                        const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
+
+/*
  * Q4_K prefill GEMM on the tensor cores:
  *   y[m*ldy + n] = sum_{c<K} bf16(W[row_offset + n][c]) * bf16(x[m*K + c])
  * for m < M tokens and n < N weight rows, accumulated in fp32.  Each weight

@@ -38,8 +38,10 @@ int *error_word_ptr()
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t K,
-               const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream)
+               const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream,
+               int64_t up_offset = -1)
 {
+    const bool pair = up_offset >= 0;
     if (!w || !x || !y) return QK_ERR_NULL;
     if (rows <= 0 || K <= 0 || row_offset < 0) return QK_ERR_BAD_DIM;
     if (batch < 1 || batch > QK_MAX_BATCH) return QK_ERR_BATCH;
@@ -48,19 +50,21 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4))
         return QK_ERR_ALIGN;
     qk::GemvPlan plan;
-    if (!qk::gemv_plan(fmt, rows, K, batch, &plan)) {
+    if (!qk::gemv_plan(fmt, rows, K, batch, pair, &plan)) {
         // either no usable device or the activations do not fit in shared memory
         int dev_count = 0;
         if (cudaGetDeviceCount(&dev_count) != cudaSuccess || dev_count == 0) return QK_ERR_CUDA;
         return QK_ERR_TOO_LARGE;
     }
-    if (row_offset > (INT64_MAX / plan.row_bytes) - rows) return QK_ERR_BAD_DIM;
+    const int64_t last = pair ? (row_offset > up_offset ? row_offset : up_offset) : row_offset;
+    if (last > (INT64_MAX / plan.row_bytes) - rows) return QK_ERR_BAD_DIM;
     int *err = error_word_ptr();
     if (!err) return QK_ERR_CUDA;
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * plan.row_bytes;
     cudaError_t e = qk::gemv_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
                                     reinterpret_cast<cudaStream_t>(stream), plan, err,
-                                    g_wait_limit_ns.load(), g_skip_item.load(), g_programmatic.load() != 0);
+                                    g_wait_limit_ns.load(), g_skip_item.load(), g_programmatic.load() != 0,
+                                    pair ? up_offset - row_offset : 0);
     return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
 }
 
@@ -115,6 +119,20 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K, con
                  int batch, float *y, int64_t ldy, qk_stream_t stream)
 {
     return gemv_entry(qk::kFmtQ4K, w, row_offset, rows, K, x, batch, y, ldy, stream);
+}
+
+int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
+                        const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream)
+{
+    if (up_offset < 0) return QK_ERR_BAD_DIM;
+    return gemv_entry(qk::kFmtQ80, w, gate_offset, F, K, x, batch, h, ldh, stream, up_offset);
+}
+
+int qmatvec_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
+                        const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream)
+{
+    if (up_offset < 0) return QK_ERR_BAD_DIM;
+    return gemv_entry(qk::kFmtQ4K, w, gate_offset, F, K, x, batch, h, ldh, stream, up_offset);
 }
 
 int64_t qk_row_bytes_q8_0(int64_t K) { return K <= 0 ? 0 : ((K + 31) / 32) * 34; }
@@ -173,7 +191,7 @@ int64_t qk_debug_skip_item(int64_t item) { return g_skip_item.exchange(item); }
 int qk_debug_gemv_plan(int fmt, int64_t rows, int64_t K, int batch, int64_t *out, int n)
 {
     qk::GemvPlan p;
-    if (!out || !qk::gemv_plan(fmt, rows, K, batch, &p)) return -1;
+    if (!out || !qk::gemv_plan(fmt, rows, K, batch, false, &p)) return -1;
     const int64_t v[12] = {p.SW, p.R, p.nkc, p.rows_w, p.stages, p.stage_bytes, p.smem, p.grid, p.XU, p.cpl, p.nw, p.m};
     int k = 0;
     for (; k < n && k < 12; ++k) out[k] = v[k];

@@ -37,7 +37,7 @@ int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
 
 // GEMV plan: team width SW, lane units per lane per item (cpl), K chunks,
 // consumer warps, stages per warp and the shared-memory layout.
-bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &di, GemvPlan *p)
+bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, const DevInfo &di, GemvPlan *p)
 {
     const int UC = fmt == kFmtQ4K ? 128 : 32;
     const int UB = fmt == kFmtQ4K ? 144 : 34;
@@ -79,6 +79,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
         const int nkc = (LU + sw * cpl - 1) / (sw * cpl);
         const int rows_w = (32 / sw) * R;
         if (nkc > 1 && rows_w > 8) continue;
+        if (pair && sw == 32 && R % 2) continue;    // a gate row and its up row must share a lane or a team pair
         double util = static_cast<double>(LU) / (static_cast<double>(nkc) * sw * cpl);
         if (nkc > 1 && static_cast<int64_t>(sw) * cpl * UB < 2048) util *= 0.85;
         if (util > best_util + 1e-9 || (util > best_util - 1e-9 && cpl > best_cpl)) {
@@ -91,9 +92,15 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
     if (best_sw == 0) return false;
     const int SW = best_sw, nkc = best_nkc, cpl = best_cpl;
     const int rows_w = (32 / SW) * R;
-    int64_t chunk_bytes = 0, row_stride = 0, stage;
+    const int gr = pair ? rows_w / 2 : rows_w;     // output rows per row group
+    int64_t chunk_bytes = 0, row_stride = 0, stage, up_stage_off = 0;
     if (nkc == 1) {
-        stage = round_up(rows_w * row_bytes + 32, 128);
+        if (pair) {
+            up_stage_off = round_up(gr * row_bytes + 32, 16);
+            stage = round_up(up_stage_off + gr * row_bytes + 32, 128);
+        } else {
+            stage = round_up(rows_w * row_bytes + 32, 128);
+        }
     } else {
         chunk_bytes = static_cast<int64_t>(SW) * cpl * UB;
         // a Q8_0 chunk is widened to 16-byte boundaries and its last block
@@ -109,7 +116,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
     // stages a warp where the ring holds that many (a warp then has an item
     // in flight while it works on another), else one
     const int64_t rows_cta_max = (rows + grid - 1) / grid;
-    int64_t nw = std::min<int64_t>(NW, (rows_cta_max + rows_w - 1) / rows_w);
+    int64_t nw = std::min<int64_t>(NW, (rows_cta_max + gr - 1) / gr);
     nw = std::min(nw, stages);
     if (stages / nw < 2 && stages >= 2 * std::min<int64_t>(nw, 8)) nw = std::min<int64_t>(nw, stages / 2);
     const int64_t m = stages / nw;
@@ -132,6 +139,8 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
     p->cpl = cpl;
     p->nkc = nkc;
     p->rows_w = rows_w;
+    p->pair = pair ? 1 : 0;
+    p->up_stage_off = static_cast<int>(up_stage_off);
     p->chunk_bytes = static_cast<int>(chunk_bytes);
     p->row_stride = static_cast<int>(row_stride);
     p->row_bytes = row_bytes;
@@ -141,16 +150,16 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, const DevInfo &d
 }  // namespace
 
 // Launch plan of a GEMV call; returns false if it cannot fit in shared memory.
-bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p)
+bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p)
 {
     const DevInfo di = dev_info();
     if (di.sms <= 0) return false;
-    return gemv_plan_for(fmt, rows, K, batch, di, p);
+    return gemv_plan_for(fmt, rows, K, batch, pair, di, p);
 }
 
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl)
+                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows)
 {
     if (p.R != gemv_rows(fmt, batch)) return cudaErrorInvalidValue;
     GemvArgs r;
@@ -179,6 +188,9 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.off_xsum = p.off_xsum;
     r.off_xscale = p.off_xscale;
     r.off_stage = p.off_stage;
+    r.pair = p.pair;
+    r.up_rows = up_rows;
+    r.up_stage_off = p.up_stage_off;
     r.skip_item = skip_item;
     r.wait_ns = wait_ns;
     r.err = err;

@@ -67,6 +67,9 @@ __device__ __forceinline__ int q4k_nibble_shift(int c)
 // their group's largest magnitude are represented exactly; the error of any
 // other value is below 2^-31 of that magnitude.
 
+// SwiGLU's gate: silu(z) = z / (1 + e^-z), with CUDA's expf.
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
 // sum(q*m) of one group from its four plane sums, as a float.
 __device__ __forceinline__ float planes_to_float(int s0, int s1, int s2, int s3)
 {
@@ -97,6 +100,9 @@ struct GemvArgs {
     int m;              // stages per consumer warp (stage w*m + t%m holds warp w's item t)
     int stage_bytes;
     int off_x, off_xsum, off_xscale, off_stage;
+    int pair;           // 1: output row p = silu(row p) * row (p + up_rows), both rows in one item
+    int64_t up_rows;    // pair mode: distance in rows from a gate row to its up row
+    int up_stage_off;   // pair mode, whole rows: stage offset of the up rows' span
     int64_t skip_item;  // test hook: in CTA 0 warp 0's item with this number is never copied (-1: none)
     uint64_t wait_ns;
     int *err;
@@ -520,6 +526,60 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, int cwarp, int lane, 
 
 // -------------------------------------------------------------------------- kernel
 
+// Copy the item of rows [row0, row0+n) (pair mode: n gate rows and their n up
+// rows), K chunk c, into the stage at `dst`; completion on `bar`.  Whole rows
+// are contiguous: one 1-D bulk copy per span (the up span at up_stage_off),
+// else one per row (row lr at lr*row_stride; pair mode: up row lr at
+// (rows_w/2 + lr)*row_stride).  Spans are widened to 16-byte boundaries; a
+// 16-byte granule holding a byte of the tensor never crosses a page, so the
+// widened copy stays in mapped memory.
+__device__ __forceinline__ uint32_t span16(uintptr_t gs, uintptr_t ge)
+{
+    return static_cast<uint32_t>(((ge + 15) & ~static_cast<uintptr_t>(15)) - (gs & ~static_cast<uintptr_t>(15)));
+}
+
+__device__ __forceinline__ void copy_item(const GemvArgs &a, int64_t row0, int n, uint32_t c, uint32_t dst,
+                                          uint32_t bar, uint64_t pol)
+{
+    const uint8_t *g0 = a.w + row0 * a.row_bytes;
+    const uint8_t *u0 = a.pair ? g0 + a.up_rows * a.row_bytes : nullptr;
+    if (a.nkc == 1) {
+        const uintptr_t gs = reinterpret_cast<uintptr_t>(g0), ge = gs + static_cast<uintptr_t>(n * a.row_bytes);
+        uint32_t bytes = span16(gs, ge);
+        uint32_t ubytes = 0;
+        uintptr_t us = 0;
+        if (a.pair) {
+            us = reinterpret_cast<uintptr_t>(u0);
+            ubytes = span16(us, us + static_cast<uintptr_t>(n * a.row_bytes));
+        }
+        mbar_arrive_expect_tx(bar, bytes + ubytes);
+        bulk_g2s(dst, reinterpret_cast<const void *>(gs & ~static_cast<uintptr_t>(15)), bytes, bar, pol);
+        if (a.pair)
+            bulk_g2s(dst + static_cast<uint32_t>(a.up_stage_off),
+                     reinterpret_cast<const void *>(us & ~static_cast<uintptr_t>(15)), ubytes, bar, pol);
+        return;
+    }
+    const int64_t cb = static_cast<int64_t>(c) * a.chunk_bytes;
+    const int64_t cl = min(static_cast<int64_t>(a.chunk_bytes), a.row_bytes - cb);
+    const int spans = a.pair ? 2 : 1;
+    const int P = a.rows_w >> 1;
+    uint32_t total = 0;
+    for (int h = 0; h < spans; ++h)
+        for (int q = 0; q < n; ++q) {
+            const uintptr_t gs = reinterpret_cast<uintptr_t>((h ? u0 : g0) + q * a.row_bytes + cb);
+            total += span16(gs, gs + static_cast<uintptr_t>(cl));
+        }
+    mbar_arrive_expect_tx(bar, total);
+    for (int h = 0; h < spans; ++h)
+        for (int q = 0; q < n; ++q) {
+            const uintptr_t gs = reinterpret_cast<uintptr_t>((h ? u0 : g0) + q * a.row_bytes + cb);
+            const int lr = h ? P + q : q;
+            bulk_g2s(dst + static_cast<uint32_t>(lr * a.row_stride),
+                     reinterpret_cast<const void *>(gs & ~static_cast<uintptr_t>(15)),
+                     span16(gs, gs + static_cast<uintptr_t>(cl)), bar, pol);
+        }
+}
+
 template <int FMT, int B, int US>
 __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(const GemvArgs a)
 {
@@ -539,7 +599,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     const int64_t nG = gridDim.x;
     const int64_t r_begin = (a.rows * blockIdx.x) / nG;
     const int64_t r_end = (a.rows * (blockIdx.x + 1)) / nG;
-    const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + a.rows_w - 1) / a.rows_w);
+    const int gr = a.pair ? (a.rows_w >> 1) : a.rows_w;   // output rows per row group
+    const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + gr - 1) / gr);
     const uint32_t nkc = static_cast<uint32_t>(a.nkc);
 
     // programmatic dependent launch: the next grid in the stream may start
@@ -568,9 +629,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
             bool ok = true;
             uint32_t t = 0, tm = 0, use = 0;                 // item number, its stage offset and use
             for (uint32_t g = w; ok && g < n_groups; g += nw) {
-                const int64_t row0 = r_begin + static_cast<int64_t>(g) * a.rows_w;
-                const int n = static_cast<int>(min(static_cast<int64_t>(a.rows_w), r_end - row0));
-                const uint8_t *src0 = a.w + row0 * a.row_bytes;
+                const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
+                const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
                 for (uint32_t c = 0; c < nkc; ++c, ++t) {
                     const uint32_t st = w * m + tm;
                     const uint32_t bar = bar_full + 8u * st;
@@ -580,33 +640,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                     }
                     const bool skip = w == 0 && t == a.skip_item && blockIdx.x == 0;   // test hook
                     if (!skip) {
-                        const uint32_t dst = stage0 + st * static_cast<uint32_t>(a.stage_bytes);
-                        if (nkc == 1) {
-                            const uintptr_t gs = reinterpret_cast<uintptr_t>(src0);
-                            const uintptr_t ge = gs + static_cast<uintptr_t>(n * a.row_bytes);
-                            const uintptr_t lo = gs & ~static_cast<uintptr_t>(15);
-                            const uint32_t bytes =
-                                static_cast<uint32_t>(((ge + 15) & ~static_cast<uintptr_t>(15)) - lo);
-                            mbar_arrive_expect_tx(bar, bytes);
-                            bulk_g2s(dst, reinterpret_cast<const void *>(lo), bytes, bar, pol);
-                        } else {
-                            const int64_t cb = static_cast<int64_t>(c) * a.chunk_bytes;
-                            const int64_t cl = min(static_cast<int64_t>(a.chunk_bytes), a.row_bytes - cb);
-                            uint32_t total = 0;
-                            for (int q = 0; q < n; ++q) {
-                                const uintptr_t gs = reinterpret_cast<uintptr_t>(src0 + q * a.row_bytes + cb);
-                                total += static_cast<uint32_t>(((gs + cl + 15) & ~static_cast<uintptr_t>(15)) -
-                                                               (gs & ~static_cast<uintptr_t>(15)));
-                            }
-                            mbar_arrive_expect_tx(bar, total);
-                            for (int q = 0; q < n; ++q) {
-                                const uintptr_t gs = reinterpret_cast<uintptr_t>(src0 + q * a.row_bytes + cb);
-                                const uintptr_t lo = gs & ~static_cast<uintptr_t>(15);
-                                const uintptr_t hi = (gs + cl + 15) & ~static_cast<uintptr_t>(15);
-                                bulk_g2s(dst + static_cast<uint32_t>(q * a.row_stride),
-                                         reinterpret_cast<const void *>(lo), static_cast<uint32_t>(hi - lo), bar, pol);
-                            }
-                        }
+                        copy_item(a, row0, n, c, stage0 + st * static_cast<uint32_t>(a.stage_bytes), bar, pol);
                         issued_use[st] = static_cast<int>(use);
                     }
                     if (++tm == m) {
@@ -657,8 +691,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
     bool failed = false;
     for (uint32_t g = cwarp; g < n_groups && !failed; g += nw) {
-        const int64_t row0 = r_begin + static_cast<int64_t>(g) * a.rows_w;
-        const int n = static_cast<int>(min(static_cast<int64_t>(a.rows_w), r_end - row0));
+        const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
+        const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
         float acc[R][B];
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -679,15 +713,20 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
             const uint8_t *stage = smem + a.off_stage + st * static_cast<uint32_t>(a.stage_bytes);
             // where this lane's rows start their chunk in the stage (rows past
             // the group's end read its last row and are not stored)
+            // (pair mode: the item's rows lr < P are gate rows, the rest their up rows)
             const uint8_t *rowp[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int lr = min(team * R + r, n - 1);
+                int lr = team * R + r;
+                const bool up = a.pair && lr >= gr;
+                const int q = min(up ? lr - gr : lr, n - 1);      // output row within the group
+                const int64_t grow = row0 + q + (up ? a.up_rows : 0);   // weight row
                 if (nkc == 1) {
-                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>(row0 * a.row_bytes);
-                    rowp[r] = stage + (gsrc & 15u) + static_cast<int64_t>(lr) * a.row_bytes;
+                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>((row0 + (up ? a.up_rows : 0)) * a.row_bytes);
+                    rowp[r] = stage + (up ? a.up_stage_off : 0) + (gsrc & 15u) + static_cast<int64_t>(q) * a.row_bytes;
                 } else {
-                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>((row0 + lr) * a.row_bytes) +
+                    lr = up ? gr + q : q;
+                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>(grow * a.row_bytes) +
                                            static_cast<uintptr_t>(c) * a.chunk_bytes;
                     rowp[r] = stage + lr * a.row_stride + (gsrc & 15u);
                 }
@@ -756,20 +795,47 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
             }
         }
         if (failed) break;
-        // sum over the SW lanes of each team; lane 0 of the team writes
+        // sum over the SW lanes of each team (every lane of the team gets it)
+        float v[R][B];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                float v = acc[r][b];
+                float t = acc[r][b];
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) {
-                    const float t = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                    if (o < SW) v += t;
+                    const float u = __shfl_xor_sync(0xFFFFFFFFu, t, o);
+                    if (o < SW) t += u;
                 }
-                const int lr = team * R + r;
-                if (sl == 0 && lr < n) a.y[b * a.ldy + row0 + lr] = v;
+                v[r][b] = t;
             }
+        if (!a.pair) {
+            // lane 0 of the team writes its rows
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const int lr = team * R + r;
+                    if (sl == 0 && lr < n) a.y[b * a.ldy + row0 + lr] = v[r][b];
+                }
+        } else if (SW == 32) {
+            // one team: rows r < R/2 are gate rows, r + R/2 their up rows
+#pragma unroll
+            for (int r = 0; r < R / 2; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b)
+                    if (sl == 0 && r < n) a.y[b * a.ldy + row0 + r] = silu(v[r][b]) * v[r + R / 2][b];
+        } else {
+            // teams t < T/2 hold gate rows, team t + T/2 (lanes + 16) the up rows
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const float u = __shfl_down_sync(0xFFFFFFFFu, v[r][b], 16);
+                    const int lr = team * R + r;
+                    if (lane < 16 && sl == 0 && lr < n) a.y[b * a.ldy + row0 + lr] = silu(v[r][b]) * u;
+                }
+        }
     }
 }
 

@@ -12,15 +12,16 @@ constexpr int kFmtQ4K = 1;
 // stage ring, shared-memory layout and grid.
 struct GemvPlan {
     int U, LU, XU, SW, R, cpl, nkc, rows_w, chunk_bytes, row_stride;
-    int nw, m, stages, stage_bytes;
+    int nw, m, stages, stage_bytes, pair, up_stage_off;
     int off_x, off_xsum, off_xscale, off_stage, smem, grid;
     int64_t row_bytes;
 };
 
-bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, GemvPlan *p);
+// pair: rows are output rows of the SwiGLU form (a gate row and an up row each).
+bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p);
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl);
+                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows = 0);
 
 // The device error word of the current device and the bound of device waits.
 int *library_error_word();

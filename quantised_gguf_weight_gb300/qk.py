@@ -23,7 +23,7 @@ STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 
           5: "QK_ERR_CUDA", 6: "QK_ERR_TIMEOUT", 7: "QK_ERR_WORKSPACE", 8: "QK_ERR_TOO_LARGE"}
 MAX_BATCH = 8
 
-EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
+EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
            "qgemm_q4_k_noalloc", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
            "qk_version"]
@@ -54,6 +54,10 @@ def load(path: str | None = None):
         for name in ("qmatvec_q8_0", "qmatvec_q4_k"):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P]
+            fn.restype = I
+        for name in ("qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k"):
+            fn = getattr(lib, name)
+            fn.argtypes = [P, I64, I64, I64, I64, P, I, P, I64, P]
             fn.restype = I
         lib.qgemm_q4_k.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
         lib.qgemm_q4_k.restype = I
@@ -123,6 +127,22 @@ def qmatvec_q4_k(w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.T
                  y: torch.Tensor | None = None, ldy: int = 0, stream=None) -> torch.Tensor:
     """y[b][r] = sum_c W[row_offset + r][c] x[b][c] for Q4_K block bytes `w` (uint8, device)."""
     return _qmatvec("qmatvec_q4_k", w, row_offset, rows, K, x, y, ldy, stream)
+
+
+def qmatvec_swiglu(fmt: str, w: torch.Tensor, gate_offset: int, up_offset: int, F: int, K: int,
+                   x: torch.Tensor, h: torch.Tensor | None = None, ldh: int = 0, stream=None) -> torch.Tensor:
+    """h[b][p] = silu(sum_c W[gate_offset+p][c] x[b][c]) * sum_c W[up_offset+p][c] x[b][c], p < F."""
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    batch = x.shape[0]
+    if h is None:
+        h = torch.empty((batch, F), dtype=torch.float32, device=x.device)
+        ldh = F
+    name = {"q8_0": "qmatvec_swiglu_q8_0", "q4_k": "qmatvec_swiglu_q4_k"}[fmt]
+    st = getattr(load(), name)(w.data_ptr(), gate_offset, up_offset, F, K, x.data_ptr(), batch, h.data_ptr(),
+                               ldh, _stream(stream))
+    _check(st, name)
+    return h
 
 
 def gemm_workspace_bytes(M: int, N: int, K: int) -> int:

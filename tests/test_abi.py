@@ -34,8 +34,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes", "qk_status_string",
-              "qk_device_error"):
+    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qgemm_q4_k",
+              "qgemm_q4_k_workspace_bytes", "qk_status_string", "qk_device_error"):
         assert n in names
 
 
@@ -85,6 +85,27 @@ def test_argument_validation_without_gpu(lib, name):
     assert call(w=FAKE + 1) == 3     # odd w
     if name == "qmatvec_q4_k":
         assert call(w=FAKE + 8) == 3  # Q4_K needs 16-byte aligned super-blocks
+
+
+@pytest.mark.parametrize("name", ["qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k"])
+def test_swiglu_argument_validation_without_gpu(lib, name):
+    f = getattr(lib, name)
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    ok_args = dict(w=FAKE, gate=0, up=16, F=16, K=256, x=FAKE, batch=1, h=FAKE, ldh=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return f(a["w"], a["gate"], a["up"], a["F"], a["K"], a["x"], a["batch"], a["h"], a["ldh"], None)
+
+    assert call(w=None) == 1
+    assert call(h=None) == 1
+    assert call(up=-1) == 2
+    assert call(gate=-1) == 2
+    assert call(F=0) == 2
+    assert call(ldh=8) == 2          # ldh < F
+    assert call(batch=9) == 4
+    assert call(x=FAKE + 2) == 3
 
 
 def test_wait_limit_roundtrip(lib):
