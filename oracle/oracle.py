@@ -84,6 +84,8 @@ def _bind(lib):
     lib.qko_gemv.restype = ctypes.c_int
     lib.qko_gemm_bf16.argtypes = [ctypes.c_int, P, I64, P, I64, P, I64, P, P]
     lib.qko_swiglu.argtypes = [ctypes.c_int, P, I64, P, P, I64, P, I64, P, P, P, P, P]
+    lib.qko_experts.argtypes = [ctypes.c_int, P, I64, I64, I64, P, I64, P, I64, P, P]
+    lib.qko_experts.restype = ctypes.c_int
     lib.qko_swiglu.restype = ctypes.c_int
     lib.qko_gemm_bf16.restype = ctypes.c_int
     lib.qko_quantise_q8_0_row.argtypes = [P, I64, P]
@@ -170,6 +172,23 @@ def swiglu(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, gate_rows, up_rows, 
                                      *[_ptr(o) for o in out])
     assert rc == 0
     return tuple(out)
+
+
+def experts(fmt: str, wq: np.ndarray, n_experts: int, rows: int, K: int, x: np.ndarray, xk: int,
+            expid, lib=None):
+    """(y, S), f64 [n_assign][rows]: y[a][r] = sum_c W[expid[a]*rows + r][c] x[a // xk][c]."""
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    assert x.shape[1] == K
+    ids = np.ascontiguousarray(expid, dtype=np.int32)
+    n = ids.size
+    assert x.shape[0] * xk >= n
+    y = np.empty((n, rows), dtype=np.float64)
+    s = np.empty((n, rows), dtype=np.float64)
+    rc = (lib or _load()).qko_experts(FMT[fmt], _ptr(wq), n_experts, rows, K, _ptr(x), xk, _ptr(ids), n,
+                                      _ptr(y), _ptr(s))
+    assert rc == 0, rc
+    return y, s
 
 
 def gemm_bf16(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, rows=None, lib=None):

@@ -209,6 +209,39 @@ int qko_gemv(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows, int64_t
 }
 
 /*
+ * Batched expert matvec: "one batched matvec over all n_assign expert
+ * assignments.  Output row a uses expert expid_dev[a] and input row a/xk of
+ * x" (nurllama 0.18.1 API reference, kernels.nu `lk_matvec_experts`), the
+ * experts of a projection living in one 3-D tensor [n_experts][rows][K]
+ * evaluated as row ranges (nurllama README, "What it runs", llada2).  For
+ * a < n_assign and r < rows:
+ *   y[a][r] = sum_c W[expid[a]*rows + r][c] * x[a / xk][c]     (f64)
+ * s[a][r] the magnitude sum.  Returns 3 if an expert id is out of range.
+ */
+int qko_experts(int fmt, const uint8_t *wq, int64_t n_experts, int64_t rows, int64_t K, const float *x,
+                int64_t xk, const int32_t *expid, int64_t n_assign, double *y, double *s)
+{
+    if (xk < 1) return 4;
+    int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)(rows > 0 ? rows : 1));
+    if (!idx) return 2;
+    for (int64_t a = 0; a < n_assign; ++a) {
+        const int64_t e = expid[a];
+        if (e < 0 || e >= n_experts) {
+            free(idx);
+            return 3;
+        }
+        for (int64_t r = 0; r < rows; ++r) idx[r] = e * rows + r;
+        const int rc = qko_gemv(fmt, wq, K, idx, rows, x + (a / xk) * K, 1, y + a * rows, s ? s + a * rows : NULL);
+        if (rc) {
+            free(idx);
+            return rc;
+        }
+    }
+    free(idx);
+    return 0;
+}
+
+/*
  * Fused gate/up matvec with the SwiGLU product -- the decode FFN of the llama
  * shape, "RMSNorm -> GQA attention ... -> SwiGLU FFN" (nurllama README,
  * "What it runs"); silumul computes g <- silu(g) * u (nurllama 0.18.1 API

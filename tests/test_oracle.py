@@ -9,7 +9,8 @@
 * the bf16 GEMM reference against torch's bf16 rounding and against the
   exact reference on bf16-exact inputs;
 * the SwiGLU product against known values of silu, its odd-part identity
-  silu(z) - silu(-z) = z, and its limits.
+  silu(z) - silu(-z) = z, and its limits;
+* the expert matvec against experts whose rows reveal their own index.
 """
 from fractions import Fraction
 
@@ -294,3 +295,27 @@ def test_swiglu_uses_the_given_rows(orc):
     assert np.array_equal(g, x[:, [2, 0]].astype(np.float64))
     assert np.array_equal(u, x[:, [1, 3]].astype(np.float64))
     assert np.all(np.abs(h) <= np.abs(g * u) + 1e-300)       # |silu(z)| <= |z|
+
+
+# ------------------------------------------------------------ experts
+
+def _tagged_experts_q8_0(n_experts: int, rows: int) -> np.ndarray:
+    """Q8_0 expert tensor [E][rows][32]: row r of expert e is (e + 1) * e_r."""
+    rec = np.zeros(n_experts * rows, dtype=synth.Q8_0_DTYPE)
+    for e in range(n_experts):
+        for r in range(rows):
+            rec["d"][e * rows + r] = np.float16(e + 1)
+            rec["qs"][e * rows + r, r] = 1
+    return rec.view(np.uint8).copy()
+
+
+@pytest.mark.parametrize("xk", [1, 2, 3])
+def test_experts_select_expert_and_input_row(orc, xk):
+    """y[a][r] = (expid[a] + 1) * x[a // xk][r]: the expert, its rows and the input row are the stated ones."""
+    E, rows, n = 5, 7, 6
+    wq = _tagged_experts_q8_0(E, rows)
+    ids = np.array([3, 0, 4, 4, 1, 2], np.int32)
+    x = synth.small_int_activations((n + xk - 1) // xk, 32, seed=3)
+    y, s = orc.experts("q8_0", wq, E, rows, 32, x, xk, ids)
+    for a in range(n):
+        assert np.array_equal(y[a], (ids[a] + 1) * x[a // xk, :rows].astype(np.float64))

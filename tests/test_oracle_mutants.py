@@ -36,6 +36,8 @@ MUTATIONS = {
     "q4_encode_high_nibble": ("(uint8_t)(best << 4);", "(uint8_t)(best << 3);"),
     "swiglu_gate_up_swapped": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = u[i] / (1.0 + exp(-u[i])) * g[i];"),
     "silu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+    "experts_input_row_mod": ("x + (a / xk) * K, 1, y + a * rows", "x + (a % xk) * K, 1, y + a * rows"),
+    "experts_ignores_id": ("idx[r] = e * rows + r;", "idx[r] = r;"),
     "silu_missing_z": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = 1.0 / (1.0 + exp(-g[i])) * u[i];"),
 }
 
@@ -57,6 +59,7 @@ PINS = [
     (pins.test_gemm_bf16_reference_exact_on_bf16_inputs, {}),
     (pins.test_swiglu_known_values, {}),
     (pins.test_swiglu_odd_part_identity, {"z": 1.75}),
+    (pins.test_experts_select_expert_and_input_row, {"xk": 2}),
 ]
 
 
