@@ -499,7 +499,32 @@ def measure_extra_rows(torch, qk, synth, device, stream):
                       "computes": "h = silu(W_gate x) * (W_up x), one launch"}
         del ws
 
+    def experts_row(label, fmt, E, rows, K, xk, n_assign, seed):
+        """One token's top-n_assign experts of a fused gate+up expert tensor [E][rows][K]."""
+        rb = qk.row_bytes(fmt, K)
+        w = torch.from_numpy(synth.weights(fmt, E * rows, K, seed=seed)).to(device)
+        x = torch.from_numpy(synth.activations((n_assign + xk - 1) // xk, K, seed=seed)).to(device)
+        y = torch.empty((n_assign, rows), device=device)
+        fn = lib.qmatvec_experts_q8_0 if fmt == "q8_0" else lib.qmatvec_experts_q4_k
+        # distinct expert sets per call, so consecutive calls read different weights
+        sets = [torch.from_numpy((np.arange(n_assign) * 7 + 13 * c) % E).to(torch.int32).to(device)
+                for c in range(8)]
+
+        def mk(ids):
+            def f(sh):
+                st = fn(w.data_ptr(), E, rows, K, x.data_ptr(), xk, ids.data_ptr(), n_assign, y.data_ptr(), rows, sh)
+                assert st == 0
+            return f
+        avg_ms = time_calls(torch, stream, [mk(i) for i in sets], 20)
+        b = n_assign * rows * rb + x.numel() * 4 + n_assign * rows * 4
+        out[label] = {"bytes": b, "avg_us": round(avg_ms * 1e3, 2),
+                      "GB/s": round(b / (avg_ms * 1e-3) / 1e9, 1),
+                      "cache": "cold (expert tensor > L2, 8 expert sets)" if E * rows * rb > l2 else "hot (L2-resident)",
+                      "computes": f"{n_assign} assignments x {rows} rows, expert ids from device memory"}
+        del w
+
     gemm_row("q4_k_gemm_512x4096x14336", 512, 14336, 4096, 4, 2)
+    experts_row("q4_k_experts_moe_top8_128x1536x2048", "q4_k", 128, 1536, 2048, 8, 8, 5)
     swiglu_row("q4_k_swiglu_llama8b_ffn_14336x4096_b1", "q4_k", 14336, 4096, 1, 2, 4)
     gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1)
     gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1)

@@ -64,7 +64,9 @@ typedef enum {
     QK_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed                     */
     QK_ERR_TIMEOUT = 6,     /* a bounded device wait ran out (from qk_device_error)     */
     QK_ERR_WORKSPACE = 7,   /* workspace NULL, misaligned or smaller than required      */
-    QK_ERR_TOO_LARGE = 8    /* a size exceeds what the kernels support (see each call)  */
+    QK_ERR_TOO_LARGE = 8,   /* a size exceeds what the kernels support (see each call)  */
+    QK_ERR_BAD_INDEX = 9    /* an index read from device memory was out of range        */
+                            /* (from qk_device_error; see qmatvec_experts_*)             */
 } qk_status;
 
 #define QK_MAX_BATCH 8
@@ -118,6 +120,32 @@ int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, i
                         const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
 int qmatvec_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
                         const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
+
+/*
+ * Batched expert GEMV over n_assign expert assignments:
+ *   y[a*ldy + r] = sum_{c<K} W[expert_ids[a]*rows + r][c] * x[(a / xk)*K + c]
+ * for a < n_assign and r < rows.  "One batched matvec over all n_assign
+ * expert assignments.  Output row a uses expert expid_dev[a] and input row
+ * a/xk of x" (nurllama 0.18.1 API reference, kernels.nu
+ * `lk_matvec_experts`); the experts of a projection live in one 3-D tensor
+ * [n_experts][rows][K] evaluated as row ranges (nurllama README, "What it
+ * runs", llada2).
+ *   w           device block bytes of the whole expert tensor (alignment as
+ *               the plain GEMV of the format).
+ *   x           device fp32 [ceil(n_assign / xk)][K]; xk >= 1 assignments per
+ *               input row (e.g. the experts chosen per token).
+ *   expert_ids  device int32 [n_assign], 4-byte aligned; it may be written by
+ *               the kernel just before this call on the same stream (the
+ *               kernel reads it after the previous kernel completes).
+ *   y           device fp32 [n_assign][ldy], ldy == 0 means ldy = rows.
+ * An id outside [0, n_experts) is not dereferenced: that assignment's rows
+ * are set to NaN and qk_device_error() reports QK_ERR_BAD_INDEX.  Error
+ * bound as the plain GEMV (1e-5 * sum|w*x| + 1e-6).
+ */
+int qmatvec_experts_q8_0(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                         const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream);
+int qmatvec_experts_q4_k(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                         const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream);
 
 /*
  * Q4_K prefill GEMM on the tensor cores:
@@ -177,8 +205,9 @@ const char *qk_status_string(int status);
 
 /*
  * Reads and clears the device error word of the current device after
- * synchronising `stream`: QK_OK, QK_ERR_TIMEOUT (a bounded wait ran out) or
- * QK_ERR_CUDA (the synchronisation itself failed).  Meant for tests and
+ * synchronising `stream`: QK_OK, QK_ERR_TIMEOUT (a bounded wait ran out),
+ * QK_ERR_BAD_INDEX (an expert id was out of range) or QK_ERR_CUDA (the
+ * synchronisation itself failed).  Meant for tests and
  * debugging; the compute calls never synchronise.
  */
 int qk_device_error(qk_stream_t stream);

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/qk.h"
+#include "qk_device.cuh"
 #include "qk_internal.h"
 
 namespace {
@@ -135,6 +136,50 @@ int qmatvec_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, i
     return gemv_entry(qk::kFmtQ4K, w, gate_offset, F, K, x, batch, h, ldh, stream, up_offset);
 }
 
+}  // extern "C"
+
+namespace {
+
+int experts_entry(int fmt, const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                  const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream)
+{
+    if (!w || !x || !y || !expert_ids) return QK_ERR_NULL;
+    if (n_experts <= 0 || rows <= 0 || K <= 0 || xk <= 0 || n_assign <= 0) return QK_ERR_BAD_DIM;
+    if (ldy == 0) ldy = rows;
+    if (ldy < rows) return QK_ERR_BAD_DIM;
+    if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4) || !aligned(expert_ids, 4))
+        return QK_ERR_ALIGN;
+    qk::GemvPlan plan;
+    if (!qk::gemv_plan(fmt, rows, K, 1, false, &plan, n_assign)) {
+        int dev_count = 0;
+        if (cudaGetDeviceCount(&dev_count) != cudaSuccess || dev_count == 0) return QK_ERR_CUDA;
+        return QK_ERR_TOO_LARGE;
+    }
+    if (n_experts > (INT64_MAX / plan.row_bytes) / rows) return QK_ERR_BAD_DIM;
+    int *err = error_word_ptr();
+    if (!err) return QK_ERR_CUDA;
+    cudaError_t e = qk::gemv_launch(fmt, static_cast<const uint8_t *>(w), rows, K, x, 1, y, ldy,
+                                    reinterpret_cast<cudaStream_t>(stream), plan, err, g_wait_limit_ns.load(),
+                                    g_skip_item.load(), g_programmatic.load() != 0, 0, expert_ids, n_experts, xk);
+    return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmatvec_experts_q8_0(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                         const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream)
+{
+    return experts_entry(qk::kFmtQ80, w, n_experts, rows, K, x, xk, expert_ids, n_assign, y, ldy, stream);
+}
+
+int qmatvec_experts_q4_k(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                         const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream)
+{
+    return experts_entry(qk::kFmtQ4K, w, n_experts, rows, K, x, xk, expert_ids, n_assign, y, ldy, stream);
+}
+
 int64_t qk_row_bytes_q8_0(int64_t K) { return K <= 0 ? 0 : ((K + 31) / 32) * 34; }
 int64_t qk_row_bytes_q4_k(int64_t K) { return K <= 0 ? 0 : ((K + 255) / 256) * 144; }
 
@@ -150,6 +195,7 @@ const char *qk_status_string(int status)
     case QK_ERR_TIMEOUT: return "a bounded device wait ran out";
     case QK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case QK_ERR_TOO_LARGE: return "size beyond what the kernels support";
+    case QK_ERR_BAD_INDEX: return "an index read from device memory was out of range";
     default: return "unknown status";
     }
 }
@@ -164,7 +210,7 @@ int qk_device_error(qk_stream_t stream)
     if (v) {
         const int zero = 0;
         if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QK_ERR_CUDA;
-        return QK_ERR_TIMEOUT;
+        return (v & qk::kErrBadIndex) ? QK_ERR_BAD_INDEX : QK_ERR_TIMEOUT;
     }
     return QK_OK;
 }

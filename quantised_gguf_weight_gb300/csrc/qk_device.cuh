@@ -13,7 +13,8 @@
 
 namespace qk {
 
-constexpr int kErrTimeout = 1;   // bit in the device error word
+constexpr int kErrTimeout = 1;   // bits in the device error word: a bounded wait ran out,
+constexpr int kErrBadIndex = 2;  // an index read from device memory was out of range
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

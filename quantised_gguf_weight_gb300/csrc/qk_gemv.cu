@@ -37,7 +37,8 @@ int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
 
 // GEMV plan: team width SW, lane units per lane per item (cpl), K chunks,
 // consumer warps, stages per warp and the shared-memory layout.
-bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, const DevInfo &di, GemvPlan *p)
+bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64_t n_assign, const DevInfo &di,
+                   GemvPlan *p)
 {
     const int UC = fmt == kFmtQ4K ? 128 : 32;
     const int UB = fmt == kFmtQ4K ? 144 : 34;
@@ -62,8 +63,14 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, const
     const int64_t budget = di.smem_optin;
     if (off_stage >= budget) return false;
 
-    int64_t grid = di.sms;
+    int64_t grid = di.sms, cpa = 0;
     if (grid > rows) grid = rows;
+    if (n_assign > 0) {
+        // experts mode: each CTA takes part of one assignment's rows
+        cpa = std::max<int64_t>(1, std::min<int64_t>(rows, di.sms / n_assign));
+        grid = n_assign * cpa;
+        if (grid > (1LL << 31) - 1) return false;
+    }
     const int NW = gemv_warps(fmt, batch);
     // The way a row is cut into lanes and K chunks fixes the order of its
     // additions, so it depends on K (and the format and batch) only: the
@@ -115,7 +122,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, const
     // consumer warps that get row groups, and stages per warp: two or more
     // stages a warp where the ring holds that many (a warp then has an item
     // in flight while it works on another), else one
-    const int64_t rows_cta_max = (rows + grid - 1) / grid;
+    const int64_t rows_cta_max = n_assign > 0 ? (rows + cpa - 1) / cpa : (rows + grid - 1) / grid;
     int64_t nw = std::min<int64_t>(NW, (rows_cta_max + gr - 1) / gr);
     nw = std::min(nw, stages);
     if (stages / nw < 2 && stages >= 2 * std::min<int64_t>(nw, 8)) nw = std::min<int64_t>(nw, stages / 2);
@@ -140,6 +147,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, const
     p->nkc = nkc;
     p->rows_w = rows_w;
     p->pair = pair ? 1 : 0;
+    p->cpa = static_cast<int>(cpa);
     p->up_stage_off = static_cast<int>(up_stage_off);
     p->chunk_bytes = static_cast<int>(chunk_bytes);
     p->row_stride = static_cast<int>(row_stride);
@@ -150,16 +158,17 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, const
 }  // namespace
 
 // Launch plan of a GEMV call; returns false if it cannot fit in shared memory.
-bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p)
+bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p, int64_t n_assign)
 {
     const DevInfo di = dev_info();
     if (di.sms <= 0) return false;
-    return gemv_plan_for(fmt, rows, K, batch, pair, di, p);
+    return gemv_plan_for(fmt, rows, K, batch, pair, n_assign, di, p);
 }
 
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows)
+                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows,
+                        const int32_t *expid, int64_t n_experts, int xk)
 {
     if (p.R != gemv_rows(fmt, batch)) return cudaErrorInvalidValue;
     GemvArgs r;
@@ -191,6 +200,10 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.pair = p.pair;
     r.up_rows = up_rows;
     r.up_stage_off = p.up_stage_off;
+    r.expid = expid;
+    r.n_experts = n_experts;
+    r.xk = xk;
+    r.cpa = p.cpa;
     r.skip_item = skip_item;
     r.wait_ns = wait_ns;
     r.err = err;

@@ -103,6 +103,10 @@ struct GemvArgs {
     int pair;           // 1: output row p = silu(row p) * row (p + up_rows), both rows in one item
     int64_t up_rows;    // pair mode: distance in rows from a gate row to its up row
     int up_stage_off;   // pair mode, whole rows: stage offset of the up rows' span
+    const int32_t *expid;  // experts mode (cpa > 0): expert of each assignment, device memory
+    int64_t n_experts;  // experts mode: experts in the tensor (rows of each: `rows`)
+    int xk;             // experts mode: assignments per input row of x
+    int cpa;            // experts mode: CTAs per assignment (0: plain mode)
     int64_t skip_item;  // test hook: in CTA 0 warp 0's item with this number is never copied (-1: none)
     uint64_t wait_ns;
     int *err;
@@ -425,7 +429,7 @@ __device__ __forceinline__ void q8_blk_fp(const uint32_t (&wv)[R][9], const uint
 // stores block-floating-point byte planes (one exponent per 32 columns),
 // batch >= 2 stores fp32 pre-multiplied by 2^-s for the Q4_K nibble position.
 template <int FMT, int B, int US>
-__device__ __forceinline__ void stage_x(const GemvArgs &a, int cwarp, int lane, int nthreads, uint32_t xs_addr,
+__device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int cwarp, int lane, int nthreads, uint32_t xs_addr,
                                              float *xsum, float *xscale)
 {
     constexpr int UC = FMT == kFmtQ4K ? 128 : 32;
@@ -434,10 +438,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, int cwarp, int lane, 
     const int XH = XU >> 1;
     const int K = static_cast<int>(a.K);
     const int g_total = a.U * G;
-    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15u) == 0);
+    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x0) & 15u) == 0);
     constexpr int UNR = 4;
     for (int b = 0; b < B; ++b) {
-        const float *xb = a.x + static_cast<int64_t>(b) * K;
+        const float *xb = x0 + static_cast<int64_t>(b) * K;
         for (int base = cwarp * 32; base < g_total; base += UNR * nthreads) {
             float4 v[UNR];
 #pragma unroll
@@ -538,10 +542,10 @@ __device__ __forceinline__ uint32_t span16(uintptr_t gs, uintptr_t ge)
     return static_cast<uint32_t>(((ge + 15) & ~static_cast<uintptr_t>(15)) - (gs & ~static_cast<uintptr_t>(15)));
 }
 
-__device__ __forceinline__ void copy_item(const GemvArgs &a, int64_t row0, int n, uint32_t c, uint32_t dst,
-                                          uint32_t bar, uint64_t pol)
+__device__ __forceinline__ void copy_item(const GemvArgs &a, const uint8_t *w0, int64_t row0, int n, uint32_t c,
+                                          uint32_t dst, uint32_t bar, uint64_t pol)
 {
-    const uint8_t *g0 = a.w + row0 * a.row_bytes;
+    const uint8_t *g0 = w0 + row0 * a.row_bytes;
     const uint8_t *u0 = a.pair ? g0 + a.up_rows * a.row_bytes : nullptr;
     if (a.nkc == 1) {
         const uintptr_t gs = reinterpret_cast<uintptr_t>(g0), ge = gs + static_cast<uintptr_t>(n * a.row_bytes);
@@ -596,9 +600,33 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 512);
     int *issued_use = reinterpret_cast<int *>(smem + 528);   // per stage: use of its last copy, -1 none
 
-    const int64_t nG = gridDim.x;
-    const int64_t r_begin = (a.rows * blockIdx.x) / nG;
-    const int64_t r_end = (a.rows * (blockIdx.x + 1)) / nG;
+    // this CTA's rows, weights, activations and outputs
+    const uint8_t *w0 = a.w;
+    const float *x0 = a.x;
+    float *y0 = a.y;
+    int64_t r_begin, r_end;
+    if (a.cpa > 0) {
+        // experts mode: CTA -> (assignment, part of the expert's rows); the
+        // expert id comes from an earlier kernel, so wait for it first
+        const int64_t asg = blockIdx.x / a.cpa, j = blockIdx.x - asg * a.cpa;
+        r_begin = (a.rows * j) / a.cpa;
+        r_end = (a.rows * (j + 1)) / a.cpa;
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int64_t e = a.expid[asg];
+        y0 = a.y + asg * a.ldy;
+        if (e < 0 || e >= a.n_experts) {
+            // an id outside the tensor: nothing is read, the rows are NaN
+            for (int64_t r = r_begin + tid; r < r_end; r += blockDim.x) y0[r] = __int_as_float(0x7FC00000);
+            if (tid == 0) record_error(a.err, kErrBadIndex);
+            return;
+        }
+        w0 = a.w + e * a.rows * a.row_bytes;
+        x0 = a.x + (asg / a.xk) * a.K;
+    } else {
+        const int64_t nG = gridDim.x;
+        r_begin = (a.rows * blockIdx.x) / nG;
+        r_end = (a.rows * (blockIdx.x + 1)) / nG;
+    }
     const int gr = a.pair ? (a.rows_w >> 1) : a.rows_w;   // output rows per row group
     const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + gr - 1) / gr);
     const uint32_t nkc = static_cast<uint32_t>(a.nkc);
@@ -640,7 +668,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                     }
                     const bool skip = w == 0 && t == a.skip_item && blockIdx.x == 0;   // test hook
                     if (!skip) {
-                        copy_item(a, row0, n, c, stage0 + st * static_cast<uint32_t>(a.stage_bytes), bar, pol);
+                        copy_item(a, w0, row0, n, c, stage0 + st * static_cast<uint32_t>(a.stage_bytes), bar, pol);
                         issued_use[st] = static_cast<int>(use);
                     }
                     if (++tm == m) {
@@ -678,14 +706,14 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     // the weights do not depend on earlier kernels, x may: with programmatic
     // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    stage_x<FMT, B, US>(a, static_cast<int>(cwarp), lane, 32 * NW, smem_u32(xs),
+    stage_x<FMT, B, US>(a, x0, static_cast<int>(cwarp), lane, 32 * NW, smem_u32(xs),
                              reinterpret_cast<float *>(smem + a.off_xsum),
                              reinterpret_cast<float *>(smem + a.off_xscale));
     named_bar_sync(1, 32 * NW);
     if (cwarp >= nw) return;
 
     const uint32_t gs_rt = 16u * static_cast<uint32_t>(XU);
-    const uintptr_t wbase = reinterpret_cast<uintptr_t>(a.w);
+    const uintptr_t wbase = reinterpret_cast<uintptr_t>(w0);
     const int chunk_lu = SW * cpl;                 // lane units per chunk
     const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
     uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
@@ -816,7 +844,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
                     const int lr = team * R + r;
-                    if (sl == 0 && lr < n) a.y[b * a.ldy + row0 + lr] = v[r][b];
+                    if (sl == 0 && lr < n) y0[b * a.ldy + row0 + lr] = v[r][b];
                 }
         } else if (SW == 32) {
             // one team: rows r < R/2 are gate rows, r + R/2 their up rows
@@ -824,7 +852,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
             for (int r = 0; r < R / 2; ++r)
 #pragma unroll
                 for (int b = 0; b < B; ++b)
-                    if (sl == 0 && r < n) a.y[b * a.ldy + row0 + r] = silu(v[r][b]) * v[r + R / 2][b];
+                    if (sl == 0 && r < n) y0[b * a.ldy + row0 + r] = silu(v[r][b]) * v[r + R / 2][b];
         } else {
             // teams t < T/2 hold gate rows, team t + T/2 (lanes + 16) the up rows
 #pragma unroll
@@ -833,7 +861,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                 for (int b = 0; b < B; ++b) {
                     const float u = __shfl_down_sync(0xFFFFFFFFu, v[r][b], 16);
                     const int lr = team * R + r;
-                    if (lane < 16 && sl == 0 && lr < n) a.y[b * a.ldy + row0 + lr] = silu(v[r][b]) * u;
+                    if (lane < 16 && sl == 0 && lr < n) y0[b * a.ldy + row0 + lr] = silu(v[r][b]) * u;
                 }
         }
     }

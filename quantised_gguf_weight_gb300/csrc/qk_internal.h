@@ -12,16 +12,18 @@ constexpr int kFmtQ4K = 1;
 // stage ring, shared-memory layout and grid.
 struct GemvPlan {
     int U, LU, XU, SW, R, cpl, nkc, rows_w, chunk_bytes, row_stride;
-    int nw, m, stages, stage_bytes, pair, up_stage_off;
+    int nw, m, stages, stage_bytes, pair, up_stage_off, cpa;
     int off_x, off_xsum, off_xscale, off_stage, smem, grid;
     int64_t row_bytes;
 };
 
 // pair: rows are output rows of the SwiGLU form (a gate row and an up row each).
-bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p);
+// n_assign > 0: experts mode, `rows` rows per expert and n_assign assignments.
+bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p, int64_t n_assign = 0);
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
-                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows = 0);
+                        int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows = 0,
+                        const int32_t *expid = nullptr, int64_t n_experts = 0, int xk = 1);
 
 // The device error word of the current device and the bound of device waits.
 int *library_error_word();

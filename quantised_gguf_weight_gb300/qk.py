@@ -20,10 +20,12 @@ _lock = threading.Lock()
 
 QK_OK = 0
 STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 4: "QK_ERR_BATCH",
-          5: "QK_ERR_CUDA", 6: "QK_ERR_TIMEOUT", 7: "QK_ERR_WORKSPACE", 8: "QK_ERR_TOO_LARGE"}
+          5: "QK_ERR_CUDA", 6: "QK_ERR_TIMEOUT", 7: "QK_ERR_WORKSPACE", 8: "QK_ERR_TOO_LARGE",
+          9: "QK_ERR_BAD_INDEX"}
 MAX_BATCH = 8
 
-EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
+EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k",
+           "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
            "qgemm_q4_k_noalloc", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
            "qk_version"]
@@ -58,6 +60,10 @@ def load(path: str | None = None):
         for name in ("qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k"):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, I64, P, I, P, I64, P]
+            fn.restype = I
+        for name in ("qmatvec_experts_q8_0", "qmatvec_experts_q4_k"):
+            fn = getattr(lib, name)
+            fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P, I64, P]
             fn.restype = I
         lib.qgemm_q4_k.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
         lib.qgemm_q4_k.restype = I
@@ -143,6 +149,23 @@ def qmatvec_swiglu(fmt: str, w: torch.Tensor, gate_offset: int, up_offset: int, 
                                ldh, _stream(stream))
     _check(st, name)
     return h
+
+
+def qmatvec_experts(fmt: str, w: torch.Tensor, n_experts: int, rows: int, K: int, x: torch.Tensor, xk: int,
+                    expert_ids: torch.Tensor, y: torch.Tensor | None = None, ldy: int = 0,
+                    stream=None) -> torch.Tensor:
+    """y[a][r] = sum_c W[expert_ids[a]*rows + r][c] x[a // xk][c] (expert_ids: int32 device tensor)."""
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    n_assign = expert_ids.numel()
+    if y is None:
+        y = torch.empty((n_assign, rows), dtype=torch.float32, device=x.device)
+        ldy = rows
+    name = {"q8_0": "qmatvec_experts_q8_0", "q4_k": "qmatvec_experts_q4_k"}[fmt]
+    st = getattr(load(), name)(w.data_ptr(), n_experts, rows, K, x.data_ptr(), xk, expert_ids.data_ptr(),
+                               n_assign, y.data_ptr(), ldy, _stream(stream))
+    _check(st, name)
+    return y
 
 
 def gemm_workspace_bytes(M: int, N: int, K: int) -> int:

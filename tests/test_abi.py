@@ -34,7 +34,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qgemm_q4_k",
+    for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k",
+              "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qgemm_q4_k",
               "qgemm_q4_k_workspace_bytes", "qk_status_string", "qk_device_error"):
         assert n in names
 
@@ -45,8 +46,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
-        assert lib.qk_status_string(s)
+    for s in range(10):
+        assert lib.qk_status_string(s) and lib.qk_status_string(s) != b"unknown status"
     assert lib.qk_status_string(99) == b"unknown status"
 
 
@@ -106,6 +107,28 @@ def test_swiglu_argument_validation_without_gpu(lib, name):
     assert call(ldh=8) == 2          # ldh < F
     assert call(batch=9) == 4
     assert call(x=FAKE + 2) == 3
+
+
+@pytest.mark.parametrize("name", ["qmatvec_experts_q8_0", "qmatvec_experts_q4_k"])
+def test_experts_argument_validation_without_gpu(lib, name):
+    f = getattr(lib, name)
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    ok_args = dict(w=FAKE, E=4, rows=16, K=256, x=FAKE, xk=2, ids=FAKE, n=4, y=FAKE, ldy=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return f(a["w"], a["E"], a["rows"], a["K"], a["x"], a["xk"], a["ids"], a["n"], a["y"], a["ldy"], None)
+
+    assert call(ids=None) == 1
+    assert call(w=None) == 1
+    assert call(E=0) == 2
+    assert call(xk=0) == 2
+    assert call(n=0) == 2
+    assert call(rows=0) == 2
+    assert call(ldy=3) == 2
+    assert call(ids=FAKE + 2) == 3
+    assert call(x=FAKE + 1) == 3
 
 
 def test_wait_limit_roundtrip(lib):
