@@ -23,9 +23,9 @@ SRC = os.path.join(HERE, "qk_oracle.c")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "libqk_oracle.so")
 
-FMT = {"q8_0": 0, "q4_k": 1}
-QK = {"q8_0": 32, "q4_k": 256}
-BLOCK_BYTES = {"q8_0": 34, "q4_k": 144}
+FMT = {"q8_0": 0, "q4_k": 1, "q6_k": 2}
+QK = {"q8_0": 32, "q4_k": 256, "q6_k": 256}
+BLOCK_BYTES = {"q8_0": 34, "q4_k": 144, "q6_k": 210}
 
 _lib = None
 _lock = threading.Lock()

@@ -32,6 +32,9 @@
  *             m  = (scales[j+4] >> 4) | ((scales[j]   >> 6) << 4)
  *     qs is 4 chunks of 32 bytes; weight i of sub-block 2c is the low
  *     nibble of qs[32c+i], weight i of sub-block 2c+1 its high nibble.
+ *   Q6_K (210 B): ql[128] | qh[64] | scales[16] int8 | fp16 d; weight i of
+ *     a super-block takes 4 low bits from ql and 2 high bits from qh (see
+ *     qko_decode_q6_k_row), w = d * scales[i/16] * (q - 32).
  *   A row is ceil(K/QK) whole blocks; columns >= K are ignored.
  *
  * The fp16 and bf16 conversions are written from the IEEE 754 encodings.
@@ -44,6 +47,7 @@
 
 #define QKO_Q8_0 0
 #define QKO_Q4_K 1
+#define QKO_Q6_K 2
 
 /* ---------------------------------------------------------------- fp16 / bf16 */
 
@@ -153,14 +157,39 @@ void qko_decode_q4_k_row(const uint8_t *row, int64_t K, double *w)
     }
 }
 
+/*
+ * Q6_K (210 B per 256 weights): ql[128] | qh[64] | scales[16] int8 | fp16 d.
+ * Weight i: n = i/128, cc = i%128, t = cc/32, l = cc%32; the low 4 bits are
+ * the low (t < 2) or high (t >= 2) nibble of ql[64n + l + 32*(t%2)], the
+ * high 2 bits are (qh[32n + l] >> 2t) & 3; w = d * scales[i/16] * (q - 32).
+ */
+void qko_decode_q6_k_row(const uint8_t *row, int64_t K, double *w)
+{
+    for (int64_t c = 0; c < K; ++c) {
+        const uint8_t *blk = row + (c / 256) * 210;
+        const int i = (int)(c % 256);
+        const int n = i / 128, cc = i % 128, t = cc / 32, l = cc % 32;
+        const uint8_t lbyte = blk[64 * n + l + 32 * (t % 2)];
+        const int lo = t < 2 ? (lbyte & 15) : (lbyte >> 4);
+        const int hi = (blk[128 + 32 * n + l] >> (2 * t)) & 3;
+        const int q = lo | (hi << 4);
+        const int sc = (int)(int8_t)blk[192 + i / 16];
+        const double d = qko_fp16_to_f64(le16(blk + 208));
+        w[c] = d * (double)sc * (double)(q - 32);
+    }
+}
+
 static int64_t row_stride(int fmt, int64_t K)
 {
-    return fmt == QKO_Q8_0 ? ((K + 31) / 32) * 34 : ((K + 255) / 256) * 144;
+    if (fmt == QKO_Q8_0) return ((K + 31) / 32) * 34;
+    if (fmt == QKO_Q6_K) return ((K + 255) / 256) * 210;
+    return ((K + 255) / 256) * 144;
 }
 
 static void decode_row(int fmt, const uint8_t *row, int64_t K, double *w)
 {
     if (fmt == QKO_Q8_0) qko_decode_q8_0_row(row, K, w);
+    else if (fmt == QKO_Q6_K) qko_decode_q6_k_row(row, K, w);
     else qko_decode_q4_k_row(row, K, w);
 }
 
@@ -168,7 +197,7 @@ static void decode_row(int fmt, const uint8_t *row, int64_t K, double *w)
 int qko_decode_rows(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows,
                     int64_t n_rows, double *out)
 {
-    if (fmt != QKO_Q8_0 && fmt != QKO_Q4_K) return 1;
+    if (fmt != QKO_Q8_0 && fmt != QKO_Q4_K && fmt != QKO_Q6_K) return 1;
     int64_t stride = row_stride(fmt, K);
     for (int64_t i = 0; i < n_rows; ++i)
         decode_row(fmt, wq + rows[i] * stride, K, out + i * K);
@@ -187,7 +216,7 @@ int qko_decode_rows(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows,
 int qko_gemv(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows, int64_t n_rows,
              const float *x, int64_t batch, double *y, double *s)
 {
-    if (fmt != QKO_Q8_0 && fmt != QKO_Q4_K) return 1;
+    if (fmt != QKO_Q8_0 && fmt != QKO_Q4_K && fmt != QKO_Q6_K) return 1;
     int64_t stride = row_stride(fmt, K);
     double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     if (!w) return 2;
@@ -275,7 +304,7 @@ int qko_swiglu(int fmt, const uint8_t *wq, int64_t K, const int64_t *gate_rows, 
 int qko_gemm_bf16(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows, int64_t n_rows,
                   const float *x, int64_t M, double *y, double *s)
 {
-    if (fmt != QKO_Q8_0 && fmt != QKO_Q4_K) return 1;
+    if (fmt != QKO_Q8_0 && fmt != QKO_Q4_K && fmt != QKO_Q6_K) return 1;
     int64_t stride = row_stride(fmt, K);
     double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     double *xb = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));

@@ -34,9 +34,10 @@ _STREAM_MULT = 0xD1B54A32D192ED03
 Q8_0_DTYPE = np.dtype([("d", "<f2"), ("qs", "i1", (32,))])
 Q4_K_DTYPE = np.dtype([("d", "<f2"), ("dmin", "<f2"), ("scales", "u1", (12,)),
                        ("qs", "u1", (128,))])
-assert Q8_0_DTYPE.itemsize == 34 and Q4_K_DTYPE.itemsize == 144
+Q6_K_DTYPE = np.dtype([("ql", "u1", (128,)), ("qh", "u1", (64,)), ("scales", "i1", (16,)), ("d", "<f2")])
+assert Q8_0_DTYPE.itemsize == 34 and Q4_K_DTYPE.itemsize == 144 and Q6_K_DTYPE.itemsize == 210
 
-BLOCK = {"q8_0": (32, 34, Q8_0_DTYPE), "q4_k": (256, 144, Q4_K_DTYPE)}
+BLOCK = {"q8_0": (32, 34, Q8_0_DTYPE), "q4_k": (256, 144, Q4_K_DTYPE), "q6_k": (256, 210, Q6_K_DTYPE)}
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -120,11 +121,29 @@ def q4_k_weights(rows: int, K: int, seed: int, d_sigma: float = 0.01,
     return rec.view(np.uint8).reshape(-1)
 
 
+def q6_k_weights(rows: int, K: int, seed: int, d_sigma: float = 1e-4, stream0: int = 0) -> np.ndarray:
+    """Q6_K tensor [rows][ceil(K/256)] as raw bytes (uint8, flat).
+
+    ql and qh uniform random bytes (6-bit quants uniform in [0, 63]); int8
+    scales uniform in [-127, 127]; d = fp16(|N(0, d_sigma)|).  The unused
+    tail of a row's last super-block is random too.
+    """
+    nb = rows * blocks_per_row("q6_k", K)
+    rec = np.empty(nb, dtype=Q6_K_DTYPE)
+    rec["ql"] = random_bytes(seed, stream0 + 0, nb * 128).reshape(nb, 128)
+    rec["qh"] = random_bytes(seed, stream0 + 1, nb * 64).reshape(nb, 64)
+    rec["scales"] = randint(seed, stream0 + 2, nb * 16, -127, 127).astype(np.int8).reshape(nb, 16)
+    rec["d"] = (np.abs(normal(seed, stream0 + 3, nb)) * d_sigma).astype(np.float16)
+    return rec.view(np.uint8).reshape(-1)
+
+
 def weights(fmt: str, rows: int, K: int, seed: int, stream0: int = 0) -> np.ndarray:
     if fmt == "q8_0":
         return q8_0_weights(rows, K, seed, stream0=stream0)
     if fmt == "q4_k":
         return q4_k_weights(rows, K, seed, stream0=stream0)
+    if fmt == "q6_k":
+        return q6_k_weights(rows, K, seed, stream0=stream0)
     raise ValueError(fmt)
 
 

@@ -6,8 +6,8 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-QK = {"q8_0": 32, "q4_k": 256}
-BB = {"q8_0": 34, "q4_k": 144}
+QK = {"q8_0": 32, "q4_k": 256, "q6_k": 256}
+BB = {"q8_0": 34, "q4_k": 144, "q6_k": 210}
 
 
 def load(fmt: str):

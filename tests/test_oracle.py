@@ -21,7 +21,7 @@ import torch
 from quantised_gguf_weight_gb300 import synth
 from tests import golden_probes
 
-FMTS = ["q8_0", "q4_k"]
+FMTS = ["q8_0", "q4_k", "q6_k"]
 
 
 # ------------------------------------------------------------ scalar codecs
@@ -83,7 +83,7 @@ def test_layout_probes(orc, fmt):
 # ------------------------------------------------------------ dot product
 
 @pytest.mark.parametrize("fmt,rows,K", [("q8_0", 3, 96), ("q4_k", 3, 512), ("q4_k", 2, 300),
-                                        ("q8_0", 2, 40)])
+                                        ("q8_0", 2, 40), ("q6_k", 3, 512), ("q6_k", 2, 300)])
 def test_unit_vectors_recover_matrix(orc, fmt, rows, K):
     """x = e_c gives y[r] = W[r][c]: the dot indexes W row-major, column fastest."""
     wq = synth.weights(fmt, rows, K, seed=11)
@@ -102,7 +102,7 @@ def test_all_zero_blocks(orc, fmt):
     assert np.all(y == 0.0) and np.all(s == 0.0)
 
 
-@pytest.mark.parametrize("fmt,w_const,n_blocks", [("q8_0", 3.0, 7), ("q4_k", 2.5, 3)])
+@pytest.mark.parametrize("fmt,w_const,n_blocks", [("q8_0", 3.0, 7), ("q4_k", 2.5, 3), ("q6_k", 2.5, 3)])
 def test_constant_block_closed_form(orc, fmt, w_const, n_blocks):
     """A row of identical constant blocks and x = v gives y = K * w * v exactly."""
     name, K0, raw, exp = [p for p in golden_probes.load(fmt) if p[0] == "constant_block"][0]
@@ -131,7 +131,7 @@ def test_exact_integer_dot(orc, fmt):
             assert Fraction(float(y[b, r])) == exact
 
 
-@pytest.mark.parametrize("fmt,rows,K,B", [("q8_0", 17, 576, 3), ("q4_k", 9, 896, 2),
+@pytest.mark.parametrize("fmt,rows,K,B", [("q8_0", 17, 576, 3), ("q4_k", 9, 896, 2), ("q6_k", 9, 896, 2),
                                           ("q4_k", 5, 4096, 1)])
 def test_dot_matches_blas(orc, fmt, rows, K, B):
     wq = synth.weights(fmt, rows, K, seed=3)

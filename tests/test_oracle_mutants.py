@@ -36,6 +36,11 @@ MUTATIONS = {
     "q4_encode_high_nibble": ("(uint8_t)(best << 4);", "(uint8_t)(best << 3);"),
     "swiglu_gate_up_swapped": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = u[i] / (1.0 + exp(-u[i])) * g[i];"),
     "silu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+    "q6_qh_shift": ("(blk[128 + 32 * n + l] >> (2 * t)) & 3;", "(blk[128 + 32 * n + l] >> t) & 3;"),
+    "q6_ql_half": ("blk[64 * n + l + 32 * (t % 2)];", "blk[64 * n + l + 32 * (t / 2)];"),
+    "q6_scale_index": ("blk[192 + i / 16];", "blk[192 + i / 32];"),
+    "q6_offset": ("(double)(q - 32);", "(double)(q - 31);"),
+    "q6_scale_unsigned": ("(int)(int8_t)blk[192 + i / 16];", "(int)blk[192 + i / 16];"),
     "experts_input_row_mod": ("x + (a / xk) * K, 1, y + a * rows", "x + (a % xk) * K, 1, y + a * rows"),
     "experts_ignores_id": ("idx[r] = e * rows + r;", "idx[r] = r;"),
     "silu_missing_z": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = 1.0 / (1.0 + exp(-g[i])) * u[i];"),
@@ -47,6 +52,7 @@ PINS = [
     (pins.test_bf16_round_matches_torch, {}),
     (pins.test_layout_probes, {"fmt": "q8_0"}),
     (pins.test_layout_probes, {"fmt": "q4_k"}),
+    (pins.test_layout_probes, {"fmt": "q6_k"}),
     (pins.test_unit_vectors_recover_matrix, {"fmt": "q4_k", "rows": 3, "K": 512}),
     (pins.test_unit_vectors_recover_matrix, {"fmt": "q8_0", "rows": 3, "K": 96}),
     (pins.test_all_zero_blocks, {"fmt": "q4_k"}),
