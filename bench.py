@@ -438,7 +438,7 @@ def measure_extra_rows(torch, qk, synth, device, stream):
               for c in range(copies)]
         x = torch.from_numpy(synth.activations(batch, K, seed=seed)).to(device)
         y = torch.empty((batch, rows), device=device)
-        fn = lib.qmatvec_q8_0 if fmt == "q8_0" else lib.qmatvec_q4_k
+        fn = {"q8_0": lib.qmatvec_q8_0, "q4_k": lib.qmatvec_q4_k, "q6_k": lib.qmatvec_q6_k}[fmt]
         def mk(w):
             def f(sh):
                 st = fn(w.data_ptr(), 0, rows, K, x.data_ptr(), batch, y.data_ptr(), rows, sh)
@@ -530,6 +530,8 @@ def measure_extra_rows(torch, qk, synth, device, stream):
     gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1)
     gemv_row("q8_0_lm_head_151936x896_b1", "q8_0", 151936, 896, 1, 3, 3)
     gemv_row("q8_0_lm_head_151936x896_b8", "q8_0", 151936, 896, 8, 3, 3)
+    gemv_row("q6_k_lm_head_128256x4096_b1", "q6_k", 128256, 4096, 1, 6, 1)
+    gemv_row("q6_k_ffn_down_4096x14336_b1", "q6_k", 4096, 14336, 1, 7, 4)
     return out
 
 

@@ -96,6 +96,20 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
                  const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
 
 /*
+ * Q6_K GEMV, batch 1..8.  Same contract as qmatvec_q8_0 (w 2-byte aligned:
+ * 210-byte super-blocks).  Q6_K is the format of lm_head / ffn_down in the
+ * Q4_K_M files people download ("in a Q4_K_M file output.weight is Q4_K or
+ * Q6_K", nx_f32_llm_v4.nx source, lm_head binder comment; kernel `mv_q6_k`,
+ * nurllama 0.18.1 API reference, kernels.nu).  Block reading (GGUF):
+ * ql[128] | qh[64] | scales[16] int8 | fp16 d per 256 weights; weight i of
+ * half n = i/128 (cc = i%128, t = cc/32, l = cc%32) takes its low 4 bits
+ * from ql[64n + l + 32*(t%2)] (low nibble if t < 2, else high) and its high
+ * 2 bits from (qh[32n + l] >> 2t) & 3;  w = d * scales[i/16] * (q - 32).
+ */
+int qmatvec_q6_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
+                 const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
+
+/*
  * Fused gate/up GEMV with the SwiGLU product, batch 1..8:
  *   g = sum_{c<K} W[gate_offset + p][c] * x[b*K + c]
  *   u = sum_{c<K} W[up_offset + p][c]   * x[b*K + c]
@@ -119,6 +133,8 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
 int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
                         const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
 int qmatvec_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
+                        const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
+int qmatvec_swiglu_q6_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
                         const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream);
 
 /*
@@ -145,6 +161,8 @@ int qmatvec_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, i
 int qmatvec_experts_q8_0(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
                          const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream);
 int qmatvec_experts_q4_k(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                         const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream);
+int qmatvec_experts_q6_k(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
                          const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream);
 
 /*
@@ -194,11 +212,12 @@ int qgemm_q4_k_noalloc(const void *w, int64_t row_offset, int64_t N, int64_t K, 
                        float *y, int64_t ldy, qk_stream_t stream);
 
 /*
- * Bytes of one row of a tensor with K columns: ceil(K/32)*34 (Q8_0) or
- * ceil(K/256)*144 (Q4_K).
+ * Bytes of one row of a tensor with K columns: ceil(K/32)*34 (Q8_0),
+ * ceil(K/256)*144 (Q4_K) or ceil(K/256)*210 (Q6_K).
  */
 int64_t qk_row_bytes_q8_0(int64_t K);
 int64_t qk_row_bytes_q4_k(int64_t K);
+int64_t qk_row_bytes_q6_k(int64_t K);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *qk_status_string(int status);

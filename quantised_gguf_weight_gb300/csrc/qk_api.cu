@@ -122,6 +122,19 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K, con
     return gemv_entry(qk::kFmtQ4K, w, row_offset, rows, K, x, batch, y, ldy, stream);
 }
 
+int qmatvec_q6_k(const void *w, int64_t row_offset, int64_t rows, int64_t K, const float *x,
+                 int batch, float *y, int64_t ldy, qk_stream_t stream)
+{
+    return gemv_entry(qk::kFmtQ6K, w, row_offset, rows, K, x, batch, y, ldy, stream);
+}
+
+int qmatvec_swiglu_q6_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
+                        const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream)
+{
+    if (up_offset < 0) return QK_ERR_BAD_DIM;
+    return gemv_entry(qk::kFmtQ6K, w, gate_offset, F, K, x, batch, h, ldh, stream, up_offset);
+}
+
 int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
                         const float *x, int batch, float *h, int64_t ldh, qk_stream_t stream)
 {
@@ -179,6 +192,14 @@ int qmatvec_experts_q4_k(const void *w, int64_t n_experts, int64_t rows, int64_t
 {
     return experts_entry(qk::kFmtQ4K, w, n_experts, rows, K, x, xk, expert_ids, n_assign, y, ldy, stream);
 }
+
+int qmatvec_experts_q6_k(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
+                         const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream)
+{
+    return experts_entry(qk::kFmtQ6K, w, n_experts, rows, K, x, xk, expert_ids, n_assign, y, ldy, stream);
+}
+
+int64_t qk_row_bytes_q6_k(int64_t K) { return K <= 0 ? 0 : ((K + 255) / 256) * 210; }
 
 int64_t qk_row_bytes_q8_0(int64_t K) { return K <= 0 ? 0 : ((K + 31) / 32) * 34; }
 int64_t qk_row_bytes_q4_k(int64_t K) { return K <= 0 ? 0 : ((K + 255) / 256) * 144; }

@@ -40,9 +40,13 @@ int64_t round_up(int64_t v, int64_t m) { return ((v + m - 1) / m) * m; }
 bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64_t n_assign, const DevInfo &di,
                    GemvPlan *p)
 {
-    const int UC = fmt == kFmtQ4K ? 128 : 32;
-    const int UB = fmt == kFmtQ4K ? 144 : 34;
-    const int64_t row_bytes = fmt == kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
+    // units of x (UC columns) and of the lane work: Q8_0 blocks; Q4_K 128-column
+    // halves of super-blocks, a lane taking whole super-blocks; Q6_K halves of
+    // super-blocks, a lane taking one half (UB: bytes a lane unit occupies)
+    const int UC = fmt == kFmtQ80 ? 32 : 128;
+    const int UB = fmt == kFmtQ80 ? 34 : (fmt == kFmtQ4K ? 144 : 105);
+    const int64_t row_bytes = fmt == kFmtQ80 ? ((K + 31) / 32) * 34
+                                             : ((K + 255) / 256) * (fmt == kFmtQ4K ? 144 : 210);
     const int64_t U64 = (K + UC - 1) / UC;
     if (U64 > (1 << 20)) return false;
     const int U = static_cast<int>(U64);
@@ -54,7 +58,10 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     const int need = fmt == kFmtQ4K ? 2 * LU : U;
     const int XU = need <= 32 ? 32 : (need <= 128 ? 128 : static_cast<int>(round_up(need, 2)));
     const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
-    const int64_t xsum_bytes = fmt == kFmtQ4K ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128) : 0;
+    // Q4_K: sums of x per 32 columns (every batch row); Q6_K: per 16 columns (batch 1)
+    const int64_t xsum_bytes = fmt == kFmtQ4K   ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128)
+                               : fmt == kFmtQ6K ? (batch == 1 ? round_up(static_cast<int64_t>(8) * XU * 4, 128) : 0)
+                                                : 0;
     const int64_t xscale_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 4, 128) : 0;
     const int64_t off_x = kGemvBarBytes;
     const int64_t off_xsum = off_x + x_bytes;
@@ -86,6 +93,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
         const int nkc = (LU + sw * cpl - 1) / (sw * cpl);
         const int rows_w = (32 / sw) * R;
         if (nkc > 1 && rows_w > 8) continue;
+        if (fmt == kFmtQ6K && nkc > 1 && (sw * cpl) % 2) continue;   // chunks of whole super-blocks
         if (pair && sw == 32 && R % 2) continue;    // a gate row and its up row must share a lane or a team pair
         double util = static_cast<double>(LU) / (static_cast<double>(nkc) * sw * cpl);
         if (nkc > 1 && static_cast<int64_t>(sw) * cpl * UB < 2048) util *= 0.85;
@@ -110,8 +118,8 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
         }
     } else {
         chunk_bytes = static_cast<int64_t>(SW) * cpl * UB;
-        // a Q8_0 chunk is widened to 16-byte boundaries and its last block
-        // read as nine whole words
+        // a Q8_0 or Q6_K chunk is widened to 16-byte boundaries and its last
+        // block read a few bytes past its end (whole aligned words)
         row_stride = fmt == kFmtQ4K ? chunk_bytes : round_up(chunk_bytes + 30, 16) + 16;
         stage = round_up(rows_w * row_stride, 128);
     }
@@ -209,6 +217,7 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.err = err;
     const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
     if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, r, p.grid, p.smem, st, pdl);
+    if (fmt == kFmtQ6K) return gemv_launch_q6k(batch, us, r, p.grid, p.smem, st, pdl);
     return gemv_launch_q80(batch, us, r, p.grid, p.smem, st, pdl);
 }
 

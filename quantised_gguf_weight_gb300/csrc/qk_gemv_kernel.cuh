@@ -118,13 +118,13 @@ struct GemvArgs {
 __host__ __device__ constexpr int gemv_warps(int /*fmt*/, int batch) { return batch == 1 ? 11 : 8; }
 __host__ __device__ constexpr int gemv_rows(int fmt, int batch)
 {
-    return fmt == kFmtQ4K ? (batch <= 4 ? 2 : 1) : (batch == 1 ? 2 : (batch == 2 ? 4 : 2));
+    return fmt != kFmtQ80 ? (batch <= 4 ? 2 : 1) : (batch == 1 ? 2 : (batch == 2 ? 4 : 2));
 }
 // Lane units a lane may hold in registers per item (Q4_K: one super-block of
-// R rows; Q8_0: up to 72 words of blocks).
+// R rows; Q6_K: one half super-block; Q8_0: up to 72 words of blocks).
 __host__ __device__ constexpr int gemv_cpl_max(int fmt, int batch)
 {
-    return fmt == kFmtQ4K ? 1 : (batch == 1 ? 4 : (batch <= 4 ? 2 : 1));
+    return fmt != kFmtQ80 ? 1 : (batch == 1 ? 4 : (batch <= 4 ? 2 : 1));
 }
 
 // -------------------------------------------------------------------------- Q4_K, batch 1
@@ -421,6 +421,168 @@ __device__ __forceinline__ void q8_blk_fp(const uint32_t (&wv)[R][9], const uint
         }
 }
 
+// -------------------------------------------------------------------------- Q6_K
+//
+// A Q6_K super-block (210 bytes, 256 weights): ql[128] | qh[64] |
+// scales[16] int8 | fp16 d; weight i of half n = i/128 (cc = i%128,
+// t = cc/32, l = cc%32) takes 4 low bits from ql[64n + l + 32*(t%2)] (low
+// nibble for t < 2, high for t >= 2) and 2 high bits (qh[32n + l] >> 2t) & 3;
+// w = d * scales[i/16] * (q - 32).  The lane unit is half a super-block (128
+// weights).  Blocks start 0 or 2 bytes past a 4-byte boundary, so a lane
+// loads the aligned words around each field and realigns them with byte
+// permutes.
+
+// N words of a field starting at the 2-byte-aligned shared address p, read as
+// N+1 aligned words (up to 4 bytes past the field, inside the stage slack).
+template <int N>
+__device__ __forceinline__ void lds_realign(const uint8_t *p, uint32_t (&out)[N])
+{
+    const uintptr_t ad = reinterpret_cast<uintptr_t>(p);
+    const uint32_t o = static_cast<uint32_t>(ad & 3u);
+    const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - o);
+    const uint32_t sel = o ? 0x5432u : 0x3210u;
+    uint32_t prev = wp[0];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const uint32_t nx = wp[i + 1];
+        out[i] = __byte_perm(prev, nx, sel);
+        prev = nx;
+    }
+}
+
+// One half super-block in registers: its ql (64 bytes), qh (32 bytes), the 8
+// scales (int8) and the word holding d in its low 16 bits.
+struct Q6Half {
+    uint32_t ql[16], qh[8], sc[2], dw;
+};
+
+__device__ __forceinline__ void q6_load(const uint8_t *blk, int n, Q6Half &h)
+{
+    lds_realign<16>(blk + 64 * n, h.ql);
+    lds_realign<8>(blk + 128 + 32 * n, h.qh);
+    lds_realign<2>(blk + 192 + 8 * n, h.sc);
+    uint32_t dw[1];
+    lds_realign<1>(blk + 208, dw);
+    h.dw = dw[0];
+}
+
+// The 6-bit quants of columns 32t + 4k .. 32t + 4k + 3, one per byte.
+__device__ __forceinline__ uint32_t q6_quad(const Q6Half &h, int t, int k)
+{
+    const uint32_t a = h.ql[k + 8 * (t & 1)];
+    const uint32_t b = h.qh[k];
+    const uint32_t lo = (t < 2 ? a : (a >> 4)) & 0x0F0F0F0Fu;
+    const uint32_t hi = (t == 0 ? (b << 4) : t == 1 ? (b << 2) : t == 2 ? b : (b >> 2)) & 0x30303030u;
+    return lo | hi;
+}
+
+// d * scales[j] (j < 8 of this half); exact (11 x 8 significant bits).
+__device__ __forceinline__ float q6_dscale(const Q6Half &h, float d, int j)
+{
+    const int s = static_cast<int8_t>((h.sc[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+    return d * static_cast<float>(s);
+}
+
+// Batch 1: block-floating-point planes of the half's 128 columns at xa (group
+// g at xa + g*gs); per 16-column sub-block j the plain sum x16[j*XU] (for the
+// -32 offset) and per 32-column group the plane scale xsc[(j/2)*XU].
+template <int R, int US>
+__device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_t *xa, uint32_t gs_rt,
+                                             const float *x16, const float *xsc, int xstride, float (&acc)[R][1])
+{
+    const uint32_t gs = US ? 16u * US : gs_rt;
+    const int xstr = US ? US : xstride;
+    float d[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) d[r] = half_bits_to_float(hr[r].dw);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        int sp[R][2][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sp[r][h][k] = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xa + (8 * t + k) * gs);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t q = q6_quad(hr[r], t, k);
+                const int h = k >> 2;                   // 16-column sub-block 2t + h
+                sp[r][h][0] = dp4a_uu(q, xv.x, sp[r][h][0]);
+                sp[r][h][1] = dp4a_uu(q, xv.y, sp[r][h][1]);
+                sp[r][h][2] = dp4a_uu(q, xv.z, sp[r][h][2]);
+                sp[r][h][3] = dp4a_us(q, xv.w, sp[r][h][3]);
+            }
+        }
+        const float S = xsc[t * xstr];
+        const float X0 = x16[(2 * t) * xstr], X1 = x16[(2 * t + 1) * xstr];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float ds0 = q6_dscale(hr[r], d[r], 2 * t), ds1 = q6_dscale(hr[r], d[r], 2 * t + 1);
+            float a = acc[r][0];
+            a = fmaf(ds0 * S, planes_to_float(sp[r][0][0], sp[r][0][1], sp[r][0][2], sp[r][0][3]), a);
+            a = fmaf(ds0 * -32.0f, X0, a);
+            a = fmaf(ds1 * S, planes_to_float(sp[r][1][0], sp[r][1][1], sp[r][1][2], sp[r][1][3]), a);
+            a = fmaf(ds1 * -32.0f, X1, a);
+            acc[r][0] = a;
+        }
+    }
+}
+
+// Batch >= 2: fp32 x; each 6-bit quant becomes the exact float 2^23 + q (one
+// byte permute into the magic pattern) and 2^23 + 32 is subtracted, giving
+// q - 32 exactly; packed f32x2 arithmetic.
+template <int B, int R, int US>
+__device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t *xa, uint32_t gs_rt,
+                                            float (&acc)[R][B])
+{
+    const uint32_t gs = US ? 16u * US : gs_rt;
+    const uint64_t neg_bias = pack2f(-(kTwo23 + 32.0f), -(kTwo23 + 32.0f));
+    float d[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) d[r] = half_bits_to_float(hr[r].dw);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {                      // 16-column sub-block j: t = j/2, k = 4*(j%2) ..
+        uint64_t part[R][B];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) part[r][b] = 0ull;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int t = j >> 1, k = 4 * (j & 1) + kk;
+            uint64_t q01[R], q23[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t q = q6_quad(hr[r], t, k);
+                q01[r] = add_f32x2(pack2(__byte_perm(q, kMagic, 0x7440u), __byte_perm(q, kMagic, 0x7441u)), neg_bias);
+                q23[r] = add_f32x2(pack2(__byte_perm(q, kMagic, 0x7442u), __byte_perm(q, kMagic, 0x7443u)), neg_bias);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xa + (b * 32 + 8 * t + k) * gs);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    part[r][b] = fma_f32x2(q01[r], xv.x, part[r][b]);
+                    part[r][b] = fma_f32x2(q23[r], xv.y, part[r][b]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float ds = q6_dscale(hr[r], d[r], j);
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const float2 p2 = unpack2f(part[r][b]);
+                acc[r][b] = fmaf(ds, p2.x + p2.y, acc[r][b]);
+            }
+        }
+    }
+}
+
 // -------------------------------------------------------------------------- activations -> shared memory
 //
 // One warp-uniform pass: each lane loads float4 group f of batch row b
@@ -432,7 +594,7 @@ template <int FMT, int B, int US>
 __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int cwarp, int lane, int nthreads, uint32_t xs_addr,
                                              float *xsum, float *xscale)
 {
-    constexpr int UC = FMT == kFmtQ4K ? 128 : 32;
+    constexpr int UC = FMT == kFmtQ80 ? 32 : 128;
     constexpr int G = UC / 4;
     const int XU = US ? US : a.XU;
     const int XH = XU >> 1;
@@ -472,11 +634,13 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int 
                     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
                     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
                     float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                    if constexpr (FMT == kFmtQ4K) {
+                    if constexpr (FMT != kFmtQ80) {
+                        // Q4_K: sums of 32 columns; Q6_K: of 16 columns (read below)
                         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
                         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
                     }
+                    const float sum16 = sum;
+                    if constexpr (FMT == kFmtQ4K) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
                     const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 255u);
                     const bool finite = ebits != 255;
                     const int E = max(ebits - 127, -96);
@@ -495,11 +659,13 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int 
                     const uint32_t p0 = __byte_perm(t0, t1, 0x5410u), p1 = __byte_perm(t0, t1, 0x7632u);
                     const uint32_t p2 = __byte_perm(t2, t3, 0x5410u), p3 = __byte_perm(t2, t3, 0x7632u);
                     if (f < g_total) {
-                        const int grp = FMT == kFmtQ4K ? (g >> 3) : 0;
+                        const int grp = FMT == kFmtQ80 ? 0 : (g >> 3);
                         if ((lane & 7) == 0) {
                             xscale[grp * XU + us] = finite ? down : __int_as_float(0x7FC00000);
                             if constexpr (FMT == kFmtQ4K) xsum[grp * XU + us] = sum;
                         }
+                        if constexpr (FMT == kFmtQ6K)
+                            if ((lane & 3) == 0) xsum[(g >> 2) * XU + us] = sum16;
                         const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(g * XU + us);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                      ::"r"(dst), "r"(p0), "r"(p1), "r"(p2), "r"(p3) : "memory");
@@ -591,7 +757,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     constexpr int R = gemv_rows(FMT, B);
     constexpr int NW = gemv_warps(FMT, B);
     constexpr int CM = gemv_cpl_max(FMT, B);
-    constexpr int UB = FMT == kFmtQ4K ? 144 : 34;    // bytes per lane unit
+    constexpr int UB = FMT == kFmtQ4K ? 144 : 34;    // bytes per lane unit (Q4_K, Q8_0)
     const int tid = threadIdx.x;
     const uint32_t nw = static_cast<uint32_t>(a.nw);  // consumer warps with row groups
     const uint32_t m = static_cast<uint32_t>(a.m);    // stages per consumer warp
@@ -787,6 +953,24 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                     else
                         q4k_sb_fp<B, R, US>(hd, qs, has_hi, xa0, xa1, gs_rt, xsum + lu, xsum + XH + lu, XU, acc);
                 }
+            } else if constexpr (FMT == kFmtQ6K) {
+                // lane unit = half super-block: block li/2 of the chunk, half li%2
+                // (a chunk holds whole super-blocks: chunk_lu is even when nkc > 1)
+                Q6Half hr[R];
+                const bool valid = lu0 < a.LU;
+                if (valid) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) q6_load(rowp[r] + (sl >> 1) * 210, lu0 & 1, hr[r]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
+                if (valid) {
+                    const uint8_t *xa = xs + 16 * lu0;
+                    if constexpr (B == 1)
+                        q6k_half_dig<R, US>(hr, xa, gs_rt, xsum + lu0, xscale + lu0, XU, acc);
+                    else
+                        q6k_half_fp<B, R, US>(hr, xa, gs_rt, acc);
+                }
             } else {
                 uint32_t wv[CM][R][9], off[CM][R];
 #pragma unroll
@@ -867,9 +1051,10 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     }
 }
 
-// Launch one instantiation (defined per format in qk_gemv_q4k.cu / qk_gemv_q80.cu).
+// Launch one instantiation (defined per format in qk_gemv_q4k.cu / qk_gemv_q80.cu / qk_gemv_q6k.cu).
 cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q80(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q6k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
 template <int FMT, int B, int US>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)

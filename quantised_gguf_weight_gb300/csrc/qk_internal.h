@@ -8,6 +8,7 @@ namespace qk {
 
 constexpr int kFmtQ80 = 0;
 constexpr int kFmtQ4K = 1;
+constexpr int kFmtQ6K = 2;
 // Launch plan of one GEMV call (qk_gemv_kernel.cuh): team shape, K chunks,
 // stage ring, shared-memory layout and grid.
 struct GemvPlan {

@@ -24,8 +24,9 @@ STATUS = {0: "QK_OK", 1: "QK_ERR_NULL", 2: "QK_ERR_BAD_DIM", 3: "QK_ERR_ALIGN", 
           9: "QK_ERR_BAD_INDEX"}
 MAX_BATCH = 8
 
-EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k",
-           "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
+EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_q6_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k",
+           "qmatvec_swiglu_q6_k", "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qmatvec_experts_q6_k",
+           "qk_row_bytes_q6_k", "qgemm_q4_k", "qgemm_q4_k_workspace_bytes",
            "qgemm_q4_k_noalloc", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
            "qk_version"]
@@ -53,15 +54,15 @@ def load(path: str | None = None):
             raise RuntimeError(f"libqk.so not built ({p}); run __graft_entry__.build()")
         lib = ctypes.CDLL(p)
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        for name in ("qmatvec_q8_0", "qmatvec_q4_k"):
+        for name in ("qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_q6_k"):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P]
             fn.restype = I
-        for name in ("qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k"):
+        for name in ("qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qmatvec_swiglu_q6_k"):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, I64, P, I, P, I64, P]
             fn.restype = I
-        for name in ("qmatvec_experts_q8_0", "qmatvec_experts_q4_k"):
+        for name in ("qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qmatvec_experts_q6_k"):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P, I64, P]
             fn.restype = I
@@ -71,7 +72,7 @@ def load(path: str | None = None):
         lib.qgemm_q4_k_workspace_bytes.restype = ctypes.c_size_t
         lib.qk_debug_gemm_skip_chunk.argtypes = [I]
         lib.qk_debug_gemm_skip_chunk.restype = I
-        for name in ("qk_row_bytes_q8_0", "qk_row_bytes_q4_k"):
+        for name in ("qk_row_bytes_q8_0", "qk_row_bytes_q4_k", "qk_row_bytes_q6_k"):
             getattr(lib, name).argtypes = [I64]
             getattr(lib, name).restype = I64
         lib.qk_status_string.argtypes = [I]
@@ -101,7 +102,7 @@ def _stream(stream) -> int:
 
 def row_bytes(fmt: str, K: int) -> int:
     lib = load()
-    return int(lib.qk_row_bytes_q8_0(K) if fmt == "q8_0" else lib.qk_row_bytes_q4_k(K))
+    return int({"q8_0": lib.qk_row_bytes_q8_0, "q4_k": lib.qk_row_bytes_q4_k, "q6_k": lib.qk_row_bytes_q6_k}[fmt](K))
 
 
 def _check(status: int, what: str):
@@ -144,7 +145,7 @@ def qmatvec_swiglu(fmt: str, w: torch.Tensor, gate_offset: int, up_offset: int, 
     if h is None:
         h = torch.empty((batch, F), dtype=torch.float32, device=x.device)
         ldh = F
-    name = {"q8_0": "qmatvec_swiglu_q8_0", "q4_k": "qmatvec_swiglu_q4_k"}[fmt]
+    name = {"q8_0": "qmatvec_swiglu_q8_0", "q4_k": "qmatvec_swiglu_q4_k", "q6_k": "qmatvec_swiglu_q6_k"}[fmt]
     st = getattr(load(), name)(w.data_ptr(), gate_offset, up_offset, F, K, x.data_ptr(), batch, h.data_ptr(),
                                ldh, _stream(stream))
     _check(st, name)
@@ -161,11 +162,17 @@ def qmatvec_experts(fmt: str, w: torch.Tensor, n_experts: int, rows: int, K: int
     if y is None:
         y = torch.empty((n_assign, rows), dtype=torch.float32, device=x.device)
         ldy = rows
-    name = {"q8_0": "qmatvec_experts_q8_0", "q4_k": "qmatvec_experts_q4_k"}[fmt]
+    name = {"q8_0": "qmatvec_experts_q8_0", "q4_k": "qmatvec_experts_q4_k", "q6_k": "qmatvec_experts_q6_k"}[fmt]
     st = getattr(load(), name)(w.data_ptr(), n_experts, rows, K, x.data_ptr(), xk, expert_ids.data_ptr(),
                                n_assign, y.data_ptr(), ldy, _stream(stream))
     _check(st, name)
     return y
+
+
+def qmatvec_q6_k(w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.Tensor,
+                 y: torch.Tensor | None = None, ldy: int = 0, stream=None) -> torch.Tensor:
+    """y[b][r] = sum_c W[row_offset + r][c] x[b][c] for Q6_K block bytes `w` (uint8, device)."""
+    return _qmatvec("qmatvec_q6_k", w, row_offset, rows, K, x, y, ldy, stream)
 
 
 def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
@@ -223,7 +230,7 @@ PLAN_FIELDS = ("SW", "R", "nkc", "rows_w", "stages", "stage_bytes", "smem", "gri
 def debug_gemv_plan(fmt: str, rows: int, K: int, batch: int) -> dict:
     """Test hook: the launch plan a GEMV call of this shape uses (needs a GPU)."""
     out = (ctypes.c_int64 * len(PLAN_FIELDS))()
-    n = load().qk_debug_gemv_plan({"q8_0": 0, "q4_k": 1}[fmt], int(rows), int(K), int(batch), out, len(PLAN_FIELDS))
+    n = load().qk_debug_gemv_plan({"q8_0": 0, "q4_k": 1, "q6_k": 2}[fmt], int(rows), int(K), int(batch), out, len(PLAN_FIELDS))
     if n < 0:
         raise QKError(8, "no GEMV plan fits")
     return dict(zip(PLAN_FIELDS, list(out)[:n]))

@@ -56,13 +56,15 @@ def test_row_bytes(lib):
     assert lib.qk_row_bytes_q8_0(40) == 2 * 34
     assert lib.qk_row_bytes_q4_k(896) == 4 * 144
     assert lib.qk_row_bytes_q4_k(4096) == 16 * 144
+    assert lib.qk_row_bytes_q6_k(4096) == 16 * 210
+    assert lib.qk_row_bytes_q6_k(300) == 2 * 210
     assert lib.qk_row_bytes_q4_k(0) == 0
 
 
 FAKE = 0x10000  # never dereferenced: validation fails first
 
 
-@pytest.mark.parametrize("name", ["qmatvec_q8_0", "qmatvec_q4_k"])
+@pytest.mark.parametrize("name", ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_q6_k"])
 def test_argument_validation_without_gpu(lib, name):
     f = getattr(lib, name)
     ok_args = dict(w=FAKE, off=0, rows=16, K=256, x=FAKE, batch=1, y=FAKE, ldy=0)
@@ -88,7 +90,7 @@ def test_argument_validation_without_gpu(lib, name):
         assert call(w=FAKE + 8) == 3  # Q4_K needs 16-byte aligned super-blocks
 
 
-@pytest.mark.parametrize("name", ["qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k"])
+@pytest.mark.parametrize("name", ["qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qmatvec_swiglu_q6_k"])
 def test_swiglu_argument_validation_without_gpu(lib, name):
     f = getattr(lib, name)
     f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -109,7 +111,7 @@ def test_swiglu_argument_validation_without_gpu(lib, name):
     assert call(x=FAKE + 2) == 3
 
 
-@pytest.mark.parametrize("name", ["qmatvec_experts_q8_0", "qmatvec_experts_q4_k"])
+@pytest.mark.parametrize("name", ["qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qmatvec_experts_q6_k"])
 def test_experts_argument_validation_without_gpu(lib, name):
     f = getattr(lib, name)
     f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,

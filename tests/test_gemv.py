@@ -19,7 +19,7 @@ REL, ABS = 1e-5, 1e-6
 def gpu_gemv(qk, fmt, wq, row_offset, rows, K, x, y=None, ldy=0):
     wd = torch.from_numpy(np.ascontiguousarray(wq)).cuda()
     xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
-    fn = qk.qmatvec_q8_0 if fmt == "q8_0" else qk.qmatvec_q4_k
+    fn = {"q8_0": qk.qmatvec_q8_0, "q4_k": qk.qmatvec_q4_k, "q6_k": qk.qmatvec_q6_k}[fmt]
     out = fn(wd, row_offset, rows, K, xd, y=y, ldy=ldy)
     torch.cuda.synchronize()
     return out
