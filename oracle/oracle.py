@@ -85,6 +85,8 @@ def _bind(lib):
     lib.qko_gemm_bf16.argtypes = [ctypes.c_int, P, I64, P, I64, P, I64, P, P]
     lib.qko_swiglu.argtypes = [ctypes.c_int, P, I64, P, P, I64, P, I64, P, P, P, P, P]
     lib.qko_experts.argtypes = [ctypes.c_int, P, I64, I64, I64, P, I64, P, I64, P, P]
+    lib.qko_swiglu_gemm_bf16.argtypes = [ctypes.c_int, P, I64, P, P, I64, P, I64, P, P, P, P, P]
+    lib.qko_swiglu_gemm_bf16.restype = ctypes.c_int
     lib.qko_experts.restype = ctypes.c_int
     lib.qko_swiglu.restype = ctypes.c_int
     lib.qko_gemm_bf16.restype = ctypes.c_int
@@ -170,6 +172,24 @@ def swiglu(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, gate_rows, up_rows, 
     out = [np.empty((B, n), dtype=np.float64) for _ in range(5)]
     rc = (lib or _load()).qko_swiglu(FMT[fmt], _ptr(wq), K, _ptr(gr), _ptr(ur), n, _ptr(x), B,
                                      *[_ptr(o) for o in out])
+    assert rc == 0
+    return tuple(out)
+
+
+def swiglu_gemm_bf16(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, gate_rows, up_rows, lib=None):
+    """(h, g, u, Sg, Su), f64 [M][n]: g, u the bf16 GEMM references of the gate and
+    up rows, h = silu(g) * u."""
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    assert x.shape[1] == K
+    nr = wq.size // row_bytes(fmt, K)
+    gr = _rows_arg(gate_rows, nr)
+    ur = _rows_arg(up_rows, nr)
+    assert gr.size == ur.size
+    M, n = x.shape[0], gr.size
+    out = [np.empty((M, n), dtype=np.float64) for _ in range(5)]
+    rc = (lib or _load()).qko_swiglu_gemm_bf16(FMT[fmt], _ptr(wq), K, _ptr(gr), _ptr(ur), n, _ptr(x), M,
+                                               *[_ptr(o) for o in out])
     assert rc == 0
     return tuple(out)
 

@@ -270,6 +270,9 @@ int qko_experts(int fmt, const uint8_t *wq, int64_t n_experts, int64_t rows, int
     return 0;
 }
 
+/* silu(z) = z * sigma(z) = z / (1 + e^-z) */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
 /*
  * Fused gate/up matvec with the SwiGLU product -- the decode FFN of the llama
  * shape, "RMSNorm -> GQA attention ... -> SwiGLU FFN" (nurllama README,
@@ -291,7 +294,7 @@ int qko_swiglu(int fmt, const uint8_t *wq, int64_t K, const int64_t *gate_rows, 
     if (rc) return rc;
     rc = qko_gemv(fmt, wq, K, up_rows, n, x, batch, u, su);
     if (rc) return rc;
-    for (int64_t i = 0; i < batch * n; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+    for (int64_t i = 0; i < batch * n; ++i) h[i] = silu(g[i]) * u[i];
     return 0;
 }
 
@@ -327,6 +330,24 @@ int qko_gemm_bf16(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows, in
     }
     free(w);
     free(xb);
+    return 0;
+}
+
+/*
+ * The SwiGLU form of the bf16 prefill GEMM (loom's gen_gemm.py "modes:
+ * store, acc, swiglu", loom-port-llm SKILL.md, "What the starter
+ * generates"): g and u are the bf16 references of qko_gemm_bf16 for the gate
+ * and up rows, h = silu(g) * u in f64 (layout [M][n]).
+ */
+int qko_swiglu_gemm_bf16(int fmt, const uint8_t *wq, int64_t K, const int64_t *gate_rows, const int64_t *up_rows,
+                         int64_t n, const float *x, int64_t M, double *h, double *g, double *u, double *sg,
+                         double *su)
+{
+    int rc = qko_gemm_bf16(fmt, wq, K, gate_rows, n, x, M, g, sg);
+    if (rc) return rc;
+    rc = qko_gemm_bf16(fmt, wq, K, up_rows, n, x, M, u, su);
+    if (rc) return rc;
+    for (int64_t i = 0; i < M * n; ++i) h[i] = silu(g[i]) * u[i];
     return 0;
 }
 

@@ -319,3 +319,28 @@ def test_experts_select_expert_and_input_row(orc, xk):
     y, s = orc.experts("q8_0", wq, E, rows, 32, x, xk, ids)
     for a in range(n):
         assert np.array_equal(y[a], (ids[a] + 1) * x[a // xk, :rows].astype(np.float64))
+
+
+def test_swiglu_gemm_reference_on_bf16_exact_inputs(orc):
+    """Weights and activations exact in bf16: the bf16 GEMM form of SwiGLU equals
+    the exact one, and a unit-vector gate/up pair gives silu(x0) * x1."""
+    wq = _unit_rows_q8_0(4)
+    x = np.zeros((3, 32), np.float32)
+    x[:, 0] = [0.5, -2.0, 3.0]          # bf16-exact values
+    x[:, 1] = [1.0, 0.25, -1.5]
+    h, g, u, _, _ = orc.swiglu_gemm_bf16("q8_0", wq, 32, x, [0], [1])
+    he, _, _, _, _ = orc.swiglu("q8_0", wq, 32, x, [0], [1])
+    assert np.array_equal(h, he)
+    assert np.array_equal(g[:, 0], x[:, 0].astype(np.float64)) and np.array_equal(u[:, 0], x[:, 1].astype(np.float64))
+    assert abs(h[0, 0] - 0.5 / (1 + np.exp(-0.5)) * 1.0) < 1e-15
+
+
+def test_swiglu_gemm_reference_rounds_to_bf16(orc):
+    """A gate value that bf16 cannot hold is rounded before silu: x0 = 1 + 2^-9
+    is bf16 1.0 (ties to even), so g = 1 exactly."""
+    wq = _unit_rows_q8_0(2)
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 1] = 1.0 + 2.0 ** -9, 1.0
+    h, g, u, _, _ = orc.swiglu_gemm_bf16("q8_0", wq, 32, x, [0], [1])
+    assert g[0, 0] == 1.0
+    assert abs(h[0, 0] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15

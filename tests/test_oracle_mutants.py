@@ -34,8 +34,8 @@ MUTATIONS = {
     "gemm_skips_w_rounding": ("w[c] = qko_bf16_to_f64(qko_f32_to_bf16((float)w[c]));", "w[c] = (double)(float)w[c];"),
     "q8_encode_no_clamp_sign": ("if (q < -127.0) q = -127.0;", "if (q < -127.0) q = 127.0;"),
     "q4_encode_high_nibble": ("(uint8_t)(best << 4);", "(uint8_t)(best << 3);"),
-    "swiglu_gate_up_swapped": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = u[i] / (1.0 + exp(-u[i])) * g[i];"),
-    "silu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+    "swiglu_gate_up_swapped": ("i < batch * n; ++i) h[i] = silu(g[i]) * u[i];", "i < batch * n; ++i) h[i] = silu(u[i]) * g[i];"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     "q6_qh_shift": ("(blk[128 + 32 * n + l] >> (2 * t)) & 3;", "(blk[128 + 32 * n + l] >> t) & 3;"),
     "q6_ql_half": ("blk[64 * n + l + 32 * (t % 2)];", "blk[64 * n + l + 32 * (t / 2)];"),
     "q6_scale_index": ("blk[192 + i / 16];", "blk[192 + i / 32];"),
@@ -43,7 +43,10 @@ MUTATIONS = {
     "q6_scale_unsigned": ("(int)(int8_t)blk[192 + i / 16];", "(int)blk[192 + i / 16];"),
     "experts_input_row_mod": ("x + (a / xk) * K, 1, y + a * rows", "x + (a % xk) * K, 1, y + a * rows"),
     "experts_ignores_id": ("idx[r] = e * rows + r;", "idx[r] = r;"),
-    "silu_missing_z": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = 1.0 / (1.0 + exp(-g[i])) * u[i];"),
+    "swiglu_gemm_exact_gate": ("int rc = qko_gemm_bf16(fmt, wq, K, gate_rows, n, x, M, g, sg);",
+                               "int rc = qko_gemv(fmt, wq, K, gate_rows, n, x, M, g, sg);"),
+    "silu_missing_z": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    "swiglu_gemm_gate_up_swapped": ("i < M * n; ++i) h[i] = silu(g[i]) * u[i];", "i < M * n; ++i) h[i] = silu(u[i]) * g[i];"),
 }
 
 PINS = [
@@ -66,6 +69,8 @@ PINS = [
     (pins.test_swiglu_known_values, {}),
     (pins.test_swiglu_odd_part_identity, {"z": 1.75}),
     (pins.test_experts_select_expert_and_input_row, {"xk": 2}),
+    (pins.test_swiglu_gemm_reference_rounds_to_bf16, {}),
+    (pins.test_swiglu_gemm_reference_on_bf16_exact_inputs, {}),
 ]
 
 
