@@ -187,6 +187,30 @@ int qmatvec_experts_q6_k(const void *w, int64_t n_experts, int64_t rows, int64_t
 int qgemm_q4_k(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
                float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream);
 
+/*
+ * Accumulating form of qgemm_q4_k: y[m*ldy + n] += sum_k bf16(W[row_offset+n][k]) * bf16(x[m*K + k]),
+ * the "acc" mode of loom's prefill GEMMs ("Modes: store, acc, swiglu",
+ * loom-port-llm SKILL.md, "What the starter generates", gen_gemm.py): the
+ * product lands on what y holds (e.g. the residual stream).  Same arguments,
+ * errors and bound as qgemm_q4_k, plus one fp32 rounding of the final add.
+ */
+int qgemm_q4_k_acc(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+                   float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream);
+
+/*
+ * SwiGLU form of the prefill GEMM (loom's "swiglu" mode, same source): for
+ * m < M and p < F
+ *   g = sum_k bf16(W[gate_offset + p][k]) * bf16(x[m*K + k])
+ *   u = sum_k bf16(W[up_offset + p][k])   * bf16(x[m*K + k])
+ *   h[m*ldh + p] = silu(g) * u,   silu(z) = z / (1 + e^-z)  (CUDA expf),
+ * g and u accumulated in fp32 on the tensor cores exactly as qgemm_q4_k's
+ * outputs.  Gate and up are row ranges of one Q4_K tensor (or of one
+ * allocation holding both); gate_offset, up_offset >= 0.  Workspace and
+ * errors as qgemm_q4_k (ldh == 0 means ldh = F).
+ */
+int qgemm_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K, const float *x,
+                      int64_t M, float *h, int64_t ldh, void *workspace, size_t workspace_bytes, qk_stream_t stream);
+
 /* Workspace bytes qgemm_q4_k needs for M tokens and K columns (N unused). */
 size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

@@ -23,6 +23,7 @@
 // Double-buffered stages synchronise through mbarriers; every wait is bounded
 // and a wait that runs out aborts the CTA cleanly (copies drained, MMAs
 // completed, tensor memory freed) and records the device error word.
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,24 +37,35 @@ namespace qk {
 
 namespace gemm {
 
-constexpr int kBM = 128;                 // weight rows per CTA (MMA M)
+constexpr int kBM = 128;                 // weight rows per tile (MMA M)
 constexpr int kBN = 256;                 // tokens per MMA (MMA N)
-constexpr int kHalves = 2;               // tokens per CTA pass = kBN * kHalves
 constexpr int kBK = 64;                  // K columns per stage (one 128-byte swizzle row)
 constexpr int kStages = 2;
 constexpr int kRawStages = 2;
 constexpr int kRawBytes = kBM * 144;     // one Q4_K super-block column of 128 rows
-constexpr int kBStage = kHalves * kBN * kBK * 2;   // 64 KB
-constexpr int kAStage = kBM * kBK * 2;             // 16 KB
-constexpr int kOffB = 0;
-constexpr int kOffA = kOffB + kStages * kBStage;
-constexpr int kOffRaw = kOffA + kStages * kAStage;
-constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 
-// barrier slots (8 bytes each) after kOffBar
+// Modes: Y = X W^T (store), Y += X W^T (acc), or H = silu(X Wg^T) * (X Wu^T)
+// (swiglu: a gate tile and an up tile per CTA, half the tokens).
+constexpr int kStore = 0, kAcc = 1, kSwiglu = 2;
+
+template <int MODE>
+struct Shape {
+    static constexpr int halves = MODE == kSwiglu ? 1 : 2;   // token blocks of kBN per CTA pass
+    static constexpr int tiles = MODE == kSwiglu ? 2 : 1;    // weight tiles per K chunk
+    static constexpr int b_stage = halves * kBN * kBK * 2;
+    static constexpr int a_tile = kBM * kBK * 2;             // 16 KB
+    static constexpr int a_stage = tiles * a_tile;
+    static constexpr int raw_stage = tiles * kRawBytes;
+    static constexpr int off_b = 0;
+    static constexpr int off_a = off_b + kStages * b_stage;
+    static constexpr int off_raw = off_a + kStages * a_stage;
+    static constexpr int off_bar = off_raw + kRawStages * raw_stage;
+    static constexpr int smem = off_bar + 256 + 1024;        // + alignment slack
+};
+
+// barrier slots (8 bytes each) after the barrier offset
 constexpr int kBarXFull = 0, kBarAFull = 2, kBarEmpty = 4, kBarRawFull = 6, kBarRawEmpty = 8, kBarAcc = 10,
               kBarDone = 11;
 constexpr int kOffTmemSlot = 96, kOffAbort = 100;
@@ -61,6 +73,7 @@ constexpr int kOffTmemSlot = 96, kOffAbort = 100;
 struct Args {
     float *y;
     int64_t N, K, M, ldy;
+    int row0[2];       // tensor-map row of output row 0 for the weight tile (swiglu: gate, up)
     int n_tiles;
     int nk;            // number of 64-column K chunks
     int skip_chunk;    // test hook: CTA 0 never loads the activations of this chunk (-1: none)
@@ -78,9 +91,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     return false;
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const Args a)
 {
+    using L = Shape<MODE>;
+    constexpr int kHalves = L::halves, kTiles = L::tiles;
+    constexpr int kOffB = L::off_b, kOffA = L::off_a, kOffRaw = L::off_raw, kOffBar = L::off_bar;
+    constexpr int kBStage = L::b_stage, kAStage = L::a_stage, kRawStage = L::raw_stage;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
@@ -95,7 +113,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int m_block = blockIdx.x / a.n_tiles;
     const int n0 = n_tile * kBM;
     const int m0 = m_block * (kBN * kHalves);
-    const int nh = (a.M - m0) > kBN ? 2 : 1;          // token halves used in this pass
+    const int nh = (kHalves == 2 && (a.M - m0) > kBN) ? 2 : 1;   // token blocks of kBN used in this pass
     const int nk = a.nk;
 
     if (tid == 0) {
@@ -137,8 +155,10 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         !wait_or_abort(bar(kBarRawEmpty + r), ((kb / kRawStages) - 1) & 1, a.wait_ns, abort_flag,
                                        a.err))
                         break;
-                    mbar_arrive_expect_tx(bar(kBarRawFull + r), kRawBytes);
-                    tma_load_2d(base_u32 + kOffRaw + r * kRawBytes, &tm_w, kb * 144, n0, bar(kBarRawFull + r), pol_w);
+                    mbar_arrive_expect_tx(bar(kBarRawFull + r), kTiles * kRawBytes);
+                    for (int i = 0; i < kTiles; ++i)
+                        tma_load_2d(base_u32 + kOffRaw + r * kRawStage + i * kRawBytes, &tm_w, kb * 144,
+                                    a.row0[i] + n0, bar(kBarRawFull + r), pol_w);
                     ++issued_raw;
                 }
                 const int s = kc % kStages;
@@ -178,10 +198,14 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const uint32_t b_base = base_u32 + kOffB + s * kBStage;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128_kmajor(a_base + 32u * kk);
-                    for (int h = 0; h < nh; ++h) {
-                        const uint64_t bd = smem_desc_sw128_kmajor(b_base + h * (kBN * kBK * 2) + 32u * kk);
-                        tc_mma_bf16(taddr + static_cast<uint32_t>(h * kBN), ad, bd, idesc, (kc | kk) != 0);
+#pragma unroll
+                    for (int i = 0; i < kTiles; ++i) {
+                        const uint64_t ad = smem_desc_sw128_kmajor(a_base + i * L::a_tile + 32u * kk);
+                        for (int h = 0; h < nh; ++h) {
+                            // accumulator columns: token block h (store/acc) or weight tile i (swiglu)
+                            const uint64_t bd = smem_desc_sw128_kmajor(b_base + h * (kBN * kBK * 2) + 32u * kk);
+                            tc_mma_bf16(taddr + static_cast<uint32_t>((h + i) * kBN), ad, bd, idesc, (kc | kk) != 0);
+                        }
                     }
                 }
                 any = true;
@@ -206,50 +230,53 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (kc >= kStages &&
                 !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
                 break;
-            const uint8_t *row = base + kOffRaw + r * kRawBytes + t * 144;
-            const uint4 hd = *reinterpret_cast<const uint4 *>(row);
-            const float d = half_bits_to_float(hd.x);
-            const float dmin = half_bits_to_float(hd.x >> 16);
-            // 6-bit scale and min of sub-blocks 2c (low nibbles) and 2c+1 (high)
-            const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
-            const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-            const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-            const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
-            const int j0 = 2 * (c & 1);   // byte of the packed words for sub-block 2c
-            const float sc0 = static_cast<float>((scw >> (8 * j0)) & 0xFFu);
-            const float sc1 = static_cast<float>((scw >> (8 * j0 + 8)) & 0xFFu);
-            const float mm0 = static_cast<float>((mw >> (8 * j0)) & 0xFFu);
-            const float mm1 = static_cast<float>((mw >> (8 * j0 + 8)) & 0xFFu);
-            const float ds0 = d * sc0, ds1 = d * sc1, dm0 = dmin * mm0, dm1 = dmin * mm1;
-            const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
-            const uint32_t a_row = base_u32 + kOffA + s * kAStage + t * 128;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {            // bytes 16*half .. 16*half+15 of the chunk
-                const uint4 qv = qs[half];
-                const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-                for (int sel = 0; sel < 2; ++sel) {           // 0: low nibbles (cols i), 1: high (cols 32+i)
-                    const float ds = sel ? ds1 : ds0, dm = sel ? dm1 : dm0;
-                    // 16 weights: columns 32*sel + 16*half + [0, 16) of this chunk
-                    uint32_t packed[8];
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const uint32_t v = sel ? (w4[wi] >> 4) : w4[wi];
-                        const float q0 = static_cast<float>(v & 15u), q1 = static_cast<float>((v >> 8) & 15u);
-                        const float q2 = static_cast<float>((v >> 16) & 15u), q3 = static_cast<float>((v >> 24) & 15u);
-                        const __nv_bfloat162 p01 = __floats2bfloat162_rn(fmaf(q0, ds, -dm), fmaf(q1, ds, -dm));
-                        const __nv_bfloat162 p23 = __floats2bfloat162_rn(fmaf(q2, ds, -dm), fmaf(q3, ds, -dm));
-                        packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
-                        packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
-                    }
-                    // two 16-byte chunks (8 columns each) of the swizzled row
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
-                        const int chunk = 4 * sel + 2 * half + h8;          // logical 16-byte chunk 0..7
-                        const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
-                                     "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
-                                     : "memory");
+            for (int i = 0; i < kTiles; ++i) {
+                const uint8_t *row = base + kOffRaw + r * kRawStage + i * kRawBytes + t * 144;
+                const uint4 hd = *reinterpret_cast<const uint4 *>(row);
+                const float d = half_bits_to_float(hd.x);
+                const float dmin = half_bits_to_float(hd.x >> 16);
+                // 6-bit scale and min of sub-blocks 2c (low nibbles) and 2c+1 (high)
+                const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
+                const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+                const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+                const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
+                const int j0 = 2 * (c & 1);   // byte of the packed words for sub-block 2c
+                const float sc0 = static_cast<float>((scw >> (8 * j0)) & 0xFFu);
+                const float sc1 = static_cast<float>((scw >> (8 * j0 + 8)) & 0xFFu);
+                const float mm0 = static_cast<float>((mw >> (8 * j0)) & 0xFFu);
+                const float mm1 = static_cast<float>((mw >> (8 * j0 + 8)) & 0xFFu);
+                const float ds0 = d * sc0, ds1 = d * sc1, dm0 = dmin * mm0, dm1 = dmin * mm1;
+                const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
+                const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
+    #pragma unroll
+                for (int half = 0; half < 2; ++half) {            // bytes 16*half .. 16*half+15 of the chunk
+                    const uint4 qv = qs[half];
+                    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+    #pragma unroll
+                    for (int sel = 0; sel < 2; ++sel) {           // 0: low nibbles (cols i), 1: high (cols 32+i)
+                        const float ds = sel ? ds1 : ds0, dm = sel ? dm1 : dm0;
+                        // 16 weights: columns 32*sel + 16*half + [0, 16) of this chunk
+                        uint32_t packed[8];
+    #pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const uint32_t v = sel ? (w4[wi] >> 4) : w4[wi];
+                            const float q0 = static_cast<float>(v & 15u), q1 = static_cast<float>((v >> 8) & 15u);
+                            const float q2 = static_cast<float>((v >> 16) & 15u), q3 = static_cast<float>((v >> 24) & 15u);
+                            const __nv_bfloat162 p01 = __floats2bfloat162_rn(fmaf(q0, ds, -dm), fmaf(q1, ds, -dm));
+                            const __nv_bfloat162 p23 = __floats2bfloat162_rn(fmaf(q2, ds, -dm), fmaf(q3, ds, -dm));
+                            packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
+                            packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                        }
+                        // two 16-byte chunks (8 columns each) of the swizzled row
+    #pragma unroll
+                        for (int h8 = 0; h8 < 2; ++h8) {
+                            const int chunk = 4 * sel + 2 * half + h8;          // logical 16-byte chunk 0..7
+                            const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
+                                         "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
+                                         : "memory");
+                        }
                     }
                 }
             }
@@ -257,21 +284,39 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             mbar_arrive(bar(kBarAFull + s));
             if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
         }
-        // epilogue: tensor memory -> registers -> Y
+        // epilogue: tensor memory -> registers -> Y (store, acc) or H (swiglu)
         if (wait_or_abort(bar(kBarAcc), 0, a.wait_ns, abort_flag, a.err)) {
             tc_fence_after();
             const int q = warp & 3;                         // lane quarter this warp may access
             const int n = n0 + 32 * q + lane;
+            const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * q) << 16);
             const int cols = nh * kBN;
             for (int j0 = 0; j0 < cols; j0 += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(j0), v);
-                tmem_ld_wait();
-                if (n < a.N) {
+                tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
+                if constexpr (MODE == kSwiglu) {
+                    uint32_t u[32];                            // the up tile's accumulators
+                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kBN + j0), u);
+                    tmem_ld_wait();
+                    if (n < a.N) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int64_t m = m0 + j0 + i;
-                        if (m < a.M) a.y[m * a.ldy + n] = __uint_as_float(v[i]);
+                        for (int i = 0; i < 32; ++i) {
+                            const int64_t m = m0 + j0 + i;
+                            const float g = __uint_as_float(v[i]);
+                            if (m < a.M) a.y[m * a.ldy + n] = g / (1.0f + expf(-g)) * __uint_as_float(u[i]);
+                        }
+                    }
+                } else {
+                    tmem_ld_wait();
+                    if (n < a.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int64_t m = m0 + j0 + i;
+                            if (m < a.M) {
+                                float *yp = a.y + m * a.ldy + n;
+                                *yp = MODE == kAcc ? *yp + __uint_as_float(v[i]) : __uint_as_float(v[i]);
+                            }
+                        }
                     }
                 }
             }
@@ -323,9 +368,31 @@ int64_t gemm_k8(int64_t K) { return (K + 7) / 8 * 8; }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t K) { return static_cast<size_t>(M * gemm_k8(K) * 2 + 256); }
 
+namespace {
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const gemm::Args &a, int64_t grid,
+                        cudaStream_t st)
+{
+    using namespace gemm;
+    static int granted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && granted[dev] == 0) {
+        e = cudaFuncSetAttribute(gemm_q4k_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<MODE>::smem);
+        if (e != cudaSuccess) return e;
+        granted[dev] = 1;
+    }
+    gemm_q4k_kernel<MODE><<<static_cast<unsigned>(grid), kThreads, Shape<MODE>::smem, st>>>(tm_x, tm_w, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                             int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
-                            bool *encode_failed)
+                            bool *encode_failed, int mode, int64_t up_rows)
 {
     using namespace gemm;
     *encode_failed = false;
@@ -358,12 +425,17 @@ cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const f
             return cudaErrorInvalidValue;
         }
     }
+    // the weight map spans the rows of every tile: [0, N) and, for swiglu,
+    // the up rows [up_rows, up_rows + N) relative to w_rows
+    const int64_t lo = mode == kSwiglu ? std::min<int64_t>(0, up_rows) : 0;
+    const int64_t hi = mode == kSwiglu ? std::max<int64_t>(N, up_rows + N) : N;
     {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(N)};
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(hi - lo)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
         const cuuint32_t box[2] = {144u, static_cast<cuuint32_t>(kBM)};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows), dims, strides, box, estr,
+        if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows + lo * row_bytes), dims,
+                strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
             *encode_failed = true;
@@ -376,24 +448,19 @@ cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const f
     a.K = K;
     a.M = M;
     a.ldy = ldy;
+    a.row0[0] = static_cast<int>(-lo);
+    a.row0[1] = static_cast<int>(up_rows - lo);
     a.n_tiles = static_cast<int>((N + kBM - 1) / kBM);
     a.nk = static_cast<int>((K8 + kBK - 1) / kBK);
     a.skip_chunk = skip_chunk;
     a.wait_ns = wait_ns;
     a.err = err;
-    const int64_t m_blocks = (M + kBN * kHalves - 1) / (kBN * kHalves);
+    const int64_t per_cta = mode == kSwiglu ? kBN : 2 * kBN;   // tokens per CTA pass
+    const int64_t m_blocks = (M + per_cta - 1) / per_cta;
     const int64_t grid = a.n_tiles * m_blocks;
-    static int granted[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && granted[dev] == 0) {
-        e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        granted[dev] = 1;
-    }
-    gemm_q4k_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(tm_x, tm_w, a);
-    return cudaGetLastError();
+    if (mode == kSwiglu) return launch_mode<kSwiglu>(tm_x, tm_w, a, grid, st);
+    if (mode == kAcc) return launch_mode<kAcc>(tm_x, tm_w, a, grid, st);
+    return launch_mode<kStore>(tm_x, tm_w, a, grid, st);
 }
 
 }  // namespace qk
