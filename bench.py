@@ -452,10 +452,10 @@ def measure_extra_rows(torch, qk, synth, device, stream):
                       "cache": "cold (rotated copies > L2)" if copies * rows * rb > l2 else "hot (L2-resident)"}
         del ws
 
-    def gemm_row(label, M, N, K, seed, copies, mode="store"):
+    def gemm_row(label, M, N, K, seed, copies, mode="store", fmt="q4_k"):
         """mode store: y = x W^T; swiglu: N gate rows and N up rows, h = silu(g) * u."""
         wrows = 2 * N if mode == "swiglu" else N
-        ws = [torch.from_numpy(synth.weights("q4_k", wrows, K, seed=seed, stream0=50 * c)).to(device)
+        ws = [torch.from_numpy(synth.weights(fmt, wrows, K, seed=seed, stream0=50 * c)).to(device)
               for c in range(copies)]
         x = torch.from_numpy(synth.activations(M, K, seed=seed)).to(device)
         y = torch.empty((M, N), device=device)
@@ -465,11 +465,11 @@ def measure_extra_rows(torch, qk, synth, device, stream):
         def mk(w):
             def f(sh):
                 if mode == "swiglu":
-                    st = lib.qgemm_swiglu_q4_k(w.data_ptr(), 0, N, N, K, x.data_ptr(), M, y.data_ptr(), N,
-                                               wsp.data_ptr(), nbytes, sh)
+                    fn = lib.qgemm_swiglu_q4_k if fmt == "q4_k" else lib.qgemm_swiglu_q8_0
+                    st = fn(w.data_ptr(), 0, N, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(), nbytes, sh)
                 else:
-                    st = lib.qgemm_q4_k(w.data_ptr(), 0, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(),
-                                        nbytes, sh)
+                    fn = lib.qgemm_q4_k if fmt == "q4_k" else lib.qgemm_q8_0
+                    st = fn(w.data_ptr(), 0, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(), nbytes, sh)
                 assert st == 0
             return f
         avg_ms = time_calls(torch, stream, [mk(w) for w in ws] * max(1, 4 // copies), 20)
@@ -531,6 +531,8 @@ def measure_extra_rows(torch, qk, synth, device, stream):
 
     gemm_row("q4_k_gemm_512x4096x14336", 512, 14336, 4096, 4, 2)
     gemm_row("q4_k_gemm_swiglu_512x4096x2x14336", 512, 14336, 4096, 4, 2, mode="swiglu")
+    gemm_row("q8_0_gemm_512x4096x14336", 512, 14336, 4096, 4, 2, fmt="q8_0")
+    gemm_row("q8_0_gemm_512x896x4864", 512, 4864, 896, 1, 1, fmt="q8_0")
     experts_row("q4_k_experts_moe_top8_128x1536x2048", "q4_k", 128, 1536, 2048, 8, 8, 5)
     swiglu_row("q4_k_swiglu_llama8b_ffn_14336x4096_b1", "q4_k", 14336, 4096, 1, 2, 4)
     gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1)

@@ -211,7 +211,20 @@ int qgemm_q4_k_acc(const void *w, int64_t row_offset, int64_t N, int64_t K, cons
 int qgemm_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K, const float *x,
                       int64_t M, float *h, int64_t ldh, void *workspace, size_t workspace_bytes, qk_stream_t stream);
 
-/* Workspace bytes qgemm_q4_k needs for M tokens and K columns (N unused). */
+/*
+ * Q8_0 forms of the prefill GEMM (loom's prefill GEMM formats include q8_0,
+ * loom-port-llm SKILL.md, "What the starter generates", gen_gemm.py): the same
+ * three modes with Q8_0 weights (w = d*q, rounded to bf16), w 2-byte aligned
+ * (34-byte blocks); arguments, workspace, errors and bounds as the Q4_K forms.
+ */
+int qgemm_q8_0(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+               float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream);
+int qgemm_q8_0_acc(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+                   float *y, int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream);
+int qgemm_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K, const float *x,
+                      int64_t M, float *h, int64_t ldh, void *workspace, size_t workspace_bytes, qk_stream_t stream);
+
+/* Workspace bytes the prefill GEMMs need for M tokens and K columns (N unused). */
 size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*

@@ -89,7 +89,7 @@ size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K)
 
 namespace {
 
-int gemm_entry(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+int gemm_entry(int fmt, const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream, int mode,
                int64_t up_offset)
 {
@@ -97,21 +97,21 @@ int gemm_entry(const void *w, int64_t row_offset, int64_t N, int64_t K, const fl
     if (N <= 0 || K <= 0 || M <= 0 || row_offset < 0 || up_offset < 0) return QK_ERR_BAD_DIM;
     if (ldy == 0) ldy = N;
     if (ldy < N) return QK_ERR_BAD_DIM;
-    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
+    if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < qk::gemm_workspace_bytes(M, K))
         return QK_ERR_WORKSPACE;
     // tensor-map limits: at most 2^31 tokens and rows per call
     const int64_t last = row_offset > up_offset ? row_offset : up_offset;
     if (M > (1LL << 31) - 1 || K > (1LL << 31) - 1 || last > (1LL << 31) - 1 - N) return QK_ERR_TOO_LARGE;
-    const int64_t row_bytes = ((K + 255) / 256) * 144;
+    const int64_t row_bytes = fmt == qk::kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
     if (last > (INT64_MAX / row_bytes) - N) return QK_ERR_BAD_DIM;
     int *err = error_word_ptr();
     if (!err) return QK_ERR_CUDA;
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * row_bytes;
     bool encode_failed = false;
-    cudaError_t e = qk::gemm_q4k_launch(w_rows, N, K, x, M, y, ldy, workspace,
-                                        reinterpret_cast<cudaStream_t>(stream), err, g_wait_limit_ns.load(),
-                                        g_gemm_skip_chunk.load(), &encode_failed, mode, up_offset - row_offset);
+    cudaError_t e = qk::gemm_launch(fmt, w_rows, N, K, x, M, y, ldy, workspace,
+                                    reinterpret_cast<cudaStream_t>(stream), err, g_wait_limit_ns.load(),
+                                    g_gemm_skip_chunk.load(), &encode_failed, mode, up_offset - row_offset);
     if (encode_failed) return QK_ERR_CUDA;
     return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
 }
@@ -123,19 +123,38 @@ extern "C" {
 int qgemm_q4_k(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream)
 {
-    return gemm_entry(w, row_offset, N, K, x, M, y, ldy, workspace, workspace_bytes, stream, 0, 0);
+    return gemm_entry(qk::kFmtQ4K, w, row_offset, N, K, x, M, y, ldy, workspace, workspace_bytes, stream, 0, 0);
 }
 
 int qgemm_q4_k_acc(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                    int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream)
 {
-    return gemm_entry(w, row_offset, N, K, x, M, y, ldy, workspace, workspace_bytes, stream, 1, 0);
+    return gemm_entry(qk::kFmtQ4K, w, row_offset, N, K, x, M, y, ldy, workspace, workspace_bytes, stream, 1, 0);
+}
+
+int qgemm_q8_0(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+               int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream)
+{
+    return gemm_entry(qk::kFmtQ80, w, row_offset, N, K, x, M, y, ldy, workspace, workspace_bytes, stream, 0, 0);
+}
+
+int qgemm_q8_0_acc(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                   int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream)
+{
+    return gemm_entry(qk::kFmtQ80, w, row_offset, N, K, x, M, y, ldy, workspace, workspace_bytes, stream, 1, 0);
+}
+
+int qgemm_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K, const float *x,
+                      int64_t M, float *h, int64_t ldh, void *workspace, size_t workspace_bytes, qk_stream_t stream)
+{
+    return gemm_entry(qk::kFmtQ80, w, gate_offset, F, K, x, M, h, ldh, workspace, workspace_bytes, stream, 2,
+                      up_offset);
 }
 
 int qgemm_swiglu_q4_k(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K, const float *x,
                       int64_t M, float *h, int64_t ldh, void *workspace, size_t workspace_bytes, qk_stream_t stream)
 {
-    return gemm_entry(w, gate_offset, F, K, x, M, h, ldh, workspace, workspace_bytes, stream, 2, up_offset);
+    return gemm_entry(qk::kFmtQ4K, w, gate_offset, F, K, x, M, h, ldh, workspace, workspace_bytes, stream, 2, up_offset);
 }
 
 int qmatvec_q8_0(const void *w, int64_t row_offset, int64_t rows, int64_t K, const float *x,

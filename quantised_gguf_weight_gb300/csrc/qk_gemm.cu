@@ -1,7 +1,8 @@
-// qk_gemm.cu -- prefill GEMM with GGUF Q4_K weights on the tcgen05 tensor
-// cores (sm_103a):  Y[m][n] = sum_k bf16(x[m][k]) * bf16(w[n][k]),
-// f32 accumulation, where w = d*sc*q - dmin*m is computed in fp32 and rounded
-// to bf16 (round to nearest even) in shared memory, once per weight.
+// qk_gemm.cu -- prefill GEMM with GGUF Q4_K or Q8_0 weights on the tcgen05
+// tensor cores (sm_103a):  Y[m][n] = sum_k bf16(x[m][k]) * bf16(w[n][k]),
+// f32 accumulation, where w (Q4_K: d*sc*q - dmin*m; Q8_0: d*q) is computed in
+// fp32 and rounded to bf16 (round to nearest even) in shared memory, once per
+// weight.
 //
 // This is the prefill counterpart of the decode matvec: the chunked prefill
 // runs the matmuls over many positions at once so that "each weight is read
@@ -50,14 +51,14 @@ constexpr uint32_t kTmemCols = 512;
 // (swiglu: a gate tile and an up tile per CTA, half the tokens).
 constexpr int kStore = 0, kAcc = 1, kSwiglu = 2;
 
-template <int MODE>
+template <int FMT, int MODE>
 struct Shape {
     static constexpr int halves = MODE == kSwiglu ? 1 : 2;   // token blocks of kBN per CTA pass
     static constexpr int tiles = MODE == kSwiglu ? 2 : 1;    // weight tiles per K chunk
     static constexpr int b_stage = halves * kBN * kBK * 2;
     static constexpr int a_tile = kBM * kBK * 2;             // 16 KB
     static constexpr int a_stage = tiles * a_tile;
-    static constexpr int raw_stage = tiles * kRawBytes;
+    static constexpr int raw_stage = FMT == kFmtQ80 ? 0 : tiles * kRawBytes;   // Q8_0 reads weights directly
     static constexpr int off_b = 0;
     static constexpr int off_a = off_b + kStages * b_stage;
     static constexpr int off_raw = off_a + kStages * a_stage;
@@ -74,6 +75,9 @@ struct Args {
     float *y;
     int64_t N, K, M, ldy;
     int row0[2];       // tensor-map row of output row 0 for the weight tile (swiglu: gate, up)
+    const uint8_t *wq8[2];  // Q8_0: first byte of output row 0 of each weight tile (read directly)
+    int64_t row_bytes;      // Q8_0: bytes of one weight row
+    int nb;                 // Q8_0: blocks of 32 per row
     int n_tiles;
     int nk;            // number of 64-column K chunks
     int skip_chunk;    // test hook: CTA 0 never loads the activations of this chunk (-1: none)
@@ -91,11 +95,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     return false;
 }
 
-template <int MODE>
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const Args a)
 {
-    using L = Shape<MODE>;
+    constexpr bool kQ8 = FMT == kFmtQ80;        // Q8_0: weights read directly by the dequantising threads
+    using L = Shape<FMT, MODE>;
     constexpr int kHalves = L::halves, kTiles = L::tiles;
     constexpr int kOffB = L::off_b, kOffA = L::off_a, kOffRaw = L::off_raw, kOffBar = L::off_bar;
     constexpr int kBStage = L::b_stage, kAStage = L::a_stage, kRawStage = L::raw_stage;
@@ -131,7 +136,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
-        tma_prefetch_desc(&tm_w);
+        if (!kQ8) tma_prefetch_desc(&tm_w);
     }
     if (warp == 1) {
         tmem_alloc(base_u32 + kOffBar + kOffTmemSlot, kTmemCols);
@@ -149,7 +154,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint64_t pol_x = l2_evict_last_policy();
             int issued_x = 0, issued_raw = 0;
             for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
-                if ((kc & 3) == 0) {
+                if (!kQ8 && (kc & 3) == 0) {
                     const int kb = kc >> 2, r = kb % kRawStages;
                     if (kb >= kRawStages &&
                         !wait_or_abort(bar(kBarRawEmpty + r), ((kb / kRawStages) - 1) & 1, a.wait_ns, abort_flag,
@@ -222,56 +227,135 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     } else {
         // ------------------------------------------------------------ dequantise + epilogue
         const int t = tid - 64;          // 0..127: the weight row of this thread inside the tile
-        for (int kc = 0; kc < nk; ++kc) {
-            const int s = kc % kStages;
-            const int kb = kc >> 2, c = kc & 3, r = kb % kRawStages;
-            if (c == 0 && !wait_or_abort(bar(kBarRawFull + r), (kb / kRawStages) & 1, a.wait_ns, abort_flag, a.err))
-                break;
-            if (kc >= kStages &&
-                !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
-                break;
-#pragma unroll
-            for (int i = 0; i < kTiles; ++i) {
-                const uint8_t *row = base + kOffRaw + r * kRawStage + i * kRawBytes + t * 144;
-                const uint4 hd = *reinterpret_cast<const uint4 *>(row);
-                const float d = half_bits_to_float(hd.x);
-                const float dmin = half_bits_to_float(hd.x >> 16);
-                // 6-bit scale and min of sub-blocks 2c (low nibbles) and 2c+1 (high)
-                const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
-                const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-                const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-                const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
-                const int j0 = 2 * (c & 1);   // byte of the packed words for sub-block 2c
-                const float sc0 = static_cast<float>((scw >> (8 * j0)) & 0xFFu);
-                const float sc1 = static_cast<float>((scw >> (8 * j0 + 8)) & 0xFFu);
-                const float mm0 = static_cast<float>((mw >> (8 * j0)) & 0xFFu);
-                const float mm1 = static_cast<float>((mw >> (8 * j0 + 8)) & 0xFFu);
-                const float ds0 = d * sc0, ds1 = d * sc1, dm0 = dmin * mm0, dm1 = dmin * mm1;
-                const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
-                const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
+        if constexpr (!kQ8) {
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kStages;
+                const int kb = kc >> 2, c = kc & 3, r = kb % kRawStages;
+                if (c == 0 && !wait_or_abort(bar(kBarRawFull + r), (kb / kRawStages) & 1, a.wait_ns, abort_flag, a.err))
+                    break;
+                if (kc >= kStages &&
+                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
+                    break;
     #pragma unroll
-                for (int half = 0; half < 2; ++half) {            // bytes 16*half .. 16*half+15 of the chunk
-                    const uint4 qv = qs[half];
-                    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
-    #pragma unroll
-                    for (int sel = 0; sel < 2; ++sel) {           // 0: low nibbles (cols i), 1: high (cols 32+i)
-                        const float ds = sel ? ds1 : ds0, dm = sel ? dm1 : dm0;
-                        // 16 weights: columns 32*sel + 16*half + [0, 16) of this chunk
-                        uint32_t packed[8];
-    #pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            const uint32_t v = sel ? (w4[wi] >> 4) : w4[wi];
-                            const float q0 = static_cast<float>(v & 15u), q1 = static_cast<float>((v >> 8) & 15u);
-                            const float q2 = static_cast<float>((v >> 16) & 15u), q3 = static_cast<float>((v >> 24) & 15u);
-                            const __nv_bfloat162 p01 = __floats2bfloat162_rn(fmaf(q0, ds, -dm), fmaf(q1, ds, -dm));
-                            const __nv_bfloat162 p23 = __floats2bfloat162_rn(fmaf(q2, ds, -dm), fmaf(q3, ds, -dm));
-                            packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
-                            packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                for (int i = 0; i < kTiles; ++i) {
+                    const uint8_t *row = base + kOffRaw + r * kRawStage + i * kRawBytes + t * 144;
+                    const uint4 hd = *reinterpret_cast<const uint4 *>(row);
+                    const float d = half_bits_to_float(hd.x);
+                    const float dmin = half_bits_to_float(hd.x >> 16);
+                    // 6-bit scale and min of sub-blocks 2c (low nibbles) and 2c+1 (high)
+                    const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
+                    const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+                    const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+                    const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
+                    const int j0 = 2 * (c & 1);   // byte of the packed words for sub-block 2c
+                    const float sc0 = static_cast<float>((scw >> (8 * j0)) & 0xFFu);
+                    const float sc1 = static_cast<float>((scw >> (8 * j0 + 8)) & 0xFFu);
+                    const float mm0 = static_cast<float>((mw >> (8 * j0)) & 0xFFu);
+                    const float mm1 = static_cast<float>((mw >> (8 * j0 + 8)) & 0xFFu);
+                    const float ds0 = d * sc0, ds1 = d * sc1, dm0 = dmin * mm0, dm1 = dmin * mm1;
+                    const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
+                    const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
+        #pragma unroll
+                    for (int half = 0; half < 2; ++half) {            // bytes 16*half .. 16*half+15 of the chunk
+                        const uint4 qv = qs[half];
+                        const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+        #pragma unroll
+                        for (int sel = 0; sel < 2; ++sel) {           // 0: low nibbles (cols i), 1: high (cols 32+i)
+                            const float ds = sel ? ds1 : ds0, dm = sel ? dm1 : dm0;
+                            // 16 weights: columns 32*sel + 16*half + [0, 16) of this chunk
+                            uint32_t packed[8];
+        #pragma unroll
+                            for (int wi = 0; wi < 4; ++wi) {
+                                const uint32_t v = sel ? (w4[wi] >> 4) : w4[wi];
+                                const float q0 = static_cast<float>(v & 15u), q1 = static_cast<float>((v >> 8) & 15u);
+                                const float q2 = static_cast<float>((v >> 16) & 15u), q3 = static_cast<float>((v >> 24) & 15u);
+                                const __nv_bfloat162 p01 = __floats2bfloat162_rn(fmaf(q0, ds, -dm), fmaf(q1, ds, -dm));
+                                const __nv_bfloat162 p23 = __floats2bfloat162_rn(fmaf(q2, ds, -dm), fmaf(q3, ds, -dm));
+                                packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
+                                packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                            }
+                            // two 16-byte chunks (8 columns each) of the swizzled row
+        #pragma unroll
+                            for (int h8 = 0; h8 < 2; ++h8) {
+                                const int chunk = 4 * sel + 2 * half + h8;          // logical 16-byte chunk 0..7
+                                const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
+                                             "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
+                                             : "memory");
+                            }
                         }
-                        // two 16-byte chunks (8 columns each) of the swizzled row
-    #pragma unroll
-                        for (int h8 = 0; h8 < 2; ++h8) {
-                            const int chunk = 4 * sel + 2 * half + h8;          // logical 16-byte chunk 0..7
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarAFull + s));
+                if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
+            }
+        } else {
+            // Q8_0: this thread's row of each tile (rows past N repeat the last
+            // row, unstored); a K chunk is blocks 2kc and 2kc+1 of the row, read
+            // as the nine aligned words around each 34-byte block, one chunk ahead
+            const int64_t nr = min(static_cast<int64_t>(n0 + t), a.N - 1);
+            uint32_t nxt[kTiles][2][9], nof[kTiles][2];
+            auto fetch = [&](int kc, uint32_t (&wv)[kTiles][2][9], uint32_t (&of)[kTiles][2]) {
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i)
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int j = 2 * kc + b;
+                        if (j < a.nb) {
+                            const uintptr_t ad = reinterpret_cast<uintptr_t>(a.wq8[i] + nr * a.row_bytes + 34 * j);
+                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad & ~static_cast<uintptr_t>(3));
+#pragma unroll
+                            for (int k = 0; k < 9; ++k) wv[i][b][k] = __ldg(wp + k);
+                            of[i][b] = static_cast<uint32_t>(ad & 3u);     // 0 or 2: blocks are 2-byte aligned
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 9; ++k) wv[i][b][k] = 0u;
+                            of[i][b] = 0u;
+                        }
+                    }
+            };
+            fetch(0, nxt, nof);
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kStages;
+                uint32_t cur[kTiles][2][9], cof[kTiles][2];
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i)
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        cof[i][b] = nof[i][b];
+#pragma unroll
+                        for (int k = 0; k < 9; ++k) cur[i][b][k] = nxt[i][b][k];
+                    }
+                if (kc + 1 < nk) fetch(kc + 1, nxt, nof);
+                if (kc >= kStages &&
+                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
+                    break;
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i) {
+                    const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const uint32_t off = cof[i][b];
+                        const float d = half_bits_to_float(cur[i][b][0] >> (8 * off));
+                        const uint32_t sel = off ? 0x7654u : 0x5432u;
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            // quants 4k..4k+3 of the block (bytes 2+4k.. past its start)
+                            const uint32_t v = __byte_perm(cur[i][b][k], cur[i][b][k + 1], sel);
+                            const float q0 = static_cast<float>(static_cast<int8_t>(v & 0xFFu));
+                            const float q1 = static_cast<float>(static_cast<int8_t>((v >> 8) & 0xFFu));
+                            const float q2 = static_cast<float>(static_cast<int8_t>((v >> 16) & 0xFFu));
+                            const float q3 = static_cast<float>(static_cast<int8_t>(v >> 24));
+                            const __nv_bfloat162 p01 = __floats2bfloat162_rn(d * q0, d * q1);
+                            const __nv_bfloat162 p23 = __floats2bfloat162_rn(d * q2, d * q3);
+                            packed[2 * k] = *reinterpret_cast<const uint32_t *>(&p01);
+                            packed[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                        }
+#pragma unroll
+                        for (int h8 = 0; h8 < 4; ++h8) {
+                            const int chunk = 4 * b + h8;                     // logical 16-byte chunk 0..7
                             const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
                             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
                                          "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
@@ -279,10 +363,9 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         }
                     }
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarAFull + s));
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarAFull + s));
-            if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
         }
         // epilogue: tensor memory -> registers -> Y (store, acc) or H (swiglu)
         if (wait_or_abort(bar(kBarAcc), 0, a.wait_ns, abort_flag, a.err)) {
@@ -370,34 +453,36 @@ size_t gemm_workspace_bytes(int64_t M, int64_t K) { return static_cast<size_t>(M
 
 namespace {
 
-template <int MODE>
+template <int FMT, int MODE>
 cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const gemm::Args &a, int64_t grid,
                         cudaStream_t st)
 {
     using namespace gemm;
+    constexpr int smem = Shape<FMT, MODE>::smem;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && granted[dev] == 0) {
-        e = cudaFuncSetAttribute(gemm_q4k_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<MODE>::smem);
+        e = cudaFuncSetAttribute(gemm_q4k_kernel<FMT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         granted[dev] = 1;
     }
-    gemm_q4k_kernel<MODE><<<static_cast<unsigned>(grid), kThreads, Shape<MODE>::smem, st>>>(tm_x, tm_w, a);
+    gemm_q4k_kernel<FMT, MODE><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm_x, tm_w, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
-                            int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
-                            bool *encode_failed, int mode, int64_t up_rows)
+cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                        int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
+                        bool *encode_failed, int mode, int64_t up_rows)
 {
     using namespace gemm;
     *encode_failed = false;
+    const bool q8 = fmt == kFmtQ80;
     const int64_t K8 = gemm_k8(K);
-    const int64_t row_bytes = ((K + 255) / 256) * 144;
+    const int64_t row_bytes = q8 ? ((K + 31) / 32) * 34 : ((K + 255) / 256) * 144;
     __nv_bfloat16 *xb = static_cast<__nv_bfloat16 *>(workspace);
     {
         const int64_t total = M * K8;
@@ -429,7 +514,9 @@ cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const f
     // the up rows [up_rows, up_rows + N) relative to w_rows
     const int64_t lo = mode == kSwiglu ? std::min<int64_t>(0, up_rows) : 0;
     const int64_t hi = mode == kSwiglu ? std::max<int64_t>(N, up_rows + N) : N;
-    {
+    if (q8) {
+        tm_w = tm_x;       // Q8_0 weights are read directly: the map is not used
+    } else {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(hi - lo)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
         const cuuint32_t box[2] = {144u, static_cast<cuuint32_t>(kBM)};
@@ -450,6 +537,10 @@ cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const f
     a.ldy = ldy;
     a.row0[0] = static_cast<int>(-lo);
     a.row0[1] = static_cast<int>(up_rows - lo);
+    a.wq8[0] = w_rows;
+    a.wq8[1] = w_rows + up_rows * row_bytes;
+    a.row_bytes = row_bytes;
+    a.nb = static_cast<int>((K + 31) / 32);
     a.n_tiles = static_cast<int>((N + kBM - 1) / kBM);
     a.nk = static_cast<int>((K8 + kBK - 1) / kBK);
     a.skip_chunk = skip_chunk;
@@ -458,9 +549,21 @@ cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const f
     const int64_t per_cta = mode == kSwiglu ? kBN : 2 * kBN;   // tokens per CTA pass
     const int64_t m_blocks = (M + per_cta - 1) / per_cta;
     const int64_t grid = a.n_tiles * m_blocks;
-    if (mode == kSwiglu) return launch_mode<kSwiglu>(tm_x, tm_w, a, grid, st);
-    if (mode == kAcc) return launch_mode<kAcc>(tm_x, tm_w, a, grid, st);
-    return launch_mode<kStore>(tm_x, tm_w, a, grid, st);
+    if (q8) {
+        if (mode == kSwiglu) return launch_mode<kFmtQ80, kSwiglu>(tm_x, tm_w, a, grid, st);
+        if (mode == kAcc) return launch_mode<kFmtQ80, kAcc>(tm_x, tm_w, a, grid, st);
+        return launch_mode<kFmtQ80, kStore>(tm_x, tm_w, a, grid, st);
+    }
+    if (mode == kSwiglu) return launch_mode<kFmtQ4K, kSwiglu>(tm_x, tm_w, a, grid, st);
+    if (mode == kAcc) return launch_mode<kFmtQ4K, kAcc>(tm_x, tm_w, a, grid, st);
+    return launch_mode<kFmtQ4K, kStore>(tm_x, tm_w, a, grid, st);
+}
+
+cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                            int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
+                            bool *encode_failed)
+{
+    return gemm_launch(kFmtQ4K, w_rows, N, K, x, M, y, ldy, workspace, st, err, wait_ns, skip_chunk, encode_failed);
 }
 
 }  // namespace qk

@@ -32,10 +32,15 @@ uint64_t library_wait_limit_ns();
 
 int64_t gemm_k8(int64_t K);
 size_t gemm_workspace_bytes(int64_t M, int64_t K);
-// mode 0: y = x W^T, 1: y += x W^T, 2: y = silu(x Wg^T) * (x Wu^T) with the up
-// rows at w_rows + up_rows rows.
+// Prefill GEMM of format fmt (kFmtQ4K or kFmtQ80).  mode 0: y = x W^T,
+// 1: y += x W^T, 2: y = silu(x Wg^T) * (x Wu^T) with the up rows at
+// w_rows + up_rows rows.
+cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                        int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
+                        bool *encode_failed, int mode = 0, int64_t up_rows = 0);
+// The Q4_K store form (the plain prefill GEMM).
 cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                             int64_t ldy, void *workspace, cudaStream_t st, int *err, uint64_t wait_ns, int skip_chunk,
-                            bool *encode_failed, int mode = 0, int64_t up_rows = 0);
+                            bool *encode_failed);
 
 }  // namespace qk

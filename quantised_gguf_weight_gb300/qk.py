@@ -26,7 +26,8 @@ MAX_BATCH = 8
 
 EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_q6_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k",
            "qmatvec_swiglu_q6_k", "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qmatvec_experts_q6_k",
-           "qk_row_bytes_q6_k", "qgemm_q4_k", "qgemm_q4_k_acc", "qgemm_swiglu_q4_k", "qgemm_q4_k_workspace_bytes",
+           "qk_row_bytes_q6_k", "qgemm_q4_k", "qgemm_q4_k_acc", "qgemm_swiglu_q4_k", "qgemm_q8_0",
+           "qgemm_q8_0_acc", "qgemm_swiglu_q8_0", "qgemm_q4_k_workspace_bytes",
            "qgemm_q4_k_noalloc", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
            "qk_version"]
@@ -66,11 +67,12 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = [P, I64, I64, I64, P, I, P, I64, P, I64, P]
             fn.restype = I
-        for name in ("qgemm_q4_k", "qgemm_q4_k_acc"):
+        for name in ("qgemm_q4_k", "qgemm_q4_k_acc", "qgemm_q8_0", "qgemm_q8_0_acc"):
             getattr(lib, name).argtypes = [P, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
             getattr(lib, name).restype = I
-        lib.qgemm_swiglu_q4_k.argtypes = [P, I64, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
-        lib.qgemm_swiglu_q4_k.restype = I
+        for name in ("qgemm_swiglu_q4_k", "qgemm_swiglu_q8_0"):
+            getattr(lib, name).argtypes = [P, I64, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
+            getattr(lib, name).restype = I
         lib.qgemm_q4_k_workspace_bytes.argtypes = [I64, I64, I64]
         lib.qgemm_q4_k_workspace_bytes.restype = ctypes.c_size_t
         lib.qk_debug_gemm_skip_chunk.argtypes = [I]
@@ -182,6 +184,20 @@ def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().qgemm_q4_k_workspace_bytes(M, N, K))
 
 
+def _gemm(name: str, w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor,
+          y: torch.Tensor | None, ldy: int, workspace: torch.Tensor | None, stream) -> torch.Tensor:
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+        ldy = N
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=x.device)
+    st = getattr(load(), name)(w.data_ptr(), row_offset, N, K, x.data_ptr(), M, y.data_ptr(), ldy,
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, name)
+    return y
+
+
 def qgemm_q4_k(w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor,
                y: torch.Tensor | None = None, ldy: int = 0, workspace: torch.Tensor | None = None,
                stream=None) -> torch.Tensor:
@@ -189,47 +205,46 @@ def qgemm_q4_k(w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor
 
     `workspace` is caller-owned device scratch (uint8) of gemm_workspace_bytes(M, N, K) bytes;
     it is allocated here through torch when not given."""
-    M = x.shape[0]
-    if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-        ldy = N
-    nbytes = gemm_workspace_bytes(M, N, K)
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
-    st = load().qgemm_q4_k(w.data_ptr(), row_offset, N, K, x.data_ptr(), M, y.data_ptr(), ldy,
-                           workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(st, "qgemm_q4_k")
-    return y
+    return _gemm("qgemm_q4_k", w, row_offset, N, K, x, y, ldy, workspace, stream)
 
 
-def qgemm_q4_k_acc(w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
-                   ldy: int = 0, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+def qgemm_q8_0(w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor,
+               y: torch.Tensor | None = None, ldy: int = 0, workspace: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """qgemm_q4_k for Q8_0 block bytes `w`."""
+    return _gemm("qgemm_q8_0", w, row_offset, N, K, x, y, ldy, workspace, stream)
+
+
+def qgemm_acc(fmt: str, w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
+              ldy: int = 0, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y[m][n] += sum_c bf16(W[row_offset + n][c]) bf16(x[m][c]) (in place on `y`)."""
-    M = x.shape[0]
-    nbytes = gemm_workspace_bytes(M, N, K)
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
-    st = load().qgemm_q4_k_acc(w.data_ptr(), row_offset, N, K, x.data_ptr(), M, y.data_ptr(), ldy,
-                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(st, "qgemm_q4_k_acc")
-    return y
+    name = {"q4_k": "qgemm_q4_k_acc", "q8_0": "qgemm_q8_0_acc"}[fmt]
+    return _gemm(name, w, row_offset, N, K, x, y, ldy, workspace, stream)
 
 
-def qgemm_swiglu_q4_k(w: torch.Tensor, gate_offset: int, up_offset: int, F: int, K: int, x: torch.Tensor,
-                      h: torch.Tensor | None = None, ldh: int = 0, workspace: torch.Tensor | None = None,
-                      stream=None) -> torch.Tensor:
+def qgemm_q4_k_acc(w, row_offset, N, K, x, y, ldy=0, workspace=None, stream=None):
+    return qgemm_acc("q4_k", w, row_offset, N, K, x, y, ldy, workspace, stream)
+
+
+def qgemm_swiglu(fmt: str, w: torch.Tensor, gate_offset: int, up_offset: int, F: int, K: int, x: torch.Tensor,
+                 h: torch.Tensor | None = None, ldh: int = 0, workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
     """h[m][p] = silu(g) * u with g, u the bf16 GEMM rows gate_offset + p and up_offset + p."""
     M = x.shape[0]
     if h is None:
         h = torch.empty((M, F), dtype=torch.float32, device=x.device)
         ldh = F
-    nbytes = gemm_workspace_bytes(M, F, K)
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
-    st = load().qgemm_swiglu_q4_k(w.data_ptr(), gate_offset, up_offset, F, K, x.data_ptr(), M, h.data_ptr(), ldh,
-                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(st, "qgemm_swiglu_q4_k")
+        workspace = torch.empty(gemm_workspace_bytes(M, F, K), dtype=torch.uint8, device=x.device)
+    name = {"q4_k": "qgemm_swiglu_q4_k", "q8_0": "qgemm_swiglu_q8_0"}[fmt]
+    st = getattr(load(), name)(w.data_ptr(), gate_offset, up_offset, F, K, x.data_ptr(), M, h.data_ptr(), ldh,
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, name)
     return h
+
+
+def qgemm_swiglu_q4_k(w, gate_offset, up_offset, F, K, x, h=None, ldh=0, workspace=None, stream=None):
+    return qgemm_swiglu("q4_k", w, gate_offset, up_offset, F, K, x, h, ldh, workspace, stream)
 
 
 def debug_gemm_skip_chunk(chunk: int) -> int:

@@ -35,7 +35,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k",
-              "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qgemm_q4_k",
+              "qmatvec_experts_q8_0", "qmatvec_experts_q4_k", "qgemm_q4_k", "qgemm_q4_k_acc",
+              "qgemm_swiglu_q4_k", "qgemm_q8_0", "qgemm_q8_0_acc", "qgemm_swiglu_q8_0",
               "qgemm_q4_k_workspace_bytes", "qk_status_string", "qk_device_error"):
         assert n in names
 
@@ -87,7 +88,7 @@ def test_argument_validation_without_gpu(lib, name):
     assert call(y=FAKE + 1) == 3
     assert call(w=FAKE + 1) == 3     # odd w
     if name == "qmatvec_q4_k":
-        assert call(w=FAKE + 8) == 3  # Q4_K needs 16-byte aligned super-blocks
+        assert call(w=FAKE + (8 if "q4_k" in name else 1)) == 3   # Q4_K: 16-byte, Q8_0: 2-byte alignment  # Q4_K needs 16-byte aligned super-blocks
 
 
 @pytest.mark.parametrize("name", ["qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qmatvec_swiglu_q6_k"])
@@ -147,8 +148,11 @@ def test_product_path_does_not_import_the_oracle():
         assert not pat.search(open(path, errors="replace").read()), path
 
 
-def test_gemm_argument_validation_without_gpu(lib):
-    f = lib.qgemm_q4_k
+@pytest.mark.parametrize("name", ["qgemm_q4_k", "qgemm_q4_k_acc", "qgemm_q8_0", "qgemm_q8_0_acc"])
+def test_gemm_argument_validation_without_gpu(lib, name):
+    f = getattr(lib, name)
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     ok = dict(w=FAKE, off=0, N=128, K=256, x=FAKE, M=4, y=FAKE, ldy=0, ws=FAKE, wsb=1 << 20)
 
     def call(**kw):
@@ -161,7 +165,7 @@ def test_gemm_argument_validation_without_gpu(lib):
     assert call(M=0) == 2
     assert call(K=-1) == 2
     assert call(ldy=64) == 2
-    assert call(w=FAKE + 8) == 3
+    assert call(w=FAKE + (8 if "q4_k" in name else 1)) == 3   # Q4_K: 16-byte, Q8_0: 2-byte alignment
     assert call(ws=None) == 7
     assert call(ws=FAKE + 16) == 7
     assert call(wsb=100) == 7
