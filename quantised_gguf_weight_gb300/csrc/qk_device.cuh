@@ -115,6 +115,9 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h16)
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h16 & 0xFFFFu)));
 }
 
+constexpr uint32_t kMagic = 0x4B000000u;   // 2^23 as an fp32 bit pattern
+constexpr float kTwo23 = 8388608.0f;
+
 // ---------------------------------------------------------------- packed fp32 pairs
 // A float pair lives in one 64-bit register pair (low half = first value);
 // the arithmetic is done with the f32x2 instructions.

@@ -44,7 +44,8 @@ constexpr int kBK = 64;                  // K columns per stage (one 128-byte sw
 constexpr int kStages = 2;
 constexpr int kRawStages = 2;
 constexpr int kRawBytes = kBM * 144;     // one Q4_K super-block column of 128 rows
-constexpr int kThreads = 192;
+constexpr int kDeq = 256;                // dequantising threads: two per weight row
+constexpr int kThreads = 64 + kDeq;
 constexpr uint32_t kTmemCols = 512;
 
 // Modes: Y = X W^T (store), Y += X W^T (acc), or H = silu(X Wg^T) * (X Wu^T)
@@ -124,12 +125,12 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarXFull + s), 1);
-            mbar_init(bar(kBarAFull + s), 128);
+            mbar_init(bar(kBarAFull + s), kDeq);
             mbar_init(bar(kBarEmpty + s), 1);
         }
         for (int r = 0; r < kRawStages; ++r) {
             mbar_init(bar(kBarRawFull + r), 1);
-            mbar_init(bar(kBarRawEmpty + r), 128);
+            mbar_init(bar(kBarRawEmpty + r), kDeq);
         }
         mbar_init(bar(kBarAcc), 1);
         mbar_init(bar(kBarDone), 1);
@@ -226,7 +227,11 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ dequantise + epilogue
-        const int t = tid - 64;          // 0..127: the weight row of this thread inside the tile
+        // thread -> weight row t of the tile and half `sel` of each 64-column
+        // chunk: Q4_K sub-block 2c + sel (the low or the high nibbles of the
+        // chunk's 32 bytes), Q8_0 block 2kc + sel
+        const int t = (tid - 64) & (kBM - 1);
+        const int sel = (tid - 64) >> 7;
         if constexpr (!kQ8) {
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
@@ -236,126 +241,58 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (kc >= kStages &&
                     !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
                     break;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
                     const uint8_t *row = base + kOffRaw + r * kRawStage + i * kRawBytes + t * 144;
                     const uint4 hd = *reinterpret_cast<const uint4 *>(row);
                     const float d = half_bits_to_float(hd.x);
                     const float dmin = half_bits_to_float(hd.x >> 16);
-                    // 6-bit scale and min of sub-blocks 2c (low nibbles) and 2c+1 (high)
-                    const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
-                    const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-                    const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-                    const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
-                    const int j0 = 2 * (c & 1);   // byte of the packed words for sub-block 2c
-                    const float sc0 = static_cast<float>((scw >> (8 * j0)) & 0xFFu);
-                    const float sc1 = static_cast<float>((scw >> (8 * j0 + 8)) & 0xFFu);
-                    const float mm0 = static_cast<float>((mw >> (8 * j0)) & 0xFFu);
-                    const float mm1 = static_cast<float>((mw >> (8 * j0 + 8)) & 0xFFu);
-                    const float ds0 = d * sc0, ds1 = d * sc1, dm0 = dmin * mm0, dm1 = dmin * mm1;
+                    // 6-bit scale and min of sub-block j = 2c + sel
+                    const int j = 2 * c + sel;
+                    uint32_t scv, mv;
+                    if (j < 4) {
+                        scv = (hd.y >> (8 * j)) & 63u;
+                        mv = (hd.z >> (8 * j)) & 63u;
+                    } else {
+                        const int k = j - 4;
+                        scv = ((hd.w >> (8 * k)) & 15u) | (((hd.y >> (8 * k)) >> 6 & 3u) << 4);
+                        mv = ((hd.w >> (8 * k + 4)) & 15u) | (((hd.z >> (8 * k)) >> 6 & 3u) << 4);
+                    }
+                    const float ds = d * static_cast<float>(scv), dm = dmin * static_cast<float>(mv);
+                    // a nibble at bit position p (0 or 8) of a word becomes the exact
+                    // float 2^23 + q 2^p (one LOP3); fma(ds 2^-p, ., -ds 2^-p 2^23) = ds q
+                    // exactly, and one subtraction of dm rounds w = ds q - dm once, the
+                    // same as fma(q, ds, -dm)
+                    const int sh = 4 * sel;                      // nibble offset in a byte
+                    const float s0 = ds, s1 = ds * (1.0f / 256.0f);  // fields at bits 0 and 8 after the shift
+                    const uint64_t sc01 = pack2f(s0, s1);
+                    const uint64_t of01 = pack2f(s0 * -kTwo23, s1 * -kTwo23);
+                    const uint64_t ndm = pack2f(-dm, -dm);
                     const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
                     const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
-        #pragma unroll
-                    for (int half = 0; half < 2; ++half) {            // bytes 16*half .. 16*half+15 of the chunk
-                        const uint4 qv = qs[half];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {                  // bytes 16*hf .. 16*hf+15 of the sub-block
+                        const uint4 qv = qs[hf];
                         const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
-        #pragma unroll
-                        for (int sel = 0; sel < 2; ++sel) {           // 0: low nibbles (cols i), 1: high (cols 32+i)
-                            const float ds = sel ? ds1 : ds0, dm = sel ? dm1 : dm0;
-                            // 16 weights: columns 32*sel + 16*half + [0, 16) of this chunk
-                            uint32_t packed[8];
-        #pragma unroll
-                            for (int wi = 0; wi < 4; ++wi) {
-                                const uint32_t v = sel ? (w4[wi] >> 4) : w4[wi];
-                                const float q0 = static_cast<float>(v & 15u), q1 = static_cast<float>((v >> 8) & 15u);
-                                const float q2 = static_cast<float>((v >> 16) & 15u), q3 = static_cast<float>((v >> 24) & 15u);
-                                const __nv_bfloat162 p01 = __floats2bfloat162_rn(fmaf(q0, ds, -dm), fmaf(q1, ds, -dm));
-                                const __nv_bfloat162 p23 = __floats2bfloat162_rn(fmaf(q2, ds, -dm), fmaf(q3, ds, -dm));
-                                packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
-                                packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
-                            }
-                            // two 16-byte chunks (8 columns each) of the swizzled row
-        #pragma unroll
-                            for (int h8 = 0; h8 < 2; ++h8) {
-                                const int chunk = 4 * sel + 2 * half + h8;          // logical 16-byte chunk 0..7
-                                const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
-                                             "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
-                                             : "memory");
-                            }
+                        uint32_t packed[8];
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            // the word's 4 nibbles (bytes 0..3, offset sh): bytes 0, 1 from the
+                            // word at bits sh, sh+8; bytes 2, 3 from the word >> 16 likewise
+                            const uint32_t v = w4[wi] >> sh, v2 = w4[wi] >> (16 + sh);
+                            const uint64_t f01 = pack2(magic_field<0xFu>(v), magic_field<0xF00u>(v));
+                            const uint64_t f23 = pack2(magic_field<0xFu>(v2), magic_field<0xF00u>(v2));
+                            const float2 w01 = unpack2f(add_f32x2(fma_f32x2(f01, sc01, of01), ndm));
+                            const float2 w23 = unpack2f(add_f32x2(fma_f32x2(f23, sc01, of01), ndm));
+                            const __nv_bfloat162 p01 = __floats2bfloat162_rn(w01.x, w01.y);
+                            const __nv_bfloat162 p23 = __floats2bfloat162_rn(w23.x, w23.y);
+                            packed[2 * wi] = *reinterpret_cast<const uint32_t *>(&p01);
+                            packed[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&p23);
                         }
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(kBarAFull + s));
-                if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
-            }
-        } else {
-            // Q8_0: this thread's row of each tile (rows past N repeat the last
-            // row, unstored); a K chunk is blocks 2kc and 2kc+1 of the row, read
-            // as the nine aligned words around each 34-byte block, one chunk ahead
-            const int64_t nr = min(static_cast<int64_t>(n0 + t), a.N - 1);
-            uint32_t nxt[kTiles][2][9], nof[kTiles][2];
-            auto fetch = [&](int kc, uint32_t (&wv)[kTiles][2][9], uint32_t (&of)[kTiles][2]) {
+                        // two 16-byte chunks (8 columns each) of the swizzled row
 #pragma unroll
-                for (int i = 0; i < kTiles; ++i)
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int j = 2 * kc + b;
-                        if (j < a.nb) {
-                            const uintptr_t ad = reinterpret_cast<uintptr_t>(a.wq8[i] + nr * a.row_bytes + 34 * j);
-                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad & ~static_cast<uintptr_t>(3));
-#pragma unroll
-                            for (int k = 0; k < 9; ++k) wv[i][b][k] = __ldg(wp + k);
-                            of[i][b] = static_cast<uint32_t>(ad & 3u);     // 0 or 2: blocks are 2-byte aligned
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 9; ++k) wv[i][b][k] = 0u;
-                            of[i][b] = 0u;
-                        }
-                    }
-            };
-            fetch(0, nxt, nof);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % kStages;
-                uint32_t cur[kTiles][2][9], cof[kTiles][2];
-#pragma unroll
-                for (int i = 0; i < kTiles; ++i)
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        cof[i][b] = nof[i][b];
-#pragma unroll
-                        for (int k = 0; k < 9; ++k) cur[i][b][k] = nxt[i][b][k];
-                    }
-                if (kc + 1 < nk) fetch(kc + 1, nxt, nof);
-                if (kc >= kStages &&
-                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
-                    break;
-#pragma unroll
-                for (int i = 0; i < kTiles; ++i) {
-                    const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const uint32_t off = cof[i][b];
-                        const float d = half_bits_to_float(cur[i][b][0] >> (8 * off));
-                        const uint32_t sel = off ? 0x7654u : 0x5432u;
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            // quants 4k..4k+3 of the block (bytes 2+4k.. past its start)
-                            const uint32_t v = __byte_perm(cur[i][b][k], cur[i][b][k + 1], sel);
-                            const float q0 = static_cast<float>(static_cast<int8_t>(v & 0xFFu));
-                            const float q1 = static_cast<float>(static_cast<int8_t>((v >> 8) & 0xFFu));
-                            const float q2 = static_cast<float>(static_cast<int8_t>((v >> 16) & 0xFFu));
-                            const float q3 = static_cast<float>(static_cast<int8_t>(v >> 24));
-                            const __nv_bfloat162 p01 = __floats2bfloat162_rn(d * q0, d * q1);
-                            const __nv_bfloat162 p23 = __floats2bfloat162_rn(d * q2, d * q3);
-                            packed[2 * k] = *reinterpret_cast<const uint32_t *>(&p01);
-                            packed[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&p23);
-                        }
-#pragma unroll
-                        for (int h8 = 0; h8 < 4; ++h8) {
-                            const int chunk = 4 * b + h8;                     // logical 16-byte chunk 0..7
+                        for (int h8 = 0; h8 < 2; ++h8) {
+                            const int chunk = 4 * sel + 2 * hf + h8;            // logical 16-byte chunk 0..7
                             const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
                             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
                                          "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
@@ -365,16 +302,89 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(bar(kBarAFull + s));
+                if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
+            }
+        } else {
+            // Q8_0: block 2kc + sel of this thread's row of each tile (rows past N
+            // repeat the last row, unstored), read as the nine aligned words
+            // around the 34-byte block, one chunk ahead
+            const int64_t nr = min(static_cast<int64_t>(n0 + t), a.N - 1);
+            uint32_t nxt[kTiles][9], nof[kTiles];
+            auto fetch = [&](int kc, uint32_t (&wv)[kTiles][9], uint32_t (&of)[kTiles]) {
+                const int j = 2 * kc + sel;
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i) {
+                    if (j < a.nb) {
+                        const uintptr_t ad = reinterpret_cast<uintptr_t>(a.wq8[i] + nr * a.row_bytes + 34 * j);
+                        const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad & ~static_cast<uintptr_t>(3));
+#pragma unroll
+                        for (int k = 0; k < 9; ++k) wv[i][k] = __ldg(wp + k);
+                        of[i] = static_cast<uint32_t>(ad & 3u);      // 0 or 2: blocks are 2-byte aligned
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 9; ++k) wv[i][k] = 0u;
+                        of[i] = 0u;
+                    }
+                }
+            };
+            fetch(0, nxt, nof);
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kStages;
+                uint32_t cur[kTiles][9], cof[kTiles];
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i) {
+                    cof[i] = nof[i];
+#pragma unroll
+                    for (int k = 0; k < 9; ++k) cur[i][k] = nxt[i][k];
+                }
+                if (kc + 1 < nk) fetch(kc + 1, nxt, nof);
+                if (kc >= kStages &&
+                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
+                    break;
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i) {
+                    const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
+                    const uint32_t off = cof[i];
+                    const float d = half_bits_to_float(cur[i][0] >> (8 * off));
+                    const uint32_t psel = off ? 0x7654u : 0x5432u;
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        // quants 4k..4k+3 of the block (bytes 2+4k.. past its start)
+                        const uint32_t v = __byte_perm(cur[i][k], cur[i][k + 1], psel);
+                        const float q0 = static_cast<float>(static_cast<int8_t>(v & 0xFFu));
+                        const float q1 = static_cast<float>(static_cast<int8_t>((v >> 8) & 0xFFu));
+                        const float q2 = static_cast<float>(static_cast<int8_t>((v >> 16) & 0xFFu));
+                        const float q3 = static_cast<float>(static_cast<int8_t>(v >> 24));
+                        const __nv_bfloat162 p01 = __floats2bfloat162_rn(d * q0, d * q1);
+                        const __nv_bfloat162 p23 = __floats2bfloat162_rn(d * q2, d * q3);
+                        packed[2 * k] = *reinterpret_cast<const uint32_t *>(&p01);
+                        packed[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                    }
+#pragma unroll
+                    for (int h8 = 0; h8 < 4; ++h8) {
+                        const int chunk = 4 * sel + h8;                     // logical 16-byte chunk 0..7
+                        const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
+                                     "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarAFull + s));
             }
         }
         // epilogue: tensor memory -> registers -> Y (store, acc) or H (swiglu)
         if (wait_or_abort(bar(kBarAcc), 0, a.wait_ns, abort_flag, a.err)) {
             tc_fence_after();
-            const int q = warp & 3;                         // lane quarter this warp may access
+            // warp w may read TMEM lanes 32*(w%4) ..; the two warps of each lane
+            // quarter take one half of the accumulator columns each
+            const int q = warp & 3;
             const int n = n0 + 32 * q + lane;
             const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * q) << 16);
             const int cols = nh * kBN;
-            for (int j0 = 0; j0 < cols; j0 += 32) {
+            const int part = (warp - 2) >> 2;
+            for (int j0 = part * (cols / 2); j0 < (part + 1) * (cols / 2); j0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
                 if constexpr (MODE == kSwiglu) {

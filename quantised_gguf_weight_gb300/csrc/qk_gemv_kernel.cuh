@@ -42,8 +42,6 @@
 
 namespace qk {
 
-constexpr uint32_t kMagic = 0x4B000000u;   // 2^23 as an fp32 bit pattern
-constexpr float kTwo23 = 8388608.0f;
 
 // Bit position of the nibble that carries local column c (0..127) of a
 // 128-weight half super-block inside its 32-bit qs word, after the
