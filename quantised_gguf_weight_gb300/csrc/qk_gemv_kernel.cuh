@@ -25,7 +25,7 @@
 //    stages stay in flight.  Partial sums stay in registers across the chunks
 //    of a row group and are summed over the SW lanes of a team with shuffles.
 //  * Activations are staged once per CTA in shared memory, in the layout of
-//    the unit functions: batch 1 as block floating point byte planes (four
+//    the unit functions: batch 1 as block floating point byte planes (three
 //    byte dot products per weight group), batch >= 2 as fp32 (packed f32x2
 //    arithmetic).  Q4_K half super-blocks are stored h-major (unit slot
 //    h*XH + super-block), so lanes holding consecutive super-blocks read
@@ -57,23 +57,24 @@ __device__ __forceinline__ int q4k_nibble_shift(int c)
 }
 
 // Batch 1 holds the activations as block floating point: each 32-column
-// group has one exponent E and every value becomes the 32-bit integer
-// m = rint(x * 2^(30-E)) (|m| < 2^31), stored as four byte planes (plane 3
-// signed, planes 0..2 unsigned).  A weight group then costs one 4-way byte
-// dot product per plane, sum_i q_i m_i is assembled in integers per plane and
-// the group scale 2^(E-30) turns it back into a float.  Values within 2^7 of
-// their group's largest magnitude are represented exactly; the error of any
-// other value is below 2^-31 of that magnitude.
+// group has one exponent E (its largest magnitude lies in [2^E, 2^(E+1)))
+// and every value becomes the integer m = rint(x * 2^(21-E)), |m| <= 2^22,
+// stored as three byte planes (planes 0 and 1 unsigned, plane 2 signed; a
+// fourth byte of each 16-byte slot is unused).  A weight group then costs one
+// 4-way byte dot product per plane, sum_i q_i m_i is assembled in integers
+// per plane and the group scale 2^(E-21) turns it back into a float.  The
+// error of a value is at most 2^(E-22), i.e. 2^-22 of its group's largest
+// magnitude; small integers and other values with few significant bits are
+// represented exactly.
 
 // SwiGLU's gate: silu(z) = z / (1 + e^-z), with CUDA's expf.
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
-// sum(q*m) of one group from its four plane sums, as a float.
-__device__ __forceinline__ float planes_to_float(int s0, int s1, int s2, int s3)
+// sum(q*m) of one group from its three plane sums, as a float.
+__device__ __forceinline__ float planes_to_float(int s0, int s1, int s2)
 {
-    const int hi = s3 * 256 + s2;     // exact in int32 for 32-weight groups
-    const int lo = s1 * 256 + s0;
-    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
+    const int lo = s1 * 256 + s0;     // exact in int32 for 32-weight groups
+    return fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(lo));
 }
 
 constexpr int kGemvMaxStages = 32;
@@ -179,11 +180,11 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
         }
 #pragma unroll
         for (int lc = 0; lc < 2; ++lc) {
-            int sl[R][4], sh[R][4];
+            int sl[R][3], sh[R][3];
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) sl[r][k] = sh[r][k] = 0;
+                for (int k = 0; k < 3; ++k) sl[r][k] = sh[r][k] = 0;
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
 #pragma unroll
@@ -199,12 +200,10 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
                         const uint32_t H = wd & 0xF0F0F0F0u;   // 16 q of sub-block 2lc+1
                         sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
                         sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
-                        sl[r][2] = dp4a_uu(L, xl.z, sl[r][2]);
-                        sl[r][3] = dp4a_us(L, xl.w, sl[r][3]);
+                        sl[r][2] = dp4a_us(L, xl.z, sl[r][2]);
                         sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
                         sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
-                        sh[r][2] = dp4a_uu(H, xh.z, sh[r][2]);
-                        sh[r][3] = dp4a_us(H, xh.w, sh[r][3]);
+                        sh[r][2] = dp4a_us(H, xh.z, sh[r][2]);
                     }
                 }
             }
@@ -212,8 +211,8 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
             const float S0 = xsc_u[(2 * lc) * xstr], S1 = xsc_u[(2 * lc + 1) * xstr];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2], sl[r][3]);
-                const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2], sh[r][3]);
+                const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2]);
+                const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2]);
                 float t = acc[r][0];
                 t = fmaf(ds[r][2 * lc] * S0, F0, t);
                 t = fmaf(dmn[r][2 * lc], X0, t);
@@ -353,11 +352,11 @@ __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uin
     float d[R];
     uint32_t qw[R][8];
     q8_realign<R>(wv, off, d, qw);
-    int sp[R][4];
+    int sp[R][3];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sp[r][k] = 0;
+        for (int k = 0; k < 3; ++k) sp[r][k] = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint4 xv = *reinterpret_cast<const uint4 *>(xa + k * gs);
@@ -366,13 +365,12 @@ __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uin
             const uint32_t v = qw[r][k];
             sp[r][0] = dp4a_su(v, xv.x, sp[r][0]);
             sp[r][1] = dp4a_su(v, xv.y, sp[r][1]);
-            sp[r][2] = dp4a_su(v, xv.z, sp[r][2]);
-            sp[r][3] = dp4a_ss(v, xv.w, sp[r][3]);
+            sp[r][2] = dp4a_ss(v, xv.z, sp[r][2]);
         }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r)
-        acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2], sp[r][3]), acc[r][0]);
+        acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2]), acc[r][0]);
 }
 
 // Batch >= 2: int8 quants through the magic-exponent trick (bias 128), fp32 x.
@@ -495,13 +493,13 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
     for (int r = 0; r < R; ++r) d[r] = half_bits_to_float(hr[r].dw);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        int sp[R][2][4];
+        int sp[R][2][3];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) sp[r][h][k] = 0;
+                for (int k = 0; k < 3; ++k) sp[r][h][k] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint4 xv = *reinterpret_cast<const uint4 *>(xa + (8 * t + k) * gs);
@@ -511,8 +509,7 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
                 const int h = k >> 2;                   // 16-column sub-block 2t + h
                 sp[r][h][0] = dp4a_uu(q, xv.x, sp[r][h][0]);
                 sp[r][h][1] = dp4a_uu(q, xv.y, sp[r][h][1]);
-                sp[r][h][2] = dp4a_uu(q, xv.z, sp[r][h][2]);
-                sp[r][h][3] = dp4a_us(q, xv.w, sp[r][h][3]);
+                sp[r][h][2] = dp4a_us(q, xv.z, sp[r][h][2]);
             }
         }
         const float S = xsc[t * xstr];
@@ -521,9 +518,9 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
         for (int r = 0; r < R; ++r) {
             const float ds0 = q6_dscale(hr[r], d[r], 2 * t), ds1 = q6_dscale(hr[r], d[r], 2 * t + 1);
             float a = acc[r][0];
-            a = fmaf(ds0 * S, planes_to_float(sp[r][0][0], sp[r][0][1], sp[r][0][2], sp[r][0][3]), a);
+            a = fmaf(ds0 * S, planes_to_float(sp[r][0][0], sp[r][0][1], sp[r][0][2]), a);
             a = fmaf(ds0 * -32.0f, X0, a);
-            a = fmaf(ds1 * S, planes_to_float(sp[r][1][0], sp[r][1][1], sp[r][1][2], sp[r][1][3]), a);
+            a = fmaf(ds1 * S, planes_to_float(sp[r][1][0], sp[r][1][1], sp[r][1][2]), a);
             a = fmaf(ds1 * -32.0f, X1, a);
             acc[r][0] = a;
         }
@@ -642,8 +639,8 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int 
                     const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 255u);
                     const bool finite = ebits != 255;
                     const int E = max(ebits - 127, -96);
-                    const float up = __int_as_float((157 - E) << 23);     // 2^(30-E)
-                    const float down = __int_as_float((97 + E) << 23);    // 2^(E-30)
+                    const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
+                    const float down = __int_as_float((106 + E) << 23);   // 2^(E-21)
                     uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
                     if (finite) {
                         m0 = static_cast<uint32_t>(__float2int_rn(v[i].x * up));
