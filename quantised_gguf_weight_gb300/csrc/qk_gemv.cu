@@ -53,11 +53,10 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     const int LU = fmt == kFmtQ4K ? (U + 1) / 2 : U;
     const int R = gemv_rows(fmt, batch);
     const int CM = gemv_cpl_max(fmt, batch);
-    // activation unit stride: Q4_K stores half super-blocks h-major, so it
-    // needs an even stride of at least two slots per super-block
-    const int need = fmt == kFmtQ4K ? 2 * LU : U;
-    const int XU = need <= 32 ? 32 : (need <= 128 ? 128 : static_cast<int>(round_up(need, 2)));
-    const int64_t x_bytes = round_up(static_cast<int64_t>(batch) * XU * UC * 4, 128);
+    // activation unit slots (Q4_K: half super-blocks h-major, XU/2 slots a
+    // half), each with B*UC/4 16-byte slots plus one padding slot
+    const int XU = fmt == kFmtQ4K ? 2 * LU : U;
+    const int64_t x_bytes = round_up(static_cast<int64_t>(XU) * (static_cast<int64_t>(batch) * (UC / 4) + 1) * 16, 128);
     // Q4_K: sums of x per 32 columns (every batch row); Q6_K: per 16 columns (batch 1)
     const int64_t xsum_bytes = fmt == kFmtQ4K   ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128)
                                : fmt == kFmtQ6K ? (batch == 1 ? round_up(static_cast<int64_t>(8) * XU * 4, 128) : 0)
@@ -127,13 +126,13 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     int64_t stages = (budget - off_stage) / stage;
     if (stages > kGemvMaxStages) stages = kGemvMaxStages;
     if (stages < 1) return false;
-    // consumer warps that get row groups, and stages per warp: two or more
-    // stages a warp where the ring holds that many (a warp then has an item
-    // in flight while it works on another), else one
+    // consumer warps that get row groups (all that have one) and stages per
+    // warp: a warp copies an item into registers and hands its stage back
+    // before the arithmetic, so one stage a warp already keeps a copy in
+    // flight while the warp computes
     const int64_t rows_cta_max = n_assign > 0 ? (rows + cpa - 1) / cpa : (rows + grid - 1) / grid;
     int64_t nw = std::min<int64_t>(NW, (rows_cta_max + gr - 1) / gr);
     nw = std::min(nw, stages);
-    if (stages / nw < 2 && stages >= 2 * std::min<int64_t>(nw, 8)) nw = std::min<int64_t>(nw, stages / 2);
     const int64_t m = stages / nw;
     stages = nw * m;
     p->U = U;
@@ -215,10 +214,9 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.skip_item = skip_item;
     r.wait_ns = wait_ns;
     r.err = err;
-    const int us = (p.XU == 32 || p.XU == 128) ? p.XU : 0;
-    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, us, r, p.grid, p.smem, st, pdl);
-    if (fmt == kFmtQ6K) return gemv_launch_q6k(batch, us, r, p.grid, p.smem, st, pdl);
-    return gemv_launch_q80(batch, us, r, p.grid, p.smem, st, pdl);
+    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, r, p.grid, p.smem, st, pdl);
+    if (fmt == kFmtQ6K) return gemv_launch_q6k(batch, r, p.grid, p.smem, st, pdl);
+    return gemv_launch_q80(batch, r, p.grid, p.smem, st, pdl);
 }
 
 }  // namespace qk

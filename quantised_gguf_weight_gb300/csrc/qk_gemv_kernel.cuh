@@ -27,9 +27,12 @@
 //  * Activations are staged once per CTA in shared memory, in the layout of
 //    the unit functions: batch 1 as block floating point byte planes (three
 //    byte dot products per weight group), batch >= 2 as fp32 (packed f32x2
-//    arithmetic).  Q4_K half super-blocks are stored h-major (unit slot
-//    h*XH + super-block), so lanes holding consecutive super-blocks read
-//    consecutive 16-byte words.
+//    arithmetic).  The layout is unit-major: unit slot us holds its 16-byte
+//    slots (every batch row) contiguously plus one padding slot, so lanes
+//    reading the same slot of consecutive units and lanes writing
+//    consecutive slots of one unit both hit distinct bank groups.  Q4_K half
+//    super-blocks are stored h-major (unit slot h*XH + super-block), so lanes
+//    holding consecutive super-blocks read consecutive unit slots.
 // Every wait is bounded; a wait that runs out records QK_ERR_TIMEOUT in the
 // device error word and the kernel leaves without touching the rest of y.
 #pragma once
@@ -87,7 +90,7 @@ struct GemvArgs {
     int64_t rows, K, ldy, row_bytes;
     int U;              // activation units per row (Q4_K: 128-column halves, Q8_0: blocks)
     int LU;             // lane units per row (Q4_K: super-blocks, Q8_0: blocks)
-    int XU;             // unit stride of the shared-memory activation layout
+    int XU;             // unit slots of the shared-memory activation layout (Q4_K: 2 halves of XU/2)
     int SW;             // lanes per row team (power of two, <= 32)
     int lsw;            // log2(SW)
     int cpl;            // lane units per lane per item
@@ -130,18 +133,17 @@ __host__ __device__ constexpr int gemv_cpl_max(int fmt, int batch)
 //
 // One super-block of R rows from registers: hd = bytes 0..15 (d, dmin,
 // scales[12]), qs = bytes 16..143.  x: block-floating-point byte planes of
-// the two 128-column halves at xa[h]; per 32-column group j of half h the
-// plain sum is xsum_h[j*XU] and the plane scale 2^(E-30) is xsc_h[j*XU].
+// the two 128-column halves, float4 group g of half h at xa_h + 16g; per
+// 32-column group j the plain sum is xsum_h[j] and the plane scale
+// 2^(E-21) is xsc_h[j].
 // The high nibbles are used in place (byte & 0xF0 = 16 q), which is folded
 // into their sub-block scale as d/16 (exact: a power of two).
-template <int R, int US>
+template <int R>
 __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
-                                             const uint8_t *xa0, const uint8_t *xa1, uint32_t gs_rt, const float *xsum0,
+                                             const uint8_t *xa0, const uint8_t *xa1, const float *xsum0,
                                              const float *xsum1, const float *xsc0, const float *xsc1,
-                                             int xstride, float (&acc)[R][1])
+                                             float (&acc)[R][1])
 {
-    const uint32_t gs = US ? 16u * US : gs_rt;
-    const int xstr = US ? US : xstride;
     float d[R], dmin[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -152,8 +154,8 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
     for (int h = 0; h < 2; ++h) {
         if (h == 1 && !has_hi) break;
         const uint8_t *xa = h ? xa1 : xa0;
-        const float *xsum_u = h ? xsum1 : xsum0;
-        const float *xsc_u = h ? xsc1 : xsc0;
+        const float4 xsum4 = *reinterpret_cast<const float4 *>(h ? xsum1 : xsum0);
+        const float4 xsc4 = *reinterpret_cast<const float4 *>(h ? xsc1 : xsc0);
         // d*sc and -dmin*m of the four sub-blocks 4h..4h+3: the 6-bit field
         // placed in a float's mantissa is 2^23 + v, and one FMA against the
         // matching offset gives the exact product
@@ -190,8 +192,8 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int g_lo = 16 * lc + 4 * p + k;
-                    const uint4 xl = *reinterpret_cast<const uint4 *>(xa + g_lo * gs);
-                    const uint4 xh = *reinterpret_cast<const uint4 *>(xa + (g_lo + 8) * gs);
+                    const uint4 xl = *reinterpret_cast<const uint4 *>(xa + 16 * g_lo);
+                    const uint4 xh = *reinterpret_cast<const uint4 *>(xa + 16 * (g_lo + 8));
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint4 q = qs[r][4 * h + 2 * lc + p];
@@ -207,8 +209,8 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
                     }
                 }
             }
-            const float X0 = xsum_u[(2 * lc) * xstr], X1 = xsum_u[(2 * lc + 1) * xstr];
-            const float S0 = xsc_u[(2 * lc) * xstr], S1 = xsc_u[(2 * lc + 1) * xstr];
+            const float X0 = lc ? xsum4.z : xsum4.x, X1 = lc ? xsum4.w : xsum4.y;
+            const float S0 = lc ? xsc4.z : xsc4.x, S1 = lc ? xsc4.w : xsc4.y;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2]);
@@ -229,14 +231,14 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
 // One super-block of R rows from registers against fp32 activations that are
 // pre-multiplied by 2^-s for their nibble position (see q4k_nibble_shift):
 // a nibble at bit s of a word becomes the exact float 2^23 + q*2^s with one
-// LOP3, 2^23 is subtracted, and (q*2^s)*(x*2^-s) = q*x exactly.
-template <int B, int R, int US>
+// LOP3, 2^23 is subtracted, and (q*2^s)*(x*2^-s) = q*x exactly.  Float4
+// group g of batch row b of half h is at xa_h + 16*(32b + g); the sum of
+// 32-column group j of batch row b at xsum_h[(4b + j)*xstr].
+template <int B, int R>
 __device__ __forceinline__ void q4k_sb_fp(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
-                                            const uint8_t *xa0, const uint8_t *xa1, uint32_t gs_rt, const float *xsum0,
-                                            const float *xsum1, int xstride, float (&acc)[R][B])
+                                            const uint8_t *xa0, const uint8_t *xa1, const float *xsum0,
+                                            const float *xsum1, int xstr, float (&acc)[R][B])
 {
-    const uint32_t gs = US ? 16u * US : gs_rt;
-    const int xstr = US ? US : xstride;
     const uint64_t neg_magic = pack2f(-kTwo23, -kTwo23);
     float d[R], dmin[R];
 #pragma unroll
@@ -293,8 +295,8 @@ __device__ __forceinline__ void q4k_sb_fp(const uint4 (&hd)[R], const uint4 (&qs
                     }
 #pragma unroll
                     for (int b = 0; b < B; ++b) {
-                        const ulonglong2 xl = *reinterpret_cast<const ulonglong2 *>(xa + (b * 32 + g_lo) * gs);
-                        const ulonglong2 xh = *reinterpret_cast<const ulonglong2 *>(xa + (b * 32 + g_hi) * gs);
+                        const ulonglong2 xl = *reinterpret_cast<const ulonglong2 *>(xa + 16 * (b * 32 + g_lo));
+                        const ulonglong2 xh = *reinterpret_cast<const ulonglong2 *>(xa + 16 * (b * 32 + g_hi));
                         const uint64_t xl0 = xl.x, xl1 = xl.y, xh0 = xh.x, xh1 = xh.y;
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
@@ -308,8 +310,8 @@ __device__ __forceinline__ void q4k_sb_fp(const uint4 (&hd)[R], const uint4 (&qs
             }
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                const float X0 = xsum_u[(b * 4 + 2 * lc) * xstr];
-                const float X1 = xsum_u[(b * 4 + 2 * lc + 1) * xstr];
+                const float X0 = xsum_u[(4 * b + 2 * lc) * xstr];
+                const float X1 = xsum_u[(4 * b + 2 * lc + 1) * xstr];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const float2 a0 = unpack2f(A[r][b][0]);
@@ -343,12 +345,12 @@ __device__ __forceinline__ void q8_realign(const uint32_t (&wv)[R][9], const uin
     }
 }
 
-// Batch 1: block-floating-point planes of the block's 32 columns at xa.
-template <int R, int US>
+// Batch 1: block-floating-point planes of the block's 32 columns, float4
+// group k at xa + 16k.
+template <int R>
 __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], const uint8_t *xa,
-                                            uint32_t gs_rt, float xscale, float (&acc)[R][1])
+                                            float xscale, float (&acc)[R][1])
 {
-    const uint32_t gs = US ? 16u * US : gs_rt;
     float d[R];
     uint32_t qw[R][8];
     q8_realign<R>(wv, off, d, qw);
@@ -359,7 +361,7 @@ __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uin
         for (int k = 0; k < 3; ++k) sp[r][k] = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint4 xv = *reinterpret_cast<const uint4 *>(xa + k * gs);
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xa + 16 * k);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint32_t v = qw[r][k];
@@ -373,12 +375,12 @@ __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uin
         acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2]), acc[r][0]);
 }
 
-// Batch >= 2: int8 quants through the magic-exponent trick (bias 128), fp32 x.
-template <int B, int R, int US>
+// Batch >= 2: int8 quants through the magic-exponent trick (bias 128), fp32 x
+// (float4 group k of batch row b at xa + 16*(8b + k)).
+template <int B, int R>
 __device__ __forceinline__ void q8_blk_fp(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], const uint8_t *xa,
-                                           uint32_t gs_rt, float (&acc)[R][B])
+                                           float (&acc)[R][B])
 {
-    const uint32_t gs = US ? 16u * US : gs_rt;
     float d[R];
     uint32_t qw[R][8];
     q8_realign<R>(wv, off, d, qw);
@@ -399,7 +401,7 @@ __device__ __forceinline__ void q8_blk_fp(const uint32_t (&wv)[R][9], const uint
         }
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-            const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xa + (b * 8 + k) * gs);
+            const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xa + 16 * (b * 8 + k));
             const uint64_t x01 = xv.x, x23 = xv.y;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -479,18 +481,21 @@ __device__ __forceinline__ float q6_dscale(const Q6Half &h, float d, int j)
     return d * static_cast<float>(s);
 }
 
-// Batch 1: block-floating-point planes of the half's 128 columns at xa (group
-// g at xa + g*gs); per 16-column sub-block j the plain sum x16[j*XU] (for the
-// -32 offset) and per 32-column group the plane scale xsc[(j/2)*XU].
-template <int R, int US>
-__device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_t *xa, uint32_t gs_rt,
-                                             const float *x16, const float *xsc, int xstride, float (&acc)[R][1])
+// Batch 1: block-floating-point planes of the half's 128 columns (float4
+// group g at xa + 16g); per 16-column sub-block j the plain sum x16[j] (for
+// the -32 offset) and per 32-column group the plane scale xsc[j/2].
+template <int R>
+__device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_t *xa, const float *x16,
+                                             const float *xsc, float (&acc)[R][1])
 {
-    const uint32_t gs = US ? 16u * US : gs_rt;
-    const int xstr = US ? US : xstride;
     float d[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) d[r] = half_bits_to_float(hr[r].dw);
+    const float4 x16a = *reinterpret_cast<const float4 *>(x16);
+    const float4 x16b = *reinterpret_cast<const float4 *>(x16 + 4);
+    const float4 xsc4 = *reinterpret_cast<const float4 *>(xsc);
+    const float x16v[8] = {x16a.x, x16a.y, x16a.z, x16a.w, x16b.x, x16b.y, x16b.z, x16b.w};
+    const float xscv[4] = {xsc4.x, xsc4.y, xsc4.z, xsc4.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         int sp[R][2][3];
@@ -502,7 +507,7 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
                 for (int k = 0; k < 3; ++k) sp[r][h][k] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint4 xv = *reinterpret_cast<const uint4 *>(xa + (8 * t + k) * gs);
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xa + 16 * (8 * t + k));
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t q = q6_quad(hr[r], t, k);
@@ -512,8 +517,8 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
                 sp[r][h][2] = dp4a_us(q, xv.z, sp[r][h][2]);
             }
         }
-        const float S = xsc[t * xstr];
-        const float X0 = x16[(2 * t) * xstr], X1 = x16[(2 * t + 1) * xstr];
+        const float S = xscv[t];
+        const float X0 = x16v[2 * t], X1 = x16v[2 * t + 1];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float ds0 = q6_dscale(hr[r], d[r], 2 * t), ds1 = q6_dscale(hr[r], d[r], 2 * t + 1);
@@ -529,12 +534,11 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
 
 // Batch >= 2: fp32 x; each 6-bit quant becomes the exact float 2^23 + q (one
 // byte permute into the magic pattern) and 2^23 + 32 is subtracted, giving
-// q - 32 exactly; packed f32x2 arithmetic.
-template <int B, int R, int US>
-__device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t *xa, uint32_t gs_rt,
-                                            float (&acc)[R][B])
+// q - 32 exactly; packed f32x2 arithmetic (float4 group g of batch row b at
+// xa + 16*(32b + g)).
+template <int B, int R>
+__device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t *xa, float (&acc)[R][B])
 {
-    const uint32_t gs = US ? 16u * US : gs_rt;
     const uint64_t neg_bias = pack2f(-(kTwo23 + 32.0f), -(kTwo23 + 32.0f));
     float d[R];
 #pragma unroll
@@ -558,7 +562,7 @@ __device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t
             }
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xa + (b * 32 + 8 * t + k) * gs);
+                const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xa + 16 * (b * 32 + 8 * t + k));
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     part[r][b] = fma_f32x2(q01[r], xv.x, part[r][b]);
@@ -580,27 +584,46 @@ __device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t
 
 // -------------------------------------------------------------------------- activations -> shared memory
 //
-// One warp-uniform pass: each lane loads float4 group f of batch row b
-// (columns 4f..4f+3; columns >= K are zero) and stores it at its place.  For
-// Q4_K the 8 lanes holding a 32-column group also sum it (unscaled).  Batch 1
-// stores block-floating-point byte planes (one exponent per 32 columns),
-// batch >= 2 stores fp32 pre-multiplied by 2^-s for the Q4_K nibble position.
-template <int FMT, int B, int US>
+// Layout (unit-major): unit slot us (Q4_K: h*XH + super-block for unit
+// u = 2*super-block + h; else us = u) owns SU = B*G + 1 consecutive 16-byte
+// slots, slot b*G + g holding float4 group g (columns 4g..4g+3 of the unit)
+// of batch row b; the last slot is padding.  Sums of x: Q4_K batch 1 per 32
+// columns at xsum[us*4 + j], batch >= 2 at xsum[(4b + j)*XU + us]; Q6_K
+// (batch 1) per 16 columns at xsum[us*8 + j].  Batch 1 group scales at
+// xscale[us*NJ + j].  (Per-unit sums and scales are read as one 16-byte
+// vector, the batch >= 2 sums one scalar at a time, lanes on consecutive us.)
+//
+// One warp-uniform pass per batch row: each lane loads float4 group f of the
+// row (columns 4f..4f+3; columns >= K are zero), consecutive lanes
+// consecutive groups (coalesced), four groups a lane per round with the next
+// round's loads in flight, and stores it at its slot; the 8 lanes of a
+// 32-column group reduce it with shuffles, the four groups' shuffles
+// interleaved.  Batch 1 stores block-floating-point byte planes (one
+// exponent per 32 columns; a NaN or infinity in a group makes its scale
+// NaN), batch >= 2 fp32 pre-multiplied by 2^-s for the Q4_K nibble position.
+__device__ __forceinline__ float fmax_nan(float a, float b)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+template <int FMT, int B>
 __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int cwarp, int lane, int nthreads, uint32_t xs_addr,
                                              float *xsum, float *xscale)
 {
     constexpr int UC = FMT == kFmtQ80 ? 32 : 128;
     constexpr int G = UC / 4;
-    const int XU = US ? US : a.XU;
-    const int XH = XU >> 1;
+    constexpr int NJ = UC / 32;
+    constexpr int SU = B * G + 1;
+    constexpr int UNR = 4;
+    const int XH = a.XU >> 1;
     const int K = static_cast<int>(a.K);
     const int g_total = a.U * G;
     const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x0) & 15u) == 0);
-    constexpr int UNR = 4;
     for (int b = 0; b < B; ++b) {
         const float *xb = x0 + static_cast<int64_t>(b) * K;
-        for (int base = cwarp * 32; base < g_total; base += UNR * nthreads) {
-            float4 v[UNR];
+        auto load = [&](int base, float4 (&v)[UNR]) {
 #pragma unroll
             for (int i = 0; i < UNR; ++i) {
                 const int f = base + i * nthreads + lane;
@@ -617,74 +640,104 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int 
                     }
                 }
             }
+        };
+        float4 v[UNR], nx[UNR];
+        int base = cwarp * 32;
+        if (base < g_total) load(base, v);
+        for (; base < g_total; base += UNR * nthreads) {
+            if (base + UNR * nthreads < g_total) load(base + UNR * nthreads, nx);   // warp-uniform
+            int f[UNR], us[UNR], g[UNR];
 #pragma unroll
             for (int i = 0; i < UNR; ++i) {
-                if (base + i * nthreads >= g_total) break;   // warp-uniform
-                const int f = base + i * nthreads + lane;
-                const int u = f / G, g = f % G;
-                const int us = FMT == kFmtQ4K ? ((u & 1) * XH + (u >> 1)) : u;   // unit slot
-                if constexpr (B == 1) {
-                    float amax = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-                    float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                    if constexpr (FMT != kFmtQ80) {
-                        // Q4_K: sums of 32 columns; Q6_K: of 16 columns (read below)
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                    }
-                    const float sum16 = sum;
-                    if constexpr (FMT == kFmtQ4K) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-                    const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 255u);
+                f[i] = base + i * nthreads + lane;
+                const int u = f[i] / G;
+                g[i] = f[i] % G;
+                us[i] = FMT == kFmtQ4K ? ((u & 1) * XH + (u >> 1)) : u;   // unit slot
+            }
+            // plain sums: per float4, then over 4 lanes (16 columns) and 8 (32)
+            float sum[UNR], sum16[UNR];
+#pragma unroll
+            for (int i = 0; i < UNR; ++i) sum[i] = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+            if constexpr (FMT != kFmtQ80) {
+#pragma unroll
+                for (int i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 1);
+#pragma unroll
+                for (int i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 2);
+#pragma unroll
+                for (int i = 0; i < UNR; ++i) sum16[i] = sum[i];
+                if constexpr (FMT == kFmtQ4K) {
+#pragma unroll
+                    for (int i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 4);
+                }
+            }
+            if constexpr (B == 1) {
+                float amax[UNR];
+#pragma unroll
+                for (int i = 0; i < UNR; ++i)
+                    amax[i] = fmax_nan(fmax_nan(fabsf(v[i].x), fabsf(v[i].y)), fmax_nan(fabsf(v[i].z), fabsf(v[i].w)));
+#pragma unroll
+                for (int o = 1; o <= 4; o <<= 1)
+#pragma unroll
+                    for (int i = 0; i < UNR; ++i) amax[i] = fmax_nan(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], o));
+#pragma unroll
+                for (int i = 0; i < UNR; ++i) {
+                    const int ebits = static_cast<int>((__float_as_uint(amax[i]) >> 23) & 255u);
                     const bool finite = ebits != 255;
                     const int E = max(ebits - 127, -96);
                     const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
                     const float down = __int_as_float((106 + E) << 23);   // 2^(E-21)
+                    // m = rint(x * 2^(21-E)), |m| <= 2^22: adding 1.5 * 2^23 in one
+                    // fp32 FMA rounds the exact x * 2^(21-E) to the nearest
+                    // integer (ties to even); the sum's bits minus those of
+                    // 1.5 * 2^23 are m
+                    constexpr float kRound = 12582912.0f;
+                    constexpr uint32_t kRoundBits = 0x4B400000u;
                     uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
                     if (finite) {
-                        m0 = static_cast<uint32_t>(__float2int_rn(v[i].x * up));
-                        m1 = static_cast<uint32_t>(__float2int_rn(v[i].y * up));
-                        m2 = static_cast<uint32_t>(__float2int_rn(v[i].z * up));
-                        m3 = static_cast<uint32_t>(__float2int_rn(v[i].w * up));
+                        m0 = __float_as_uint(fmaf(v[i].x, up, kRound)) - kRoundBits;
+                        m1 = __float_as_uint(fmaf(v[i].y, up, kRound)) - kRoundBits;
+                        m2 = __float_as_uint(fmaf(v[i].z, up, kRound)) - kRoundBits;
+                        m3 = __float_as_uint(fmaf(v[i].w, up, kRound)) - kRoundBits;
                     }
                     // byte-plane transpose: plane k holds byte k of the four columns
                     const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
                     const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
                     const uint32_t p0 = __byte_perm(t0, t1, 0x5410u), p1 = __byte_perm(t0, t1, 0x7632u);
                     const uint32_t p2 = __byte_perm(t2, t3, 0x5410u), p3 = __byte_perm(t2, t3, 0x7632u);
-                    if (f < g_total) {
-                        const int grp = FMT == kFmtQ80 ? 0 : (g >> 3);
+                    if (f[i] < g_total) {
+                        const int grp = g[i] >> 3;                     // 32-column group of the unit
                         if ((lane & 7) == 0) {
-                            xscale[grp * XU + us] = finite ? down : __int_as_float(0x7FC00000);
-                            if constexpr (FMT == kFmtQ4K) xsum[grp * XU + us] = sum;
+                            xscale[us[i] * NJ + grp] = finite ? down : __int_as_float(0x7FC00000);
+                            if constexpr (FMT == kFmtQ4K) xsum[us[i] * 4 + grp] = sum[i];
                         }
                         if constexpr (FMT == kFmtQ6K)
-                            if ((lane & 3) == 0) xsum[(g >> 2) * XU + us] = sum16;
-                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(g * XU + us);
+                            if ((lane & 3) == 0) xsum[us[i] * 8 + (g[i] >> 2)] = sum16[i];
+                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(us[i] * SU + g[i]);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                      ::"r"(dst), "r"(p0), "r"(p1), "r"(p2), "r"(p3) : "memory");
                     }
-                    continue;
                 }
-                if constexpr (FMT == kFmtQ4K) {
-                    float sum = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-                    if (f < g_total && (lane & 7) == 0) xsum[(b * 4 + (g >> 3)) * XU + us] = sum;
-                    const int c = 4 * g;
-                    v[i].x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
-                    v[i].y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
-                    v[i].z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
-                    v[i].w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
-                }
-                if (f < g_total) {
-                    const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>((b * G + g) * XU + us);
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(dst), "f"(v[i].x), "f"(v[i].y), "f"(v[i].z), "f"(v[i].w) : "memory");
+            } else {
+#pragma unroll
+                for (int i = 0; i < UNR; ++i) {
+                    float4 w = v[i];
+                    if constexpr (FMT == kFmtQ4K) {
+                        if (f[i] < g_total && (lane & 7) == 0) xsum[(b * 4 + (g[i] >> 3)) * a.XU + us[i]] = sum[i];
+                        const int c = 4 * g[i];
+                        w.x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
+                        w.y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
+                        w.z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
+                        w.w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
+                    }
+                    if (f[i] < g_total) {
+                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(us[i] * SU + b * G + g[i]);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                                     ::"r"(dst), "f"(w.x), "f"(w.y), "f"(w.z), "f"(w.w) : "memory");
+                    }
                 }
             }
+#pragma unroll
+            for (int i = 0; i < UNR; ++i) v[i] = nx[i];
         }
     }
 }
@@ -745,7 +798,7 @@ __device__ __forceinline__ void copy_item(const GemvArgs &a, const uint8_t *w0, 
         }
 }
 
-template <int FMT, int B, int US>
+template <int FMT, int B>
 __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -858,8 +911,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     const int team = lane >> a.lsw;
     const int sl = lane & (SW - 1);
     const int cpl = a.cpl;
-    const int XU = US ? US : a.XU;
-    const int XH = XU >> 1;
+    const int XH = a.XU >> 1;
+    constexpr int SU = B * (FMT == kFmtQ80 ? 8 : 32) + 1;   // 16-byte slots a unit slot owns
     const uint8_t *xs = smem + a.off_x;
     const float *xsum = reinterpret_cast<const float *>(smem + a.off_xsum);
     const float *xscale = reinterpret_cast<const float *>(smem + a.off_xscale);
@@ -867,13 +920,12 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     // the weights do not depend on earlier kernels, x may: with programmatic
     // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    stage_x<FMT, B, US>(a, x0, static_cast<int>(cwarp), lane, 32 * NW, smem_u32(xs),
+    stage_x<FMT, B>(a, x0, static_cast<int>(cwarp), lane, 32 * NW, smem_u32(xs),
                              reinterpret_cast<float *>(smem + a.off_xsum),
                              reinterpret_cast<float *>(smem + a.off_xscale));
     named_bar_sync(1, 32 * NW);
     if (cwarp >= nw) return;
 
-    const uint32_t gs_rt = 16u * static_cast<uint32_t>(XU);
     const uintptr_t wbase = reinterpret_cast<uintptr_t>(w0);
     const int chunk_lu = SW * cpl;                 // lane units per chunk
     const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
@@ -940,13 +992,13 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                 if (valid) {
                     const int lu = lu0;
                     const bool has_hi = 2 * lu + 1 < a.U;
-                    const uint8_t *xa0 = xs + 16 * lu;
-                    const uint8_t *xa1 = xs + 16 * (XH + lu);
+                    const uint8_t *xa0 = xs + 16 * SU * lu;
+                    const uint8_t *xa1 = xs + 16 * SU * (XH + lu);
                     if constexpr (B == 1)
-                        q4k_sb_dig<R, US>(hd, qs, has_hi, xa0, xa1, gs_rt, xsum + lu, xsum + XH + lu,
-                                            xscale + lu, xscale + XH + lu, XU, acc);
+                        q4k_sb_dig<R>(hd, qs, has_hi, xa0, xa1, xsum + 4 * lu, xsum + 4 * (XH + lu),
+                                      xscale + 4 * lu, xscale + 4 * (XH + lu), acc);
                     else
-                        q4k_sb_fp<B, R, US>(hd, qs, has_hi, xa0, xa1, gs_rt, xsum + lu, xsum + XH + lu, XU, acc);
+                        q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, acc);
                 }
             } else if constexpr (FMT == kFmtQ6K) {
                 // lane unit = half super-block: block li/2 of the chunk, half li%2
@@ -960,11 +1012,11 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
                 if (valid) {
-                    const uint8_t *xa = xs + 16 * lu0;
+                    const uint8_t *xa = xs + 16 * SU * lu0;
                     if constexpr (B == 1)
-                        q6k_half_dig<R, US>(hr, xa, gs_rt, xsum + lu0, xscale + lu0, XU, acc);
+                        q6k_half_dig<R>(hr, xa, xsum + 8 * lu0, xscale + 4 * lu0, acc);
                     else
-                        q6k_half_fp<B, R, US>(hr, xa, gs_rt, acc);
+                        q6k_half_fp<B, R>(hr, xa, acc);
                 }
             } else {
                 uint32_t wv[CM][R][9], off[CM][R];
@@ -988,11 +1040,11 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                 for (int i = 0; i < CM; ++i) {
                     const int lu = lu0 + i * SW;
                     if (i < cpl && lu < a.LU) {
-                        const uint8_t *xa = xs + 16 * lu;
+                        const uint8_t *xa = xs + 16 * SU * lu;
                         if constexpr (B == 1)
-                            q8_blk_dig<R, US>(wv[i], off[i], xa, gs_rt, xscale[lu], acc);
+                            q8_blk_dig<R>(wv[i], off[i], xa, xscale[lu], acc);
                         else
-                            q8_blk_fp<B, R, US>(wv[i], off[i], xa, gs_rt, acc);
+                            q8_blk_fp<B, R>(wv[i], off[i], xa, acc);
                     }
                 }
             }
@@ -1047,14 +1099,14 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
 }
 
 // Launch one instantiation (defined per format in qk_gemv_q4k.cu / qk_gemv_q80.cu / qk_gemv_q6k.cu).
-cudaError_t gemv_launch_q4k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
-cudaError_t gemv_launch_q80(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
-cudaError_t gemv_launch_q6k(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q4k(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q6k(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
-template <int FMT, int B, int US>
+template <int FMT, int B>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
-    auto kern = gemv_kernel<FMT, B, US>;
+    auto kern = gemv_kernel<FMT, B>;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1079,12 +1131,5 @@ cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t 
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
-
-#define QK_GEMV_DISPATCH_US(FMT, B, US_RT)                                       \
-    switch (US_RT) {                                                                  \
-    case 32: return gemv_launch_one<FMT, B, 32>(a, grid, smem, st, pdl);         \
-    case 128: return gemv_launch_one<FMT, B, 128>(a, grid, smem, st, pdl);       \
-    default: return gemv_launch_one<FMT, B, 0>(a, grid, smem, st, pdl);          \
-    }
 
 }  // namespace qk

@@ -4,17 +4,17 @@
 
 namespace qk {
 
-cudaError_t gemv_launch_q80(int batch, int us, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
+cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
     switch (batch) {
-    case 1: QK_GEMV_DISPATCH_US(kFmtQ80, 1, us)
-    case 2: QK_GEMV_DISPATCH_US(kFmtQ80, 2, us)
-    case 3: QK_GEMV_DISPATCH_US(kFmtQ80, 3, us)
-    case 4: QK_GEMV_DISPATCH_US(kFmtQ80, 4, us)
-    case 5: QK_GEMV_DISPATCH_US(kFmtQ80, 5, us)
-    case 6: QK_GEMV_DISPATCH_US(kFmtQ80, 6, us)
-    case 7: QK_GEMV_DISPATCH_US(kFmtQ80, 7, us)
-    case 8: QK_GEMV_DISPATCH_US(kFmtQ80, 8, us)
+    case 1: return gemv_launch_one<kFmtQ80, 1>(a, grid, smem, st, pdl);
+    case 2: return gemv_launch_one<kFmtQ80, 2>(a, grid, smem, st, pdl);
+    case 3: return gemv_launch_one<kFmtQ80, 3>(a, grid, smem, st, pdl);
+    case 4: return gemv_launch_one<kFmtQ80, 4>(a, grid, smem, st, pdl);
+    case 5: return gemv_launch_one<kFmtQ80, 5>(a, grid, smem, st, pdl);
+    case 6: return gemv_launch_one<kFmtQ80, 6>(a, grid, smem, st, pdl);
+    case 7: return gemv_launch_one<kFmtQ80, 7>(a, grid, smem, st, pdl);
+    case 8: return gemv_launch_one<kFmtQ80, 8>(a, grid, smem, st, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -140,6 +140,23 @@ def test_nonfinite_scales_propagate(qk, orc, fmt):
     assert_close(y[:, keep], yr[:, keep], s[:, keep], "finite rows")
 
 
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q6_k"])
+@pytest.mark.parametrize("batch", [1, 2])
+def test_nonfinite_activations_propagate(qk, orc, fmt, batch):
+    """A NaN (or an infinity) in x makes every output of its batch row non-finite, as in the oracle."""
+    rows, K = 48, 768
+    wq = synth.weights(fmt, rows, K, seed=16)
+    x = synth.activations(batch, K, seed=16)
+    x[0, 37] = np.nan
+    if batch > 1:
+        x[1, 300] = np.inf
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert np.all(np.isnan(yr[0])) and np.all(np.isnan(y[0]))
+    if batch > 1:
+        assert not np.any(np.isfinite(yr[1])) and not np.any(np.isfinite(y[1]))
+
+
 def test_too_large_is_rejected_before_launch(qk):
     K, B = 14336 * 3, 8
     w = torch.zeros(qk.row_bytes("q4_k", K), dtype=torch.uint8, device="cuda")
