@@ -77,11 +77,14 @@ typedef enum {
  *   x      device fp32 [batch][K], row stride K; 4-byte aligned.
  *   y      device fp32 [batch][ldy]; writes y[b*ldy + r] for r < rows only;
  *          4-byte aligned.  ldy == 0 means ldy = rows.
- *   K      columns, any K >= 1.  The kernel keeps the whole activation batch
- *          (batch * K * 4 bytes, K rounded up to the block size) in shared
- *          memory next to at least two staged tiles of rows; calls where that
- *          does not fit in the device's shared memory per block (for example
- *          batch * K above about 45000 on GB300) return QK_ERR_TOO_LARGE.
+ *   K      columns, any K >= 1.  A launch keeps its activation rows (about
+ *          4.1 to 4.6 bytes a column each, K rounded up to the block size) in
+ *          shared memory next to at least one staged tile of weight rows; a
+ *          batch whose activations do not fit in the device's shared memory
+ *          per block is computed by several launches of fewer batch rows
+ *          (each batch row's result is the same as in a call of that size).
+ *          A K for which one activation row does not fit (above about 48000
+ *          on GB300) returns QK_ERR_TOO_LARGE before any launch.
  * Arithmetic is fp32; results differ from the exact dot by at most
  * 1e-5 * sum|w*x| + 1e-6 per element (the tests check this bound).
  */

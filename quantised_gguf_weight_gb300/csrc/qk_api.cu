@@ -50,9 +50,14 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     if (ldy < rows) return QK_ERR_BAD_DIM;
     if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4))
         return QK_ERR_ALIGN;
+    // the kernel keeps a launch's activation rows in shared memory: a batch
+    // whose activations do not fit is cut into launches of fewer rows (as
+    // even as possible); only a single row that does not fit is refused
     qk::GemvPlan plan;
-    if (!qk::gemv_plan(fmt, rows, K, batch, pair, &plan)) {
-        // either no usable device or the activations do not fit in shared memory
+    int bmax = batch;
+    while (bmax > 0 && !qk::gemv_plan(fmt, rows, K, bmax, pair, &plan)) --bmax;
+    if (bmax == 0) {
+        // either no usable device or one activation row does not fit
         int dev_count = 0;
         if (cudaGetDeviceCount(&dev_count) != cudaSuccess || dev_count == 0) return QK_ERR_CUDA;
         return QK_ERR_TOO_LARGE;
@@ -62,11 +67,22 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     int *err = error_word_ptr();
     if (!err) return QK_ERR_CUDA;
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * plan.row_bytes;
-    cudaError_t e = qk::gemv_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
-                                    reinterpret_cast<cudaStream_t>(stream), plan, err,
-                                    g_wait_limit_ns.load(), g_skip_item.load(), g_programmatic.load() != 0,
-                                    pair ? up_offset - row_offset : 0);
-    return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
+    const int parts = (batch + bmax - 1) / bmax;
+    for (int p = 0, b0 = 0, planned = bmax; p < parts; ++p) {
+        const int nb = (batch - b0) / (parts - p);
+        if (nb != planned) {
+            if (!qk::gemv_plan(fmt, rows, K, nb, pair, &plan)) return QK_ERR_CUDA;
+            planned = nb;
+        }
+        cudaError_t e = qk::gemv_launch(fmt, w_rows, rows, K, x + static_cast<int64_t>(b0) * K, nb,
+                                        y + static_cast<int64_t>(b0) * ldy, ldy,
+                                        reinterpret_cast<cudaStream_t>(stream), plan, err,
+                                        g_wait_limit_ns.load(), g_skip_item.load(), g_programmatic.load() != 0,
+                                        pair ? up_offset - row_offset : 0);
+        if (e != cudaSuccess) return QK_ERR_CUDA;
+        b0 += nb;
+    }
+    return QK_OK;
 }
 
 }  // namespace

@@ -157,8 +157,40 @@ def test_nonfinite_activations_propagate(qk, orc, fmt, batch):
         assert not np.any(np.isfinite(yr[1])) and not np.any(np.isfinite(y[1]))
 
 
+@pytest.mark.parametrize("fmt,K,batch", [("q4_k", 14336, 8), ("q4_k", 14336, 4), ("q6_k", 14336, 5),
+                                         ("q8_0", 30000, 3), ("q4_k", 40960, 2)])
+def test_batch_split_when_activations_do_not_fit(qk, orc, fmt, K, batch):
+    """Batches whose activations exceed shared memory run as several launches of fewer rows."""
+    rows = 37
+    wq = synth.weights(fmt, rows, K, seed=17)
+    x = synth.activations(batch, K, seed=17)
+    with pytest.raises(qk.QKError):
+        qk.debug_gemv_plan(fmt, rows, K, batch)          # the whole batch does not fit
+    bmax = next(b for b in range(batch, 0, -1) if _fits(qk, fmt, rows, K, b))
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    assert_close(y, yr, s, f"split {fmt} K={K} B={batch}")
+    # the launches are as even as possible; each part gives the bits of a call of its size
+    parts = -(-batch // bmax)
+    b0 = 0
+    for p in range(parts):
+        nb = (batch - b0) // (parts - p)
+        yp = gpu_gemv(qk, fmt, wq, 0, rows, K, x[b0:b0 + nb]).cpu().numpy()
+        assert np.array_equal(yp, y[b0:b0 + nb])
+        b0 += nb
+
+
+def _fits(qk, fmt, rows, K, b):
+    try:
+        qk.debug_gemv_plan(fmt, rows, K, b)
+        return True
+    except qk.QKError:
+        return False
+
+
 def test_too_large_is_rejected_before_launch(qk):
-    K, B = 14336 * 3, 8
+    """One activation row of K = 57344 (229 KB) does not fit in shared memory."""
+    K, B = 14336 * 4, 8
     w = torch.zeros(qk.row_bytes("q4_k", K), dtype=torch.uint8, device="cuda")
     x = torch.zeros((B, K), device="cuda")
     y = torch.full((B, 1), 5.0, device="cuda")
