@@ -10,20 +10,26 @@
 // port runs prefill through GEMMs that dequantise the weight format in the
 // kernel ("loom-port-llm" SKILL.md, "What the starter generates", gen_gemm.py).
 //
-// Kernel shape (one CTA per 128 weight rows x up to 512 tokens):
-//  * warp 0 issues the TMA copies: the raw Q4_K bytes of 128 rows x one
-//    super-block (a 2-D tensor map over the rows, 144 x 128 bytes) and the
-//    bf16 activations of each 64-column K chunk (a 2-D tensor map with the
-//    128-byte swizzle, two boxes of 256 tokens);
-//  * warp 1 owns the tensor memory (512 f32 columns = 128 lanes x 512 tokens)
-//    and one of its threads issues tcgen05.mma (M = 128 weight rows, N = 256
-//    tokens, K = 16) and tcgen05.commit;
-//  * warps 2-5 dequantise each 64-column chunk of the 128 rows into the
+// Kernel shape: a cluster of two CTAs (a CTA pair) per 256 weight rows x up
+// to 512 tokens; one tcgen05.mma.cta_group::2 covers M = 256 weight rows
+// (128 in each CTA's shared memory) x N = 256 tokens (128 in each CTA's
+// shared memory) x K = 16, and each CTA's tensor memory accumulates its own
+// 128 rows x 512 tokens (512 f32 columns).  In each CTA:
+//  * warp 0 issues the TMA copies: the raw Q4_K bytes of its 128 rows x one
+//    super-block (a 2-D tensor map over the rows, 144 x 128 bytes) and its
+//    128-token slice of the bf16 activations of each 64-column K chunk (a
+//    2-D tensor map with the 128-byte swizzle, one box per token block);
+//  * warp 1 owns the tensor memory; in the even CTA one thread issues the
+//    pair's MMAs and commits (multicast to both CTAs' mbarriers), in the odd
+//    CTA one thread forwards "stage ready" (its own activations landed and
+//    weights dequantised) to the even CTA;
+//  * warps 2-9 dequantise each 64-column chunk of the 128 rows into the
 //    K-major 128-byte-swizzled bf16 layout the MMA reads, then run the
 //    epilogue: tcgen05.ld of 32 lanes x 32 columns -> coalesced stores of Y.
-// Double-buffered stages synchronise through mbarriers; every wait is bounded
-// and a wait that runs out aborts the CTA cleanly (copies drained, MMAs
-// completed, tensor memory freed) and records the device error word.
+// Three (Q8_0: four) 48 KB stages synchronise through mbarriers; every wait is
+// bounded, a wait that runs out aborts the CTA cleanly (copies drained, MMAs
+// completed, tensor memory freed) and records the device error word, and
+// both CTAs meet at a cluster barrier before the tensor memory is freed.
 #include <algorithm>
 #include <cstdint>
 #include <cuda.h>
@@ -38,12 +44,12 @@ namespace qk {
 
 namespace gemm {
 
-constexpr int kBM = 128;                 // weight rows per tile (MMA M)
-constexpr int kBN = 256;                 // tokens per MMA (MMA N)
+constexpr int kBM = 128;                 // weight rows per CTA (half of the pair's MMA M = 256)
+constexpr int kBN = 256;                 // tokens per MMA (MMA N), kBN/2 in each CTA
+constexpr int kBNc = kBN / 2;            // tokens of one CTA's slice of a token block
 constexpr int kBK = 64;                  // K columns per stage (one 128-byte swizzle row)
-constexpr int kStages = 2;
-constexpr int kRawStages = 2;
-constexpr int kRawBytes = kBM * 144;     // one Q4_K super-block column of 128 rows
+constexpr int kRawHdr = kBM * 16;       // Q4_K: the 16-byte header (d, dmin, scales) of 128 rows
+constexpr int kRawChunk = kBM * 48;      // Q4_K per chunk: headers + the 32 quant bytes of 128 rows
 constexpr int kDeq = 256;                // dequantising threads: two per weight row
 constexpr int kThreads = 64 + kDeq;
 constexpr uint32_t kTmemCols = 512;
@@ -56,21 +62,26 @@ template <int FMT, int MODE>
 struct Shape {
     static constexpr int halves = MODE == kSwiglu ? 1 : 2;   // token blocks of kBN per CTA pass
     static constexpr int tiles = MODE == kSwiglu ? 2 : 1;    // weight tiles per K chunk
-    static constexpr int b_stage = halves * kBN * kBK * 2;
+    static constexpr int b_half = kBNc * kBK * 2;            // 16 KB: a CTA's slice of one token block
+    static constexpr int b_stage = halves * b_half;
     static constexpr int a_tile = kBM * kBK * 2;             // 16 KB
     static constexpr int a_stage = tiles * a_tile;
-    static constexpr int raw_stage = FMT == kFmtQ80 ? 0 : tiles * kRawBytes;   // Q8_0 reads weights directly
+    static constexpr int raw_stage = FMT == kFmtQ80 ? 0 : tiles * kRawChunk;   // Q8_0 reads weights directly
+    static constexpr int stages = (FMT == kFmtQ4K && MODE == kSwiglu) ? 3 : 4;
     static constexpr int off_b = 0;
-    static constexpr int off_a = off_b + kStages * b_stage;
-    static constexpr int off_raw = off_a + kStages * a_stage;
-    static constexpr int off_bar = off_raw + kRawStages * raw_stage;
+    static constexpr int off_a = off_b + stages * b_stage;
+    static constexpr int off_raw = off_a + stages * a_stage;
+    static constexpr int off_bar = off_raw + stages * raw_stage;
     static constexpr int smem = off_bar + 256 + 1024;        // + alignment slack
 };
 
-// barrier slots (8 bytes each) after the barrier offset
-constexpr int kBarXFull = 0, kBarAFull = 2, kBarEmpty = 4, kBarRawFull = 6, kBarRawEmpty = 8, kBarAcc = 10,
-              kBarDone = 11;
-constexpr int kOffTmemSlot = 96, kOffAbort = 100;
+// barrier slots (8 bytes each) after the barrier offset, four per stage kind:
+// XFull (this CTA's copies of the stage landed: activations and Q4_K bytes),
+// AFull (this CTA's dequantising warps wrote the stage; implies XFull),
+// Empty (the pair's MMAs of the stage completed), Peer (even CTA: the odd
+// CTA's stage is complete)
+constexpr int kBarXFull = 0, kBarAFull = 4, kBarEmpty = 8, kBarPeer = 12, kBarAcc = 16, kBarDone = 17;
+constexpr int kOffTmemSlot = 184, kOffAbort = 188;
 
 struct Args {
     float *y;
@@ -79,18 +90,19 @@ struct Args {
     const uint8_t *wq8[2];  // Q8_0: first byte of output row 0 of each weight tile (read directly)
     int64_t row_bytes;      // Q8_0: bytes of one weight row
     int nb;                 // Q8_0: blocks of 32 per row
-    int n_tiles;
+    int n_tiles;            // pair tiles of 2*kBM weight rows
     int nk;            // number of 64-column K chunks
     int skip_chunk;    // test hook: CTA 0 never loads the activations of this chunk (-1: none)
+    int tma_y;         // 1: the output is written through the tensor map of Y (16-byte aligned rows)
     uint64_t wait_ns;
     int *err;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit, volatile int *abort_flag,
-                                              int *err)
+                                              int *err, bool poll = false)
 {
     if (*abort_flag) return false;
-    if (mbar_wait(bar, parity, limit)) return true;
+    if (poll ? mbar_wait_poll(bar, parity, limit) : mbar_wait(bar, parity, limit)) return true;
     *abort_flag = 1;
     record_error(err, kErrTimeout);
     return false;
@@ -98,11 +110,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const Args a)
+gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_y, const Args a)
 {
     constexpr bool kQ8 = FMT == kFmtQ80;        // Q8_0: weights read directly by the dequantising threads
     using L = Shape<FMT, MODE>;
-    constexpr int kHalves = L::halves, kTiles = L::tiles;
+    constexpr int kHalves = L::halves, kTiles = L::tiles, kStages = L::stages;
     constexpr int kOffB = L::off_b, kOffA = L::off_a, kOffRaw = L::off_raw, kOffBar = L::off_bar;
     constexpr int kBStage = L::b_stage, kAStage = L::a_stage, kRawStage = L::raw_stage;
     extern __shared__ uint8_t smem_raw[];
@@ -115,9 +128,11 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int n_tile = blockIdx.x % a.n_tiles;
-    const int m_block = blockIdx.x / a.n_tiles;
-    const int n0 = n_tile * kBM;
+    const uint32_t rank = cluster_ctarank();     // 0: the CTA that issues the pair's MMAs
+    const int pair = blockIdx.x >> 1;
+    const int n_tile = pair % a.n_tiles;
+    const int m_block = pair / a.n_tiles;
+    const int n0 = n_tile * (2 * kBM) + static_cast<int>(rank) * kBM;   // this CTA's first weight row
     const int m0 = m_block * (kBN * kHalves);
     const int nh = (kHalves == 2 && (a.M - m0) > kBN) ? 2 : 1;   // token blocks of kBN used in this pass
     const int nk = a.nk;
@@ -125,80 +140,80 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarXFull + s), 1);
-            mbar_init(bar(kBarAFull + s), kDeq);
+            mbar_init(bar(kBarAFull + s), kDeq / 32);   // one arrival per dequantising warp
             mbar_init(bar(kBarEmpty + s), 1);
-        }
-        for (int r = 0; r < kRawStages; ++r) {
-            mbar_init(bar(kBarRawFull + r), 1);
-            mbar_init(bar(kBarRawEmpty + r), kDeq);
+            mbar_init(bar(kBarPeer + s), 1);
         }
         mbar_init(bar(kBarAcc), 1);
         mbar_init(bar(kBarDone), 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
-        if (!kQ8) tma_prefetch_desc(&tm_w);
+        if (!kQ8) {
+            tma_prefetch_desc(&tm_w);
+            tma_prefetch_desc(&tm_q);
+        }
     }
     if (warp == 1) {
-        tmem_alloc(base_u32 + kOffBar + kOffTmemSlot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(base_u32 + kOffBar + kOffTmemSlot, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();          // both CTAs' mbarriers initialised, tensor memory allocated
     tc_fence_after();
     const uint32_t taddr = *tmem_slot;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // per chunk: this CTA's 128-token slices of the activations and, for
+        // Q4_K, the headers and the chunk's 32 quant bytes of its 128 rows
         if (lane == 0) {
             const uint64_t pol_w = l2_evict_first_policy();
             const uint64_t pol_x = l2_evict_last_policy();
-            int issued_x = 0, issued_raw = 0;
+            int issued = 0;
             for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
-                if (!kQ8 && (kc & 3) == 0) {
-                    const int kb = kc >> 2, r = kb % kRawStages;
-                    if (kb >= kRawStages &&
-                        !wait_or_abort(bar(kBarRawEmpty + r), ((kb / kRawStages) - 1) & 1, a.wait_ns, abort_flag,
-                                       a.err))
-                        break;
-                    mbar_arrive_expect_tx(bar(kBarRawFull + r), kTiles * kRawBytes);
-                    for (int i = 0; i < kTiles; ++i)
-                        tma_load_2d(base_u32 + kOffRaw + r * kRawStage + i * kRawBytes, &tm_w, kb * 144,
-                                    a.row0[i] + n0, bar(kBarRawFull + r), pol_w);
-                    ++issued_raw;
-                }
                 const int s = kc % kStages;
-                if (kc >= kStages &&
-                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
+                if (kc >= kStages && !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns,
+                                                    abort_flag, a.err, true))
                     break;
                 if (!(kc == a.skip_chunk && blockIdx.x == 0)) {
-                    mbar_arrive_expect_tx(bar(kBarXFull + s), static_cast<uint32_t>(nh * kBN * kBK * 2));
+                    const uint32_t full = bar(kBarXFull + s);
+                    const uint32_t tx = static_cast<uint32_t>(nh * L::b_half + L::raw_stage);
+                    mbar_arrive_expect_tx(full, tx);
                     for (int h = 0; h < nh; ++h)
-                        tma_load_2d(base_u32 + kOffB + s * kBStage + h * (kBN * kBK * 2), &tm_x, kc * kBK,
-                                    m0 + h * kBN, bar(kBarXFull + s), pol_x);
+                        tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kc * kBK,
+                                    m0 + h * kBN + static_cast<int>(rank) * kBNc, full, pol_x);
+                    if (!kQ8) {
+                        const int kb = kc >> 2, c = kc & 3;
+                        for (int i = 0; i < kTiles; ++i) {
+                            const uint32_t raw = base_u32 + kOffRaw + s * kRawStage + i * kRawChunk;
+                            tma_load_2d(raw, &tm_w, kb * 144, a.row0[i] + n0, full, pol_w);
+                            tma_load_2d(raw + kRawHdr, &tm_q, kb * 144 + 16 + 32 * c, a.row0[i] + n0, full, pol_w);
+                        }
+                    }
                 }
-                ++issued_x;
+                ++issued;
             }
             // let every copy issued land before the CTA can exit
-            for (int t = issued_x - kStages; t < issued_x; ++t) {
+            for (int t = issued - kStages; t < issued; ++t) {
                 if (t < 0 || (t == a.skip_chunk && blockIdx.x == 0)) continue;
                 mbar_wait(bar(kBarXFull + t % kStages), (t / kStages) & 1, a.wait_ns);
             }
-            for (int t = issued_raw - kRawStages; t < issued_raw; ++t) {
-                if (t < 0) continue;
-                mbar_wait(bar(kBarRawFull + t % kRawStages), (t / kRawStages) & 1, a.wait_ns);
-            }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
-            bool any = false;
+        if (lane == 0 && rank == 0) {
+            // -------------------------------------------------------- MMA issuer (even CTA)
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN);
+            bool any = false, ready = false;
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
                 const uint32_t par = (kc / kStages) & 1;
-                if (!wait_or_abort(bar(kBarAFull + s), par, a.wait_ns, abort_flag, a.err)) break;
-                if (!wait_or_abort(bar(kBarXFull + s), par, a.wait_ns, abort_flag, a.err)) break;
+                // polled: the issuing thread must not sleep past the phase
+                if (!ready) {
+                    if (!wait_or_abort(bar(kBarAFull + s), par, a.wait_ns, abort_flag, a.err, true)) break;
+                    if (!wait_or_abort(bar(kBarPeer + s), par, a.wait_ns, abort_flag, a.err, true)) break;
+                }
+                ready = false;
                 tc_fence_after();
                 const uint32_t a_base = base_u32 + kOffA + s * kAStage;
                 const uint32_t b_base = base_u32 + kOffB + s * kBStage;
@@ -209,20 +224,38 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         const uint64_t ad = smem_desc_sw128_kmajor(a_base + i * L::a_tile + 32u * kk);
                         for (int h = 0; h < nh; ++h) {
                             // accumulator columns: token block h (store/acc) or weight tile i (swiglu)
-                            const uint64_t bd = smem_desc_sw128_kmajor(b_base + h * (kBN * kBK * 2) + 32u * kk);
-                            tc_mma_bf16(taddr + static_cast<uint32_t>((h + i) * kBN), ad, bd, idesc, (kc | kk) != 0);
+                            const uint64_t bd = smem_desc_sw128_kmajor(b_base + h * L::b_half + 32u * kk);
+                            tc_mma_bf16_pair(taddr + static_cast<uint32_t>((h + i) * kBN), ad, bd, idesc,
+                                             (kc | kk) != 0);
                         }
+                    }
+                    if (kk == 0 && kc + 1 < nk) {
+                        // while this chunk's MMAs are queued: is the next stage
+                        // complete already?  Then its MMAs follow without a gap
+                        const int s1 = (kc + 1) % kStages;
+                        const uint32_t par1 = ((kc + 1) / kStages) & 1;
+                        ready = mbar_test(bar(kBarAFull + s1), par1) && mbar_test(bar(kBarPeer + s1), par1);
                     }
                 }
                 any = true;
-                tc_commit(bar(kBarEmpty + s));   // stage s reusable once these MMAs complete
+                tc_commit_pair(bar(kBarEmpty + s), 0x3);   // stage s reusable in both CTAs once these complete
             }
-            if (!*abort_flag) tc_commit(bar(kBarAcc));
+            if (!*abort_flag) tc_commit_pair(bar(kBarAcc), 0x3);
             if (any) {
                 // no MMA may still read shared memory or write tensor memory
                 // when the tensor memory is freed below
-                tc_commit(bar(kBarDone));
+                tc_commit_pair(bar(kBarDone), 0x1);
                 mbar_wait(bar(kBarDone), 0, a.wait_ns);
+            }
+        } else if (lane == 0) {
+            // -------------------------------------------------------- stage-ready forwarder (odd CTA)
+            // AFull of a stage implies its copies landed (the dequantising
+            // warps waited for them)
+            const uint32_t peer0 = mapa_shared(bar(kBarPeer), 0);
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kStages;
+                if (!wait_or_abort(bar(kBarAFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err, true)) break;
+                mbar_arrive_remote(peer0 + 8u * s);
             }
         }
     } else {
@@ -235,16 +268,15 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if constexpr (!kQ8) {
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
-                const int kb = kc >> 2, c = kc & 3, r = kb % kRawStages;
-                if (c == 0 && !wait_or_abort(bar(kBarRawFull + r), (kb / kRawStages) & 1, a.wait_ns, abort_flag, a.err))
-                    break;
-                if (kc >= kStages &&
-                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
-                    break;
+                const int c = kc & 3;
+                // the stage's copies landed (which also means its MMAs of
+                // kStages chunks back completed: the producer waited for that)
+                const bool ok = wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
 #pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
-                    const uint8_t *row = base + kOffRaw + r * kRawStage + i * kRawBytes + t * 144;
-                    const uint4 hd = *reinterpret_cast<const uint4 *>(row);
+                    const uint8_t *raw = base + kOffRaw + s * kRawStage + i * kRawChunk;
+                    const uint4 hd = *reinterpret_cast<const uint4 *>(raw + t * 16);
                     const float d = half_bits_to_float(hd.x);
                     const float dmin = half_bits_to_float(hd.x >> 16);
                     // 6-bit scale and min of sub-block j = 2c + sel
@@ -268,7 +300,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     const uint64_t sc01 = pack2f(s0, s1);
                     const uint64_t of01 = pack2f(s0 * -kTwo23, s1 * -kTwo23);
                     const uint64_t ndm = pack2f(-dm, -dm);
-                    const uint4 *qs = reinterpret_cast<const uint4 *>(row + 16 + 32 * c);
+                    const uint4 *qs = reinterpret_cast<const uint4 *>(raw + kRawHdr + t * 32);
                     const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {                  // bytes 16*hf .. 16*hf+15 of the sub-block
@@ -300,9 +332,11 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         }
                     }
                 }
+                // every lane's stores are made visible to the tensor cores, then
+                // one lane arrives for the warp
                 fence_proxy_async_smem();
-                mbar_arrive(bar(kBarAFull + s));
-                if (c == 3 || kc == nk - 1) mbar_arrive(bar(kBarRawEmpty + r));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarAFull + s));
             }
         } else {
             // Q8_0: block 2kc + sel of this thread's row of each tile (rows past N
@@ -338,9 +372,10 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int k = 0; k < 9; ++k) cur[i][k] = nxt[i][k];
                 }
                 if (kc + 1 < nk) fetch(kc + 1, nxt, nof);
-                if (kc >= kStages &&
-                    !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err))
-                    break;
+                // the stage's activation copy landed, so its MMAs of kStages chunks
+                // back completed (the producer waited for that)
+                const bool ok = wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
 #pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
                     const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
@@ -371,11 +406,13 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(bar(kBarAFull + s));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarAFull + s));
             }
         }
         // epilogue: tensor memory -> registers -> Y (store, acc) or H (swiglu)
-        if (wait_or_abort(bar(kBarAcc), 0, a.wait_ns, abort_flag, a.err)) {
+        // warp-uniform: tcgen05.ld below is a whole-warp instruction
+        if (__all_sync(0xFFFFFFFFu, wait_or_abort(bar(kBarAcc), 0, a.wait_ns, abort_flag, a.err))) {
             tc_fence_after();
             // warp w may read TMEM lanes 32*(w%4) ..; the two warps of each lane
             // quarter take one half of the accumulator columns each
@@ -384,30 +421,74 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * q) << 16);
             const int cols = nh * kBN;
             const int part = (warp - 2) >> 2;
-            for (int j0 = part * (cols / 2); j0 < (part + 1) * (cols / 2); j0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
-                if constexpr (MODE == kSwiglu) {
-                    uint32_t u[32];                            // the up tile's accumulators
-                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kBN + j0), u);
-                    tmem_ld_wait();
-                    if (n < a.N) {
+            if (a.tma_y) {
+                // each 32 rows x 32 tokens go through a 4 KB shared-memory tile
+                // ([token][row], two per warp, the stages' space is free now)
+                // and one TMA store (acc: f32 add-reduce) of the tile
+                const uint32_t buf0 = base_u32 + static_cast<uint32_t>(warp - 2) * 8192u;
+                const bool rows_in = n0 + 32 * q < a.N;
+                uint32_t nb = 0;
+                for (int j0 = part * (cols / 2); j0 < (part + 1) * (cols / 2); j0 += 32) {
+                    if (!rows_in || m0 + j0 >= a.M) break;        // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
+                    if constexpr (MODE == kSwiglu) {
+                        uint32_t u[32];                            // the up tile's accumulators
+                        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kBN + j0), u);
+                        tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int64_t m = m0 + j0 + i;
                             const float g = __uint_as_float(v[i]);
-                            if (m < a.M) a.y[m * a.ldy + n] = g / (1.0f + expf(-g)) * __uint_as_float(u[i]);
+                            v[i] = __float_as_uint(g / (1.0f + expf(-g)) * __uint_as_float(u[i]));
                         }
+                    } else {
+                        tmem_ld_wait();
                     }
-                } else {
-                    tmem_ld_wait();
-                    if (n < a.N) {
+                    if (lane == 0) bulk_wait_group_read<1>();     // this tile's buffer is read out
+                    __syncwarp();
+                    const uint32_t buf = buf0 + nb * 4096u;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int64_t m = m0 + j0 + i;
-                            if (m < a.M) {
-                                float *yp = a.y + m * a.ldy + n;
-                                *yp = MODE == kAcc ? *yp + __uint_as_float(v[i]) : __uint_as_float(v[i]);
+                    for (int i = 0; i < 32; ++i)
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + static_cast<uint32_t>(i * 32 + lane) * 4u),
+                                     "r"(v[i])
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d<MODE == kAcc>(&tm_y, buf, n0 + 32 * q, m0 + j0);
+                        bulk_commit_group();
+                    }
+                    nb ^= 1u;
+                }
+                if (lane == 0) bulk_wait_group_all();
+            } else {
+                // rows not 16-byte aligned: direct stores, one token of 32 rows
+                // a warp instruction
+                for (int j0 = part * (cols / 2); j0 < (part + 1) * (cols / 2); j0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
+                    if constexpr (MODE == kSwiglu) {
+                        uint32_t u[32];                            // the up tile's accumulators
+                        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kBN + j0), u);
+                        tmem_ld_wait();
+                        if (n < a.N) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int64_t m = m0 + j0 + i;
+                                const float g = __uint_as_float(v[i]);
+                                if (m < a.M) a.y[m * a.ldy + n] = g / (1.0f + expf(-g)) * __uint_as_float(u[i]);
+                            }
+                        }
+                    } else {
+                        tmem_ld_wait();
+                        if (n < a.N) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int64_t m = m0 + j0 + i;
+                                if (m < a.M) {
+                                    float *yp = a.y + m * a.ldy + n;
+                                    *yp = MODE == kAcc ? *yp + __uint_as_float(v[i]) : __uint_as_float(v[i]);
+                                }
                             }
                         }
                     }
@@ -416,10 +497,10 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();          // no CTA of the pair leaves while the other may still use its memory
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(taddr, kTmemCols);
+        tmem_dealloc_pair(taddr, kTmemCols);
     }
 }
 
@@ -464,8 +545,8 @@ size_t gemm_workspace_bytes(int64_t M, int64_t K) { return static_cast<size_t>(M
 namespace {
 
 template <int FMT, int MODE>
-cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const gemm::Args &a, int64_t grid,
-                        cudaStream_t st)
+cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const CUtensorMap &tm_q,
+                        const CUtensorMap &tm_y, const gemm::Args &a, int64_t grid, cudaStream_t st)
 {
     using namespace gemm;
     constexpr int smem = Shape<FMT, MODE>::smem;
@@ -478,7 +559,20 @@ cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const 
         if (e != cudaSuccess) return e;
         granted[dev] = 1;
     }
-    gemm_q4k_kernel<FMT, MODE><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm_x, tm_w, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;     // CTA pairs
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_q4k_kernel<FMT, MODE>, tm_x, tm_w, tm_q, tm_y, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -511,7 +605,7 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K8), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K8 * 2)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBN)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBNc)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -524,22 +618,43 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     // the up rows [up_rows, up_rows + N) relative to w_rows
     const int64_t lo = mode == kSwiglu ? std::min<int64_t>(0, up_rows) : 0;
     const int64_t hi = mode == kSwiglu ? std::max<int64_t>(N, up_rows + N) : N;
+    // two maps over the Q4_K rows: the 16-byte headers and the 32 quant
+    // bytes of one 64-column chunk, 128 rows a box (x offsets are multiples
+    // of 16 bytes: 144 kb and 144 kb + 16 + 32 c)
+    CUtensorMap tm_q;
     if (q8) {
-        tm_w = tm_x;       // Q8_0 weights are read directly: the map is not used
+        tm_w = tm_x;       // Q8_0 weights are read directly: the maps are not used
+        tm_q = tm_x;
     } else {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(hi - lo)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-        const cuuint32_t box[2] = {144u, static_cast<cuuint32_t>(kBM)};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows + lo * row_bytes), dims,
-                strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-            *encode_failed = true;
-            return cudaErrorInvalidValue;
+        for (int m = 0; m < 2; ++m) {
+            const cuuint32_t box[2] = {m ? 32u : 16u, static_cast<cuuint32_t>(kBM)};
+            if (enc(m ? &tm_q : &tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows + lo * row_bytes),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+                *encode_failed = true;
+                return cudaErrorInvalidValue;
+            }
         }
     }
+    // the output through a tensor map of 32 x 32 boxes when its rows allow
+    // (16-byte aligned base and row stride); else the kernel stores directly
+    CUtensorMap tm_y = tm_x;
+    bool tma_y = false;
+    if ((reinterpret_cast<uintptr_t>(y) & 15u) == 0 && (ldy % 4) == 0) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldy) * 4u};
+        const cuuint32_t box[2] = {32u, 32u};
+        const cuuint32_t estr[2] = {1, 1};
+        tma_y = enc(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        if (!tma_y) tm_y = tm_x;
+    }
     Args a;
+    a.tma_y = tma_y ? 1 : 0;
     a.y = y;
     a.N = N;
     a.K = K;
@@ -551,22 +666,22 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     a.wq8[1] = w_rows + up_rows * row_bytes;
     a.row_bytes = row_bytes;
     a.nb = static_cast<int>((K + 31) / 32);
-    a.n_tiles = static_cast<int>((N + kBM - 1) / kBM);
+    a.n_tiles = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));
     a.nk = static_cast<int>((K8 + kBK - 1) / kBK);
     a.skip_chunk = skip_chunk;
     a.wait_ns = wait_ns;
     a.err = err;
     const int64_t per_cta = mode == kSwiglu ? kBN : 2 * kBN;   // tokens per CTA pass
     const int64_t m_blocks = (M + per_cta - 1) / per_cta;
-    const int64_t grid = a.n_tiles * m_blocks;
+    const int64_t grid = 2 * a.n_tiles * m_blocks;          // CTA pairs
     if (q8) {
-        if (mode == kSwiglu) return launch_mode<kFmtQ80, kSwiglu>(tm_x, tm_w, a, grid, st);
-        if (mode == kAcc) return launch_mode<kFmtQ80, kAcc>(tm_x, tm_w, a, grid, st);
-        return launch_mode<kFmtQ80, kStore>(tm_x, tm_w, a, grid, st);
+        if (mode == kSwiglu) return launch_mode<kFmtQ80, kSwiglu>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+        if (mode == kAcc) return launch_mode<kFmtQ80, kAcc>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+        return launch_mode<kFmtQ80, kStore>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
     }
-    if (mode == kSwiglu) return launch_mode<kFmtQ4K, kSwiglu>(tm_x, tm_w, a, grid, st);
-    if (mode == kAcc) return launch_mode<kFmtQ4K, kAcc>(tm_x, tm_w, a, grid, st);
-    return launch_mode<kFmtQ4K, kStore>(tm_x, tm_w, a, grid, st);
+    if (mode == kSwiglu) return launch_mode<kFmtQ4K, kSwiglu>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+    if (mode == kAcc) return launch_mode<kFmtQ4K, kAcc>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+    return launch_mode<kFmtQ4K, kStore>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
 }
 
 cudaError_t gemm_q4k_launch(const uint8_t *w_rows, int64_t N, int64_t K, const float *x, int64_t M, float *y,
