@@ -608,26 +608,37 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
     return r;
 }
 
-template <int FMT, int B>
-__device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int cwarp, int lane, int nthreads, uint32_t xs_addr,
-                                             float *xsum, float *xscale)
+template <int FMT, int B, int NTH>
+__device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint32_t cwarp, uint32_t lane,
+                                        uint32_t xs_addr, float *xsum, float *xscale)
 {
-    constexpr int UC = FMT == kFmtQ80 ? 32 : 128;
-    constexpr int G = UC / 4;
-    constexpr int NJ = UC / 32;
-    constexpr int SU = B * G + 1;
-    constexpr int UNR = 4;
-    const int XH = a.XU >> 1;
-    const int K = static_cast<int>(a.K);
-    const int g_total = a.U * G;
+    constexpr uint32_t UC = FMT == kFmtQ80 ? 32 : 128;
+    constexpr uint32_t G = UC / 4;          // float4 groups of a unit (a power of two)
+    constexpr uint32_t NJ = UC / 32;
+    constexpr uint32_t SU = B * G + 1;
+    constexpr uint32_t UNR = 4;
+    static_assert(NTH % 32 == 0, "whole warps");
+    const uint32_t XH = static_cast<uint32_t>(a.XU) >> 1;
+    const uint32_t K = static_cast<uint32_t>(a.K);
+    const uint32_t g_total = static_cast<uint32_t>(a.U) * G;
     const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x0) & 15u) == 0);
-    for (int b = 0; b < B; ++b) {
-        const float *xb = x0 + static_cast<int64_t>(b) * K;
-        auto load = [&](int base, float4 (&v)[UNR]) {
+    for (uint32_t b = 0; b < B; ++b) {
+        const float *xb = x0 + static_cast<uint64_t>(b) * K;
+        // the float4 groups base + i*NTH + lane (i < UNR) of a round; when the
+        // whole round lies inside K and x is 16-byte aligned the loads are
+        // unconditional (the same test for every lane of the warp)
+        auto load = [&](uint32_t base, float4 (&v)[UNR]) {
+            const uint32_t last = base + (UNR - 1) * NTH + 31;
+            if (vec && last < g_total && 4 * last + 3 < K) {
+                const float4 *p = reinterpret_cast<const float4 *>(xb) + base + lane;
 #pragma unroll
-            for (int i = 0; i < UNR; ++i) {
-                const int f = base + i * nthreads + lane;
-                const int c0 = 4 * f;
+                for (uint32_t i = 0; i < UNR; ++i) v[i] = __ldg(p + i * NTH);
+                return;
+            }
+#pragma unroll
+            for (uint32_t i = 0; i < UNR; ++i) {
+                const uint32_t f = base + i * NTH + lane;
+                const uint32_t c0 = 4 * f;
                 v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (f < g_total) {
                     if (vec && c0 + 3 < K) {
@@ -642,102 +653,107 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, int 
             }
         };
         float4 v[UNR], nx[UNR];
-        int base = cwarp * 32;
+        uint32_t base = cwarp * 32;
         if (base < g_total) load(base, v);
-        for (; base < g_total; base += UNR * nthreads) {
-            if (base + UNR * nthreads < g_total) load(base + UNR * nthreads, nx);   // warp-uniform
-            int f[UNR], us[UNR], g[UNR];
+        for (; base < g_total; base += UNR * NTH) {
+            if (base + UNR * NTH < g_total) load(base + UNR * NTH, nx);   // warp-uniform
+            uint32_t us[UNR], g[UNR];
+            bool in[UNR];
 #pragma unroll
-            for (int i = 0; i < UNR; ++i) {
-                f[i] = base + i * nthreads + lane;
-                const int u = f[i] / G;
-                g[i] = f[i] % G;
+            for (uint32_t i = 0; i < UNR; ++i) {
+                const uint32_t f = base + i * NTH + lane;
+                const uint32_t u = f / G;
+                g[i] = f % G;
+                in[i] = f < g_total;
                 us[i] = FMT == kFmtQ4K ? ((u & 1) * XH + (u >> 1)) : u;   // unit slot
             }
             // plain sums: per float4, then over 4 lanes (16 columns) and 8 (32)
             float sum[UNR], sum16[UNR];
 #pragma unroll
-            for (int i = 0; i < UNR; ++i) sum[i] = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+            for (uint32_t i = 0; i < UNR; ++i) sum[i] = (v[i].x + v[i].y) + (v[i].z + v[i].w);
             if constexpr (FMT != kFmtQ80) {
 #pragma unroll
-                for (int i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 1);
+                for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 1);
 #pragma unroll
-                for (int i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 2);
+                for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 2);
 #pragma unroll
-                for (int i = 0; i < UNR; ++i) sum16[i] = sum[i];
+                for (uint32_t i = 0; i < UNR; ++i) sum16[i] = sum[i];
                 if constexpr (FMT == kFmtQ4K) {
 #pragma unroll
-                    for (int i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 4);
+                    for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 4);
                 }
             }
             if constexpr (B == 1) {
                 float amax[UNR];
 #pragma unroll
-                for (int i = 0; i < UNR; ++i)
+                for (uint32_t i = 0; i < UNR; ++i)
                     amax[i] = fmax_nan(fmax_nan(fabsf(v[i].x), fabsf(v[i].y)), fmax_nan(fabsf(v[i].z), fabsf(v[i].w)));
 #pragma unroll
                 for (int o = 1; o <= 4; o <<= 1)
 #pragma unroll
-                    for (int i = 0; i < UNR; ++i) amax[i] = fmax_nan(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], o));
+                    for (uint32_t i = 0; i < UNR; ++i) amax[i] = fmax_nan(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], o));
+                uint32_t pl[UNR][4];
+                float dn[UNR];
 #pragma unroll
-                for (int i = 0; i < UNR; ++i) {
+                for (uint32_t i = 0; i < UNR; ++i) {
                     const int ebits = static_cast<int>((__float_as_uint(amax[i]) >> 23) & 255u);
-                    const bool finite = ebits != 255;
+                    const uint32_t keep = ebits != 255 ? 0xFFFFFFFFu : 0u;   // a NaN or infinity: planes 0, scale NaN
                     const int E = max(ebits - 127, -96);
                     const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
-                    const float down = __int_as_float((106 + E) << 23);   // 2^(E-21)
+                    dn[i] = keep ? __int_as_float((106 + E) << 23) : __int_as_float(0x7FC00000);   // 2^(E-21)
                     // m = rint(x * 2^(21-E)), |m| <= 2^22: adding 1.5 * 2^23 in one
                     // fp32 FMA rounds the exact x * 2^(21-E) to the nearest
                     // integer (ties to even); the sum's bits minus those of
                     // 1.5 * 2^23 are m
                     constexpr float kRound = 12582912.0f;
                     constexpr uint32_t kRoundBits = 0x4B400000u;
-                    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-                    if (finite) {
-                        m0 = __float_as_uint(fmaf(v[i].x, up, kRound)) - kRoundBits;
-                        m1 = __float_as_uint(fmaf(v[i].y, up, kRound)) - kRoundBits;
-                        m2 = __float_as_uint(fmaf(v[i].z, up, kRound)) - kRoundBits;
-                        m3 = __float_as_uint(fmaf(v[i].w, up, kRound)) - kRoundBits;
-                    }
+                    const uint32_t m0 = (__float_as_uint(fmaf(v[i].x, up, kRound)) - kRoundBits) & keep;
+                    const uint32_t m1 = (__float_as_uint(fmaf(v[i].y, up, kRound)) - kRoundBits) & keep;
+                    const uint32_t m2 = (__float_as_uint(fmaf(v[i].z, up, kRound)) - kRoundBits) & keep;
+                    const uint32_t m3 = (__float_as_uint(fmaf(v[i].w, up, kRound)) - kRoundBits) & keep;
                     // byte-plane transpose: plane k holds byte k of the four columns
                     const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
                     const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
-                    const uint32_t p0 = __byte_perm(t0, t1, 0x5410u), p1 = __byte_perm(t0, t1, 0x7632u);
-                    const uint32_t p2 = __byte_perm(t2, t3, 0x5410u), p3 = __byte_perm(t2, t3, 0x7632u);
-                    if (f[i] < g_total) {
-                        const int grp = g[i] >> 3;                     // 32-column group of the unit
-                        if ((lane & 7) == 0) {
-                            xscale[us[i] * NJ + grp] = finite ? down : __int_as_float(0x7FC00000);
-                            if constexpr (FMT == kFmtQ4K) xsum[us[i] * 4 + grp] = sum[i];
-                        }
-                        if constexpr (FMT == kFmtQ6K)
-                            if ((lane & 3) == 0) xsum[us[i] * 8 + (g[i] >> 2)] = sum16[i];
-                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(us[i] * SU + g[i]);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                     ::"r"(dst), "r"(p0), "r"(p1), "r"(p2), "r"(p3) : "memory");
+                    pl[i][0] = __byte_perm(t0, t1, 0x5410u);
+                    pl[i][1] = __byte_perm(t0, t1, 0x7632u);
+                    pl[i][2] = __byte_perm(t2, t3, 0x5410u);
+                    pl[i][3] = __byte_perm(t2, t3, 0x7632u);
+                }
+#pragma unroll
+                for (uint32_t i = 0; i < UNR; ++i) {
+                    if (!in[i]) continue;
+                    const uint32_t grp = g[i] >> 3;                    // 32-column group of the unit
+                    if ((lane & 7) == 0) {
+                        xscale[us[i] * NJ + grp] = dn[i];
+                        if constexpr (FMT == kFmtQ4K) xsum[us[i] * 4 + grp] = sum[i];
                     }
+                    if constexpr (FMT == kFmtQ6K)
+                        if ((lane & 3) == 0) xsum[us[i] * 8 + (g[i] >> 2)] = sum16[i];
+                    const uint32_t dst = xs_addr + 16u * (us[i] * SU + g[i]);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(dst), "r"(pl[i][0]), "r"(pl[i][1]), "r"(pl[i][2]), "r"(pl[i][3]) : "memory");
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < UNR; ++i) {
+                for (uint32_t i = 0; i < UNR; ++i) {
                     float4 w = v[i];
                     if constexpr (FMT == kFmtQ4K) {
-                        if (f[i] < g_total && (lane & 7) == 0) xsum[(b * 4 + (g[i] >> 3)) * a.XU + us[i]] = sum[i];
-                        const int c = 4 * g[i];
+                        if (in[i] && (lane & 7) == 0) xsum[(b * 4 + (g[i] >> 3)) * static_cast<uint32_t>(a.XU) + us[i]] = sum[i];
+                        const int c = static_cast<int>(4 * g[i]);
                         w.x *= __int_as_float((127 - q4k_nibble_shift(c)) << 23);
                         w.y *= __int_as_float((127 - q4k_nibble_shift(c + 1)) << 23);
                         w.z *= __int_as_float((127 - q4k_nibble_shift(c + 2)) << 23);
                         w.w *= __int_as_float((127 - q4k_nibble_shift(c + 3)) << 23);
                     }
-                    if (f[i] < g_total) {
-                        const uint32_t dst = xs_addr + 16u * static_cast<uint32_t>(us[i] * SU + b * G + g[i]);
+                    if (in[i]) {
+                        const uint32_t dst = xs_addr + 16u * (us[i] * SU + b * G + g[i]);
                         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                                      ::"r"(dst), "f"(w.x), "f"(w.y), "f"(w.z), "f"(w.w) : "memory");
                     }
                 }
             }
 #pragma unroll
-            for (int i = 0; i < UNR; ++i) v[i] = nx[i];
+            for (uint32_t i = 0; i < UNR; ++i) v[i] = nx[i];
         }
     }
 }
@@ -920,7 +936,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
     // the weights do not depend on earlier kernels, x may: with programmatic
     // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    stage_x<FMT, B>(a, x0, static_cast<int>(cwarp), lane, 32 * NW, smem_u32(xs),
+    stage_x<FMT, B, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
                              reinterpret_cast<float *>(smem + a.off_xsum),
                              reinterpret_cast<float *>(smem + a.off_xscale));
     named_bar_sync(1, 32 * NW);
