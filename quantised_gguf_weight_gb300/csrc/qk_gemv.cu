@@ -172,6 +172,18 @@ bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan 
     return gemv_plan_for(fmt, rows, K, batch, pair, n_assign, di, p);
 }
 
+// The plan for a device with `sms` SMs and `smem_optin` bytes of shared
+// memory per block (host only: lets the planner be checked without a GPU).
+bool gemv_plan_host(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64_t n_assign, int sms,
+                    int smem_optin, GemvPlan *p)
+{
+    if (sms <= 0 || smem_optin <= 0) return false;
+    DevInfo di;
+    di.sms = sms;
+    di.smem_optin = smem_optin;
+    return gemv_plan_for(fmt, rows, K, batch, pair, n_assign, di, p);
+}
+
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
                         int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows,

@@ -21,6 +21,8 @@ struct GemvPlan {
 // pair: rows are output rows of the SwiGLU form (a gate row and an up row each).
 // n_assign > 0: experts mode, `rows` rows per expert and n_assign assignments.
 bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p, int64_t n_assign = 0);
+bool gemv_plan_host(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64_t n_assign, int sms,
+                    int smem_optin, GemvPlan *p);
 cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
                         int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows = 0,

@@ -93,6 +93,8 @@ def load(path: str | None = None):
         lib.qk_debug_skip_item.restype = I64
         lib.qk_debug_gemv_plan.argtypes = [I, I64, I64, I, ctypes.POINTER(ctypes.c_int64), I]
         lib.qk_debug_gemv_plan.restype = I
+        lib.qk_debug_gemv_plan_for.argtypes = [I, I64, I64, I, I, I64, I, I, ctypes.POINTER(ctypes.c_int64), I]
+        lib.qk_debug_gemv_plan_for.restype = I
         _lib = lib
         return lib
 
@@ -273,6 +275,22 @@ def debug_skip_item(item: int) -> int:
 
 
 PLAN_FIELDS = ("SW", "R", "nkc", "rows_w", "stages", "stage_bytes", "smem", "grid", "XU", "cpl", "nw", "m")
+
+
+PLAN_FOR_FIELDS = PLAN_FIELDS + ("LU", "cpa", "off_stage")
+
+
+def debug_gemv_plan_for(fmt: str, rows: int, K: int, batch: int, sms: int, smem_optin: int,
+                        pair: bool = False, n_assign: int = 0) -> dict | None:
+    """Test hook: the GEMV plan for an explicit device, computed on the host (no GPU needed);
+    None if nothing fits."""
+    out = (ctypes.c_int64 * len(PLAN_FOR_FIELDS))()
+    n = load().qk_debug_gemv_plan_for({"q8_0": 0, "q4_k": 1, "q6_k": 2}[fmt], int(rows), int(K), int(batch),
+                                      int(bool(pair)), int(n_assign), int(sms), int(smem_optin), out,
+                                      len(PLAN_FOR_FIELDS))
+    if n < 0:
+        return None
+    return dict(zip(PLAN_FOR_FIELDS, list(out)[:n]))
 
 
 def debug_gemv_plan(fmt: str, rows: int, K: int, batch: int) -> dict:

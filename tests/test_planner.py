@@ -1,0 +1,62 @@
+"""Host-side checks of the GEMV launch planner (no GPU: an explicit device of
+152 SMs and 227 KB of shared memory per block, the GB300 figures)."""
+import pytest
+
+from quantised_gguf_weight_gb300 import qk
+
+SMS, SMEM = 152, 232448
+UNIT = {"q8_0": 32, "q4_k": 256, "q6_k": 128}       # columns of a lane unit
+ROWS = [1, 7, 100, 1000, 4096, 28672, 151936]
+KS = [32, 33, 256, 300, 896, 1024, 4096, 5120, 14336, 20000]
+
+
+def plan(fmt, rows, K, batch, **kw):
+    return qk.debug_gemv_plan_for(fmt, rows, K, batch, SMS, SMEM, **kw)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q6_k"])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+def test_row_decomposition_depends_on_K_only(fmt, batch):
+    """SW, cpl and nkc fix the order of a row's additions: equal for every row count."""
+    for K in KS:
+        shapes = {(p["SW"], p["cpl"], p["nkc"], p["R"]) for rows in ROWS if (p := plan(fmt, rows, K, batch))}
+        assert len(shapes) <= 1, (fmt, K, batch, shapes)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q6_k"])
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_plan_covers_the_row_and_fits(fmt, batch):
+    for K in KS:
+        for rows in ROWS:
+            p = plan(fmt, rows, K, batch)
+            if p is None:
+                continue
+            lu = -(-K // UNIT[fmt])
+            assert p["LU"] == lu
+            assert p["SW"] * p["cpl"] * p["nkc"] >= lu                  # every lane unit has a lane
+            assert p["SW"] * p["cpl"] * (p["nkc"] - 1) < lu             # no empty trailing chunk
+            assert 32 % p["SW"] == 0 and p["rows_w"] == (32 // p["SW"]) * p["R"]
+            assert 1 <= p["nw"] <= (11 if batch == 1 else 8) and p["m"] >= 1
+            assert p["stages"] == p["nw"] * p["m"] <= 32
+            assert p["off_stage"] + p["stages"] * p["stage_bytes"] == p["smem"] <= SMEM
+            assert p["grid"] == min(SMS, rows)
+            assert p["stage_bytes"] % 128 == 0
+
+
+def test_activations_that_do_not_fit_have_no_plan():
+    # Llama-8B ffn_down: batch 3 fits, batch 4 does not (the host splits it)
+    assert plan("q4_k", 4096, 14336, 3) is not None
+    assert plan("q4_k", 4096, 14336, 4) is None
+    # one row of K = 57344 does not fit at all
+    assert plan("q4_k", 16, 57344, 1) is None
+    assert plan("q8_0", 16, 49152, 1) is None
+    assert plan("q8_0", 16, 40960, 1) is not None
+
+
+def test_pair_and_expert_modes():
+    p = plan("q4_k", 14336, 4096, 1, pair=True)
+    assert p is not None and p["R"] % 2 == 0
+    q = plan("q4_k", 1536, 2048, 1, n_assign=8)
+    assert q["cpa"] == SMS // 8 and q["grid"] == 8 * q["cpa"]
+    r = plan("q4_k", 1536, 2048, 1, n_assign=400)
+    assert r["cpa"] == 1 and r["grid"] == 400
