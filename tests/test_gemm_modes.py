@@ -99,3 +99,26 @@ def test_gemm_swiglu_equals_store_then_silu(qk):
     torch.cuda.synchronize()
     ref = (g / (1.0 + torch.exp(-g))) * u
     assert torch.allclose(h, ref, rtol=2e-6, atol=1e-30)
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q8_0"])
+@pytest.mark.parametrize("mode", ["store", "acc", "swiglu"])
+def test_gemm_epilogue_paths_give_the_same_bits(qk, fmt, mode):
+    """Y rows 16-byte aligned (TMA-store epilogue) and not (direct stores): identical results."""
+    M, N, K = 300, 256, 512
+    wq = synth.weights(fmt, 2 * N, K, seed=74)
+    wd = torch.from_numpy(wq).cuda()
+    xd = torch.from_numpy(synth.activations(M, K, seed=74)).cuda()
+    y0 = torch.from_numpy(synth.activations(M, N + 1, seed=75)).cuda()
+    ya = y0[:, :N].contiguous()                # ldy = N: aligned rows
+    yb = y0.clone()                            # ldy = N + 1: rows 4 bytes apart from alignment
+    for y, ldy in ((ya, N), (yb, N + 1)):
+        if mode == "store":
+            qk._gemm({"q4_k": "qgemm_q4_k", "q8_0": "qgemm_q8_0"}[fmt], wd, 0, N, K, xd, y, ldy, None, None)
+        elif mode == "acc":
+            qk.qgemm_acc(fmt, wd, 0, N, K, xd, y, ldy)
+        else:
+            qk.qgemm_swiglu(fmt, wd, 0, N, N, K, xd, h=y, ldh=ldy)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yb[:, :N])
+    assert torch.equal(yb[:, N], y0[:, N])        # the column past N is not written
