@@ -50,6 +50,8 @@ constexpr int kBNc = kBN / 2;            // tokens of one CTA's slice of a token
 constexpr int kBK = 64;                  // K columns per stage (one 128-byte swizzle row)
 constexpr int kRawHdr = kBM * 16;       // Q4_K: the 16-byte header (d, dmin, scales) of 128 rows
 constexpr int kRawChunk = kBM * 48;      // Q4_K per chunk: headers + the 32 quant bytes of 128 rows
+constexpr int kQ8Box = 80;               // Q8_0 by TMA: the 16-byte-aligned 80 bytes holding a chunk's 2 blocks
+constexpr int kFmtQ80T = 3;              // Q8_0 with 16-byte row strides (K a multiple of 256): weights by TMA
 constexpr int kDeq = 256;                // dequantising threads: two per weight row
 constexpr int kThreads = 64 + kDeq;
 constexpr uint32_t kTmemCols = 512;
@@ -66,8 +68,10 @@ struct Shape {
     static constexpr int b_stage = halves * b_half;
     static constexpr int a_tile = kBM * kBK * 2;             // 16 KB
     static constexpr int a_stage = tiles * a_tile;
-    static constexpr int raw_stage = FMT == kFmtQ80 ? 0 : tiles * kRawChunk;   // Q8_0 reads weights directly
-    static constexpr int stages = (FMT == kFmtQ4K && MODE == kSwiglu) ? 3 : 4;
+    // raw weight bytes of a chunk (Q8_0 from a row stride that is not a
+    // multiple of 16 bytes: none, the dequantising threads read them directly)
+    static constexpr int raw_stage = FMT == kFmtQ80 ? 0 : tiles * (FMT == kFmtQ80T ? kBM * kQ8Box : kRawChunk);
+    static constexpr int stages = FMT == kFmtQ80 ? 4 : (FMT == kFmtQ80T || MODE == kSwiglu ? 3 : 4);
     static constexpr int off_b = 0;
     static constexpr int off_a = off_b + stages * b_stage;
     static constexpr int off_raw = off_a + stages * a_stage;
@@ -114,6 +118,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_y, const Args a)
 {
     constexpr bool kQ8 = FMT == kFmtQ80;        // Q8_0: weights read directly by the dequantising threads
+    constexpr bool kQ8T = FMT == kFmtQ80T;      // Q8_0: weights by TMA
     using L = Shape<FMT, MODE>;
     constexpr int kHalves = L::halves, kTiles = L::tiles, kStages = L::stages;
     constexpr int kOffB = L::off_b, kOffA = L::off_a, kOffRaw = L::off_raw, kOffBar = L::off_bar;
@@ -149,10 +154,8 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
-        if (!kQ8) {
-            tma_prefetch_desc(&tm_w);
-            tma_prefetch_desc(&tm_q);
-        }
+        if (!kQ8) tma_prefetch_desc(&tm_w);
+        if (!kQ8 && !kQ8T) tma_prefetch_desc(&tm_q);
     }
     if (warp == 1) {
         tmem_alloc_pair(base_u32 + kOffBar + kOffTmemSlot, kTmemCols);
@@ -183,7 +186,12 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int h = 0; h < nh; ++h)
                         tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kc * kBK,
                                     m0 + h * kBN + static_cast<int>(rank) * kBNc, full, pol_x);
-                    if (!kQ8) {
+                    if constexpr (kQ8T) {
+                        // blocks 2kc, 2kc+1 span bytes 68kc .. 68kc+67 of a row
+                        for (int i = 0; i < kTiles; ++i)
+                            tma_load_2d(base_u32 + kOffRaw + s * kRawStage + i * (kBM * kQ8Box), &tm_w,
+                                        (68 * kc) & ~15, a.row0[i] + n0, full, pol_w);
+                    } else if constexpr (!kQ8) {
                         const int kb = kc >> 2, c = kc & 3;
                         for (int i = 0; i < kTiles; ++i) {
                             const uint32_t raw = base_u32 + kOffRaw + s * kRawStage + i * kRawChunk;
@@ -265,7 +273,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // chunk's 32 bytes), Q8_0 block 2kc + sel
         const int t = (tid - 64) & (kBM - 1);
         const int sel = (tid - 64) >> 7;
-        if constexpr (!kQ8) {
+        if constexpr (!kQ8 && !kQ8T) {
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
                 const int c = kc & 3;
@@ -334,6 +342,53 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 // every lane's stores are made visible to the tensor cores, then
                 // one lane arrives for the warp
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarAFull + s));
+            }
+        } else if constexpr (kQ8T) {
+            // Q8_0 by TMA: block 2kc + sel of this thread's row sits at byte
+            // (68kc & 15) + 34 sel of the row's 80-byte slot; the nine aligned
+            // words around it are realigned as in the direct path
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kStages;
+                const bool ok = wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
+                const uint32_t pos = static_cast<uint32_t>((68 * kc) & 15) + 34u * static_cast<uint32_t>(sel);
+                const uint32_t off = pos & 3u;                  // 0 or 2
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i) {
+                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(
+                        base + kOffRaw + s * kRawStage + i * (kBM * kQ8Box) + t * kQ8Box + (pos & ~3u));
+                    uint32_t cur[9];
+#pragma unroll
+                    for (int k = 0; k < 9; ++k) cur[k] = wp[k];
+                    const uint32_t a_row = base_u32 + kOffA + s * kAStage + i * L::a_tile + t * 128;
+                    const float d = half_bits_to_float(cur[0] >> (8 * off));
+                    const uint32_t psel = off ? 0x7654u : 0x5432u;
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        // quants 4k..4k+3 of the block (bytes 2+4k.. past its start)
+                        const uint32_t v = __byte_perm(cur[k], cur[k + 1], psel);
+                        const float q0 = static_cast<float>(static_cast<int8_t>(v & 0xFFu));
+                        const float q1 = static_cast<float>(static_cast<int8_t>((v >> 8) & 0xFFu));
+                        const float q2 = static_cast<float>(static_cast<int8_t>((v >> 16) & 0xFFu));
+                        const float q3 = static_cast<float>(static_cast<int8_t>(v >> 24));
+                        const __nv_bfloat162 p01 = __floats2bfloat162_rn(d * q0, d * q1);
+                        const __nv_bfloat162 p23 = __floats2bfloat162_rn(d * q2, d * q3);
+                        packed[2 * k] = *reinterpret_cast<const uint32_t *>(&p01);
+                        packed[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                    }
+#pragma unroll
+                    for (int h8 = 0; h8 < 4; ++h8) {
+                        const int chunk = 4 * sel + h8;                     // logical 16-byte chunk 0..7
+                        const uint32_t dst = a_row + ((static_cast<uint32_t>(chunk) ^ (t & 7u)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * h8]),
+                                     "r"(packed[4 * h8 + 1]), "r"(packed[4 * h8 + 2]), "r"(packed[4 * h8 + 3])
+                                     : "memory");
+                    }
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarAFull + s));
@@ -622,7 +677,23 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     // bytes of one 64-column chunk, 128 rows a box (x offsets are multiples
     // of 16 bytes: 144 kb and 144 kb + 16 + 32 c)
     CUtensorMap tm_q;
-    if (q8) {
+    // Q8_0 rows of a multiple of 16 bytes (K a multiple of 256) from a
+    // 16-byte aligned tensor come by TMA, 128 rows x 80 bytes a box; other
+    // Q8_0 rows are read directly
+    const bool q8_tma = q8 && row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(w_rows + lo * row_bytes) & 15u) == 0;
+    if (q8_tma) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(hi - lo)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t estr[2] = {1, 1};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQ8Box), static_cast<cuuint32_t>(kBM)};
+        if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows + lo * row_bytes), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *encode_failed = true;
+            return cudaErrorInvalidValue;
+        }
+        tm_q = tm_x;
+    } else if (q8) {
         tm_w = tm_x;       // Q8_0 weights are read directly: the maps are not used
         tm_q = tm_x;
     } else {
@@ -674,6 +745,11 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     const int64_t per_cta = mode == kSwiglu ? kBN : 2 * kBN;   // tokens per CTA pass
     const int64_t m_blocks = (M + per_cta - 1) / per_cta;
     const int64_t grid = 2 * a.n_tiles * m_blocks;          // CTA pairs
+    if (q8_tma) {
+        if (mode == kSwiglu) return launch_mode<kFmtQ80T, kSwiglu>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+        if (mode == kAcc) return launch_mode<kFmtQ80T, kAcc>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+        return launch_mode<kFmtQ80T, kStore>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
+    }
     if (q8) {
         if (mode == kSwiglu) return launch_mode<kFmtQ80, kSwiglu>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
         if (mode == kAcc) return launch_mode<kFmtQ80, kAcc>(tm_x, tm_w, tm_q, tm_y, a, grid, st);

@@ -116,3 +116,22 @@ def test_gemm_q8_0_timeout_is_recorded(qk):
     y = qk.qgemm_q8_0(wd, 0, N, K, xd)
     torch.cuda.synchronize()
     assert torch.isfinite(y).all()
+
+
+@pytest.mark.parametrize("K,shift", [(512, 0), (512, 2), (4096, 0)])
+def test_gemm_q8_0_tma_and_direct_weight_paths(qk, orc, K, shift):
+    """K a multiple of 256 with a 16-byte aligned tensor: weights by TMA; the same tensor
+    2 bytes off alignment: read directly.  Both against the oracle, and store + acc."""
+    M, N = 300, 260
+    wq = synth.weights("q8_0", N, K, seed=90)
+    buf = torch.zeros(wq.size + 16, dtype=torch.uint8, device="cuda")
+    buf[shift:shift + wq.size] = torch.from_numpy(wq).cuda()
+    wd = buf[shift:shift + wq.size]
+    x = synth.activations(M, K, seed=90)
+    xd = torch.from_numpy(x).cuda()
+    y = qk.qgemm_q8_0(wd, 3, N - 3, K, xd)
+    check(y.cpu().numpy().astype(np.float64), orc, wq, K, x, np.arange(3, N), f"q8_0 K{K} shift {shift}")
+    y0 = synth.activations(M, N - 3, seed=91)
+    yd = torch.from_numpy(y0.copy()).cuda()
+    qk.qgemm_acc("q8_0", wd, 3, N - 3, K, xd, yd)
+    check(yd.cpu().numpy().astype(np.float64), orc, wq, K, x, np.arange(3, N), "q8_0 acc", base=y0.astype(np.float64))
