@@ -2,18 +2,18 @@
  * qk.h -- C ABI of the GB300 (sm_103a) quantised-weight GEMV / GEMM library.
  *
  * The library multiplies GGUF block-quantised weights by fp32 activations,
- * decoding every block inside the multiply.  That is the operation behind
- * "Weights stay QUANTISED on the device: a matvec whose weight type has a
- * device kernel ... uploads the GGUF bytes verbatim and decodes each block
- * inside the matmul" (nurllama 0.18.1 API reference, model.nu) and behind the
- * quantised matvec dispatch `lk_matvec_q ks gt wd xd yd rows cols batch`
- * (same page, kernels.nu).  One entry point per weight format; there is no
+ * decoding every block inside the multiply.  That is what the nurllama
+ * runtime does with weight types it has a device kernel for: their GGUF bytes
+ * go to the device unchanged and each block is decoded inside the matmul
+ * (nurllama 0.18.1 API reference, model.nu), through its quantised matvec
+ * dispatch `lk_matvec_q ks gt wd xd yd rows cols batch` (same page,
+ * kernels.nu).  One entry point per weight format; there is no
  * type dispatch and no host fallback.
  *
  * Operation (every entry point):
  *   y[b][r] = sum_{c < K} W[row_offset + r][c] * x[b][c]
- * with W row-major, the column index fastest ("weight W[out,in] -> W[r*in + c],
- * matvec y[r] = sum_c W[r*in+c] x[c]", kernels.nu layout contract).
+ * with W row-major, the column index fastest: row r of W starts at element
+ * r*K (the layout contract of kernels.nu).
  *
  * Block formats (the pages name them, the bytes follow the GGUF layouts):
  *   Q8_0 : 34-byte blocks of 32 weights: fp16 d, then 32 int8 q;  w = d*q.
@@ -117,10 +117,10 @@ int qmatvec_q6_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
  *   g = sum_{c<K} W[gate_offset + p][c] * x[b*K + c]
  *   u = sum_{c<K} W[up_offset + p][c]   * x[b*K + c]
  *   h[b*ldh + p] = silu(g) * u,   silu(z) = z / (1 + e^-z),   for p < F.
- * The llama FFN "SwiGLU" (nurllama README, "What it runs") as silumul
+ * The SwiGLU of the llama FFN (nurllama README, "What it runs") as silumul
  * g <- silu(g) * u (nurllama 0.18.1 API reference, kernels.nu `lk_silumul`),
- * folded into the matvec as in loom's "matvecs ... with fused SwiGLU"
- * (loom-port-llm SKILL.md, "Kernel inventory").  Gate and up rows may be row
+ * folded into the matvec as loom's decode matvecs fuse it (loom-port-llm
+ * SKILL.md, "Kernel inventory").  Gate and up rows may be row
  * ranges of one fused tensor (phi3's ffn_up: gate_offset 0, up_offset F;
  * nurllama README, "What it runs"), or of two tensors passed as one
  * allocation with the offsets between them.
@@ -174,8 +174,8 @@ int qmatvec_experts_q6_k(const void *w, int64_t n_experts, int64_t rows, int64_t
  * for m < M tokens and n < N weight rows, accumulated in fp32.  Each weight
  * is decoded to fp32 (w = d*sc*q - dmin*m) and rounded to bf16, each
  * activation is rounded to bf16 (round to nearest even).  This is the
- * batched (prefill) form of the matvec: the "matmuls run over up to
- * LM_CHUNK positions at once ... each weight is read once per chunk"
+ * batched (prefill) form of the matvec: the chunked prefill multiplies a
+ * whole chunk of positions at once, so a chunk reads each weight only once
  * (nurllama 0.18.1 API reference, model.nu).
  *   w          device Q4_K block bytes of the whole tensor; 16-byte aligned.
  *   x          device fp32 [M][K], row stride K; 4-byte aligned.

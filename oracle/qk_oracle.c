@@ -11,8 +11,8 @@
  *   1. Every weight is decoded on its own to double (f64):
  *        Q8_0 : w = d * q                     (d fp16, q int8)
  *        Q4_K : w = d * sc * q - dmin * m     (d, dmin fp16; sc, m 6-bit; q 4-bit)
- *      "Weights stay QUANTISED on the device ... decodes each block inside the
- *      matmul" and the host dequantisation oracle (nurllama 0.18.1 API
+ *      The device keeps the weights quantised and decodes each block inside
+ *      the matmul, checked against a host dequantisation (nurllama 0.18.1 API
  *      reference, model.nu; nurllama README, "How it is checked").
  *   2. y[b][r] = sum_{c<K} W[r][c] * x[b][c] in f64, c in natural order,
  *      W row-major with the column index fastest (nurllama 0.18.1 API
@@ -275,11 +275,10 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /*
  * Fused gate/up matvec with the SwiGLU product -- the decode FFN of the llama
- * shape, "RMSNorm -> GQA attention ... -> SwiGLU FFN" (nurllama README,
- * "What it runs"); silumul computes g <- silu(g) * u (nurllama 0.18.1 API
- * reference, kernels.nu `lk_silumul`, beside `lk_gelumul`), and the matvecs
- * "with fused SwiGLU" (loom-port-llm SKILL.md, "Kernel inventory") fold it
- * into the gate/up matvec; gate and up may be row ranges of one tensor (the
+ * shape is a SwiGLU FFN (nurllama README, "What it runs"); silumul computes
+ * g <- silu(g) * u (nurllama 0.18.1 API reference, kernels.nu `lk_silumul`,
+ * beside `lk_gelumul`), and loom's decode matvecs fold it into the gate/up
+ * matvec (loom-port-llm SKILL.md, "Kernel inventory"); gate and up may be row ranges of one tensor (the
  * phi3 ffn_up).  For p < n:
  *   g[b][p] = sum_c W[gate_rows[p]][c] x[b][c]
  *   u[b][p] = sum_c W[up_rows[p]][c]   x[b][c]

@@ -5,10 +5,10 @@
 // weight.
 //
 // This is the prefill counterpart of the decode matvec: the chunked prefill
-// runs the matmuls over many positions at once so that "each weight is read
-// once per chunk" (nurllama 0.18.1 API reference, model.nu), and the loom
-// port runs prefill through GEMMs that dequantise the weight format in the
-// kernel ("loom-port-llm" SKILL.md, "What the starter generates", gen_gemm.py).
+// multiplies a whole chunk of positions at once, so a chunk reads each weight
+// only once (nurllama 0.18.1 API reference, model.nu), and the loom port runs
+// prefill through GEMMs that dequantise the weight format in the kernel
+// (loom-port-llm SKILL.md, "What the starter generates", gen_gemm.py).
 //
 // Kernel shape: a cluster of two CTAs (a CTA pair) per 256 weight rows x up
 // to 512 tokens; one tcgen05.mma.cta_group::2 covers M = 256 weight rows
