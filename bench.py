@@ -537,6 +537,8 @@ def measure_extra_rows(torch, qk, synth, device, stream):
     swiglu_row("q4_k_swiglu_llama8b_ffn_14336x4096_b1", "q4_k", 14336, 4096, 1, 2, 4)
     gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1)
     gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1)
+    gemv_row("q4_k_896x4864_b1", "q4_k", 896, 4864, 1, 1, 1)
+    gemv_row("q4_k_llama8b_gate_up_28672x4096_b4", "q4_k", 28672, 4096, 4, 2, 2)
     gemv_row("q8_0_lm_head_151936x896_b1", "q8_0", 151936, 896, 1, 3, 3)
     gemv_row("q8_0_lm_head_151936x896_b8", "q8_0", 151936, 896, 8, 3, 3)
     gemv_row("q6_k_lm_head_128256x4096_b1", "q6_k", 128256, 4096, 1, 6, 1)
