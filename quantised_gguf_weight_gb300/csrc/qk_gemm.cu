@@ -173,6 +173,31 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if (lane == 0) {
             const uint64_t pol_w = l2_evict_first_policy();
             const uint64_t pol_x = l2_evict_last_policy();
+            auto raw_copies = [&](int kc, int s, uint32_t full) {
+                if constexpr (kQ8T) {
+                    // blocks 2kc, 2kc+1 span bytes 68kc .. 68kc+67 of a row
+                    for (int i = 0; i < kTiles; ++i)
+                        tma_load_2d(base_u32 + kOffRaw + s * kRawStage + i * (kBM * kQ8Box), &tm_w,
+                                    (68 * kc) & ~15, a.row0[i] + n0, full, pol_w);
+                } else if constexpr (!kQ8) {
+                    const int kb = kc >> 2, c = kc & 3;
+                    for (int i = 0; i < kTiles; ++i) {
+                        const uint32_t raw = base_u32 + kOffRaw + s * kRawStage + i * kRawChunk;
+                        tma_load_2d(raw, &tm_w, kb * 144, a.row0[i] + n0, full, pol_w);
+                        tma_load_2d(raw + kRawHdr, &tm_q, kb * 144 + 16 + 32 * c, a.row0[i] + n0, full, pol_w);
+                    }
+                }
+            };
+            // the weights do not depend on the kernel before this one: the
+            // first stages' weight copies go out before the wait for it (their
+            // bytes are announced without an arrival), the activations after
+            const int pre = nk < kStages ? nk : kStages;
+            if (L::raw_stage > 0)
+                for (int kc = 0; kc < pre; ++kc) {
+                    mbar_expect_tx(bar(kBarXFull + kc), static_cast<uint32_t>(L::raw_stage));
+                    raw_copies(kc, kc, bar(kBarXFull + kc));
+                }
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
             for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
                 const int s = kc % kStages;
@@ -181,24 +206,12 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     break;
                 if (!(kc == a.skip_chunk && blockIdx.x == 0)) {
                     const uint32_t full = bar(kBarXFull + s);
-                    const uint32_t tx = static_cast<uint32_t>(nh * L::b_half + L::raw_stage);
-                    mbar_arrive_expect_tx(full, tx);
+                    const bool early = kc < pre;           // weights already on their way
+                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(nh * L::b_half + (early ? 0 : L::raw_stage)));
                     for (int h = 0; h < nh; ++h)
                         tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kc * kBK,
                                     m0 + h * kBN + static_cast<int>(rank) * kBNc, full, pol_x);
-                    if constexpr (kQ8T) {
-                        // blocks 2kc, 2kc+1 span bytes 68kc .. 68kc+67 of a row
-                        for (int i = 0; i < kTiles; ++i)
-                            tma_load_2d(base_u32 + kOffRaw + s * kRawStage + i * (kBM * kQ8Box), &tm_w,
-                                        (68 * kc) & ~15, a.row0[i] + n0, full, pol_w);
-                    } else if constexpr (!kQ8) {
-                        const int kb = kc >> 2, c = kc & 3;
-                        for (int i = 0; i < kTiles; ++i) {
-                            const uint32_t raw = base_u32 + kOffRaw + s * kRawStage + i * kRawChunk;
-                            tma_load_2d(raw, &tm_w, kb * 144, a.row0[i] + n0, full, pol_w);
-                            tma_load_2d(raw + kRawHdr, &tm_q, kb * 144 + 16 + 32 * c, a.row0[i] + n0, full, pol_w);
-                        }
-                    }
+                    if (!early) raw_copies(kc, s, full);
                 }
                 ++issued;
             }
@@ -563,6 +576,8 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 __global__ void x_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ xb, int64_t M, int64_t K,
                                  int64_t K8)
 {
+    // the GEMM launched after it may start its prologue and weight copies now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t total = M * K8;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -619,13 +634,17 @@ cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;     // CTA pairs
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch after the x -> bf16 pre-pass: only the
+    // activation copies wait for it (griddepcontrol.wait in the producer)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, gemm_q4k_kernel<FMT, MODE>, tm_x, tm_w, tm_q, tm_y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
