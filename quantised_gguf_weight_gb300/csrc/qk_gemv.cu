@@ -77,7 +77,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
         grid = n_assign * cpa;
         if (grid > (1LL << 31) - 1) return false;
     }
-    const int NW = gemv_warps(fmt, batch);
+    int NW = gemv_warps(fmt, batch);
     // The way a row is cut into lanes and K chunks fixes the order of its
     // additions, so it depends on K (and the format and batch) only: the
     // rows of a call get the same bits as the same rows of a larger call.
@@ -131,6 +131,10 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     // before the arithmetic, so one stage a warp already keeps a copy in
     // flight while the warp computes
     const int64_t rows_cta_max = n_assign > 0 ? (rows + cpa - 1) / cpa : (rows + grid - 1) / grid;
+    // Q4_K batch 1 with more items a CTA than the 11 consumer warps: the
+    // 16-warp form (same arithmetic in the same order, more warps in flight)
+    const bool wide = fmt == kFmtQ4K && batch == 1 && (rows_cta_max + gr - 1) / gr * nkc > NW;
+    if (wide) NW = gemv_warps(fmt, batch, true);
     int64_t nw = std::min<int64_t>(NW, (rows_cta_max + gr - 1) / gr);
     nw = std::min(nw, stages);
     const int64_t m = stages / nw;
@@ -155,6 +159,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     p->rows_w = rows_w;
     p->pair = pair ? 1 : 0;
     p->cpa = static_cast<int>(cpa);
+    p->wide = wide ? 1 : 0;
     p->up_stage_off = static_cast<int>(up_stage_off);
     p->chunk_bytes = static_cast<int>(chunk_bytes);
     p->row_stride = static_cast<int>(row_stride);
@@ -226,7 +231,7 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.skip_item = skip_item;
     r.wait_ns = wait_ns;
     r.err = err;
-    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, r, p.grid, p.smem, st, pdl);
+    if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, p.wide != 0, r, p.grid, p.smem, st, pdl);
     if (fmt == kFmtQ6K) return gemv_launch_q6k(batch, r, p.grid, p.smem, st, pdl);
     return gemv_launch_q80(batch, r, p.grid, p.smem, st, pdl);
 }

@@ -116,8 +116,12 @@ struct GemvArgs {
 
 // Consumer warps per CTA and rows per thread of the ring kernel.
 // (B = 1: 12 warps in all, three per scheduler, which leaves 168 registers a
-// thread; B >= 2: 9 warps.)
-__host__ __device__ constexpr int gemv_warps(int /*fmt*/, int batch) { return batch == 1 ? 11 : 8; }
+// thread; the wide Q4_K batch-1 form: 16 warps, four per scheduler, 128
+// registers, a lane holding half a super-block at a time; B >= 2: 9 warps.)
+__host__ __device__ constexpr int gemv_warps(int /*fmt*/, int batch, bool wide = false)
+{
+    return batch == 1 ? (wide ? 15 : 11) : 8;
+}
 __host__ __device__ constexpr int gemv_rows(int fmt, int batch)
 {
     return fmt != kFmtQ80 ? (batch <= 4 ? 2 : 1) : (batch == 1 ? 2 : (batch == 2 ? 4 : 2));
@@ -197,6 +201,94 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint4 q = qs[r][4 * h + 2 * lc + p];
+                        const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+                        const uint32_t L = wd & 0x0F0F0F0Fu;   // q of sub-block 2lc
+                        const uint32_t H = wd & 0xF0F0F0F0u;   // 16 q of sub-block 2lc+1
+                        sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
+                        sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
+                        sl[r][2] = dp4a_us(L, xl.z, sl[r][2]);
+                        sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
+                        sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
+                        sh[r][2] = dp4a_us(H, xh.z, sh[r][2]);
+                    }
+                }
+            }
+            const float X0 = lc ? xsum4.z : xsum4.x, X1 = lc ? xsum4.w : xsum4.y;
+            const float S0 = lc ? xsc4.z : xsc4.x, S1 = lc ? xsc4.w : xsc4.y;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2]);
+                const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2]);
+                float t = acc[r][0];
+                t = fmaf(ds[r][2 * lc] * S0, F0, t);
+                t = fmaf(dmn[r][2 * lc], X0, t);
+                t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
+                t = fmaf(dmn[r][2 * lc + 1], X1, t);
+                acc[r][0] = t;
+            }
+        }
+    }
+}
+
+// The same for one 128-column half H of the super-block, its 64 quant bytes
+// in qs (the wide batch-1 form).  Accumulates in the same order as
+// q4k_sb_dig: half 0, then half 1.
+template <int R, int H>
+__device__ __forceinline__ void q4k_half_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][4],
+                                             const uint8_t *xa, const float *xsum_h, const float *xsc_h,
+                                             float (&acc)[R][1])
+{
+    float d[R], dmin[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        d[r] = half_bits_to_float(hd[r].x);
+        dmin[r] = half_bits_to_float(hd[r].x >> 16);
+    }
+    {
+        constexpr int h = H;
+        const float4 xsum4 = *reinterpret_cast<const float4 *>(xsum_h);
+        const float4 xsc4 = *reinterpret_cast<const float4 *>(xsc_h);
+        // d*sc and -dmin*m of the four sub-blocks 4h..4h+3: the 6-bit field
+        // placed in a float's mantissa is 2^23 + v, and one FMA against the
+        // matching offset gives the exact product
+        float ds[R][4], dmn[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            uint32_t scw, mw;
+            if (h == 0) {
+                scw = hd[r].y & 0x3F3F3F3Fu;
+                mw = hd[r].z & 0x3F3F3F3Fu;
+            } else {
+                scw = (hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u);
+                mw = ((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u);
+            }
+            const float dlo = d[r], dhi = d[r] * 0.0625f;
+            const float clo = dlo * -kTwo23, chi = dhi * -kTwo23, cm = dmin[r] * kTwo23;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float fs = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j));
+                const float fm = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j));
+                ds[r][j] = (j & 1) ? fmaf(dhi, fs, chi) : fmaf(dlo, fs, clo);
+                dmn[r][j] = fmaf(-dmin[r], fm, cm);
+            }
+        }
+#pragma unroll
+        for (int lc = 0; lc < 2; ++lc) {
+            int sl[R][3], sh[R][3];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int k = 0; k < 3; ++k) sl[r][k] = sh[r][k] = 0;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int g_lo = 16 * lc + 4 * p + k;
+                    const uint4 xl = *reinterpret_cast<const uint4 *>(xa + 16 * g_lo);
+                    const uint4 xh = *reinterpret_cast<const uint4 *>(xa + 16 * (g_lo + 8));
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint4 q = qs[r][2 * lc + p];
                         const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
                         const uint32_t L = wd & 0x0F0F0F0Fu;   // q of sub-block 2lc
                         const uint32_t H = wd & 0xF0F0F0F0u;   // 16 q of sub-block 2lc+1
@@ -814,12 +906,12 @@ __device__ __forceinline__ void copy_item(const GemvArgs &a, const uint8_t *w0, 
         }
 }
 
-template <int FMT, int B>
-__global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(const GemvArgs a)
+template <int FMT, int B, bool WIDE = false>
+__global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int R = gemv_rows(FMT, B);
-    constexpr int NW = gemv_warps(FMT, B);
+    constexpr int NW = gemv_warps(FMT, B, WIDE);
     constexpr int CM = gemv_cpl_max(FMT, B);
     constexpr int UB = FMT == kFmtQ4K ? 144 : 34;    // bytes per lane unit (Q4_K, Q8_0)
     const int tid = threadIdx.x;
@@ -992,8 +1084,38 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
             // the chunk's start, lane unit c*chunk_lu + i*SW + sl of the row
             const int lu0 = static_cast<int>(c) * chunk_lu + sl;
             if constexpr (FMT == kFmtQ4K) {
-                uint4 hd[R], qs[R][8];
                 const bool valid = lu0 < a.LU;
+              if constexpr (B == 1 && WIDE) {
+                // one 128-column half at a time: the stage is handed back once
+                // the second half is in registers
+                uint4 hd[R], q4[R][4];
+                const int lu = lu0;
+                const bool has_hi = 2 * lu + 1 < a.U;
+                if (valid) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + sl * UB);
+                        hd[r] = p[0];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q4[r][i] = p[1 + i];
+                    }
+                    q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, acc);
+                    if (has_hi) {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + sl * UB);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) q4[r][i] = p[5 + i];
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
+                if (valid && has_hi)
+                    q4k_half_dig<R, 1>(hd, q4, xs + 16 * SU * (XH + lu), xsum + 4 * (XH + lu),
+                                       xscale + 4 * (XH + lu), acc);
+              } else {
+                uint4 hd[R], qs[R][8];
                 if (valid) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
@@ -1016,6 +1138,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
                     else
                         q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, acc);
                 }
+              }
             } else if constexpr (FMT == kFmtQ6K) {
                 // lane unit = half super-block: block li/2 of the chunk, half li%2
                 // (a chunk holds whole super-blocks: chunk_lu is even when nkc > 1)
@@ -1115,14 +1238,14 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B) + 1), 1) gemv_kernel(
 }
 
 // Launch one instantiation (defined per format in qk_gemv_q4k.cu / qk_gemv_q80.cu / qk_gemv_q6k.cu).
-cudaError_t gemv_launch_q4k(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q4k(int batch, bool wide, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q6k(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
-template <int FMT, int B>
+template <int FMT, int B, bool WIDE = false>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
-    auto kern = gemv_kernel<FMT, B>;
+    auto kern = gemv_kernel<FMT, B, WIDE>;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1135,7 +1258,7 @@ cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(32 * (gemv_warps(FMT, B) + 1));
+    cfg.blockDim = dim3(32 * (gemv_warps(FMT, B, WIDE) + 1));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -36,7 +36,8 @@ def test_plan_covers_the_row_and_fits(fmt, batch):
             assert p["SW"] * p["cpl"] * p["nkc"] >= lu                  # every lane unit has a lane
             assert p["SW"] * p["cpl"] * (p["nkc"] - 1) < lu             # no empty trailing chunk
             assert 32 % p["SW"] == 0 and p["rows_w"] == (32 // p["SW"]) * p["R"]
-            assert 1 <= p["nw"] <= (11 if batch == 1 else 8) and p["m"] >= 1
+            assert 1 <= p["nw"] <= ((15 if p["wide"] else 11) if batch == 1 else 8) and p["m"] >= 1
+            assert not p["wide"] or (fmt == "q4_k" and batch == 1)
             assert p["stages"] == p["nw"] * p["m"] <= 32
             assert p["off_stage"] + p["stages"] * p["stage_bytes"] == p["smem"] <= SMEM
             assert p["grid"] == min(SMS, rows)
@@ -60,3 +61,12 @@ def test_pair_and_expert_modes():
     assert q["cpa"] == SMS // 8 and q["grid"] == 8 * q["cpa"]
     r = plan("q4_k", 1536, 2048, 1, n_assign=400)
     assert r["cpa"] == 1 and r["grid"] == 400
+
+
+def test_wide_form_for_calls_with_many_items():
+    """Q4_K batch 1: more items a CTA than 11 warps -> the 16-warp form."""
+    assert plan("q4_k", 6144, 4096, 1)["wide"] == 0          # 11 items a CTA (qkv)
+    assert plan("q4_k", 4096, 4096, 1)["wide"] == 0          # 7 (attn_output)
+    assert plan("q4_k", 28672, 4096, 1)["wide"] == 1         # 48 (gate+up)
+    assert plan("q4_k", 4096, 14336, 1)["wide"] == 1         # 28 (ffn_down, 2 chunks a row)
+    assert plan("q4_k", 28672, 4096, 2)["wide"] == 0
