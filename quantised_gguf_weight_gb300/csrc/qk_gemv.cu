@@ -131,9 +131,11 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     // before the arithmetic, so one stage a warp already keeps a copy in
     // flight while the warp computes
     const int64_t rows_cta_max = n_assign > 0 ? (rows + cpa - 1) / cpa : (rows + grid - 1) / grid;
-    // Q4_K batch 1 with more items a CTA than the 11 consumer warps: the
-    // 16-warp form (same arithmetic in the same order, more warps in flight)
-    const bool wide = fmt == kFmtQ4K && batch == 1 && (rows_cta_max + gr - 1) / gr * nkc > NW;
+    // Batch 1: the 16-warp form (same arithmetic in the same order, more
+    // warps in flight) for Q6_K, and for Q4_K when a CTA has more items than
+    // the 11 consumer warps of the other form
+    const bool wide = batch == 1 && (fmt == kFmtQ6K ||
+                                     (fmt == kFmtQ4K && (rows_cta_max + gr - 1) / gr * nkc > NW));
     if (wide) NW = gemv_warps(fmt, batch, true);
     int64_t nw = std::min<int64_t>(NW, (rows_cta_max + gr - 1) / gr);
     nw = std::min(nw, stages);
@@ -232,7 +234,7 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.wait_ns = wait_ns;
     r.err = err;
     if (fmt == kFmtQ4K) return gemv_launch_q4k(batch, p.wide != 0, r, p.grid, p.smem, st, pdl);
-    if (fmt == kFmtQ6K) return gemv_launch_q6k(batch, r, p.grid, p.smem, st, pdl);
+    if (fmt == kFmtQ6K) return gemv_launch_q6k(batch, p.wide != 0, r, p.grid, p.smem, st, pdl);
     return gemv_launch_q80(batch, r, p.grid, p.smem, st, pdl);
 }
 

@@ -1240,7 +1240,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
 // Launch one instantiation (defined per format in qk_gemv_q4k.cu / qk_gemv_q80.cu / qk_gemv_q6k.cu).
 cudaError_t gemv_launch_q4k(int batch, bool wide, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
-cudaError_t gemv_launch_q6k(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
+cudaError_t gemv_launch_q6k(int batch, bool wide, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
 template <int FMT, int B, bool WIDE = false>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)

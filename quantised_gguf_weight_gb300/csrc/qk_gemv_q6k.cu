@@ -4,10 +4,12 @@
 
 namespace qk {
 
-cudaError_t gemv_launch_q6k(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
+cudaError_t gemv_launch_q6k(int batch, bool wide, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
     switch (batch) {
-    case 1: return gemv_launch_one<kFmtQ6K, 1>(a, grid, smem, st, pdl);
+    case 1:
+        return wide ? gemv_launch_one<kFmtQ6K, 1, true>(a, grid, smem, st, pdl)
+                    : gemv_launch_one<kFmtQ6K, 1>(a, grid, smem, st, pdl);
     case 2: return gemv_launch_one<kFmtQ6K, 2>(a, grid, smem, st, pdl);
     case 3: return gemv_launch_one<kFmtQ6K, 3>(a, grid, smem, st, pdl);
     case 4: return gemv_launch_one<kFmtQ6K, 4>(a, grid, smem, st, pdl);

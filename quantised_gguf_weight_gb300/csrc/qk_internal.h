@@ -14,7 +14,7 @@ constexpr int kFmtQ6K = 2;
 struct GemvPlan {
     int U, LU, XU, SW, R, cpl, nkc, rows_w, chunk_bytes, row_stride;
     int nw, m, stages, stage_bytes, pair, up_stage_off, cpa;
-    int wide;   // Q4_K batch 1: the 16-warp form (a lane holds half a super-block at a time)
+    int wide;   // batch 1: the 16-warp form (Q4_K: a lane holds half a super-block at a time)
     int off_x, off_xsum, off_xscale, off_stage, smem, grid;
     int64_t row_bytes;
 };

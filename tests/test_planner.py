@@ -37,7 +37,8 @@ def test_plan_covers_the_row_and_fits(fmt, batch):
             assert p["SW"] * p["cpl"] * (p["nkc"] - 1) < lu             # no empty trailing chunk
             assert 32 % p["SW"] == 0 and p["rows_w"] == (32 // p["SW"]) * p["R"]
             assert 1 <= p["nw"] <= ((15 if p["wide"] else 11) if batch == 1 else 8) and p["m"] >= 1
-            assert not p["wide"] or (fmt == "q4_k" and batch == 1)
+            assert not p["wide"] or batch == 1
+            assert p["wide"] or fmt != "q6_k" or batch != 1
             assert p["stages"] == p["nw"] * p["m"] <= 32
             assert p["off_stage"] + p["stages"] * p["stage_bytes"] == p["smem"] <= SMEM
             assert p["grid"] == min(SMS, rows)
