@@ -651,7 +651,10 @@ def run_only(args, torch, qk, synth, device):
     x = torch.from_numpy(synth.activations(batch, K, seed=1)).to(device)
     y = torch.empty((batch, rows), device=device)
     lib = qk.load()
-    fn = lib.qmatvec_q8_0 if fmt == "q8_0" else lib.qmatvec_q4_k
+    fns = {"q8_0": lib.qmatvec_q8_0, "q4_k": lib.qmatvec_q4_k, "q6_k": lib.qmatvec_q6_k}
+    if fmt not in fns:
+        raise SystemExit(f"--only: unknown format {fmt!r} (q8_0, q4_k or q6_k)")
+    fn = fns[fmt]
     stream = torch.cuda.Stream(device=device)
 
     def mk(w):
