@@ -20,8 +20,10 @@
  *   Q4_K : 144-byte super-blocks of 256 weights: fp16 d, fp16 dmin, 12 bytes
  *          of packed 6-bit sub-block scales sc and mins m (8 sub-blocks of
  *          32), 128 bytes of 4-bit quants q;  w = d*sc*q - dmin*m.
- *   A row holds ceil(K / 32) (Q8_0) or ceil(K / 256) (Q4_K) whole blocks;
- *   columns >= K inside a row's last block are ignored.
+ *   A row holds ceil(K / 32) (Q8_0) or ceil(K / 256) (Q4_K, Q6_K) whole
+ *   blocks; columns >= K inside a row's last block are ignored.  In
+ *   strict-blocks mode (qk_set_strict_blocks) a K that is not a whole number
+ *   of blocks is refused instead (QK_ERR_BAD_DIM).
  *
  * Row addressing: `w` points at the first byte of the whole tensor, and a call
  * uses rows [row_offset, row_offset + rows).  Row r starts at byte
@@ -58,7 +60,8 @@ typedef struct CUstream_st *qk_stream_t;
 typedef enum {
     QK_OK = 0,
     QK_ERR_NULL = 1,        /* a required pointer is NULL                              */
-    QK_ERR_BAD_DIM = 2,     /* rows/N/M <= 0, K <= 0, row_offset < 0, ldy too small     */
+    QK_ERR_BAD_DIM = 2,     /* rows/N/M <= 0, K <= 0, row_offset < 0, ldy too small;
+                               strict-blocks mode: K not a whole number of blocks      */
     QK_ERR_ALIGN = 3,       /* w, x or y misaligned (see each call)                     */
     QK_ERR_BATCH = 4,       /* GEMV batch outside [1, QK_MAX_BATCH]                     */
     QK_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed                     */
@@ -287,6 +290,18 @@ uint64_t qk_set_wait_limit_ns(uint64_t ns);
  * order.  Meant for decode loops whose weights are loaded once.
  */
 int qk_set_programmatic_launch(int enable);
+
+/*
+ * Strict-blocks mode for later calls (returns the previous setting).  Off by
+ * default, where any K >= 1 is accepted and a row's last block may be
+ * partly used; on, every compute call whose K is not a multiple of its
+ * format's block (32 columns for Q8_0, 256 for Q4_K and Q6_K) returns
+ * QK_ERR_BAD_DIM before any launch.  The library starts with it on when the
+ * environment holds QK_STRICT=1 at load time.  A GGUF row always holds whole
+ * blocks (nurllama README, "What it runs"); the mode is for callers that want
+ * such shapes rejected rather than read with an unused tail.
+ */
+int qk_set_strict_blocks(int enable);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int qk_version(void);

@@ -6,6 +6,8 @@
 // qk_gemv.cu and qk_gemm.cu; there is no host fallback of any kind.
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <cuda_runtime.h>
 
 #include "../../include/qk.h"
@@ -22,6 +24,14 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int64_t> g_skip_item{-1};
 std::atomic<int> g_programmatic{0};
 std::atomic<int> g_gemm_skip_chunk{-1};
+
+// Strict-blocks mode starts on when the environment sets QK_STRICT=1.
+int strict_from_env()
+{
+    const char *v = std::getenv("QK_STRICT");
+    return (v && std::strcmp(v, "1") == 0) ? 1 : 0;
+}
+std::atomic<int> g_strict_blocks{strict_from_env()};
 
 int *error_word_ptr()
 {
@@ -48,6 +58,7 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     if (batch < 1 || batch > QK_MAX_BATCH) return QK_ERR_BATCH;
     if (ldy == 0) ldy = rows;
     if (ldy < rows) return QK_ERR_BAD_DIM;
+    if (qk::strict_blocks_reject(fmt, K)) return QK_ERR_BAD_DIM;
     if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4))
         return QK_ERR_ALIGN;
     // the kernel keeps a launch's activation rows in shared memory: a batch
@@ -90,6 +101,11 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
 namespace qk {
 int *library_error_word() { return error_word_ptr(); }
 uint64_t library_wait_limit_ns() { return g_wait_limit_ns.load(); }
+bool strict_blocks_reject(int fmt, int64_t K)
+{
+    const int64_t qk = fmt == kFmtQ80 ? 32 : 256;
+    return g_strict_blocks.load() != 0 && K % qk != 0;
+}
 }  // namespace qk
 
 extern "C" {
@@ -113,6 +129,7 @@ int gemm_entry(int fmt, const void *w, int64_t row_offset, int64_t N, int64_t K,
     if (N <= 0 || K <= 0 || M <= 0 || row_offset < 0 || up_offset < 0) return QK_ERR_BAD_DIM;
     if (ldy == 0) ldy = N;
     if (ldy < N) return QK_ERR_BAD_DIM;
+    if (qk::strict_blocks_reject(fmt, K)) return QK_ERR_BAD_DIM;
     if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < qk::gemm_workspace_bytes(M, K))
         return QK_ERR_WORKSPACE;
@@ -223,6 +240,7 @@ int experts_entry(int fmt, const void *w, int64_t n_experts, int64_t rows, int64
     if (n_experts <= 0 || rows <= 0 || K <= 0 || xk <= 0 || n_assign <= 0) return QK_ERR_BAD_DIM;
     if (ldy == 0) ldy = rows;
     if (ldy < rows) return QK_ERR_BAD_DIM;
+    if (qk::strict_blocks_reject(fmt, K)) return QK_ERR_BAD_DIM;
     if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4) || !aligned(expert_ids, 4))
         return QK_ERR_ALIGN;
     qk::GemvPlan plan;
@@ -272,7 +290,9 @@ const char *qk_status_string(int status)
     switch (status) {
     case QK_OK: return "ok";
     case QK_ERR_NULL: return "null pointer argument";
-    case QK_ERR_BAD_DIM: return "bad dimension (rows/N/M/K <= 0, negative row_offset, or ldy too small)";
+    case QK_ERR_BAD_DIM:
+        return "bad dimension (rows/N/M/K <= 0, negative row_offset, ldy too small, or in strict-blocks mode "
+               "K not a whole number of blocks)";
     case QK_ERR_ALIGN: return "misaligned pointer";
     case QK_ERR_BATCH: return "batch outside [1, 8]";
     case QK_ERR_CUDA: return "CUDA error";
@@ -306,6 +326,8 @@ uint64_t qk_set_wait_limit_ns(uint64_t ns)
 }
 
 int qk_set_programmatic_launch(int enable) { return g_programmatic.exchange(enable ? 1 : 0); }
+
+int qk_set_strict_blocks(int enable) { return g_strict_blocks.exchange(enable ? 1 : 0); }
 
 int qk_version(void) { return 100; }
 

@@ -32,6 +32,9 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
 // The device error word of the current device and the bound of device waits.
 int *library_error_word();
 uint64_t library_wait_limit_ns();
+// Strict-blocks mode: true when it is on and K is not a whole number of the
+// format's blocks (32 columns for Q8_0, 256 for Q4_K and Q6_K).
+bool strict_blocks_reject(int fmt, int64_t K);
 
 int64_t gemm_k8(int64_t K);
 size_t gemm_workspace_bytes(int64_t M, int64_t K);

@@ -55,6 +55,7 @@ int qgemm_q4_k_noalloc(const void *w, int64_t row_offset, int64_t N, int64_t K, 
     if (N <= 0 || K <= 0 || M <= 0 || row_offset < 0) return QK_ERR_BAD_DIM;
     if (ldy == 0) ldy = N;
     if (ldy < N) return QK_ERR_BAD_DIM;
+    if (qk::strict_blocks_reject(qk::kFmtQ4K, K)) return QK_ERR_BAD_DIM;
     if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
     // the bf16 copy of x has to fit in the fixed scratch array
     if (M > (1LL << 31) - 1 || K > (1LL << 31) - 1 || qk::gemm_workspace_bytes(M, K) > kQkNoallocScratchBytes)

@@ -30,7 +30,7 @@ EXPORTS = ["qmatvec_q8_0", "qmatvec_q4_k", "qmatvec_q6_k", "qmatvec_swiglu_q8_0"
            "qgemm_q8_0_acc", "qgemm_swiglu_q8_0", "qgemm_q4_k_workspace_bytes",
            "qgemm_q4_k_noalloc", "qk_row_bytes_q8_0", "qk_row_bytes_q4_k",
            "qk_status_string", "qk_device_error", "qk_set_wait_limit_ns", "qk_set_programmatic_launch",
-           "qk_version"]
+           "qk_set_strict_blocks", "qk_version"]
 
 
 class QKError(RuntimeError):
@@ -89,6 +89,8 @@ def load(path: str | None = None):
         lib.qk_version.restype = I
         lib.qk_set_programmatic_launch.argtypes = [I]
         lib.qk_set_programmatic_launch.restype = I
+        lib.qk_set_strict_blocks.argtypes = [I]
+        lib.qk_set_strict_blocks.restype = I
         lib.qk_debug_skip_item.argtypes = [I64]
         lib.qk_debug_skip_item.restype = I64
         lib.qk_debug_gemv_plan.argtypes = [I, I64, I64, I, ctypes.POINTER(ctypes.c_int64), I]
@@ -266,6 +268,12 @@ def set_wait_limit_ns(ns: int) -> int:
 def set_programmatic_launch(enable: bool) -> bool:
     """Programmatic dependent launch for later calls (see include/qk.h)."""
     return bool(load().qk_set_programmatic_launch(1 if enable else 0))
+
+
+def set_strict_blocks(enable: bool) -> bool:
+    """Strict-blocks mode for later calls: a K that is not a whole number of the
+    format's blocks is refused with QK_ERR_BAD_DIM (see include/qk.h)."""
+    return bool(load().qk_set_strict_blocks(1 if enable else 0))
 
 
 def debug_skip_item(item: int) -> int:

@@ -88,7 +88,7 @@ def test_argument_validation_without_gpu(lib, name):
     assert call(y=FAKE + 1) == 3
     assert call(w=FAKE + 1) == 3     # odd w
     if name == "qmatvec_q4_k":
-        assert call(w=FAKE + (8 if "q4_k" in name else 1)) == 3   # Q4_K: 16-byte, Q8_0: 2-byte alignment  # Q4_K needs 16-byte aligned super-blocks
+        assert call(w=FAKE + 8) == 3     # Q4_K rows need 16-byte alignment
 
 
 @pytest.mark.parametrize("name", ["qmatvec_swiglu_q8_0", "qmatvec_swiglu_q4_k", "qmatvec_swiglu_q6_k"])
@@ -170,3 +170,81 @@ def test_gemm_argument_validation_without_gpu(lib, name):
     assert call(ws=FAKE + 16) == 7
     assert call(wsb=100) == 7
     assert lib.qgemm_q4_k_workspace_bytes(512, 14336, 4096) >= 512 * 4096 * 2
+
+
+# K that is not a whole number of blocks, and one that is, per format
+STRICT_K = {"q8_0": (40, 64), "q4_k": (896, 1024), "q6_k": (300, 512)}
+
+
+@pytest.fixture
+def strict(lib):
+    old = lib.qk_set_strict_blocks(1)
+    yield lib
+    lib.qk_set_strict_blocks(old)
+
+
+def strict_calls(lib):
+    """(format, call(K, x)) for every compute entry point.  The tests pass a
+    misaligned x to every call, so no call can get past validation to a launch
+    whatever the strict-blocks check does; the fake pointers are never
+    dereferenced."""
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    out = []
+    for fmt in ("q8_0", "q4_k", "q6_k"):
+        f = getattr(lib, "qmatvec_" + fmt)
+        out.append((fmt, lambda K, x, f=f: f(FAKE, 0, 16, K, x, 1, FAKE, 0, None)))
+        f = getattr(lib, "qmatvec_swiglu_" + fmt)
+        f.argtypes = [P, I64, I64, I64, I64, P, I, P, I64, P]
+        out.append((fmt, lambda K, x, f=f: f(FAKE, 0, 16, 16, K, x, 1, FAKE, 0, None)))
+        f = getattr(lib, "qmatvec_experts_" + fmt)
+        f.argtypes = [P, I64, I64, I64, P, I, P, I64, P, I64, P]
+        out.append((fmt, lambda K, x, f=f: f(FAKE, 4, 16, K, x, 1, FAKE, 2, FAKE, 0, None)))
+    gemm_types = [P, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
+    for fmt, names in (("q4_k", ("qgemm_q4_k", "qgemm_q4_k_acc")), ("q8_0", ("qgemm_q8_0", "qgemm_q8_0_acc"))):
+        for n in names:
+            f = getattr(lib, n)
+            f.argtypes = gemm_types
+            out.append((fmt, lambda K, x, f=f: f(FAKE, 0, 128, K, x, 4, FAKE, 0, FAKE, 1 << 20, None)))
+        f = getattr(lib, "qgemm_swiglu_" + fmt)
+        f.argtypes = [P, I64, I64, I64, I64, P, I64, P, I64, P, ctypes.c_size_t, P]
+        out.append((fmt, lambda K, x, f=f: f(FAKE, 0, 128, 128, K, x, 4, FAKE, 0, FAKE, 1 << 20, None)))
+    f = lib.qgemm_q4_k_noalloc
+    f.argtypes = [P, I64, I64, I64, P, I64, P, I64, P]
+    out.append(("q4_k", lambda K, x, f=f: f(FAKE, 0, 128, K, x, 4, FAKE, 0, None)))
+    return out
+
+
+def test_strict_blocks_mode_refuses_partial_blocks(strict):
+    calls = strict_calls(strict)
+    assert len(calls) == 16
+    for fmt, call in calls:
+        bad, good = STRICT_K[fmt]
+        assert call(bad, FAKE + 2) == 2, fmt        # refused before the pointer checks
+        assert call(good, FAKE + 2) == 3, fmt       # a whole number of blocks passes on to them
+
+
+def test_strict_blocks_mode_off_accepts_partial_blocks(lib):
+    old = lib.qk_set_strict_blocks(0)
+    try:
+        for fmt, call in strict_calls(lib):
+            bad, _ = STRICT_K[fmt]
+            assert call(bad, FAKE + 2) == 3, fmt    # K passes; the misaligned x is what is refused
+    finally:
+        lib.qk_set_strict_blocks(old)
+
+
+def test_strict_blocks_mode_from_environment(lib):
+    """QK_STRICT=1 in the environment turns the mode on when the library loads."""
+    import subprocess
+    import sys
+    from quantised_gguf_weight_gb300 import qk
+    code = ("import ctypes, sys; lib = ctypes.CDLL(sys.argv[1]); "
+            "print(lib.qk_set_strict_blocks(0), lib.qk_set_strict_blocks(0))")
+    path = qk.library_path()
+    for env_value, first in (("1", "1"), ("0", "0"), (None, "0")):
+        env = {k: v for k, v in os.environ.items() if k != "QK_STRICT"}
+        if env_value is not None:
+            env["QK_STRICT"] = env_value
+        out = subprocess.run([sys.executable, "-c", code, path], env=env, capture_output=True, text=True,
+                             check=True).stdout.split()
+        assert out == [first, "0"], (env_value, out)
