@@ -582,10 +582,16 @@ def cpu_baseline(budget_s: float = 12.0):
         passes += 1
         if passes == 1:
             frac = min(1.0, frac * max(1.0, budget_s / 4 / max(t, 1e-3)))
+    # the same oracle on one thread (bit-identical results), about 2 s
+    b1, t1 = oracle_sample_run(orc, synth, 0.002, 1, seed=1)
+    frac1 = min(1.0, 0.002 * max(1.0, 2.0 / max(t1, 1e-3)))
+    b1, t1 = oracle_sample_run(orc, synth, frac1, 1, seed=1)
     return {"value": round(tot_b / tot_t / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{passes} passes over evenly spaced rows of every Llama-8B layer tensor "
                       f"(up to {frac:.2f} of the rows per pass), f64 decode-then-dot, {threads} host "
-                      f"threads over row bands, {tot_t:.1f} s of oracle time"}
+                      f"threads over row bands, {tot_t:.1f} s of oracle time",
+            "single_thread": {"value": round(b1 / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{frac1:.3f} of the rows of every layer tensor, {t1:.1f} s"}}
 
 
 def run_reference(args):
