@@ -432,16 +432,16 @@ def measure_extra_rows(torch, qk, synth, device, stream):
     out = {}
     l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20) or (128 << 20)
 
-    def gemv_row(label, fmt, rows, K, batch, seed, copies):
+    def gemv_row(label, fmt, rows, K, batch, seed, copies, cold_too=False):
         rb = qk.row_bytes(fmt, K)
         ws = [torch.from_numpy(synth.weights(fmt, rows, K, seed=seed, stream0=50 * c)).to(device)
               for c in range(copies)]
         x = torch.from_numpy(synth.activations(batch, K, seed=seed)).to(device)
         y = torch.empty((batch, rows), device=device)
         fn = {"q8_0": lib.qmatvec_q8_0, "q4_k": lib.qmatvec_q4_k, "q6_k": lib.qmatvec_q6_k}[fmt]
-        def mk(w):
+        def mk(w, off=0):
             def f(sh):
-                st = fn(w.data_ptr(), 0, rows, K, x.data_ptr(), batch, y.data_ptr(), rows, sh)
+                st = fn(w.data_ptr(), off, rows, K, x.data_ptr(), batch, y.data_ptr(), rows, sh)
                 assert st == 0
             return f
         fns = [mk(w) for w in ws] * max(1, 8 // len(ws))
@@ -450,6 +450,17 @@ def measure_extra_rows(torch, qk, synth, device, stream):
         out[label] = {"bytes": b, "avg_us": round(avg_ms * 1e3, 2),
                       "GB/s": round(b / (avg_ms * 1e-3) / 1e9, 1),
                       "cache": "cold (rotated copies > L2)" if copies * rows * rb > l2 else "hot (L2-resident)"}
+        if cold_too:
+            # the same call on row ranges of one tensor holding n copies of the
+            # weights (2 x L2 in all): each call's bytes were last touched
+            # n - 1 calls earlier, so they come from HBM
+            n = math.ceil(2 * l2 / (rows * rb)) + 1
+            big = ws[0].repeat(n)
+            avg_ms = time_calls(torch, stream, [mk(big, c * rows) for c in range(n)], 5)
+            out[label + "_cold"] = {"bytes": b, "avg_us": round(avg_ms * 1e3, 2),
+                                    "GB/s": round(b / (avg_ms * 1e-3) / 1e9, 1),
+                                    "cache": f"cold ({n} copies, row ranges of one {n * rows * rb / 1e6:.0f} MB tensor)"}
+            del big
         del ws
 
     def gemm_row(label, M, N, K, seed, copies, mode="store", fmt="q4_k"):
@@ -535,9 +546,9 @@ def measure_extra_rows(torch, qk, synth, device, stream):
     gemm_row("q8_0_gemm_512x896x4864", 512, 4864, 896, 1, 1, fmt="q8_0")
     experts_row("q4_k_experts_moe_top8_128x1536x2048", "q4_k", 128, 1536, 2048, 8, 8, 5)
     swiglu_row("q4_k_swiglu_llama8b_ffn_14336x4096_b1", "q4_k", 14336, 4096, 1, 2, 4)
-    gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1)
-    gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1)
-    gemv_row("q4_k_896x4864_b1", "q4_k", 896, 4864, 1, 1, 1)
+    gemv_row("q8_0_576x576_b1", "q8_0", 576, 576, 1, 0, 1, cold_too=True)
+    gemv_row("q4_k_4864x896_b1", "q4_k", 4864, 896, 1, 1, 1, cold_too=True)
+    gemv_row("q4_k_896x4864_b1", "q4_k", 896, 4864, 1, 1, 1, cold_too=True)
     gemv_row("q4_k_llama8b_gate_up_28672x4096_b4", "q4_k", 28672, 4096, 4, 2, 2)
     gemv_row("q8_0_lm_head_151936x896_b1", "q8_0", 151936, 896, 1, 3, 3)
     gemv_row("q8_0_lm_head_151936x896_b8", "q8_0", 151936, 896, 8, 3, 3)

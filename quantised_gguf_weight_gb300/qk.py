@@ -119,14 +119,76 @@ def _check(status: int, what: str):
         raise QKError(status, what)
 
 
+def _on_device(t, name: str, dtype=None) -> None:
+    """A tensor the library reads or writes through its data pointer: a CUDA
+    tensor on the current device, of the given dtype."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+
+
+def _bytes_after(t: torch.Tensor) -> int:
+    """Bytes from t's first element to the end of its storage."""
+    return t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+
+
+def _check_w(w, rows_end: int, rb: int) -> None:
+    """Weight bytes: rows [0, rows_end) of rb bytes each, contiguous from w."""
+    _on_device(w, "w")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    if rows_end * rb > _bytes_after(w):
+        raise ValueError(f"w holds {_bytes_after(w)} bytes, the call reads {rows_end * rb}")
+
+
+def _check_x(x, K: int, name: str = "x") -> None:
+    """Activations [n][K] fp32, row stride K."""
+    _on_device(x, name, torch.float32)
+    if x.dim() != 2 or x.shape[1] != K or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [n][{K}] tensor, got shape {tuple(x.shape)}")
+
+
+def _check_out(y, n: int, cols: int, ld: int, name: str = "y") -> None:
+    """Output rows b < n of `cols` fp32 values, row b at element b*ld of y: a
+    [>= n][>= cols] tensor whose rows are ld apart, or a flat one."""
+    _on_device(y, name, torch.float32)
+    if y.dim() == 0 or y.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride in its last dimension")
+    ld = ld or cols
+    if y.dim() == 2:
+        if y.shape[0] < n or y.shape[1] < cols:
+            raise ValueError(f"{name} {tuple(y.shape)} is too small for {n} rows of {cols}")
+        if n > 1 and y.stride(0) != ld:
+            raise ValueError(f"{name} rows are {y.stride(0)} elements apart, the call writes them {ld} apart")
+    elif not y.is_contiguous() or y.numel() < (n - 1) * ld + cols:
+        raise ValueError(f"{name} is too small for {n} rows of {cols} at stride {ld} (or not contiguous)")
+    if ((n - 1) * ld + cols) * 4 > _bytes_after(y):
+        raise ValueError(f"{name} is too small for {n} rows of {cols} at stride {ld}")
+
+
+def _fmt_row_bytes(fmt: str, K: int) -> int:
+    """Row bytes computed here (no library call), for the binding's checks."""
+    if K <= 0:
+        return 0
+    return {"q8_0": -(-K // 32) * 34, "q4_k": -(-K // 256) * 144, "q6_k": -(-K // 256) * 210}[fmt]
+
+
 def _qmatvec(name: str, w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.Tensor,
              y: torch.Tensor | None, ldy: int, stream) -> torch.Tensor:
-    if x.dim() == 1:
+    if isinstance(x, torch.Tensor) and x.dim() == 1:
         x = x.view(1, -1)
+    _check_x(x, K)
     batch = x.shape[0]
+    if rows > 0 and row_offset >= 0:
+        _check_w(w, row_offset + rows, _fmt_row_bytes(name[-4:], K))
     if y is None:
         y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
         ldy = rows
+    if rows > 0:
+        _check_out(y, batch, rows, ldy)
     st = getattr(load(), name)(w.data_ptr(), row_offset, rows, K, x.data_ptr(), batch, y.data_ptr(),
                                ldy, _stream(stream))
     _check(st, name)
@@ -148,12 +210,17 @@ def qmatvec_q4_k(w: torch.Tensor, row_offset: int, rows: int, K: int, x: torch.T
 def qmatvec_swiglu(fmt: str, w: torch.Tensor, gate_offset: int, up_offset: int, F: int, K: int,
                    x: torch.Tensor, h: torch.Tensor | None = None, ldh: int = 0, stream=None) -> torch.Tensor:
     """h[b][p] = silu(sum_c W[gate_offset+p][c] x[b][c]) * sum_c W[up_offset+p][c] x[b][c], p < F."""
-    if x.dim() == 1:
+    if isinstance(x, torch.Tensor) and x.dim() == 1:
         x = x.view(1, -1)
+    _check_x(x, K)
     batch = x.shape[0]
+    if F > 0 and gate_offset >= 0 and up_offset >= 0:
+        _check_w(w, max(gate_offset, up_offset) + F, _fmt_row_bytes(fmt, K))
     if h is None:
         h = torch.empty((batch, F), dtype=torch.float32, device=x.device)
         ldh = F
+    if F > 0:
+        _check_out(h, batch, F, ldh, "h")
     name = {"q8_0": "qmatvec_swiglu_q8_0", "q4_k": "qmatvec_swiglu_q4_k", "q6_k": "qmatvec_swiglu_q6_k"}[fmt]
     st = getattr(load(), name)(w.data_ptr(), gate_offset, up_offset, F, K, x.data_ptr(), batch, h.data_ptr(),
                                ldh, _stream(stream))
@@ -165,12 +232,22 @@ def qmatvec_experts(fmt: str, w: torch.Tensor, n_experts: int, rows: int, K: int
                     expert_ids: torch.Tensor, y: torch.Tensor | None = None, ldy: int = 0,
                     stream=None) -> torch.Tensor:
     """y[a][r] = sum_c W[expert_ids[a]*rows + r][c] x[a // xk][c] (expert_ids: int32 device tensor)."""
-    if x.dim() == 1:
+    if isinstance(x, torch.Tensor) and x.dim() == 1:
         x = x.view(1, -1)
+    _check_x(x, K)
+    _on_device(expert_ids, "expert_ids", torch.int32)
+    if not expert_ids.is_contiguous():
+        raise ValueError("expert_ids must be contiguous")
     n_assign = expert_ids.numel()
+    if n_assign > 0 and xk > 0 and (n_assign - 1) // xk >= x.shape[0]:
+        raise ValueError(f"x has {x.shape[0]} rows, assignment {n_assign - 1} reads row {(n_assign - 1) // xk}")
+    if n_experts > 0 and rows > 0:
+        _check_w(w, n_experts * rows, _fmt_row_bytes(fmt, K))
     if y is None:
         y = torch.empty((n_assign, rows), dtype=torch.float32, device=x.device)
         ldy = rows
+    if n_assign > 0 and rows > 0:
+        _check_out(y, n_assign, rows, ldy)
     name = {"q8_0": "qmatvec_experts_q8_0", "q4_k": "qmatvec_experts_q4_k", "q6_k": "qmatvec_experts_q6_k"}[fmt]
     st = getattr(load(), name)(w.data_ptr(), n_experts, rows, K, x.data_ptr(), xk, expert_ids.data_ptr(),
                                n_assign, y.data_ptr(), ldy, _stream(stream))
@@ -190,12 +267,18 @@ def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
 
 def _gemm(name: str, w: torch.Tensor, row_offset: int, N: int, K: int, x: torch.Tensor,
           y: torch.Tensor | None, ldy: int, workspace: torch.Tensor | None, stream) -> torch.Tensor:
+    _check_x(x, K)
     M = x.shape[0]
+    if N > 0 and row_offset >= 0:
+        _check_w(w, row_offset + N, _fmt_row_bytes("q8_0" if "q8_0" in name else "q4_k", K))
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
         ldy = N
+    if N > 0 and M > 0:
+        _check_out(y, M, N, ldy)
     if workspace is None:
         workspace = torch.empty(gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=x.device)
+    _on_device(workspace, "workspace")
     st = getattr(load(), name)(w.data_ptr(), row_offset, N, K, x.data_ptr(), M, y.data_ptr(), ldy,
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, name)
@@ -234,12 +317,18 @@ def qgemm_swiglu(fmt: str, w: torch.Tensor, gate_offset: int, up_offset: int, F:
                  h: torch.Tensor | None = None, ldh: int = 0, workspace: torch.Tensor | None = None,
                  stream=None) -> torch.Tensor:
     """h[m][p] = silu(g) * u with g, u the bf16 GEMM rows gate_offset + p and up_offset + p."""
+    _check_x(x, K)
     M = x.shape[0]
+    if F > 0 and gate_offset >= 0 and up_offset >= 0:
+        _check_w(w, max(gate_offset, up_offset) + F, _fmt_row_bytes(fmt, K))
     if h is None:
         h = torch.empty((M, F), dtype=torch.float32, device=x.device)
         ldh = F
+    if F > 0 and M > 0:
+        _check_out(h, M, F, ldh, "h")
     if workspace is None:
         workspace = torch.empty(gemm_workspace_bytes(M, F, K), dtype=torch.uint8, device=x.device)
+    _on_device(workspace, "workspace")
     name = {"q4_k": "qgemm_swiglu_q4_k", "q8_0": "qgemm_swiglu_q8_0"}[fmt]
     st = getattr(load(), name)(w.data_ptr(), gate_offset, up_offset, F, K, x.data_ptr(), M, h.data_ptr(), ldh,
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))

@@ -248,3 +248,36 @@ def test_strict_blocks_mode_from_environment(lib):
         out = subprocess.run([sys.executable, "-c", code, path], env=env, capture_output=True, text=True,
                              check=True).stdout.split()
         assert out == [first, "0"], (env_value, out)
+
+
+def test_binding_refuses_host_tensors():
+    """The Python binding hands the library device pointers only: a tensor in
+    host memory is refused before the library is called."""
+    import torch
+    from quantised_gguf_weight_gb300 import qk
+    K = 256
+    w = torch.zeros(qk._fmt_row_bytes("q4_k", K) * 4, dtype=torch.uint8)
+    x = torch.zeros((1, K))
+    ids = torch.zeros(2, dtype=torch.int32)
+    calls = [
+        lambda: qk.qmatvec_q8_0(w, 0, 4, K, x),
+        lambda: qk.qmatvec_q4_k(w, 0, 4, K, x),
+        lambda: qk.qmatvec_q6_k(w, 0, 4, K, x),
+        lambda: qk.qmatvec_swiglu("q4_k", w, 0, 2, 2, K, x),
+        lambda: qk.qmatvec_experts("q4_k", w, 2, 2, K, x, 2, ids),
+        lambda: qk.qgemm_q4_k(w, 0, 4, K, x),
+        lambda: qk.qgemm_q8_0(w, 0, 4, K, x),
+        lambda: qk.qgemm_acc("q4_k", w, 0, 4, K, x, torch.zeros((1, 4))),
+        lambda: qk.qgemm_swiglu("q4_k", w, 0, 2, 2, K, x),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
+
+
+def test_binding_row_bytes_match_the_library(lib):
+    from quantised_gguf_weight_gb300 import qk
+    for K in (1, 31, 32, 33, 255, 256, 257, 896, 4096, 14336):
+        assert qk._fmt_row_bytes("q8_0", K) == lib.qk_row_bytes_q8_0(K)
+        assert qk._fmt_row_bytes("q4_k", K) == lib.qk_row_bytes_q4_k(K)
+        assert qk._fmt_row_bytes("q6_k", K) == lib.qk_row_bytes_q6_k(K)

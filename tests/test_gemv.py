@@ -281,3 +281,29 @@ def test_programmatic_launch_chain(qk, orc):
         # each stage is checked against the oracle fed with the GPU's own input
         assert_close(got, yr, s, f"stage {i}")
         x = xs[i + 1].cpu().numpy()
+
+
+def test_binding_refuses_wrong_tensors_before_launch(qk):
+    """Tensors too small for the call, of the wrong dtype or layout are refused
+    by the binding with ValueError; nothing is launched and y is untouched."""
+    K, rows = 512, 8
+    rb = qk.row_bytes("q4_k", K)
+    w = torch.zeros(rb * rows, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((2, K), device="cuda")
+    y = torch.full((2, rows), 7.0, device="cuda")
+    with pytest.raises(ValueError, match="w holds"):
+        qk.qmatvec_q4_k(w, 1, rows, K, x, y=y)                        # rows 1..8 of an 8-row tensor
+    with pytest.raises(ValueError, match="float32"):
+        qk.qmatvec_q4_k(w, 0, rows, K, x.double(), y=y)
+    with pytest.raises(ValueError, match=r"\[n\]\[512\]"):
+        qk.qmatvec_q4_k(w, 0, rows, K, x[:, :256], y=y)
+    with pytest.raises(ValueError, match="too small"):
+        qk.qmatvec_q4_k(w, 0, rows, K, x, y=y[:, :4])
+    with pytest.raises(ValueError, match="apart"):
+        qk.qmatvec_q4_k(w, 0, rows, K, x, y=y, ldy=rows + 1)           # y's rows are 8 apart, not 9
+    with pytest.raises(ValueError, match="int32"):
+        qk.qmatvec_experts("q4_k", w, 2, rows // 2, K, x, 1, torch.zeros(2, dtype=torch.int64, device="cuda"))
+    with pytest.raises(ValueError, match="reads row"):
+        qk.qmatvec_experts("q4_k", w, 2, rows // 2, K, x, 1, torch.zeros(3, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
