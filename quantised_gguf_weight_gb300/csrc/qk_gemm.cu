@@ -15,21 +15,26 @@
 // (128 in each CTA's shared memory) x N = 256 tokens (128 in each CTA's
 // shared memory) x K = 16, and each CTA's tensor memory accumulates its own
 // 128 rows x 512 tokens (512 f32 columns).  In each CTA:
-//  * warp 0 issues the TMA copies: the raw Q4_K bytes of its 128 rows x one
-//    super-block (a 2-D tensor map over the rows, 144 x 128 bytes) and its
-//    128-token slice of the bf16 activations of each 64-column K chunk (a
-//    2-D tensor map with the 128-byte swizzle, one box per token block);
+//  * warp 0 issues the TMA copies of each 64-column K chunk: the raw weight
+//    bytes of its 128 rows (Q4_K: two tensor maps over the rows, the 16-byte
+//    header d, dmin, scales and the chunk's 32 quant bytes; Q8_0 with 16-byte
+//    row strides: the aligned 80 bytes holding the chunk's two blocks; other
+//    Q8_0 rows are read by the dequantising threads themselves) and its
+//    128-token slices of the bf16 activations (a tensor map with the 128-byte
+//    swizzle, one box per token block);
 //  * warp 1 owns the tensor memory; in the even CTA one thread issues the
 //    pair's MMAs and commits (multicast to both CTAs' mbarriers), in the odd
 //    CTA one thread forwards "stage ready" (its own activations landed and
 //    weights dequantised) to the even CTA;
-//  * warps 2-9 dequantise each 64-column chunk of the 128 rows into the
-//    K-major 128-byte-swizzled bf16 layout the MMA reads, then run the
-//    epilogue: tcgen05.ld of 32 lanes x 32 columns -> coalesced stores of Y.
-// Three (Q8_0: four) 48 KB stages synchronise through mbarriers; every wait is
-// bounded, a wait that runs out aborts the CTA cleanly (copies drained, MMAs
-// completed, tensor memory freed) and records the device error word, and
-// both CTAs meet at a cluster barrier before the tensor memory is freed.
+//  * warps 2-9 dequantise each chunk of the 128 rows into the K-major
+//    128-byte-swizzled bf16 layout the MMA reads, then run the epilogue:
+//    tcgen05.ld of 32 lanes x 32 columns into a 4 KB [token][row] tile in
+//    shared memory and one TMA store (acc: an f32 add-reduce) per tile when
+//    Y's rows are 16-byte aligned, else direct stores.
+// Three or four stages (see Shape) synchronise through mbarriers; every wait
+// is bounded, a wait that runs out aborts the CTA cleanly (copies drained,
+// MMAs completed, tensor memory freed) and records the device error word,
+// and both CTAs meet at a cluster barrier before the tensor memory is freed.
 #include <algorithm>
 #include <cstdint>
 #include <cuda.h>
