@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -346,12 +347,21 @@ def read_traffic(kernel_key: str, avg_launch_bytes: float):
         return None
     src = os.path.join(ROOT, "quantised_gguf_weight_gb300", "csrc", ent.get("source", ""))
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fp = source_fingerprint(src)
     except OSError:
         return None
-    if sha != ent.get("source_sha"):
+    if fp != ent.get("source_fingerprint"):
         return None
     return ent.get("dram_bytes_per_launch_avg")
+
+
+def source_fingerprint(path: str) -> str:
+    """sha256 (16 hex digits) of a C/CUDA source with its comments removed and
+    its whitespace collapsed: it changes with the code, not with the comments."""
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
 
 
 def measure_e2e(args, torch, wl, stream, step_bytes, world):

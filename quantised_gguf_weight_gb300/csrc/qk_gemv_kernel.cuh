@@ -1,5 +1,5 @@
 // qk_gemv_kernel.cuh -- the GEMV kernel (sm_103a):
-// fused dequantise-and-multiply of GGUF Q8_0 / Q4_K rows against fp32
+// fused dequantise-and-multiply of GGUF Q8_0 / Q4_K / Q6_K rows against fp32
 // activations, y[b][r] = sum_c W[r][c] x[b][c], batch 1..8.
 //
 // The operation is the quantised matvec of "nurllama 0.18.1 API reference",
@@ -9,8 +9,8 @@
 //    [rows*i/G, rows*(i+1)/G).
 //  * The rows of a CTA are cut into row groups of rows_w = (32/SW)*R rows and
 //    each row into nkc K-chunks of SW*cpl lane units (a lane unit is one Q4_K
-//    super-block of 256 weights or one 32-weight Q8_0 block).  An item is one
-//    row group x one K-chunk.
+//    super-block of 256 weights, one 32-weight Q8_0 block, or half a Q6_K
+//    super-block).  An item is one row group x one K-chunk.
 //  * Consumer warp w owns row groups w, w+nw, ... and m shared-memory stages
 //    of its own; its t-th item goes to stage w*m + t%m.  Lane w of warp 0 is
 //    its producer: it streams the warp's items into its stages with 1-D bulk
@@ -33,6 +33,13 @@
 //    consecutive slots of one unit both hit distinct bank groups.  Q4_K half
 //    super-blocks are stored h-major (unit slot h*XH + super-block), so lanes
 //    holding consecutive super-blocks read consecutive unit slots.
+//  * Batch 1 has two forms with the same arithmetic in the same order: 11
+//    consumer warps, or 15 at 128 registers a thread (WIDE; Q4_K lanes then
+//    hold half a super-block in registers at a time) for calls with more
+//    items a CTA than 11 warps, and for every Q6_K call.
+//  * Pair mode (SwiGLU): an item holds gate rows and their up rows, and the
+//    team sums become silu(g)*u.  Experts mode: each CTA takes part of one
+//    assignment's rows, reading the expert id from device memory first.
 // Every wait is bounded; a wait that runs out records QK_ERR_TIMEOUT in the
 // device error word and the kernel leaves without touching the rest of y.
 #pragma once
