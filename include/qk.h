@@ -28,10 +28,10 @@
  * Row addressing: `w` points at the first byte of the whole tensor, and a call
  * uses rows [row_offset, row_offset + rows).  Row r starts at byte
  * r * row_bytes with row_bytes = blocks_per_row * block_bytes.  This is how
- * the parts of a fused tensor are addressed ("a weight here is a device
- * pointer plus a row count, so the parts are row ranges inside the uploaded
- * tensor", nurllama README, "What it runs", phi3), and how one expert of a
- * 3-D expert tensor [E][rows_e][K] is addressed: row_offset = e*rows_e + r0.
+ * the parts of a fused tensor are addressed (in nurllama too a weight is a
+ * device pointer with a row count and the parts of a fused tensor are ranges
+ * of its rows: nurllama README, "What it runs", phi3), and how one expert of
+ * a 3-D expert tensor [E][rows_e][K] is addressed: row_offset = e*rows_e + r0.
  *
  * Ownership and execution: every pointer is a device pointer owned by the
  * caller; the library allocates and frees nothing per call and keeps no
@@ -104,8 +104,8 @@ int qmatvec_q4_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
 /*
  * Q6_K GEMV, batch 1..8.  Same contract as qmatvec_q8_0 (w 2-byte aligned:
  * 210-byte super-blocks).  Q6_K is the format of lm_head / ffn_down in the
- * Q4_K_M files people download ("in a Q4_K_M file output.weight is Q4_K or
- * Q6_K", nx_f32_llm_v4.nx source, lm_head binder comment; kernel `mv_q6_k`,
+ * Q4_K_M files people download (their output weight is Q4_K or Q6_K:
+ * nx_f32_llm_v4.nx source, lm_head binder comment; kernel `mv_q6_k`,
  * nurllama 0.18.1 API reference, kernels.nu).  Block reading (GGUF):
  * ql[128] | qh[64] | scales[16] int8 | fp16 d per 256 weights; weight i of
  * half n = i/128 (cc = i%128, t = cc/32, l = cc%32) takes its low 4 bits
@@ -146,9 +146,9 @@ int qmatvec_swiglu_q6_k(const void *w, int64_t gate_offset, int64_t up_offset, i
 /*
  * Batched expert GEMV over n_assign expert assignments:
  *   y[a*ldy + r] = sum_{c<K} W[expert_ids[a]*rows + r][c] * x[(a / xk)*K + c]
- * for a < n_assign and r < rows.  "One batched matvec over all n_assign
- * expert assignments.  Output row a uses expert expid_dev[a] and input row
- * a/xk of x" (nurllama 0.18.1 API reference, kernels.nu
+ * for a < n_assign and r < rows: nurllama's batched expert matvec, one call
+ * for every assignment, output row a taken from expert expid_dev[a] with
+ * input row a/xk (nurllama 0.18.1 API reference, kernels.nu
  * `lk_matvec_experts`); the experts of a projection live in one 3-D tensor
  * [n_experts][rows][K] evaluated as row ranges (nurllama README, "What it
  * runs", llada2).
@@ -195,8 +195,8 @@ int qgemm_q4_k(const void *w, int64_t row_offset, int64_t N, int64_t K, const fl
 
 /*
  * Accumulating form of qgemm_q4_k: y[m*ldy + n] += sum_k bf16(W[row_offset+n][k]) * bf16(x[m*K + k]),
- * the "acc" mode of loom's prefill GEMMs ("Modes: store, acc, swiglu",
- * loom-port-llm SKILL.md, "What the starter generates", gen_gemm.py): the
+ * the acc mode of loom's prefill GEMMs (they come in store, acc and swiglu
+ * modes: loom-port-llm SKILL.md, "What the starter generates", gen_gemm.py): the
  * product lands on what y holds (e.g. the residual stream).  Same arguments,
  * errors and bound as qgemm_q4_k, plus one fp32 rounding of the final add.
  */

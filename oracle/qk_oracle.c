@@ -333,8 +333,8 @@ int qko_gemm_bf16(int fmt, const uint8_t *wq, int64_t K, const int64_t *rows, in
 }
 
 /*
- * The SwiGLU form of the bf16 prefill GEMM (loom's gen_gemm.py "modes:
- * store, acc, swiglu", loom-port-llm SKILL.md, "What the starter
+ * The SwiGLU form of the bf16 prefill GEMM (the swiglu mode beside store and
+ * acc in loom's gen_gemm.py, loom-port-llm SKILL.md, "What the starter
  * generates"): g and u are the bf16 references of qko_gemm_bf16 for the gate
  * and up rows, h = silu(g) * u in f64 (layout [M][n]).
  */
@@ -353,8 +353,8 @@ int qko_swiglu_gemm_bf16(int fmt, const uint8_t *wq, int64_t K, const int64_t *g
 /* ---------------------------------------------------------------- quantisers */
 
 /*
- * Q8_0 encoder for round-trip checks ("Q8_0 error bounds", nurllama README,
- * "How it is checked").  Per 32-weight block: d = fp16(amax / 127),
+ * Q8_0 encoder for round-trip checks (the nurllama README checks Q8_0
+ * against its error bounds, "How it is checked").  Per 32-weight block: d = fp16(amax / 127),
  * q = clamp(round_half_even(w / d), -127, 127); an all-zero block gets
  * d = 0 and q = 0.  Columns >= K are encoded as zero.
  */
