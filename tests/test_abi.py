@@ -281,3 +281,24 @@ def test_binding_row_bytes_match_the_library(lib):
         assert qk._fmt_row_bytes("q8_0", K) == lib.qk_row_bytes_q8_0(K)
         assert qk._fmt_row_bytes("q4_k", K) == lib.qk_row_bytes_q4_k(K)
         assert qk._fmt_row_bytes("q6_k", K) == lib.qk_row_bytes_q6_k(K)
+
+
+def test_header_compiles_as_c99_and_the_library_answers_from_c(lib, tmp_path):
+    """A plain C client (tests/c_abi_check.c) builds against include/qk.h with
+    strict C99 warnings as errors, links libqk.so and sees the documented
+    statuses; every compute call there fails validation, so nothing launches."""
+    import shutil
+    import subprocess
+    from quantised_gguf_weight_gb300 import qk
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(qk.library_path())
+    exe = str(tmp_path / "c_abi_check")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_check.c"), "-o", exe, "-L", libdir, "-lqk",
+                    "-Wl,-rpath," + libdir], check=True, capture_output=True, text=True)
+    env = {k: v for k, v in os.environ.items() if k != "QK_STRICT"}
+    r = subprocess.run([exe], env=env, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("failures 0")
