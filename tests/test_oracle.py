@@ -207,6 +207,56 @@ def test_q4_k_roundtrip_bound(orc):
     assert np.sqrt(np.mean((wh - w) ** 2)) < 0.15 * np.std(w)
 
 
+def test_q4_k_unit_scales_reduce_to_plain_nibbles(orc):
+    """dmin = 0 and every 6-bit scale 1: a Q4_K super-block is d times its 4-bit
+    quants, sub-block 2c in the low nibbles of qs[32c..32c+31] and 2c+1 in the
+    high nibbles, whatever the (unused) mins hold."""
+    rng = np.random.default_rng(21)
+    nb = 6
+    rec = np.zeros(nb, dtype=synth.Q4_K_DTYPE)
+    rec["d"] = rng.uniform(0.01, 2.0, nb).astype(np.float16)
+    rec["dmin"] = 0.0
+    sc = np.zeros((nb, 12), np.uint8)
+    sc[:, 0:4] = 1                                          # sc of sub-blocks 0..3, top bits 0
+    sc[:, 4:8] = rng.integers(0, 256, (nb, 4))              # mins of 0..3 and top bits of mins 4..7
+    sc[:, 8:12] = 1 | (rng.integers(0, 16, (nb, 4)) << 4)   # sc of 4..7 = 1, mins of 4..7 above
+    rec["scales"] = sc
+    rec["qs"] = rng.integers(0, 256, (nb, 128))
+    W = orc.decode("q4_k", rec.view(np.uint8).reshape(-1), 3 * 256)     # 2 rows of 3 super-blocks
+    qs = rec["qs"].reshape(nb, 4, 32).astype(np.float64)
+    expect = np.empty((nb, 256))
+    for c in range(4):
+        expect[:, 64 * c:64 * c + 32] = np.mod(qs[:, c], 16)
+        expect[:, 64 * c + 32:64 * c + 64] = np.floor(qs[:, c] / 16)
+    expect *= rec["d"].astype(np.float64)[:, None]
+    assert np.array_equal(W.reshape(nb, 256), expect)
+
+
+def test_q8_0_requantise_reproduces_the_bytes(orc):
+    """A Q8_0 block whose largest |q| is 127 re-encodes to exactly its own
+    bytes: amax/127 gives back d and w/d gives back every q."""
+    K = 320
+    rec = synth.weights("q8_0", 5, K, seed=22).view(synth.Q8_0_DTYPE).copy()
+    rec["d"] = np.where(rec["d"] == 0, np.float16(1.0), rec["d"])
+    rec["qs"][:, 7] = np.where(np.arange(len(rec)) % 2 == 0, 127, -127)
+    raw = rec.view(np.uint8).reshape(-1)
+    back = orc.quantise("q8_0", orc.decode("q8_0", raw, K))
+    assert np.array_equal(back, raw)
+
+
+def test_q4_k_bytes_per_weight_give_the_page_intensity(orc):
+    """144 bytes per 256 weights is 0.5625 B a weight; 2 flop a weight over
+    that is the ~3.55 flop/B the nx_f32_llm_v4.nx source gives for Q4 (3.556
+    cut to two decimals), and a second row starts 144 bytes later."""
+    assert orc.row_bytes("q4_k", 256) == 144
+    assert orc.row_bytes("q4_k", 4096) / 4096 == 0.5625
+    assert int(2 / 0.5625 * 100) == 355
+    raw = synth.weights("q4_k", 2, 256, seed=23)
+    both = orc.decode("q4_k", raw, 256)
+    assert np.array_equal(both[1], orc.decode("q4_k", raw[144:], 256)[0])
+    assert not np.array_equal(both[0], both[1])
+
+
 def test_q4_k_requantise_is_fixed_point_for_probes(orc):
     """Decoding the hand-derived constant block, re-encoding and decoding again
     gives the same weights (the encoder reproduces exactly representable rows)."""
