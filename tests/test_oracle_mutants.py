@@ -47,6 +47,9 @@ MUTATIONS = {
                                "int rc = qko_gemv(fmt, wq, K, gate_rows, n, x, M, g, sg);"),
     "silu_missing_z": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
     "swiglu_gemm_gate_up_swapped": ("i < M * n; ++i) h[i] = silu(g[i]) * u[i];", "i < M * n; ++i) h[i] = silu(u[i]) * g[i];"),
+    "q4_row_stride": ("return ((K + 255) / 256) * 144;\n}", "return ((K + 255) / 256) * 128;\n}"),
+    "q8_encode_divisor": ("qko_f64_to_fp16(amax / 127.0);", "qko_f64_to_fp16(amax / 128.0);"),
+    "q4_sc_low_mask": ("*sc = scales[j] & 63;", "*sc = scales[j] & 31;"),
 }
 
 PINS = [
@@ -71,6 +74,9 @@ PINS = [
     (pins.test_experts_select_expert_and_input_row, {"xk": 2}),
     (pins.test_swiglu_gemm_reference_rounds_to_bf16, {}),
     (pins.test_swiglu_gemm_reference_on_bf16_exact_inputs, {}),
+    (pins.test_q4_k_unit_scales_reduce_to_plain_nibbles, {}),
+    (pins.test_q8_0_requantise_reproduces_the_bytes, {}),
+    (pins.test_q4_k_bytes_per_weight_give_the_page_intensity, {}),
 ]
 
 
