@@ -81,6 +81,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: every rank of the group gets the maximum of
+    `ms` (dist None: a single process)."""
+    if dist is None:
+        return ms
+    import torch
+    tt = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_gbs(world: int, step_bytes: int, ms_step: float) -> float:
+    """Whole-job throughput: every rank runs one replica of the step, so the
+    job moves world * step_bytes in the slowest rank's step time."""
+    return world * step_bytes / (ms_step * 1e-3) / 1e9
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -267,14 +284,10 @@ def measure_ours(args, torch, qk, synth, device, rank, world):
         t1 = time.time()
         if dist:
             dist.barrier()
-    ms = start.elapsed_time(end)
-    if dist:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, device)
     clocks = summarise_clocks(sampler.samples(), t0, t1)
     ms_step = ms / args.steps
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, ms_step)
 
     # per-launch durations of the dominant kernel: each distinct call of a
     # layer is captured as a graph of one launch per layer weight set, the

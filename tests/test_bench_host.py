@@ -23,3 +23,52 @@ def test_traffic_entry_is_keyed_by_the_code_fingerprint():
     ent = d["gemv_q4_k_b1"]
     assert len(ent["source_fingerprint"]) == 16
     assert ent["dram_bytes_per_launch_avg"] > 0
+
+
+def _rank_main(rank, world, port, ms_of_rank, out_dir):
+    import os
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(ms_of_rank[rank], dist, torch.device("cpu"))
+        with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+            f.write(repr(got))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_two_ranks_report_the_slowest_rank_and_the_whole_job(tmp_path):
+    """world_size 2 over gloo: both ranks see the slower rank's time, and the
+    whole-job figure counts both replicas' bytes in that time."""
+    import torch.multiprocessing as mp
+    ms_of_rank = [3.25, 5.5]
+    mp.start_processes(_rank_main, args=(2, _free_port(), ms_of_rank, str(tmp_path)), nprocs=2,
+                       start_method="spawn")
+    got = [float(open(tmp_path / f"rank{r}.txt").read()) for r in range(2)]
+    assert got == [5.5, 5.5]
+    step_bytes = 3934781440
+    assert bench.whole_job_gbs(2, step_bytes, 5.5) == 2 * bench.whole_job_gbs(1, step_bytes, 5.5)
+    assert abs(bench.whole_job_gbs(1, step_bytes, 1.0) - step_bytes / 1e6) < 1e-6
+
+
+def test_single_process_time_is_its_own():
+    assert bench.max_over_ranks(4.0, None, None) == 4.0
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
+    """Under torchrun only rank 0 runs the oracle arm; the others return 0 at once."""
+    import argparse
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    assert bench.run_reference(argparse.Namespace(steps=1, warmup=3)) == 0
