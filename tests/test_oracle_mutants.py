@@ -6,7 +6,6 @@ operand, a wrong rounding), compiles it and runs the pins of test_oracle.py
 against it.  At least one pin has to fail for every planted mistake.  The
 oracle source itself is never modified.
 """
-import os
 import subprocess
 
 import pytest
