@@ -134,6 +134,7 @@ class ClockSampler:
         self.period_ms = period_ms
         self.proc = None
         self.file = None
+        self._rows = None
 
     def __enter__(self):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -154,29 +155,41 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-        self.file.flush()
+        self.file.close()
 
     def samples(self):
-        rows = []
-        try:
-            with open(self.file.name) as f:
-                for line in f:
-                    parts = [p.strip() for p in line.split(",")]
-                    if len(parts) < 9:
-                        continue
-                    try:
-                        ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                        frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                        rows.append({"t": ts + frac, "sm": float(parts[1]), "max": float(parts[2]),
-                                     "reasons": parts[4:9]})
-                    except (ValueError, IndexError):
-                        continue
-        finally:
+        """The parsed samples (read once; the temporary file is removed then)."""
+        if self._rows is None:
             try:
-                os.unlink(self.file.name)
+                with open(self.file.name) as f:
+                    self._rows = parse_clock_lines(f)
             except OSError:
-                pass
-        return rows
+                self._rows = []
+            finally:
+                try:
+                    os.unlink(self.file.name)
+                except OSError:
+                    pass
+        return self._rows
+
+
+def parse_clock_lines(lines):
+    """Rows of `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits`
+    as {"t": seconds, "sm": MHz, "max": MHz, "reasons": [active mask, hw_slowdown,
+    hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap]}; malformed lines are skipped."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            rows.append({"t": ts + frac, "sm": float(parts[1]), "max": float(parts[2]),
+                         "reasons": parts[4:9]})
+        except (ValueError, IndexError):
+            continue
+    return rows
 
 
 def summarise_clocks(samples, t0, t1):

@@ -72,3 +72,32 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("LOCAL_RANK", "1")
     assert bench.run_reference(argparse.Namespace(steps=1, warmup=3)) == 0
+
+
+CLOCK_LINES = [
+    "2026/12/02 22:30:01.100, 2070, 2070, 900.50, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+    "2026/12/02 22:30:01.300, 1965, 2070, 1395.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+    "garbage line\n",
+    "2026/12/02 22:30:01.500, 2070, 2070, 1010.00, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+    "2026/12/02 22:30:09.000, 1200, 2070, 300.00, 0x0000000000000008, Active, Not Active, Not Active, Not Active\n",
+]
+
+
+def test_clock_lines_parse_and_summarise_over_the_timed_window():
+    rows = bench.parse_clock_lines(CLOCK_LINES)
+    assert len(rows) == 4                                   # the malformed line is skipped
+    assert [r["sm"] for r in rows] == [2070.0, 1965.0, 2070.0, 1200.0]
+    t0, t1 = rows[0]["t"], rows[2]["t"]
+    assert abs((t1 - t0) - 0.4) < 1e-6
+    s = bench.summarise_clocks(rows, t0, t1)
+    # the slowdown sample lies outside the timed window; the power cap inside it is kept
+    assert s["samples"] == 3 and s["window"] == "timed region"
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    whole = bench.summarise_clocks(rows, rows[0]["t"], rows[3]["t"])
+    assert whole["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_clock_summary_without_nvidia_smi():
+    s = bench.summarise_clocks([], 0.0, 1.0)
+    assert s["samples"] == 0 and s["sm_mhz"] is None
