@@ -101,3 +101,31 @@ def test_clock_lines_parse_and_summarise_over_the_timed_window():
 def test_clock_summary_without_nvidia_smi():
     s = bench.summarise_clocks([], 0.0, 1.0)
     assert s["samples"] == 0 and s["sm_mhz"] is None
+
+
+def test_clock_sampler_reads_a_running_sampler(tmp_path, monkeypatch):
+    """ClockSampler end to end against a stand-in `nvidia-smi` on PATH that
+    prints one sample line every 50 ms until it is stopped."""
+    import os
+    import sys
+    import time
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text(
+        "#!" + sys.executable + "\n"
+        "import sys, time\n"
+        "while True:\n"
+        "    t = time.time()\n"
+        "    stamp = time.strftime('%Y/%m/%d %H:%M:%S', time.localtime(t)) + '.%03d' % int((t % 1) * 1000)\n"
+        "    print(stamp + ', 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active', flush=True)\n"
+        "    time.sleep(0.05)\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ.get("PATH", ""))
+    s = bench.ClockSampler(0)
+    with s:
+        t0 = time.time()
+        time.sleep(0.4)
+        t1 = time.time()
+    rows = s.samples()
+    assert len(rows) >= 4 and s.samples() is rows
+    summary = bench.summarise_clocks(rows, t0, t1)
+    assert summary["sm_mhz"] == 2070.0 and summary["reasons"] == [] and summary["samples"] >= 3
