@@ -728,6 +728,19 @@ def run_only(args, torch, qk, synth, device):
 
 # ---------------------------------------------------------------------- main
 
+def result_line(r, ws: int, args, cpu) -> dict:
+    """The JSON line of this arm from the measurements `r` of measure_ours."""
+    return {
+        "metric": METRIC, "value": round(r["value"], 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(),
+        "tok_s_equiv": round(ws * 1e3 / r["ms_per_step"], 1),
+        "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+        "gpu_launches": r["gpu_launches"], "clocks": r["clocks"], "other_configs": r["extra"],
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -782,16 +795,7 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(r["value"], 1), "unit": "GB/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": workload_config(),
-            "tok_s_equiv": round(ws * 1e3 / r["ms_per_step"], 1),
-            "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
-            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"], "other_configs": r["extra"],
-        }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(result_line(r, ws, args, cpu)), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()

@@ -129,3 +129,52 @@ def test_clock_sampler_reads_a_running_sampler(tmp_path, monkeypatch):
     assert len(rows) >= 4 and s.samples() is rows
     summary = bench.summarise_clocks(rows, t0, t1)
     assert summary["sm_mhz"] == 2070.0 and summary["reasons"] == [] and summary["samples"] >= 3
+
+
+def test_result_line_carries_every_contract_key():
+    import argparse
+    import json
+    r = {"value": 3500.04, "ms_per_step": 1.12207, "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
+         "roofline": {"bound": "hbm", "achieved": 3338.0, "peak": 6800.0, "unit": "GB/s", "frac": 0.4909,
+                      "traffic": 30754176.0},
+         "e2e": {"value": 3443.3, "unit": "GB/s", "h2d_bytes_per_step": 73728, "d2h_bytes_per_step": 16384},
+         "gpu_launches": 128000, "extra": {}}
+    cpu = {"value": 0.81, "unit": "GB/s", "cores": 16, "kind": "oracle", "sample": "…"}
+    line = json.loads(json.dumps(bench.result_line(r, 1, argparse.Namespace(steps=1000, warmup=20), cpu)))
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+              "gpu_launches", "clocks"):
+        assert k in line, k
+    assert line["n_gpus"] == 1 and line["steps"] == 1000 and line["warmup"] == 20
+    assert line["higher_is_better"] is True and line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["data"] == "synthetic" and "workload" in line["config"]
+    assert not any(k in line["config"] for k in ("model", "global_batch", "seq_len"))
+    assert set(line["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
+    assert set(line["e2e"]) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+    assert set(line["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """The oracle arm on rank 0 prints one line with impl, the contract keys, a
+    cpu_baseline describing the run and an e2e without transfers (the oracle
+    samples are stubbed here: 1 GB in 2 s a step)."""
+    import argparse
+    import json
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    calls = []
+
+    def fake_run(orc, synth, frac, threads, seed=2):
+        calls.append(frac)
+        return 1e9, 2.0
+    monkeypatch.setattr(bench, "oracle_sample_run", fake_run)
+    assert bench.run_reference(argparse.Namespace(steps=4, warmup=3)) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] == 0.5 and line["unit"] == "GB/s"
+    assert line["ms_per_step"] == 2000.0 and line["steps"] == 4 and line["warmup"] == 3
+    assert len(calls) == 1 + 3 + 4                          # calibration, warm-up, timed steps
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1 and line["cpu_baseline"]["sample"]
+    assert line["e2e"] == {"value": 0.5, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["metric"] == bench.METRIC and line["config"] == bench.workload_config()
