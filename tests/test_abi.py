@@ -302,3 +302,20 @@ def test_header_compiles_as_c99_and_the_library_answers_from_c(lib, tmp_path):
     r = subprocess.run([exe], env=env, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("failures 0")
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built CUDA library there is no fallback: loading it raises."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, sys.argv[1]); "
+            "from quantised_gguf_weight_gb300 import qk\n"
+            "try:\n"
+            "    qk.load(sys.argv[2])\n"
+            "except RuntimeError as e:\n"
+            "    print('refused:', e)\n"
+            "else:\n"
+            "    print('loaded')\n")
+    r = subprocess.run([sys.executable, "-c", code, ROOT, str(tmp_path / "libqk.so")], capture_output=True,
+                       text=True, check=True)
+    assert r.stdout.startswith("refused:") and "not built" in r.stdout
