@@ -36,6 +36,9 @@
  *     a super-block takes 4 low bits from ql and 2 high bits from qh (see
  *     qko_decode_q6_k_row), w = d * scales[i/16] * (q - 32).
  *   A row is ceil(K/QK) whole blocks; columns >= K are ignored.
+ *   Parity unpinned: these layouts against real GGUF files (none is at hand).
+ *   They are pinned only by single-field probes written by hand from the
+ *   layouts above (tests/golden/*_probes.txt).
  *
  * The fp16 and bf16 conversions are written from the IEEE 754 encodings.
  * Compile with -O2 and without -ffast-math.
