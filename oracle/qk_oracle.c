@@ -38,7 +38,7 @@
  *   A row is ceil(K/QK) whole blocks; columns >= K are ignored.
  *   Parity unpinned: these layouts against real GGUF files (none is at hand).
  *   They are pinned only by single-field probes written by hand from the
- *   layouts above (tests/golden/*_probes.txt).
+ *   layouts above (the probe files under tests/golden).
  *
  * The fp16 and bf16 conversions are written from the IEEE 754 encodings.
  * Compile with -O2 and without -ffast-math.
