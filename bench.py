@@ -46,6 +46,8 @@ LAYER = [
     ("ffn_gate_up", 28672, 4096, [(0, 28672)]),
     ("ffn_down", 4096, 14336, [(0, 4096)]),
 ]
+# the same layer with attn_qkv issued as its three output row ranges (q, k, v)
+QKV_RANGES = [(0, 4096), (4096, 1024), (5120, 1024)]
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -235,10 +237,12 @@ class LayerSetWorkload:
         self.lib = qk.load()
         self.bytes_per_layer = layer_bytes()
 
-    def launch_layer(self, li: int, stream_handle: int, on_launch=None):
+    def launch_layer(self, li: int, stream_handle: int, on_launch=None, qkv_ranges: bool = False):
         t = self.sets[li % len(self.sets)]
         fn = self.lib.qmatvec_q4_k
         for name, rows, K, calls in LAYER:
+            if qkv_ranges and name == "attn_qkv":
+                calls = QKV_RANGES
             w = t[name].data_ptr()
             x = self.x[K].data_ptr()
             ybuf = self.y[name]
@@ -251,9 +255,9 @@ class LayerSetWorkload:
                 if on_launch:
                     on_launch(1, name, n, K)
 
-    def launch_step(self, stream_handle: int, first_layer: int = 0):
+    def launch_step(self, stream_handle: int, first_layer: int = 0, qkv_ranges: bool = False):
         for l in range(LAYERS_PER_TOKEN):
-            self.launch_layer(first_layer + l, stream_handle)
+            self.launch_layer(first_layer + l, stream_handle, qkv_ranges=qkv_ranges)
 
 
 def measure_ours(args, torch, qk, synth, device, rank, world):
@@ -302,20 +306,26 @@ def measure_ours(args, torch, qk, synth, device, rank, world):
     value = whole_job_gbs(world, step_bytes, ms_step)
 
     # per-launch durations of the dominant kernel: each distinct call of a
-    # layer is captured as a graph of one launch per layer weight set, the
-    # graph is replayed back to back, CUDA events on the launching stream
+    # layer is timed on row ranges of one tensor holding enough copies of its
+    # weights to fill twice the L2 (so every call's bytes come from HBM),
+    # captured as a graph of one launch per copy and replayed back to back,
+    # CUDA events on the launching stream
     per_call = {}
     tot_b = tot_ms = 0.0
-    for name, rows, K, calls in LAYER:
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20) or (128 << 20)
+    for ti, (name, rows, K, calls) in enumerate(LAYER):
+        rb = q4k_row_bytes(K)
         for off, n in calls:
+            copies = max(DISTINCT_LAYER_SETS, math.ceil(2 * l2 / (n * rb)) + 1)
+            big = torch.from_numpy(synth.weights("q4_k", n * copies, K, seed=7, stream0=10 * ti)).to(device)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 csh = torch.cuda.current_stream().cuda_stream
-                for l in range(DISTINCT_LAYER_SETS):
-                    st = wl.lib.qmatvec_q4_k(wl.sets[l][name].data_ptr(), off, n, K, wl.x[K].data_ptr(), 1,
+                for c in range(copies):
+                    st = wl.lib.qmatvec_q4_k(big.data_ptr(), c * n, n, K, wl.x[K].data_ptr(), 1,
                                              wl.y[name].data_ptr() + 4 * off, rows, csh)
                     assert st == 0
-            reps = 20
+            reps = 10
             with torch.cuda.stream(stream):
                 g.replay()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -324,16 +334,16 @@ def measure_ours(args, torch, qk, synth, device, rank, world):
                     g.replay()
                 e1.record(stream)
             torch.cuda.synchronize()
-            dt = e0.elapsed_time(e1) / (reps * DISTINCT_LAYER_SETS)
-            b = call_bytes(q4k_row_bytes(K), n, K, 1)
+            dt = e0.elapsed_time(e1) / (reps * copies)
+            b = call_bytes(rb, n, K, 1)
             key = f"{name}[{n}x{K}]"
             if key not in per_call:
                 per_call[key] = {"bytes": b, "avg_us": round(dt * 1e3, 2), "GB/s": round(b / (dt * 1e-3) / 1e9, 1),
-                                 "launches_per_layer": 0}
+                                 "launches_per_layer": 0, "copies_rotated": copies}
             per_call[key]["launches_per_layer"] += 1
             tot_b += b
             tot_ms += dt
-            del g
+            del g, big
     achieved = tot_b / (tot_ms * 1e-3) / 1e9
     peaks = read_peaks()
     hbm, hbm_src = peak_hbm(peaks)
@@ -341,16 +351,45 @@ def measure_ours(args, torch, qk, synth, device, rank, world):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic,
                 "kernel": "gemv_kernel<Q4_K, batch 1>: the four launches of a layer, each timed as "
-                          "back-to-back graph replays",
+                          "back-to-back graph replays over weight copies filling twice the L2",
                 "peak_source": f"{hbm_src} HBM copy bandwidth",
                 "frac_of_8TBs_nominal": round(achieved / 8000.0, 4),
+                "step_frac": round(value / world / hbm, 4),
+                "step_frac_note": "the whole decode step's algorithmic bytes / its time (value per GPU) "
+                                  "over the same peak",
                 "per_call": per_call}
+
+    # the same step with attn_qkv as three row-range calls (q, k, v): 160 launches
+    g3 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g3, stream=stream):
+        wl.launch_step(torch.cuda.current_stream().cuda_stream, qkv_ranges=True)
+    torch.cuda.synchronize()
+    n3 = max(5, min(args.steps, 100))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g3.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n3):
+            g3.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms3 = e0.elapsed_time(e1) / n3
+    step3_bytes = LAYERS_PER_TOKEN * sum(call_bytes(q4k_row_bytes(K), n, K, 1)
+                                         for name, _, K, calls in LAYER
+                                         for _, n in (QKV_RANGES if name == "attn_qkv" else calls))
+    qkv_ranges_row = {"GB/s": round(step3_bytes / (ms3 * 1e-3) / 1e9, 1), "ms_per_step": round(ms3, 5),
+                      "launches_per_step": LAYERS_PER_TOKEN * (launches_per_layer() + len(QKV_RANGES) - 1),
+                      "bytes_per_step": step3_bytes, "steps": n3,
+                      "computes": "the headline step with attn_qkv issued as its q/k/v output row ranges "
+                                  "4096/1024/1024 (three calls) instead of one fused call"}
+    del g3
 
     # e2e: the same step through the C ABI from pinned host buffers
     e2e = measure_e2e(args, torch, wl, stream, step_bytes, world)
-    extra = {}
+    extra = {"llama8b_decode_step_qkv_as_3_range_calls": qkv_ranges_row}
     if not args.no_extra:
-        extra = measure_extra_rows(torch, qk, synth, device, stream)
+        extra.update(measure_extra_rows(torch, qk, synth, device, stream))
     del graph
     return {
         "value": value, "ms_per_step": ms_step, "clocks": clocks, "roofline": roofline, "e2e": e2e,
@@ -677,9 +716,10 @@ def run_reference(args):
 
 def workload_config():
     return {"workload": "llama8b_q4_k_decode_token_gemvs",
-            "description": "batch-1 Q4_K GEMVs of 32 Llama-8B-shaped layers per step: fused attn_qkv "
-                           "6144x4096 (q/k/v = output row ranges 4096/1024/1024), attn_output 4096x4096, "
-                           "fused ffn gate+up 28672x4096, ffn_down 4096x14336",
+            "description": "batch-1 Q4_K GEMVs of 32 Llama-8B-shaped layers per step, four calls a layer: "
+                           "attn_qkv 6144x4096 as one fused call (its q/k/v are the output row ranges "
+                           "4096/1024/1024; the step with three range calls is timed in other_configs), "
+                           "attn_output 4096x4096, fused ffn gate+up 28672x4096, ffn_down 4096x14336",
             "weights": "Q4_K (144-byte super-blocks)", "activations": "fp32 N(0,1)", "batch": 1,
             "layers_per_step": LAYERS_PER_TOKEN, "distinct_layer_weight_sets": DISTINCT_LAYER_SETS,
             "bytes_per_step": layer_bytes() * LAYERS_PER_TOKEN,

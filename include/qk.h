@@ -88,8 +88,28 @@ typedef enum {
  *          (each batch row's result is the same as in a call of that size).
  *          A K for which one activation row does not fit (above about 48000
  *          on GB300) returns QK_ERR_TOO_LARGE before any launch.
- * Arithmetic is fp32; results differ from the exact dot by at most
- * 1e-5 * sum|w*x| + 1e-6 per element (the tests check this bound).
+ * Accuracy (every GEMV entry point; the tests check these bounds).  The
+ * arithmetic is fp32 and a result differs from the exact dot product by at
+ * most 1e-5 * S + 1e-6 + A, per element, where
+ *   S = sum_c |x[b][c]| * (the magnitudes of the terms the weight is made
+ *       of): |w| for Q8_0, |d*sc*q| + |dmin*m| for Q4_K and
+ *       |d*scale*q| + 32*|d*scale| for Q6_K.  The kernels sum a Q4_K or Q6_K
+ *       weight's two terms separately, so this is sum|w*x| unless the terms
+ *       of the weights nearly cancel (then S is the larger);
+ *   A = 0 at batch 2..8.  Batch 1 holds each 32-column group of x as 24-bit
+ *       integers that share one binary exponent: that of the group's largest
+ *       magnitude or, when the largest is at least 2^3 times (in binary
+ *       exponent) every other value of the group, that of the second largest,
+ *       the largest value then being carried exactly on its own.  A value of
+ *       x is thus held within 2^-20 times the second largest magnitude of
+ *       its group (the largest within 2^-22 of itself), and
+ *       A = 2^-20 * sum_groups (second largest |x| of the group) *
+ *                   (sum |w| over the group's columns).
+ *       A single outlier per group, at any magnitude, therefore costs
+ *       nothing, and A is far inside 1e-5 * S unless a row's weights sit
+ *       mostly on values much smaller than their group's second largest
+ *       (for instance two values 2^20 times the rest in one group, meeting
+ *       zero weights).  NaN and infinities in x give non-finite results.
  */
 int qmatvec_q8_0(const void *w, int64_t row_offset, int64_t rows, int64_t K,
                  const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);
@@ -132,8 +152,8 @@ int qmatvec_q6_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
  *   gate_offset, up_offset  first gate / up row (>= 0), in rows of K columns.
  *   x            device fp32 [batch][K];  h  device fp32 [batch][ldh], ldh == 0
  *                means ldh = F; only h[b*ldh + p] for p < F is written.
- * g and u are computed exactly as the plain GEMV's rows (same error bound,
- * 1e-5 * sum|w*x| + 1e-6 each); silu uses CUDA's expf.  Errors: as the plain
+ * g and u are computed exactly as the plain GEMV's rows (each within the
+ * plain GEMV's accuracy bound, see qmatvec_q8_0); silu uses CUDA's expf.  Errors: as the plain
  * GEMV; a negative up_offset is QK_ERR_BAD_DIM.
  */
 int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
@@ -162,7 +182,7 @@ int qmatvec_swiglu_q6_k(const void *w, int64_t gate_offset, int64_t up_offset, i
  *   y           device fp32 [n_assign][ldy], ldy == 0 means ldy = rows.
  * An id outside [0, n_experts) is not dereferenced: that assignment's rows
  * are set to NaN and qk_device_error() reports QK_ERR_BAD_INDEX.  Error
- * bound as the plain GEMV (1e-5 * sum|w*x| + 1e-6).
+ * bound as the plain GEMV at batch 1 (see qmatvec_q8_0).
  */
 int qmatvec_experts_q8_0(const void *w, int64_t n_experts, int64_t rows, int64_t K, const float *x, int xk,
                          const int32_t *expert_ids, int64_t n_assign, float *y, int64_t ldy, qk_stream_t stream);

@@ -253,6 +253,16 @@ def gemv_threaded(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, rows, threads
     return y, s
 
 
+def gemm_bf16_threaded(fmt: str, wq: np.ndarray, K: int, x: np.ndarray, rows, threads: int, lib=None):
+    """gemm_bf16 on `threads` host threads over contiguous row bands (same
+    code and order per output as the serial call)."""
+    rows = _rows_arg(rows)
+    bands = np.array_split(rows, max(1, threads))
+    with ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+        parts = list(ex.map(lambda b: gemm_bf16(fmt, wq, K, x, b, lib=lib), bands))
+    return np.concatenate([p[0] for p in parts], axis=1), np.concatenate([p[1] for p in parts], axis=1)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))

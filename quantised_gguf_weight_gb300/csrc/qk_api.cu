@@ -33,17 +33,23 @@ int strict_from_env()
 }
 std::atomic<int> g_strict_blocks{strict_from_env()};
 
+// Device address of the error word per device, looked up once; host threads
+// that make their first call on a device at the same time may both look it
+// up, and store the same address.
+std::atomic<int *> g_error_word_addr[64];
+
 int *error_word_ptr()
 {
-    static int *cache[64] = {nullptr};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
+    int *cached = g_error_word_addr[dev].load(std::memory_order_acquire);
+    if (!cached) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_qk_error_word) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<int *>(p);
+        cached = static_cast<int *>(p);
+        g_error_word_addr[dev].store(cached, std::memory_order_release);
     }
-    return cache[dev];
+    return cached;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -121,23 +127,45 @@ size_t qgemm_q4_k_workspace_bytes(int64_t M, int64_t N, int64_t K)
 
 namespace {
 
-int gemm_entry(int fmt, const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
-               int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream, int mode,
-               int64_t up_offset)
+}  // namespace
+
+namespace qk {
+// Argument checks of every prefill GEMM entry point, in the order of their
+// statuses; the workspace is checked by the caller (between the alignment
+// and size checks), so the same checks serve the workspace-free entry point.
+int gemm_check_args(int fmt, const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+                    const float *y, int64_t *ldy, int64_t up_offset, const void *workspace, size_t workspace_bytes,
+                    bool check_workspace, int64_t *row_bytes)
 {
     if (!w || !x || !y) return QK_ERR_NULL;
     if (N <= 0 || K <= 0 || M <= 0 || row_offset < 0 || up_offset < 0) return QK_ERR_BAD_DIM;
-    if (ldy == 0) ldy = N;
-    if (ldy < N) return QK_ERR_BAD_DIM;
-    if (qk::strict_blocks_reject(fmt, K)) return QK_ERR_BAD_DIM;
-    if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < qk::gemm_workspace_bytes(M, K))
+    if (*ldy == 0) *ldy = N;
+    if (*ldy < N) return QK_ERR_BAD_DIM;
+    if (strict_blocks_reject(fmt, K)) return QK_ERR_BAD_DIM;
+    if (!aligned(w, fmt == kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
+    if (check_workspace &&
+        (!workspace || !aligned(workspace, 256) || workspace_bytes < gemm_workspace_bytes(M, K)))
         return QK_ERR_WORKSPACE;
     // tensor-map limits: at most 2^31 tokens and rows per call
     const int64_t last = row_offset > up_offset ? row_offset : up_offset;
     if (M > (1LL << 31) - 1 || K > (1LL << 31) - 1 || last > (1LL << 31) - 1 - N) return QK_ERR_TOO_LARGE;
-    const int64_t row_bytes = fmt == qk::kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
-    if (last > (INT64_MAX / row_bytes) - N) return QK_ERR_BAD_DIM;
+    *row_bytes = fmt == kFmtQ4K ? ((K + 255) / 256) * 144 : ((K + 31) / 32) * 34;
+    if (last > (INT64_MAX / *row_bytes) - N) return QK_ERR_BAD_DIM;
+    return QK_OK;
+}
+int library_gemm_skip_chunk() { return g_gemm_skip_chunk.load(); }
+}  // namespace qk
+
+namespace {
+
+int gemm_entry(int fmt, const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+               int64_t ldy, void *workspace, size_t workspace_bytes, qk_stream_t stream, int mode,
+               int64_t up_offset)
+{
+    int64_t row_bytes = 0;
+    const int st = qk::gemm_check_args(fmt, w, row_offset, N, K, x, M, y, &ldy, up_offset, workspace,
+                                       workspace_bytes, true, &row_bytes);
+    if (st != QK_OK) return st;
     int *err = error_word_ptr();
     if (!err) return QK_ERR_CUDA;
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * row_bytes;

@@ -71,6 +71,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same test with a suspend-time hint: the thread may sleep (without
+// taking issue slots) until the phase completes or about hint_ns pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait (sleeping between tests) until the phase with the given parity has
+// completed, for at most limit_ns of wall-clock time.  Returns false if the
+// limit ran out.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    const uint64_t deadline = globaltimer_ns() + limit_ns;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (globaltimer_ns() > deadline) return false;
+    }
+}
+
 // Wait until the phase with the given parity has completed, for at most
 // limit_ns of wall-clock time.  Returns false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
@@ -198,6 +226,29 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
     int d;
     asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
+}
+
+// ---------------------------------------------------------------- sub-warp reductions
+// redux.sync over the lanes named in `mask` (every lane of the mask executes
+// the same instruction with the same mask; disjoint groups of a warp may
+// reduce at once, each with its own mask).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t mask, uint32_t v)
+{
+    uint32_t r;
+    asm volatile("redux.sync.max.u32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(mask));
+    return r;
+}
+__device__ __forceinline__ uint32_t redux_add_u32(uint32_t mask, uint32_t v)
+{
+    uint32_t r;
+    asm volatile("redux.sync.add.u32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(mask));
+    return r;
+}
+__device__ __forceinline__ int redux_add_s32(uint32_t mask, int v)
+{
+    int r;
+    asm volatile("redux.sync.add.s32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(mask));
+    return r;
 }
 
 __device__ __forceinline__ void record_error(int *err, int bit)

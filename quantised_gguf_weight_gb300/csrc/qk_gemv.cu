@@ -61,11 +61,15 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     const int64_t xsum_bytes = fmt == kFmtQ4K   ? round_up(static_cast<int64_t>(batch) * 4 * XU * 4, 128)
                                : fmt == kFmtQ6K ? (batch == 1 ? round_up(static_cast<int64_t>(8) * XU * 4, 128) : 0)
                                                 : 0;
+    // batch 1: per 32-column group its scale, and its outlier's value and
+    // column (8 bytes)
     const int64_t xscale_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 4, 128) : 0;
+    const int64_t xout_bytes = batch == 1 ? round_up(static_cast<int64_t>(UC / 32) * XU * 8, 128) : 0;
     const int64_t off_x = kGemvBarBytes;
     const int64_t off_xsum = off_x + x_bytes;
     const int64_t off_xscale = off_xsum + xsum_bytes;
-    const int64_t off_stage = off_xscale + xscale_bytes;
+    const int64_t off_xout = off_xscale + xscale_bytes;
+    const int64_t off_stage = off_xout + xout_bytes;
     const int64_t budget = di.smem_optin;
     if (off_stage >= budget) return false;
 
@@ -150,6 +154,7 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     p->off_x = static_cast<int>(off_x);
     p->off_xsum = static_cast<int>(off_xsum);
     p->off_xscale = static_cast<int>(off_xscale);
+    p->off_xout = static_cast<int>(off_xout);
     p->off_stage = static_cast<int>(off_stage);
     p->smem = static_cast<int>(off_stage + stages * stage);
     p->grid = static_cast<int>(grid);
@@ -222,6 +227,7 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.off_x = p.off_x;
     r.off_xsum = p.off_xsum;
     r.off_xscale = p.off_xscale;
+    r.off_xout = p.off_xout;
     r.off_stage = p.off_stage;
     r.pair = p.pair;
     r.up_rows = up_rows;

@@ -108,7 +108,7 @@ struct GemvArgs {
     int nw;             // consumer warps that get row groups (<= the launched ones)
     int m;              // stages per consumer warp (stage w*m + t%m holds warp w's item t)
     int stage_bytes;
-    int off_x, off_xsum, off_xscale, off_stage;
+    int off_x, off_xsum, off_xscale, off_xout, off_stage;
     int pair;           // 1: output row p = silu(row p) * row (p + up_rows), both rows in one item
     int64_t up_rows;    // pair mode: distance in rows from a gate row to its up row
     int up_stage_off;   // pair mode, whole rows: stage offset of the up rows' span
@@ -142,107 +142,157 @@ __host__ __device__ constexpr int gemv_cpl_max(int fmt, int batch)
 
 // -------------------------------------------------------------------------- Q4_K, batch 1
 //
-// One super-block of R rows from registers: hd = bytes 0..15 (d, dmin,
-// scales[12]), qs = bytes 16..143.  x: block-floating-point byte planes of
-// the two 128-column halves, float4 group g of half h at xa_h + 16g; per
-// 32-column group j the plain sum is xsum_h[j] and the plane scale
-// 2^(E-21) is xsc_h[j].
-// The high nibbles are used in place (byte & 0xF0 = 16 q), which is folded
-// into their sub-block scale as d/16 (exact: a power of two).
-template <int R>
-__device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
-                                             const uint8_t *xa0, const uint8_t *xa1, const float *xsum0,
-                                             const float *xsum1, const float *xsc0, const float *xsc1,
-                                             float (&acc)[R][1])
+// Byte i (0..31) of the 32 bytes held in a (bytes 0..15) and b (16..31),
+// selected without indexing registers.
+__device__ __forceinline__ uint32_t byte_of32(const uint4 &a, const uint4 &b, int i)
 {
-    float d[R], dmin[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        d[r] = half_bits_to_float(hd[r].x);
-        dmin[r] = half_bits_to_float(hd[r].x >> 16);
+    const int wi = i >> 2;
+    uint32_t w = a.x;
+    w = wi == 1 ? a.y : w;
+    w = wi == 2 ? a.z : w;
+    w = wi == 3 ? a.w : w;
+    w = wi == 4 ? b.x : w;
+    w = wi == 5 ? b.y : w;
+    w = wi == 6 ? b.z : w;
+    w = wi == 7 ? b.w : w;
+    return (w >> (8 * (i & 3))) & 0xFFu;
+}
+
+// d*sc and -dmin*m of sub-block 4H + j from a super-block's first 16 bytes
+// hd: the 6-bit field placed in a float's mantissa is 2^23 + v, and one FMA
+// against the matching offset gives the exact product.  For odd j the scale
+// is d/16*sc, since those weights are used as 16 q (the high nibbles in place).
+template <int H>
+__device__ __forceinline__ void q4k_scales(const uint4 &hd, float d, float dmin, float (&ds)[4], float (&dmn)[4])
+{
+    uint32_t scw, mw;
+    if (H == 0) {
+        scw = hd.y & 0x3F3F3F3Fu;
+        mw = hd.z & 0x3F3F3F3Fu;
+    } else {
+        scw = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+        mw = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
     }
+    const float dlo = d, dhi = d * 0.0625f;
+    const float clo = dlo * -kTwo23, chi = dhi * -kTwo23, cm = dmin * kTwo23;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (h == 1 && !has_hi) break;
-        const uint8_t *xa = h ? xa1 : xa0;
-        const float4 xsum4 = *reinterpret_cast<const float4 *>(h ? xsum1 : xsum0);
-        const float4 xsc4 = *reinterpret_cast<const float4 *>(h ? xsc1 : xsc0);
-        // d*sc and -dmin*m of the four sub-blocks 4h..4h+3: the 6-bit field
-        // placed in a float's mantissa is 2^23 + v, and one FMA against the
-        // matching offset gives the exact product
-        float ds[R][4], dmn[R][4];
+    for (int j = 0; j < 4; ++j) {
+        const float fs = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j));
+        const float fm = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j));
+        ds[j] = (j & 1) ? fmaf(dhi, fs, chi) : fmaf(dlo, fs, clo);
+        dmn[j] = fmaf(-dmin, fm, cm);
+    }
+}
+
+// One 128-column half H of a super-block of R rows from registers:
+// hd = bytes 0..15 (d, dmin, scales[12]); qs[r][Q0 + 2lc + p] holds bytes
+// 16p..16p+15 of the half's 32-byte quant chunk lc (its low nibbles are
+// sub-block 4H + 2lc, its high nibbles sub-block 4H + 2lc + 1).  x:
+// block-floating-point byte planes of the half, float4 group g at xa + 16g;
+// per 32-column group j the plain sum is xsum_h[j] and the plane scale
+// 2^(E-21) is |xsc_h[j]|.  A negative xsc_h[j] marks a group whose outlier
+// (value xo_h[2j], column xo_h[2j+1] as int bits) is in neither the planes
+// nor the plain sum: its weight d*sc*q - dmin*m (one rounding) times its
+// value is added once the half's plane terms are in.  The high nibbles are
+// used in place (byte & 0xF0 = 16 q), which is folded into their sub-block
+// scale as d/16 (exact: a power of two).
+template <int R, int H, int N, int Q0>
+__device__ __forceinline__ void q4k_half(const float (&d)[R], const float (&dmin)[R], const uint4 (&hd)[R],
+                                         const uint4 (&qs)[R][N], const uint8_t *xa, const float *xsum_h,
+                                         const float *xsc_h, const float *xo_h, float (&acc)[R][1])
+{
+    const float4 xsum4 = *reinterpret_cast<const float4 *>(xsum_h);
+    const float4 xsc4 = *reinterpret_cast<const float4 *>(xsc_h);
+    float ds[R][4], dmn[R][4];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            uint32_t scw, mw;
-            if (h == 0) {
-                scw = hd[r].y & 0x3F3F3F3Fu;
-                mw = hd[r].z & 0x3F3F3F3Fu;
-            } else {
-                scw = (hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u);
-                mw = ((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u);
-            }
-            const float dlo = d[r], dhi = d[r] * 0.0625f;
-            const float clo = dlo * -kTwo23, chi = dhi * -kTwo23, cm = dmin[r] * kTwo23;
+    for (int r = 0; r < R; ++r) q4k_scales<H>(hd[r], d[r], dmin[r], ds[r], dmn[r]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float fs = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j));
-                const float fm = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j));
-                ds[r][j] = (j & 1) ? fmaf(dhi, fs, chi) : fmaf(dlo, fs, clo);
-                dmn[r][j] = fmaf(-dmin[r], fm, cm);
-            }
-        }
+    for (int lc = 0; lc < 2; ++lc) {
+        int sl[R][3], sh[R][3];
 #pragma unroll
-        for (int lc = 0; lc < 2; ++lc) {
-            int sl[R][3], sh[R][3];
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+            for (int k = 0; k < 3; ++k) sl[r][k] = sh[r][k] = 0;
 #pragma unroll
-                for (int k = 0; k < 3; ++k) sl[r][k] = sh[r][k] = 0;
+        for (int p = 0; p < 2; ++p) {
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
+            for (int k = 0; k < 4; ++k) {
+                const int g_lo = 16 * lc + 4 * p + k;
+                const uint4 xl = *reinterpret_cast<const uint4 *>(xa + 16 * g_lo);
+                const uint4 xh = *reinterpret_cast<const uint4 *>(xa + 16 * (g_lo + 8));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int g_lo = 16 * lc + 4 * p + k;
-                    const uint4 xl = *reinterpret_cast<const uint4 *>(xa + 16 * g_lo);
-                    const uint4 xh = *reinterpret_cast<const uint4 *>(xa + 16 * (g_lo + 8));
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint4 q = qs[r][4 * h + 2 * lc + p];
-                        const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
-                        const uint32_t L = wd & 0x0F0F0F0Fu;   // q of sub-block 2lc
-                        const uint32_t H = wd & 0xF0F0F0F0u;   // 16 q of sub-block 2lc+1
-                        sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
-                        sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
-                        sl[r][2] = dp4a_us(L, xl.z, sl[r][2]);
-                        sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
-                        sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
-                        sh[r][2] = dp4a_us(H, xh.z, sh[r][2]);
-                    }
+                for (int r = 0; r < R; ++r) {
+                    const uint4 q = qs[r][Q0 + 2 * lc + p];
+                    const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+                    const uint32_t L = wd & 0x0F0F0F0Fu;   // q of sub-block 2lc
+                    const uint32_t Hn = wd & 0xF0F0F0F0u;  // 16 q of sub-block 2lc+1
+                    sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
+                    sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
+                    sl[r][2] = dp4a_us(L, xl.z, sl[r][2]);
+                    sh[r][0] = dp4a_uu(Hn, xh.x, sh[r][0]);
+                    sh[r][1] = dp4a_uu(Hn, xh.y, sh[r][1]);
+                    sh[r][2] = dp4a_us(Hn, xh.z, sh[r][2]);
                 }
             }
-            const float X0 = lc ? xsum4.z : xsum4.x, X1 = lc ? xsum4.w : xsum4.y;
-            const float S0 = lc ? xsc4.z : xsc4.x, S1 = lc ? xsc4.w : xsc4.y;
+        }
+        const float X0 = lc ? xsum4.z : xsum4.x, X1 = lc ? xsum4.w : xsum4.y;
+        const float S0 = fabsf(lc ? xsc4.z : xsc4.x), S1 = fabsf(lc ? xsc4.w : xsc4.y);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2]);
+            const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2]);
+            float t = acc[r][0];
+            t = fmaf(ds[r][2 * lc] * S0, F0, t);
+            t = fmaf(dmn[r][2 * lc], X0, t);
+            t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
+            t = fmaf(dmn[r][2 * lc + 1], X1, t);
+            acc[r][0] = t;
+        }
+    }
+    // the outliers of the half's groups (rare: a sign bit of a group scale)
+    if ((__float_as_uint(xsc4.x) | __float_as_uint(xsc4.y) | __float_as_uint(xsc4.z) | __float_as_uint(xsc4.w)) >>
+        31) {
+        const float sc4[4] = {xsc4.x, xsc4.y, xsc4.z, xsc4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!(sc4[j] < 0.f)) continue;
+            const float xv = xo_h[2 * j];
+            const int i = __float_as_int(xo_h[2 * j + 1]);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2]);
-                const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2]);
-                float t = acc[r][0];
-                t = fmaf(ds[r][2 * lc] * S0, F0, t);
-                t = fmaf(dmn[r][2 * lc], X0, t);
-                t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
-                t = fmaf(dmn[r][2 * lc + 1], X1, t);
-                acc[r][0] = t;
+                float dsr[4], dmr[4];
+                q4k_scales<H>(hd[r], d[r], dmin[r], dsr, dmr);
+                const uint32_t byte = byte_of32(qs[r][Q0 + 2 * (j >> 1)], qs[r][Q0 + 2 * (j >> 1) + 1], i);
+                const float q = static_cast<float>(byte & ((j & 1) ? 0xF0u : 0x0Fu));
+                acc[r][0] = fmaf(fmaf(dsr[j], q, dmr[j]), xv, acc[r][0]);
             }
         }
     }
 }
 
-// The same for one 128-column half H of the super-block, its 64 quant bytes
-// in qs (the wide batch-1 form).  Accumulates in the same order as
-// q4k_sb_dig: half 0, then half 1.
-template <int R, int H>
-__device__ __forceinline__ void q4k_half_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][4],
-                                             const uint8_t *xa, const float *xsum_h, const float *xsc_h,
+// A whole super-block of R rows (qs = its 128 quant bytes): half 0, then
+// half 1 when the row has columns there.
+template <int R>
+__device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
+                                           const uint8_t *xa0, const uint8_t *xa1, const float *xsum0,
+                                           const float *xsum1, const float *xsc0, const float *xsc1,
+                                           const float *xo0, const float *xo1, float (&acc)[R][1])
+{
+    float d[R], dmin[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        d[r] = half_bits_to_float(hd[r].x);
+        dmin[r] = half_bits_to_float(hd[r].x >> 16);
+    }
+    q4k_half<R, 0, 8, 0>(d, dmin, hd, qs, xa0, xsum0, xsc0, xo0, acc);
+    if (has_hi) q4k_half<R, 1, 8, 4>(d, dmin, hd, qs, xa1, xsum1, xsc1, xo1, acc);
+}
+
+// One half HH of the super-block, its 64 quant bytes in qs (the wide
+// batch-1 form); the same arithmetic in the same order as q4k_sb_dig.
+template <int R, int HH>
+__device__ __forceinline__ void q4k_half_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][4], const uint8_t *xa,
+                                             const float *xsum_h, const float *xsc_h, const float *xo_h,
                                              float (&acc)[R][1])
 {
     float d[R], dmin[R];
@@ -251,78 +301,7 @@ __device__ __forceinline__ void q4k_half_dig(const uint4 (&hd)[R], const uint4 (
         d[r] = half_bits_to_float(hd[r].x);
         dmin[r] = half_bits_to_float(hd[r].x >> 16);
     }
-    {
-        constexpr int h = H;
-        const float4 xsum4 = *reinterpret_cast<const float4 *>(xsum_h);
-        const float4 xsc4 = *reinterpret_cast<const float4 *>(xsc_h);
-        // d*sc and -dmin*m of the four sub-blocks 4h..4h+3: the 6-bit field
-        // placed in a float's mantissa is 2^23 + v, and one FMA against the
-        // matching offset gives the exact product
-        float ds[R][4], dmn[R][4];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            uint32_t scw, mw;
-            if (h == 0) {
-                scw = hd[r].y & 0x3F3F3F3Fu;
-                mw = hd[r].z & 0x3F3F3F3Fu;
-            } else {
-                scw = (hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u);
-                mw = ((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u);
-            }
-            const float dlo = d[r], dhi = d[r] * 0.0625f;
-            const float clo = dlo * -kTwo23, chi = dhi * -kTwo23, cm = dmin[r] * kTwo23;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float fs = __uint_as_float(__byte_perm(scw, kMagic, 0x7440u + j));
-                const float fm = __uint_as_float(__byte_perm(mw, kMagic, 0x7440u + j));
-                ds[r][j] = (j & 1) ? fmaf(dhi, fs, chi) : fmaf(dlo, fs, clo);
-                dmn[r][j] = fmaf(-dmin[r], fm, cm);
-            }
-        }
-#pragma unroll
-        for (int lc = 0; lc < 2; ++lc) {
-            int sl[R][3], sh[R][3];
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int k = 0; k < 3; ++k) sl[r][k] = sh[r][k] = 0;
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int g_lo = 16 * lc + 4 * p + k;
-                    const uint4 xl = *reinterpret_cast<const uint4 *>(xa + 16 * g_lo);
-                    const uint4 xh = *reinterpret_cast<const uint4 *>(xa + 16 * (g_lo + 8));
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint4 q = qs[r][2 * lc + p];
-                        const uint32_t wd = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
-                        const uint32_t L = wd & 0x0F0F0F0Fu;   // q of sub-block 2lc
-                        const uint32_t H = wd & 0xF0F0F0F0u;   // 16 q of sub-block 2lc+1
-                        sl[r][0] = dp4a_uu(L, xl.x, sl[r][0]);
-                        sl[r][1] = dp4a_uu(L, xl.y, sl[r][1]);
-                        sl[r][2] = dp4a_us(L, xl.z, sl[r][2]);
-                        sh[r][0] = dp4a_uu(H, xh.x, sh[r][0]);
-                        sh[r][1] = dp4a_uu(H, xh.y, sh[r][1]);
-                        sh[r][2] = dp4a_us(H, xh.z, sh[r][2]);
-                    }
-                }
-            }
-            const float X0 = lc ? xsum4.z : xsum4.x, X1 = lc ? xsum4.w : xsum4.y;
-            const float S0 = lc ? xsc4.z : xsc4.x, S1 = lc ? xsc4.w : xsc4.y;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float F0 = planes_to_float(sl[r][0], sl[r][1], sl[r][2]);
-                const float F1 = planes_to_float(sh[r][0], sh[r][1], sh[r][2]);
-                float t = acc[r][0];
-                t = fmaf(ds[r][2 * lc] * S0, F0, t);
-                t = fmaf(dmn[r][2 * lc], X0, t);
-                t = fmaf(ds[r][2 * lc + 1] * S1, F1, t);
-                t = fmaf(dmn[r][2 * lc + 1], X1, t);
-                acc[r][0] = t;
-            }
-        }
-    }
+    q4k_half<R, HH, 4, 0>(d, dmin, hd, qs, xa, xsum_h, xsc_h, xo_h, acc);
 }
 
 // -------------------------------------------------------------------------- Q4_K, batch >= 2
@@ -445,10 +424,12 @@ __device__ __forceinline__ void q8_realign(const uint32_t (&wv)[R][9], const uin
 }
 
 // Batch 1: block-floating-point planes of the block's 32 columns, float4
-// group k at xa + 16k.
+// group k at xa + 16k, plane scale |xscale|; a negative xscale marks an
+// outlier (value xo[0], column xo[1] as int bits) that is not in the planes
+// and is added exactly after the plane term.
 template <int R>
 __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], const uint8_t *xa,
-                                            float xscale, float (&acc)[R][1])
+                                            float xscale, const float *xo, float (&acc)[R][1])
 {
     float d[R];
     uint32_t qw[R][8];
@@ -469,9 +450,21 @@ __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uin
             sp[r][2] = dp4a_ss(v, xv.z, sp[r][2]);
         }
     }
+    const float S = fabsf(xscale);
 #pragma unroll
     for (int r = 0; r < R; ++r)
-        acc[r][0] = fmaf(d[r] * xscale, planes_to_float(sp[r][0], sp[r][1], sp[r][2]), acc[r][0]);
+        acc[r][0] = fmaf(d[r] * S, planes_to_float(sp[r][0], sp[r][1], sp[r][2]), acc[r][0]);
+    if (xscale < 0.f) {
+        const float xv = xo[0];
+        const int i = __float_as_int(xo[1]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint4 qa = make_uint4(qw[r][0], qw[r][1], qw[r][2], qw[r][3]);
+            const uint4 qb = make_uint4(qw[r][4], qw[r][5], qw[r][6], qw[r][7]);
+            const float q = static_cast<float>(static_cast<int8_t>(byte_of32(qa, qb, i)));
+            acc[r][0] = fmaf(d[r] * q, xv, acc[r][0]);
+        }
+    }
 }
 
 // Batch >= 2: int8 quants through the magic-exponent trick (bias 128), fp32 x
@@ -583,9 +576,13 @@ __device__ __forceinline__ float q6_dscale(const Q6Half &h, float d, int j)
 // Batch 1: block-floating-point planes of the half's 128 columns (float4
 // group g at xa + 16g); per 16-column sub-block j the plain sum x16[j] (for
 // the -32 offset) and per 32-column group the plane scale xsc[j/2].
+// |xsc[j]| is the plane scale of 32-column group j; a negative xsc[j] marks
+// an outlier of the group (value xo[2j], column xo[2j+1] as int bits) that is
+// in neither the planes nor the 16-column sums: its whole term
+// d*scale*(q - 32)*x is added after the group's plane terms.
 template <int R>
 __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_t *xa, const float *x16,
-                                             const float *xsc, float (&acc)[R][1])
+                                             const float *xsc, const float *xo, float (&acc)[R][1])
 {
     float d[R];
 #pragma unroll
@@ -616,8 +613,15 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
                 sp[r][h][2] = dp4a_us(q, xv.z, sp[r][h][2]);
             }
         }
-        const float S = xscv[t];
+        const float S = fabsf(xscv[t]);
         const float X0 = x16v[2 * t], X1 = x16v[2 * t + 1];
+        const bool ot = xscv[t] < 0.f;
+        float xv = 0.f;
+        int i = 0;
+        if (ot) {
+            xv = xo[2 * t];
+            i = __float_as_int(xo[2 * t + 1]);
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float ds0 = q6_dscale(hr[r], d[r], 2 * t), ds1 = q6_dscale(hr[r], d[r], 2 * t + 1);
@@ -626,6 +630,15 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
             a = fmaf(ds0 * -32.0f, X0, a);
             a = fmaf(ds1 * S, planes_to_float(sp[r][1][0], sp[r][1][1], sp[r][1][2]), a);
             a = fmaf(ds1 * -32.0f, X1, a);
+            if (ot) {
+                // the group's outlier: d*scale*(q - 32) times its value
+                const int ko = (i >> 2) & 7;
+                uint32_t quad = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) quad = k == ko ? q6_quad(hr[r], t, k) : quad;
+                const float q = static_cast<float>((quad >> (8 * (i & 3))) & 0xFFu);
+                a = fmaf(((i >> 4) ? ds1 : ds0) * (q - 32.0f), xv, a);
+            }
             acc[r][0] = a;
         }
     }
@@ -700,16 +713,9 @@ __device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t
 // interleaved.  Batch 1 stores block-floating-point byte planes (one
 // exponent per 32 columns; a NaN or infinity in a group makes its scale
 // NaN), batch >= 2 fp32 pre-multiplied by 2^-s for the Q4_K nibble position.
-__device__ __forceinline__ float fmax_nan(float a, float b)
-{
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
 template <int FMT, int B, int NTH>
 __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint32_t cwarp, uint32_t lane,
-                                        uint32_t xs_addr, float *xsum, float *xscale)
+                                        uint32_t xs_addr, float *xsum, float *xscale, float *xout)
 {
     constexpr uint32_t UC = FMT == kFmtQ80 ? 32 : 128;
     constexpr uint32_t G = UC / 4;          // float4 groups of a unit (a power of two)
@@ -768,48 +774,109 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint
             }
             // plain sums: per float4, then over 4 lanes (16 columns) and 8 (32)
             float sum[UNR], sum16[UNR];
+            auto plain_sums = [&](const float4 (&w)[UNR]) {
 #pragma unroll
-            for (uint32_t i = 0; i < UNR; ++i) sum[i] = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-            if constexpr (FMT != kFmtQ80) {
+                for (uint32_t i = 0; i < UNR; ++i) sum[i] = (w[i].x + w[i].y) + (w[i].z + w[i].w);
+                if constexpr (FMT != kFmtQ80) {
 #pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 1);
+                    for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 1);
 #pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 2);
+                    for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 2);
 #pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) sum16[i] = sum[i];
-                if constexpr (FMT == kFmtQ4K) {
+                    for (uint32_t i = 0; i < UNR; ++i) sum16[i] = sum[i];
+                    if constexpr (FMT == kFmtQ4K) {
 #pragma unroll
-                    for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 4);
+                        for (uint32_t i = 0; i < UNR; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], 4);
+                    }
                 }
-            }
+            };
             if constexpr (B == 1) {
-                float amax[UNR];
+                // Per 32-column group (its 8 lanes): e1, the largest biased
+                // exponent (a shuffle-max tree), and the plain sum (Q4_K: 32
+                // columns, Q6_K: its 16-column halves).  An outlier is the
+                // only value of the group with exponent >= e1 - 2 (so it is
+                // at least 2^3 times every other value): two ballots count,
+                // per group, the lanes holding one or more such values.  Only
+                // a warp that holds an outlier redoes both reductions with it
+                // left out; the group's exponent is then that of the largest
+                // other value, and the outlier is kept exactly on the side.
+                uint32_t eb[UNR][4], e1[UNR];
+                float F[UNR];
 #pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i)
-                    amax[i] = fmax_nan(fmax_nan(fabsf(v[i].x), fabsf(v[i].y)), fmax_nan(fabsf(v[i].z), fabsf(v[i].w)));
+                for (uint32_t i = 0; i < UNR; ++i) {
+                    eb[i][0] = (__float_as_uint(v[i].x) >> 23) & 255u;
+                    eb[i][1] = (__float_as_uint(v[i].y) >> 23) & 255u;
+                    eb[i][2] = (__float_as_uint(v[i].z) >> 23) & 255u;
+                    eb[i][3] = (__float_as_uint(v[i].w) >> 23) & 255u;
+                    e1[i] = max(max(eb[i][0], eb[i][1]), max(eb[i][2], eb[i][3]));
+                    F[i] = (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                }
+                auto reduce = [&](uint32_t (&e)[UNR], float (&f)[UNR]) {
 #pragma unroll
-                for (int o = 1; o <= 4; o <<= 1)
+                    for (int o = 1; o <= 4; o <<= 1)
 #pragma unroll
-                    for (uint32_t i = 0; i < UNR; ++i) amax[i] = fmax_nan(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], o));
+                        for (uint32_t i = 0; i < UNR; ++i) {
+                            e[i] = max(e[i], __shfl_xor_sync(0xFFFFFFFFu, e[i], o));
+                            if (FMT == kFmtQ4K || (FMT == kFmtQ6K && o < 4))
+                                f[i] += __shfl_xor_sync(0xFFFFFFFFu, f[i], o);
+                        }
+                };
+                reduce(e1, F);
+                int oslot[UNR];                                        // this lane's outlier column, -1 none
+                bool outl[UNR], anyo = false;
+#pragma unroll
+                for (uint32_t i = 0; i < UNR; ++i) {
+                    const uint32_t t = e1[i] - 2u;                     // e1 >= 2 whenever it matters below
+                    const uint32_t c = (eb[i][0] >= t) + (eb[i][1] >= t) + (eb[i][2] >= t) + (eb[i][3] >= t);
+                    const uint32_t g1 = (__ballot_sync(0xFFFFFFFFu, c >= 1u) >> (lane & 24u)) & 0xFFu;
+                    const uint32_t g2 = (__ballot_sync(0xFFFFFFFFu, c >= 2u) >> (lane & 24u)) & 0xFFu;
+                    outl[i] = e1[i] != 255u && e1[i] >= 2u && __popc(g1) == 1 && g2 == 0u;
+                    oslot[i] = !(outl[i] && c == 1u) ? -1
+                               : (eb[i][0] >= t ? 0 : (eb[i][1] >= t ? 1 : (eb[i][2] >= t ? 2 : 3)));
+                    anyo |= outl[i];
+                }
+                uint32_t eref[UNR];
+#pragma unroll
+                for (uint32_t i = 0; i < UNR; ++i) eref[i] = e1[i];
+                if (__any_sync(0xFFFFFFFFu, anyo)) {
+                    // the same reductions without the outlier (no change for a
+                    // group that has none)
+                    float Wv[UNR];
+#pragma unroll
+                    for (uint32_t i = 0; i < UNR; ++i) {
+                        const int k = oslot[i];
+                        eref[i] = max(max(k == 0 ? 0u : eb[i][0], k == 1 ? 0u : eb[i][1]),
+                                      max(k == 2 ? 0u : eb[i][2], k == 3 ? 0u : eb[i][3]));
+                        Wv[i] = ((k == 0 ? 0.f : v[i].x) + (k == 1 ? 0.f : v[i].y)) +
+                                ((k == 2 ? 0.f : v[i].z) + (k == 3 ? 0.f : v[i].w));
+                    }
+                    reduce(eref, Wv);
+#pragma unroll
+                    for (uint32_t i = 0; i < UNR; ++i) F[i] = Wv[i];
+                }
                 uint32_t pl[UNR][4];
                 float dn[UNR];
 #pragma unroll
                 for (uint32_t i = 0; i < UNR; ++i) {
-                    const int ebits = static_cast<int>((__float_as_uint(amax[i]) >> 23) & 255u);
-                    const uint32_t keep = ebits != 255 ? 0xFFFFFFFFu : 0u;   // a NaN or infinity: planes 0, scale NaN
-                    const int E = max(ebits - 127, -96);
+                    const bool finite = e1[i] != 255u;                 // a NaN or infinity: planes 0, scale NaN
+                    const int E = max(static_cast<int>(eref[i]) - 127, -96);
                     const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
-                    dn[i] = keep ? __int_as_float((106 + E) << 23) : __int_as_float(0x7FC00000);   // 2^(E-21)
+                    const float d21 = __int_as_float((106 + E) << 23);    // 2^(E-21)
+                    dn[i] = !finite ? __int_as_float(0x7FC00000) : (outl[i] ? -d21 : d21);   // sign bit: outlier
+                    if constexpr (FMT == kFmtQ4K) sum[i] = F[i];
+                    if constexpr (FMT == kFmtQ6K) sum16[i] = F[i];
                     // m = rint(x * 2^(21-E)), |m| <= 2^22: adding 1.5 * 2^23 in one
                     // fp32 FMA rounds the exact x * 2^(21-E) to the nearest
                     // integer (ties to even); the sum's bits minus those of
-                    // 1.5 * 2^23 are m
+                    // 1.5 * 2^23 are m.  The outlier's m is 0.
                     constexpr float kRound = 12582912.0f;
                     constexpr uint32_t kRoundBits = 0x4B400000u;
-                    const uint32_t m0 = (__float_as_uint(fmaf(v[i].x, up, kRound)) - kRoundBits) & keep;
-                    const uint32_t m1 = (__float_as_uint(fmaf(v[i].y, up, kRound)) - kRoundBits) & keep;
-                    const uint32_t m2 = (__float_as_uint(fmaf(v[i].z, up, kRound)) - kRoundBits) & keep;
-                    const uint32_t m3 = (__float_as_uint(fmaf(v[i].w, up, kRound)) - kRoundBits) & keep;
+                    const uint32_t keep = finite ? 0xFFFFFFFFu : 0u;
+                    const int os = oslot[i];
+                    const uint32_t m0 = (__float_as_uint(fmaf(v[i].x, up, kRound)) - kRoundBits) & (os == 0 ? 0u : keep);
+                    const uint32_t m1 = (__float_as_uint(fmaf(v[i].y, up, kRound)) - kRoundBits) & (os == 1 ? 0u : keep);
+                    const uint32_t m2 = (__float_as_uint(fmaf(v[i].z, up, kRound)) - kRoundBits) & (os == 2 ? 0u : keep);
+                    const uint32_t m3 = (__float_as_uint(fmaf(v[i].w, up, kRound)) - kRoundBits) & (os == 3 ? 0u : keep);
                     // byte-plane transpose: plane k holds byte k of the four columns
                     const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
                     const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
@@ -826,6 +893,13 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint
                         xscale[us[i] * NJ + grp] = dn[i];
                         if constexpr (FMT == kFmtQ4K) xsum[us[i] * 4 + grp] = sum[i];
                     }
+                    if (oslot[i] >= 0) {
+                        // the outlier's value and its column within the group
+                        const int k = oslot[i];
+                        const float xv = k == 0 ? v[i].x : (k == 1 ? v[i].y : (k == 2 ? v[i].z : v[i].w));
+                        xout[2 * (us[i] * NJ + grp)] = xv;
+                        xout[2 * (us[i] * NJ + grp) + 1] = __int_as_float(static_cast<int>(4 * (g[i] & 7u)) + k);
+                    }
                     if constexpr (FMT == kFmtQ6K)
                         if ((lane & 3) == 0) xsum[us[i] * 8 + (g[i] >> 2)] = sum16[i];
                     const uint32_t dst = xs_addr + 16u * (us[i] * SU + g[i]);
@@ -833,6 +907,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint
                                  ::"r"(dst), "r"(pl[i][0]), "r"(pl[i][1]), "r"(pl[i][2]), "r"(pl[i][3]) : "memory");
                 }
             } else {
+                plain_sums(v);
 #pragma unroll
                 for (uint32_t i = 0; i < UNR; ++i) {
                     float4 w = v[i];
@@ -991,7 +1066,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                 for (uint32_t c = 0; c < nkc; ++c, ++t) {
                     const uint32_t st = w * m + tm;
                     const uint32_t bar = bar_full + 8u * st;
-                    if (*abort_flag || (use > 0 && !mbar_wait(bar_empty + 8u * st, (use - 1) & 1u, a.wait_ns))) {
+                    if (*abort_flag || (use > 0 && !mbar_wait_sleep(bar_empty + 8u * st, (use - 1) & 1u, a.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -1031,13 +1106,15 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     const uint8_t *xs = smem + a.off_x;
     const float *xsum = reinterpret_cast<const float *>(smem + a.off_xsum);
     const float *xscale = reinterpret_cast<const float *>(smem + a.off_xscale);
+    const float *xout = reinterpret_cast<const float *>(smem + a.off_xout);
 
     // the weights do not depend on earlier kernels, x may: with programmatic
     // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
     stage_x<FMT, B, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
                              reinterpret_cast<float *>(smem + a.off_xsum),
-                             reinterpret_cast<float *>(smem + a.off_xscale));
+                             reinterpret_cast<float *>(smem + a.off_xscale),
+                             reinterpret_cast<float *>(smem + a.off_xout));
     named_bar_sync(1, 32 * NW);
     if (cwarp >= nw) return;
 
@@ -1056,7 +1133,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
             for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
         for (uint32_t c = 0; c < nkc; ++c) {
             const uint32_t st = st0 + tm;
-            bool ok = *abort_flag == 0 && mbar_wait(bar_full + 8u * st, par, a.wait_ns);
+            bool ok = mbar_wait_sleep(bar_full + 8u * st, par, a.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok);   // the warp leaves together or not at all
             if (!ok) {
                 if (lane == 0) {
@@ -1106,7 +1183,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
 #pragma unroll
                         for (int i = 0; i < 4; ++i) q4[r][i] = p[1 + i];
                     }
-                    q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, acc);
+                    q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, xout + 8 * lu,
+                                       acc);
                     if (has_hi) {
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
@@ -1120,7 +1198,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                 if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
                 if (valid && has_hi)
                     q4k_half_dig<R, 1>(hd, q4, xs + 16 * SU * (XH + lu), xsum + 4 * (XH + lu),
-                                       xscale + 4 * (XH + lu), acc);
+                                       xscale + 4 * (XH + lu), xout + 8 * (XH + lu), acc);
               } else {
                 uint4 hd[R], qs[R][8];
                 if (valid) {
@@ -1141,7 +1219,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                     const uint8_t *xa1 = xs + 16 * SU * (XH + lu);
                     if constexpr (B == 1)
                         q4k_sb_dig<R>(hd, qs, has_hi, xa0, xa1, xsum + 4 * lu, xsum + 4 * (XH + lu),
-                                      xscale + 4 * lu, xscale + 4 * (XH + lu), acc);
+                                      xscale + 4 * lu, xscale + 4 * (XH + lu), xout + 8 * lu,
+                                      xout + 8 * (XH + lu), acc);
                     else
                         q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, acc);
                 }
@@ -1160,7 +1239,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                 if (valid) {
                     const uint8_t *xa = xs + 16 * SU * lu0;
                     if constexpr (B == 1)
-                        q6k_half_dig<R>(hr, xa, xsum + 8 * lu0, xscale + 4 * lu0, acc);
+                        q6k_half_dig<R>(hr, xa, xsum + 8 * lu0, xscale + 4 * lu0, xout + 8 * lu0, acc);
                     else
                         q6k_half_fp<B, R>(hr, xa, acc);
                 }
@@ -1188,7 +1267,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                     if (i < cpl && lu < a.LU) {
                         const uint8_t *xa = xs + 16 * SU * lu;
                         if constexpr (B == 1)
-                            q8_blk_dig<R>(wv[i], off[i], xa, xscale[lu], acc);
+                            q8_blk_dig<R>(wv[i], off[i], xa, xscale[lu], xout + 2 * lu, acc);
                         else
                             q8_blk_fp<B, R>(wv[i], off[i], xa, acc);
                     }

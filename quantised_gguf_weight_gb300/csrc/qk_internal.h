@@ -15,7 +15,7 @@ struct GemvPlan {
     int U, LU, XU, SW, R, cpl, nkc, rows_w, chunk_bytes, row_stride;
     int nw, m, stages, stage_bytes, pair, up_stage_off, cpa;
     int wide;   // batch 1: the 16-warp form (Q4_K: a lane holds half a super-block at a time)
-    int off_x, off_xsum, off_xscale, off_stage, smem, grid;
+    int off_x, off_xsum, off_xscale, off_xout, off_stage, smem, grid;
     int64_t row_bytes;
 };
 
@@ -37,6 +37,14 @@ uint64_t library_wait_limit_ns();
 bool strict_blocks_reject(int fmt, int64_t K);
 
 int64_t gemm_k8(int64_t K);
+// The argument checks shared by the prefill GEMM entry points (a qk_status;
+// sets *ldy when it was 0 and *row_bytes); the workspace is checked only when
+// check_workspace is true.
+int gemm_check_args(int fmt, const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M,
+                    const float *y, int64_t *ldy, int64_t up_offset, const void *workspace, size_t workspace_bytes,
+                    bool check_workspace, int64_t *row_bytes);
+// The GEMM test hook's K chunk (-1: none).
+int library_gemm_skip_chunk();
 size_t gemm_workspace_bytes(int64_t M, int64_t K);
 // Prefill GEMM of format fmt (kFmtQ4K or kFmtQ80).  mode 0: y = x W^T,
 // 1: y += x W^T, 2: y = silu(x Wg^T) * (x Wu^T) with the up rows at

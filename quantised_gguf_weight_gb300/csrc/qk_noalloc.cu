@@ -17,6 +17,7 @@
 // call shares the one array; calls that overlap on the GPU (for instance on
 // two streams at once) race on it.  Nothing in it has to start at zero: the
 // bf16 pre-pass rewrites every byte the GEMM reads (padding included).
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -30,19 +31,19 @@ constexpr size_t kQkNoallocScratchBytes = QK_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_qk_noalloc_scratch[kQkNoallocScratchBytes];
 
 // Device address of the scratch array per device; nullptr until looked up.
-void *g_scratch_addr[64];
+// Host threads that make their first call on a device at the same time may
+// both look it up and store the same address.
+std::atomic<void *> g_scratch_addr[64];
 
 void *scratch_address(int dev)
 {
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_qk_noalloc_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = p;
+    void *cached = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!cached) {
+        if (cudaGetSymbolAddress(&cached, g_qk_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev].store(cached, std::memory_order_release);
     }
-    return g_scratch_addr[dev];
+    return cached;
 }
-
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
 
@@ -51,18 +52,13 @@ extern "C" {
 int qgemm_q4_k_noalloc(const void *w, int64_t row_offset, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                        int64_t ldy, qk_stream_t stream)
 {
-    if (!w || !x || !y) return QK_ERR_NULL;
-    if (N <= 0 || K <= 0 || M <= 0 || row_offset < 0) return QK_ERR_BAD_DIM;
-    if (ldy == 0) ldy = N;
-    if (ldy < N) return QK_ERR_BAD_DIM;
-    if (qk::strict_blocks_reject(qk::kFmtQ4K, K)) return QK_ERR_BAD_DIM;
-    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return QK_ERR_ALIGN;
+    // the same checks, in the same order, as qgemm_q4_k (no workspace)
+    int64_t row_bytes = 0;
+    const int st = qk::gemm_check_args(qk::kFmtQ4K, w, row_offset, N, K, x, M, y, &ldy, 0, nullptr, 0, false,
+                                       &row_bytes);
+    if (st != QK_OK) return st;
     // the bf16 copy of x has to fit in the fixed scratch array
-    if (M > (1LL << 31) - 1 || K > (1LL << 31) - 1 || qk::gemm_workspace_bytes(M, K) > kQkNoallocScratchBytes)
-        return QK_ERR_TOO_LARGE;
-    if (N > (1LL << 31) - 1) return QK_ERR_TOO_LARGE;
-    const int64_t row_bytes = ((K + 255) / 256) * 144;
-    if (row_offset > (INT64_MAX / row_bytes) - N) return QK_ERR_BAD_DIM;
+    if (qk::gemm_workspace_bytes(M, K) > kQkNoallocScratchBytes) return QK_ERR_TOO_LARGE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QK_ERR_CUDA;
     void *scratch = scratch_address(dev);
@@ -71,7 +67,8 @@ int qgemm_q4_k_noalloc(const void *w, int64_t row_offset, int64_t N, int64_t K, 
     const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * row_bytes;
     bool encode_failed = false;
     cudaError_t e = qk::gemm_q4k_launch(w_rows, N, K, x, M, y, ldy, scratch, reinterpret_cast<cudaStream_t>(stream),
-                                        err, qk::library_wait_limit_ns(), -1, &encode_failed);
+                                        err, qk::library_wait_limit_ns(), qk::library_gemm_skip_chunk(),
+                                        &encode_failed);
     if (encode_failed) return QK_ERR_CUDA;
     return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
 }

@@ -174,3 +174,69 @@ def pow2_scaled_blocks(raw: np.ndarray, fmt: str, exps: tuple[int, ...], seed: i
         e2 = np.asarray(exps)[randint(seed, 8, n, 0, len(exps) - 1)]
         rec["dmin"] = np.ldexp(1.0, e2).astype(np.float16)
     return out
+
+
+WIDE_RANGE_KINDS = ("group_outlier_2p20", "group_outlier_2p30", "group_tiny_2m30", "outlier_channels",
+                    "two_large_per_group", "subnormal", "mixed_subnormal")
+
+
+def wide_range_activations(batch: int, K: int, seed: int, kind: str, stream: int = 300):
+    """fp32 activations x[batch][K] of wide dynamic range, and the columns that hold the large values.
+
+    Every kind starts from N(0, 1) (or a constant 0.3 for group_outlier_2p20)
+    and places large or tiny values:
+
+    * group_outlier_2p20: every 32-column group is 0.3 except one column of
+      value 2^20 (the column drawn per group);
+    * group_outlier_2p30: one column per group is 2^30 times its N(0, 1) value;
+    * group_tiny_2m30: one column per group is 2^-30 times its N(0, 1) value;
+    * outlier_channels: 8 columns in 8 different groups (the same columns in
+      every batch row), each scaled by a factor drawn uniformly from [100, 1000];
+    * two_large_per_group: two columns per group are 2^20 times their value;
+    * subnormal: every value is N(0, 1) * 2^-140 (fp32 subnormals);
+    * mixed_subnormal: even 32-column groups are scaled to subnormals, odd
+      groups stay N(0, 1), and one value per odd group is replaced by 2^-130.
+
+    Returns (x, cols): cols[b] is the sorted array of the columns that carry
+    the large values in batch row b (empty for the tiny and subnormal kinds).
+    """
+    if kind not in WIDE_RANGE_KINDS:
+        raise ValueError(kind)
+    ng = (K + 31) // 32
+    x = normal(seed, stream, batch * K).reshape(batch, K)
+    cols = []
+    for b in range(batch):
+        pick_all = randint(seed, stream + 1 + 4 * b, ng, 0, 31) + 32 * np.arange(ng)
+        pick = pick_all[pick_all < K]
+        big = np.array([], np.int64)
+        if kind == "group_outlier_2p20":
+            x[b, :] = 0.3
+            x[b, pick] = 2.0 ** 20
+            big = pick
+        elif kind == "group_outlier_2p30":
+            x[b, pick] *= 2.0 ** 30
+            big = pick
+        elif kind == "group_tiny_2m30":
+            x[b, pick] *= 2.0 ** -30
+        elif kind == "outlier_channels":
+            # 8 channels (fewer when K has fewer groups), each in a group of its own
+            groups = np.argsort(uniform(seed, stream + 2, ng))[:min(8, ng)]
+            ch = np.sort(pick_all[groups])
+            ch = ch[ch < K]
+            x[b, ch] *= 100.0 + 900.0 * uniform(seed, stream + 3, ch.size)
+            big = ch
+        elif kind == "two_large_per_group":
+            second = randint(seed, stream + 2 + 4 * b, ng, 0, 30) + 32 * np.arange(ng)
+            second = np.where(second % 32 >= pick_all % 32, second + 1, second)
+            second = second[second < K]
+            big = np.unique(np.concatenate([pick, second]))
+            x[b, big] *= 2.0 ** 20
+        elif kind == "subnormal":
+            x[b, :] *= 2.0 ** -140
+        elif kind == "mixed_subnormal":
+            g = np.arange(K) // 32
+            x[b, g % 2 == 0] *= 2.0 ** -140
+            odd = pick[(pick // 32) % 2 == 1]
+            x[b, odd] = 2.0 ** -130
+        cols.append(np.sort(big))
+    return x.astype(np.float32), cols

@@ -83,15 +83,23 @@ def test_gemm_bf16_exact_inputs(qk, orc):
     assert np.array_equal(y, r1.astype(np.float32).astype(np.float64))
 
 
-def test_gemm_full_size_sampled(qk, orc):
-    """Llama-8B ffn_gate shape: M = 512 tokens, K = 4096, N = 14336, sampled rows."""
+def test_gemm_full_size(qk, orc):
+    """Llama-8B ffn_gate shape: M = 512 tokens, K = 4096, N = 14336, every output
+    against both references (the oracle on all host cores over row bands)."""
     M, K, N = 512, 4096, 14336
     wq = synth.weights("q4_k", N, K, seed=4)
     x = synth.activations(M, K, seed=4)
     y = run_gemm(qk, wq, 0, N, K, x)
-    rng = np.random.default_rng(4)
-    rows = np.unique(np.concatenate([rng.choice(N, 48, replace=False), [0, 127, 128, N - 1]]))
-    check(y[:, rows], orc, wq, K, x, rows, "512x4096x14336")
+    rows = np.arange(N)
+    r1, s1 = orc.gemv_threaded("q4_k", wq, K, x, rows, orc.host_cores())
+    r2, s2 = orc.gemm_bf16_threaded("q4_k", wq, K, x, rows, orc.host_cores())
+    assert not (~(np.abs(y - r1) <= TOL_R1 * s1 + 1e-6)).any(), "outside 1e-2 of the exact reference"
+    bad2 = ~(np.abs(y - r2) <= TOL_R2 * s2 + 1e-6)
+    if bad2.any():
+        i = tuple(np.argwhere(bad2)[0])
+        raise AssertionError(f"{bad2.sum()} of {bad2.size} outside {TOL_R2} of the bf16 reference; "
+                             f"first {i}: gpu {y[i]!r} r2 {r2[i]!r}")
+    assert np.linalg.norm(y - r1) / np.linalg.norm(r1) < 5e-3
 
 
 def test_gemm_workspace_errors(qk):

@@ -89,15 +89,14 @@ def test_gemm_q8_0_swiglu(qk, orc, M, F, K, gate, up, seed):
     assert np.all(np.abs(h - h1) <= swiglu_bound(g1, u1, sg1, su1, TOL_R1, h1))
 
 
-def test_gemm_q8_0_qwen_ffn_up_sampled(qk, orc):
-    """Qwen2.5-0.5B-shaped ffn_up in Q8_0: 512 tokens x 4864 rows x 896, sampled rows."""
+def test_gemm_q8_0_qwen_ffn_up_full(qk, orc):
+    """Qwen2.5-0.5B-shaped ffn_up in Q8_0: 512 tokens x 4864 rows x 896, every output."""
     M, N, K = 512, 4864, 896
     wq = synth.weights("q8_0", N, K, seed=90)
     x = synth.activations(M, K, seed=90)
     y = qk.qgemm_q8_0(torch.from_numpy(wq).cuda(), 0, N, K, torch.from_numpy(x).cuda())
     torch.cuda.synchronize()
-    rows = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(90).integers(0, N, 48)]))
-    check(y.cpu().numpy()[:, rows].astype(np.float64), orc, wq, K, x, rows, "qwen ffn_up")
+    check(y.cpu().numpy().astype(np.float64), orc, wq, K, x, np.arange(N), "qwen ffn_up")
 
 
 def test_gemm_q8_0_timeout_is_recorded(qk):

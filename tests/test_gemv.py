@@ -224,39 +224,46 @@ def test_bounded_wait_times_out_and_context_survives(qk, orc, fmt, rows, K, nkc)
 
 
 # ---------------------------------------------------------------- full-size configurations
-
-def _sample_rows(rows, n, seed):
-    rng = np.random.default_rng(seed)
-    pick = rng.choice(rows, size=min(n, rows), replace=False)
-    return np.unique(np.concatenate([pick, [0, rows - 1]]))
-
+#
+# Every output element is compared; the oracle runs on all host cores over
+# row bands (the same code per output as the serial oracle).
 
 LLAMA8B = [("attn_qkv", 6144, 4096), ("attn_output", 4096, 4096), ("ffn_gate_up", 28672, 4096),
            ("ffn_down", 4096, 14336)]
 
 
 @pytest.mark.parametrize("name,rows,K", LLAMA8B)
-def test_llama8b_layer_set_sampled(qk, orc, name, rows, K):
-    """Full-size Llama-8B-shaped Q4_K tensors, batch 1, checked on sampled rows."""
+def test_llama8b_layer_set_full(qk, orc, name, rows, K):
+    """Full-size Llama-8B-shaped Q4_K tensors, batch 1, every row."""
     seed = 2
     wq = synth.weights("q4_k", rows, K, seed=seed, stream0=10 * LLAMA8B.index((name, rows, K)))
     x = synth.activations(1, K, seed=seed)
     y = gpu_gemv(qk, "q4_k", wq, 0, rows, K, x).cpu().numpy()
-    idx = _sample_rows(rows, 384, seed)
-    yr, s = orc.gemv("q4_k", wq, K, x, rows=idx)
-    assert_close(y[:, idx], yr, s, name)
+    yr, s = orc.gemv_threaded("q4_k", wq, K, x, np.arange(rows), orc.host_cores())
+    assert_close(y, yr, s, name)
 
 
 @pytest.mark.parametrize("batch", [1, 8])
-def test_lm_head_q8_0_sampled(qk, orc, batch):
-    """Q8_0 lm_head 151936 x 896 (Qwen2.5-0.5B vocab), batch 1 and 8, sampled rows."""
+def test_lm_head_q8_0_full(qk, orc, batch):
+    """Q8_0 lm_head 151936 x 896 (Qwen2.5-0.5B vocab), batch 1 and 8, every row."""
     rows, K, seed = 151936, 896, 3
     wq = synth.weights("q8_0", rows, K, seed=seed)
     x = synth.activations(batch, K, seed=seed)
     y = gpu_gemv(qk, "q8_0", wq, 0, rows, K, x).cpu().numpy()
-    idx = _sample_rows(rows, 512, seed)
-    yr, s = orc.gemv("q8_0", wq, K, x, rows=idx)
-    assert_close(y[:, idx], yr, s, f"lm_head b{batch}")
+    yr, s = orc.gemv_threaded("q8_0", wq, K, x, np.arange(rows), orc.host_cores())
+    assert_close(y, yr, s, f"lm_head b{batch}")
+
+
+@pytest.mark.parametrize("fmt,rows,K,batch", [("q8_0", 576, 576, 1), ("q4_k", 4864, 896, 1),
+                                               ("q4_k", 896, 4864, 1), ("q4_k", 28672, 4096, 4)])
+def test_other_configs_full(qk, orc, fmt, rows, K, batch):
+    """The SmolLM q-proj, the Qwen ffn_up and its transpose, and Llama-8B gate+up at batch 4."""
+    seed = {576: 0, 4864: 1, 896: 1, 28672: 2}[rows]
+    wq = synth.weights(fmt, rows, K, seed=seed)
+    x = synth.activations(batch, K, seed=seed)
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv_threaded(fmt, wq, K, x, np.arange(rows), orc.host_cores())
+    assert_close(y, yr, s, f"{fmt} {rows}x{K} b{batch}")
 
 
 def test_programmatic_launch_chain(qk, orc):

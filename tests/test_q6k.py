@@ -60,15 +60,14 @@ def test_q6k_row_ranges_equal_one_call(qk):
     assert torch.equal(whole, parts)
 
 
-def test_q6k_lm_head_sampled(qk, orc):
-    """A Q6_K output head 128256 x 4096 (Llama-3 vocabulary), batch 1, sampled rows."""
+def test_q6k_lm_head_full(qk, orc):
+    """A Q6_K output head 128256 x 4096 (Llama-3 vocabulary), batch 1, every row."""
     rows, K, seed = 128256, 4096, 58
     wq = synth.weights("q6_k", rows, K, seed=seed)
     x = synth.activations(1, K, seed=seed)
     y = gpu_gemv(qk, "q6_k", wq, 0, rows, K, x).cpu().numpy()
-    idx = np.unique(np.concatenate([[0, rows - 1], np.random.default_rng(seed).integers(0, rows, 400)]))
-    yr, s = orc.gemv("q6_k", wq, K, x, rows=idx)
-    assert_close(y[:, idx], yr, s, "q6_k lm_head")
+    yr, s = orc.gemv_threaded("q6_k", wq, K, x, np.arange(rows), orc.host_cores())
+    assert_close(y, yr, s, "q6_k lm_head")
 
 
 def test_q6k_nonfinite_scale_propagates(qk, orc):

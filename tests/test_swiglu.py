@@ -94,15 +94,15 @@ def test_swiglu_row_ranges_equal_one_call(qk):
     assert torch.equal(whole, parts)
 
 
-def test_swiglu_llama8b_ffn_sampled(qk, orc):
-    """Llama-8B ffn gate+up (one fused 28672 x 4096 tensor), batch 1, sampled rows."""
+def test_swiglu_llama8b_ffn_full(qk, orc):
+    """Llama-8B ffn gate+up (one fused 28672 x 4096 tensor), batch 1, every output."""
     K, F = 4096, 14336
     wq = synth.weights("q4_k", 2 * F, K, seed=2, stream0=20)
     x = synth.activations(1, K, seed=2)
     h = run(qk, "q4_k", wq, 0, F, F, K, x).cpu().numpy()
-    idx = np.unique(np.concatenate([[0, F - 1], np.random.default_rng(2).integers(0, F, 300)]))
+    idx = np.arange(F)
     ref = orc.swiglu("q4_k", wq, K, x, idx, idx + F)
-    assert_swiglu_close(h[:, idx], ref, "llama8b ffn")
+    assert_swiglu_close(h, ref, "llama8b ffn")
 
 
 def test_swiglu_rejects_bad_arguments(qk):
