@@ -381,7 +381,7 @@ int qk_debug_gemv_plan(int fmt, int64_t rows, int64_t K, int batch, int64_t *out
 // Test hook, not part of the public header: the GEMV plan for an explicit
 // device (SM count, shared memory per block), computed on the host only.
 // Fields: SW, R, nkc, rows_w, stages, stage_bytes, smem, grid, XU, cpl, nw,
-// m, LU, cpa, off_stage, wide.  Returns the number written, -1 if nothing fits.
+// m, LU, cpa, off_stage, wide, kw.  Returns the number written, -1 if nothing fits.
 int qk_debug_gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, int pair, int64_t n_assign, int sms,
                            int smem_optin, int64_t *out, int n)
 {
@@ -389,10 +389,10 @@ int qk_debug_gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, int pair
     if (!out || fmt < 0 || fmt > 2 || batch < 1 || batch > QK_MAX_BATCH || rows <= 0 || K <= 0 ||
         !qk::gemv_plan_host(fmt, rows, K, batch, pair != 0, n_assign, sms, smem_optin, &p))
         return -1;
-    const int64_t v[16] = {p.SW, p.R, p.nkc, p.rows_w, p.stages, p.stage_bytes, p.smem, p.grid,
-                           p.XU, p.cpl, p.nw, p.m, p.LU, p.cpa, p.off_stage, p.wide};
+    const int64_t v[17] = {p.SW, p.R, p.nkc, p.rows_w, p.stages, p.stage_bytes, p.smem, p.grid,
+                           p.XU, p.cpl, p.nw, p.m, p.LU, p.cpa, p.off_stage, p.wide, p.kw};
     int k = 0;
-    for (; k < n && k < 16; ++k) out[k] = v[k];
+    for (; k < n && k < 17; ++k) out[k] = v[k];
     return k;
 }
 

@@ -51,6 +51,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// An arrival by the threads whose `pred` is true, without a branch.
+__device__ __forceinline__ void mbar_arrive_if(uint32_t bar, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}"
+                 ::"r"(bar), "r"(static_cast<uint32_t>(pred)) : "memory");
+}
+
 // Announce `bytes` more transaction bytes for the current phase without an
 // arrival (the phase still needs its expected arrivals).
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)

@@ -141,7 +141,29 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     const bool wide = batch == 1 && (fmt == kFmtQ6K ||
                                      (fmt == kFmtQ4K && (rows_cta_max + gr - 1) / gr * nkc > NW));
     if (wide) NW = gemv_warps(fmt, batch, true);
-    int64_t nw = std::min<int64_t>(NW, (rows_cta_max + gr - 1) / gr);
+    const int64_t ng = (rows_cta_max + gr - 1) / gr;   // row groups of the fullest CTA
+    int64_t nw = std::min<int64_t>(NW, ng);
+    // Split K over warps: when a CTA has fewer row groups than warps and the
+    // rows are cut into K chunks, kw warps share each row group, one residue
+    // class of its chunks each.  Every warp keeps one sum per lane and chunk
+    // and the group's first warp adds them in chunk order, which is the
+    // order of the unsplit path, so the bits do not depend on the split.
+    int64_t kw = 1, part_bytes = 0;
+    if (nkc > 1 && ng < NW) {
+        kw = std::min<int64_t>(nkc, NW / ng);
+        if (kw > 1) {
+            nw = ng * kw;
+            part_bytes = round_up(ng * nkc * 32 * R * batch * 4, 128);
+            stages = (budget - off_stage - part_bytes) / stage;
+            if (stages > kGemvMaxStages) stages = kGemvMaxStages;
+            if (stages < nw) {                       // not enough stages: no split
+                kw = 1;
+                nw = std::min<int64_t>(NW, ng);
+                part_bytes = 0;
+                stages = std::min<int64_t>(kGemvMaxStages, (budget - off_stage) / stage);
+            }
+        }
+    }
     nw = std::min(nw, stages);
     const int64_t m = stages / nw;
     stages = nw * m;
@@ -155,8 +177,10 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
     p->off_xsum = static_cast<int>(off_xsum);
     p->off_xscale = static_cast<int>(off_xscale);
     p->off_xout = static_cast<int>(off_xout);
-    p->off_stage = static_cast<int>(off_stage);
-    p->smem = static_cast<int>(off_stage + stages * stage);
+    p->off_part = static_cast<int>(off_stage);
+    p->off_stage = static_cast<int>(off_stage + part_bytes);
+    p->kw = static_cast<int>(kw);
+    p->smem = static_cast<int>(off_stage + part_bytes + stages * stage);
     p->grid = static_cast<int>(grid);
     p->nw = static_cast<int>(nw);
     p->m = static_cast<int>(m);
@@ -223,6 +247,8 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
     r.row_stride = p.row_stride;
     r.nw = p.nw;
     r.m = p.m;
+    r.kw = p.kw;
+    r.off_part = p.off_part;
     r.stage_bytes = p.stage_bytes;
     r.off_x = p.off_x;
     r.off_xsum = p.off_xsum;

@@ -107,6 +107,9 @@ struct GemvArgs {
     int row_stride;     // bytes between rows of a stage (nkc > 1)
     int nw;             // consumer warps that get row groups (<= the launched ones)
     int m;              // stages per consumer warp (stage w*m + t%m holds warp w's item t)
+    int kw;             // consumer warps per row group: its K chunks c with c % kw == the warp's
+                        // share (kw > 1: every warp has one row group at most)
+    int off_part;       // kw > 1: per-lane chunk sums [group][chunk][lane][R][B] (fp32)
     int stage_bytes;
     int off_x, off_xsum, off_xscale, off_xout, off_stage;
     int pair;           // 1: output row p = silu(row p) * row (p + up_rows), both rows in one item
@@ -133,11 +136,11 @@ __host__ __device__ constexpr int gemv_rows(int fmt, int batch)
 {
     return fmt != kFmtQ80 ? (batch <= 4 ? 2 : 1) : (batch == 1 ? 2 : (batch == 2 ? 4 : 2));
 }
-// Lane units a lane may hold in registers per item (Q4_K: one super-block of
-// R rows; Q6_K: one half super-block; Q8_0: up to 72 words of blocks).
+// Lane units a lane takes per item (Q4_K: one super-block of R rows; Q6_K:
+// one half super-block; Q8_0: up to 4 blocks, held in registers one at a time).
 __host__ __device__ constexpr int gemv_cpl_max(int fmt, int batch)
 {
-    return fmt != kFmtQ80 ? 1 : (batch == 1 ? 4 : (batch <= 4 ? 2 : 1));
+    return fmt != kFmtQ80 ? 1 : 4;
 }
 
 // -------------------------------------------------------------------------- Q4_K, batch 1
@@ -190,16 +193,14 @@ __device__ __forceinline__ void q4k_scales(const uint4 &hd, float d, float dmin,
 // sub-block 4H + 2lc, its high nibbles sub-block 4H + 2lc + 1).  x:
 // block-floating-point byte planes of the half, float4 group g at xa + 16g;
 // per 32-column group j the plain sum is xsum_h[j] and the plane scale
-// 2^(E-21) is |xsc_h[j]|.  A negative xsc_h[j] marks a group whose outlier
-// (value xo_h[2j], column xo_h[2j+1] as int bits) is in neither the planes
-// nor the plain sum: its weight d*sc*q - dmin*m (one rounding) times its
-// value is added once the half's plane terms are in.  The high nibbles are
-// used in place (byte & 0xF0 = 16 q), which is folded into their sub-block
-// scale as d/16 (exact: a power of two).
+// 2^(E-21) is |xsc_h[j]| (a negative scale marks a group whose outlier is in
+// neither the planes nor the plain sum; the caller adds its term).  The
+// high nibbles are used in place (byte & 0xF0 = 16 q), which is folded into
+// their sub-block scale as d/16 (exact: a power of two).
 template <int R, int H, int N, int Q0>
 __device__ __forceinline__ void q4k_half(const float (&d)[R], const float (&dmin)[R], const uint4 (&hd)[R],
                                          const uint4 (&qs)[R][N], const uint8_t *xa, const float *xsum_h,
-                                         const float *xsc_h, const float *xo_h, float (&acc)[R][1])
+                                         const float *xsc_h, float (&acc)[R][1])
 {
     const float4 xsum4 = *reinterpret_cast<const float4 *>(xsum_h);
     const float4 xsc4 = *reinterpret_cast<const float4 *>(xsc_h);
@@ -249,25 +250,6 @@ __device__ __forceinline__ void q4k_half(const float (&d)[R], const float (&dmin
             acc[r][0] = t;
         }
     }
-    // the outliers of the half's groups (rare: a sign bit of a group scale)
-    if ((__float_as_uint(xsc4.x) | __float_as_uint(xsc4.y) | __float_as_uint(xsc4.z) | __float_as_uint(xsc4.w)) >>
-        31) {
-        const float sc4[4] = {xsc4.x, xsc4.y, xsc4.z, xsc4.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (!(sc4[j] < 0.f)) continue;
-            const float xv = xo_h[2 * j];
-            const int i = __float_as_int(xo_h[2 * j + 1]);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float dsr[4], dmr[4];
-                q4k_scales<H>(hd[r], d[r], dmin[r], dsr, dmr);
-                const uint32_t byte = byte_of32(qs[r][Q0 + 2 * (j >> 1)], qs[r][Q0 + 2 * (j >> 1) + 1], i);
-                const float q = static_cast<float>(byte & ((j & 1) ? 0xF0u : 0x0Fu));
-                acc[r][0] = fmaf(fmaf(dsr[j], q, dmr[j]), xv, acc[r][0]);
-            }
-        }
-    }
 }
 
 // A whole super-block of R rows (qs = its 128 quant bytes): half 0, then
@@ -276,7 +258,7 @@ template <int R>
 __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][8], bool has_hi,
                                            const uint8_t *xa0, const uint8_t *xa1, const float *xsum0,
                                            const float *xsum1, const float *xsc0, const float *xsc1,
-                                           const float *xo0, const float *xo1, float (&acc)[R][1])
+                                           float (&acc)[R][1])
 {
     float d[R], dmin[R];
 #pragma unroll
@@ -284,16 +266,15 @@ __device__ __forceinline__ void q4k_sb_dig(const uint4 (&hd)[R], const uint4 (&q
         d[r] = half_bits_to_float(hd[r].x);
         dmin[r] = half_bits_to_float(hd[r].x >> 16);
     }
-    q4k_half<R, 0, 8, 0>(d, dmin, hd, qs, xa0, xsum0, xsc0, xo0, acc);
-    if (has_hi) q4k_half<R, 1, 8, 4>(d, dmin, hd, qs, xa1, xsum1, xsc1, xo1, acc);
+    q4k_half<R, 0, 8, 0>(d, dmin, hd, qs, xa0, xsum0, xsc0, acc);
+    if (has_hi) q4k_half<R, 1, 8, 4>(d, dmin, hd, qs, xa1, xsum1, xsc1, acc);
 }
 
 // One half HH of the super-block, its 64 quant bytes in qs (the wide
 // batch-1 form); the same arithmetic in the same order as q4k_sb_dig.
 template <int R, int HH>
 __device__ __forceinline__ void q4k_half_dig(const uint4 (&hd)[R], const uint4 (&qs)[R][4], const uint8_t *xa,
-                                             const float *xsum_h, const float *xsc_h, const float *xo_h,
-                                             float (&acc)[R][1])
+                                             const float *xsum_h, const float *xsc_h, float (&acc)[R][1])
 {
     float d[R], dmin[R];
 #pragma unroll
@@ -301,7 +282,7 @@ __device__ __forceinline__ void q4k_half_dig(const uint4 (&hd)[R], const uint4 (
         d[r] = half_bits_to_float(hd[r].x);
         dmin[r] = half_bits_to_float(hd[r].x >> 16);
     }
-    q4k_half<R, HH, 4, 0>(d, dmin, hd, qs, xa, xsum_h, xsc_h, xo_h, acc);
+    q4k_half<R, HH, 4, 0>(d, dmin, hd, qs, xa, xsum_h, xsc_h, acc);
 }
 
 // -------------------------------------------------------------------------- Q4_K, batch >= 2
@@ -424,12 +405,11 @@ __device__ __forceinline__ void q8_realign(const uint32_t (&wv)[R][9], const uin
 }
 
 // Batch 1: block-floating-point planes of the block's 32 columns, float4
-// group k at xa + 16k, plane scale |xscale|; a negative xscale marks an
-// outlier (value xo[0], column xo[1] as int bits) that is not in the planes
-// and is added exactly after the plane term.
+// group k at xa + 16k, plane scale |xscale| (a negative scale marks an
+// outlier that is not in the planes; the caller adds its term).
 template <int R>
 __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uint32_t (&off)[R], const uint8_t *xa,
-                                            float xscale, const float *xo, float (&acc)[R][1])
+                                            float xscale, float (&acc)[R][1])
 {
     float d[R];
     uint32_t qw[R][8];
@@ -454,17 +434,6 @@ __device__ __forceinline__ void q8_blk_dig(const uint32_t (&wv)[R][9], const uin
 #pragma unroll
     for (int r = 0; r < R; ++r)
         acc[r][0] = fmaf(d[r] * S, planes_to_float(sp[r][0], sp[r][1], sp[r][2]), acc[r][0]);
-    if (xscale < 0.f) {
-        const float xv = xo[0];
-        const int i = __float_as_int(xo[1]);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint4 qa = make_uint4(qw[r][0], qw[r][1], qw[r][2], qw[r][3]);
-            const uint4 qb = make_uint4(qw[r][4], qw[r][5], qw[r][6], qw[r][7]);
-            const float q = static_cast<float>(static_cast<int8_t>(byte_of32(qa, qb, i)));
-            acc[r][0] = fmaf(d[r] * q, xv, acc[r][0]);
-        }
-    }
 }
 
 // Batch >= 2: int8 quants through the magic-exponent trick (bias 128), fp32 x
@@ -577,12 +546,11 @@ __device__ __forceinline__ float q6_dscale(const Q6Half &h, float d, int j)
 // group g at xa + 16g); per 16-column sub-block j the plain sum x16[j] (for
 // the -32 offset) and per 32-column group the plane scale xsc[j/2].
 // |xsc[j]| is the plane scale of 32-column group j; a negative xsc[j] marks
-// an outlier of the group (value xo[2j], column xo[2j+1] as int bits) that is
-// in neither the planes nor the 16-column sums: its whole term
-// d*scale*(q - 32)*x is added after the group's plane terms.
+// an outlier of the group, in neither the planes nor the 16-column sums (the
+// caller adds its term with q6k_outlier_term).
 template <int R>
 __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_t *xa, const float *x16,
-                                             const float *xsc, const float *xo, float (&acc)[R][1])
+                                             const float *xsc, float (&acc)[R][1])
 {
     float d[R];
 #pragma unroll
@@ -615,13 +583,6 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
         }
         const float S = fabsf(xscv[t]);
         const float X0 = x16v[2 * t], X1 = x16v[2 * t + 1];
-        const bool ot = xscv[t] < 0.f;
-        float xv = 0.f;
-        int i = 0;
-        if (ot) {
-            xv = xo[2 * t];
-            i = __float_as_int(xo[2 * t + 1]);
-        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float ds0 = q6_dscale(hr[r], d[r], 2 * t), ds1 = q6_dscale(hr[r], d[r], 2 * t + 1);
@@ -630,18 +591,52 @@ __device__ __forceinline__ void q6k_half_dig(const Q6Half (&hr)[R], const uint8_
             a = fmaf(ds0 * -32.0f, X0, a);
             a = fmaf(ds1 * S, planes_to_float(sp[r][1][0], sp[r][1][1], sp[r][1][2]), a);
             a = fmaf(ds1 * -32.0f, X1, a);
-            if (ot) {
-                // the group's outlier: d*scale*(q - 32) times its value
-                const int ko = (i >> 2) & 7;
-                uint32_t quad = 0;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) quad = k == ko ? q6_quad(hr[r], t, k) : quad;
-                const float q = static_cast<float>((quad >> (8 * (i & 3))) & 0xFFu);
-                a = fmaf(((i >> 4) ? ds1 : ds0) * (q - 32.0f), xv, a);
-            }
             acc[r][0] = a;
         }
     }
+}
+
+// The outlier term d*scale*(q - 32)*x of 32-column group t (its column i)
+// of half n of the Q6_K super-block at `blk` in shared memory (a rare path,
+// kept out of the unrolled arithmetic: the field bytes are read directly).
+static __device__ __noinline__ float q6k_outlier_term(const uint8_t *blk, int n, int t, int i, float xv)
+{
+    const uint32_t lo = blk[64 * n + i + 32 * (t & 1)];
+    const uint32_t hi = blk[128 + 32 * n + i];
+    const int q = static_cast<int>(((t < 2 ? lo : (lo >> 4)) & 15u) | (((hi >> (2 * t)) & 3u) << 4));
+    const float d = half_bits_to_float(static_cast<uint32_t>(blk[208]) | (static_cast<uint32_t>(blk[209]) << 8));
+    const float sc = static_cast<float>(static_cast<int8_t>(blk[192 + 8 * n + 2 * t + (i >> 4)]));
+    return (d * sc * static_cast<float>(q - 32)) * xv;
+}
+
+// The outlier term (d*sc*q - dmin*m)*x of column i of sub-block j of the
+// Q4_K super-block at `sb` in shared memory; the weight is formed with one
+// rounding (d*sc*q and dmin*m are exact).
+static __device__ __noinline__ float q4k_outlier_term(const uint8_t *sb, int j, int i, float xv)
+{
+    const float d = half_bits_to_float(static_cast<uint32_t>(sb[0]) | (static_cast<uint32_t>(sb[1]) << 8));
+    const float dmin = half_bits_to_float(static_cast<uint32_t>(sb[2]) | (static_cast<uint32_t>(sb[3]) << 8));
+    const uint8_t *sc = sb + 4;
+    uint32_t s6, m6;
+    if (j < 4) {
+        s6 = sc[j] & 63u;
+        m6 = sc[j + 4] & 63u;
+    } else {
+        s6 = (sc[j + 4] & 15u) | ((sc[j - 4] >> 6) << 4);
+        m6 = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+    }
+    const uint32_t byte = sb[16 + 32 * (j >> 1) + i];
+    const float q = static_cast<float>((j & 1) ? (byte >> 4) : (byte & 15u));
+    const float w = fmaf(d * static_cast<float>(s6), q, -(dmin * static_cast<float>(m6)));
+    return w * xv;
+}
+
+// The outlier term d*q*x of column i of the Q8_0 block at `blk` in shared
+// memory (2-byte aligned).
+static __device__ __noinline__ float q8_outlier_term(const uint8_t *blk, int i, float xv)
+{
+    const float d = half_bits_to_float(static_cast<uint32_t>(blk[0]) | (static_cast<uint32_t>(blk[1]) << 8));
+    return (d * static_cast<float>(static_cast<int8_t>(blk[2 + i]))) * xv;
 }
 
 // Batch >= 2: fp32 x; each 6-bit quant becomes the exact float 2^23 + q (one
@@ -713,13 +708,204 @@ __device__ __forceinline__ void q6k_half_fp(const Q6Half (&hr)[R], const uint8_t
 // interleaved.  Batch 1 stores block-floating-point byte planes (one
 // exponent per 32 columns; a NaN or infinity in a group makes its scale
 // NaN), batch >= 2 fp32 pre-multiplied by 2^-s for the Q4_K nibble position.
+// The sum of eight values in a fixed order, the one at index `skip` left out.
+__device__ __forceinline__ float sum8_skip(const float (&v)[8], int skip)
+{
+    float t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = k == skip ? 0.f : v[k];
+    return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+}
+
+// Batch 1: the activations as block-floating-point byte planes.  A lane
+// takes 8 consecutive columns (two float4 slots of a unit) per piece, so a
+// 32-column group is 4 lanes and its reductions are two shuffle levels.  Per
+// group: its largest magnitude (exponent e1) and its plain sum (Q4_K: 32
+// columns, Q6_K: its two 16-column halves).  An outlier is the only value of
+// the group with an exponent >= e1 - 2 (so it is at least 2^3 times every
+// other value).  One ballot finds groups where a single lane holds values
+// that large; only a warp with such a group counts them exactly and redoes
+// the reductions with the outlier left out.  The group's exponent is then
+// that of its largest other value, the outlier's value and column go to
+// xout for the exact side term, and the group scale's sign bit marks it.
+// Each value becomes m = rint(x * 2^(21-E)), |m| <= 2^22, stored as three
+// byte planes (planes 0, 1 unsigned, plane 2 signed; the fourth byte of each
+// 16-byte slot unused); a group holding a NaN or an infinity gets a NaN
+// scale (its planes then do not matter).
+template <int FMT, int NTH>
+__device__ __forceinline__ void stage_x1(const GemvArgs &a, const float *x0, uint32_t cwarp, uint32_t lane,
+                                         uint32_t xs_addr, float *xsum, float *xscale, float *xout)
+{
+    constexpr uint32_t UC = FMT == kFmtQ80 ? 32 : 128;
+    constexpr uint32_t PU = UC / 8;         // 8-column pieces of a unit
+    constexpr uint32_t NJ = UC / 32;
+    constexpr uint32_t SU = UC / 4 + 1;     // 16-byte slots a unit slot owns
+    constexpr uint32_t UNR = 2;
+    static_assert(NTH % 32 == 0, "whole warps");
+    const uint32_t XH = static_cast<uint32_t>(a.XU) >> 1;
+    const uint32_t K = static_cast<uint32_t>(a.K);
+    const uint32_t p_total = static_cast<uint32_t>(a.U) * PU;
+    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x0) & 15u) == 0);
+    // pieces base + i*NTH + lane (i < UNR) of a round; the next round's loads
+    // are issued before this round's arithmetic
+    auto load = [&](uint32_t base, float (&v)[UNR][8]) {
+        const uint32_t ns = min(UNR, (p_total - base + NTH - 1) / NTH);
+#pragma unroll
+        for (uint32_t i = 0; i < UNR; ++i) {
+            const uint32_t pc = base + i * NTH + lane;
+            const uint32_t c0 = 8 * pc;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[i][k] = 0.f;
+            if (i < ns && pc < p_total) {
+                if (vec && c0 + 7 < K) {
+                    const float4 lo = __ldg(reinterpret_cast<const float4 *>(x0 + c0));
+                    const float4 hi = __ldg(reinterpret_cast<const float4 *>(x0 + c0) + 1);
+                    v[i][0] = lo.x; v[i][1] = lo.y; v[i][2] = lo.z; v[i][3] = lo.w;
+                    v[i][4] = hi.x; v[i][5] = hi.y; v[i][6] = hi.z; v[i][7] = hi.w;
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (c0 + k < K) v[i][k] = __ldg(x0 + c0 + k);
+                }
+            }
+        }
+    };
+    float v[UNR][8], nx[UNR][8];
+    if (cwarp * 32 < p_total) load(cwarp * 32, v);
+    for (uint32_t base = cwarp * 32; base < p_total; base += UNR * NTH) {
+        if (base + UNR * NTH < p_total) load(base + UNR * NTH, nx);   // the same for the warp
+        // slots of this round with any piece in range (the same for the warp)
+        const uint32_t ns = min(UNR, (p_total - base + NTH - 1) / NTH);
+        uint32_t pc[UNR];
+#pragma unroll
+        for (uint32_t i = 0; i < UNR; ++i) pc[i] = base + i * NTH + lane;
+        // magnitudes as bit patterns (their order is that of the values; a
+        // NaN is above every number), the group maximum, the plain sums
+        uint32_t ab[UNR][8], lmax[UNR], gmax[UNR], gref[UNR];
+        float F[UNR];
+        int oslot[UNR];
+        bool outl[UNR];
+        auto reduce = [&](uint32_t (&e)[UNR], float (&f)[UNR]) {
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1)
+#pragma unroll
+                for (uint32_t i = 0; i < UNR; ++i)
+                    if (i < ns) {
+                        e[i] = max(e[i], __shfl_xor_sync(0xFFFFFFFFu, e[i], o));
+                        if (FMT == kFmtQ4K || (FMT == kFmtQ6K && o < 2)) f[i] += __shfl_xor_sync(0xFFFFFFFFu, f[i], o);
+                    }
+        };
+#pragma unroll
+        for (uint32_t i = 0; i < UNR; ++i) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ab[i][k] = __float_as_uint(v[i][k]) & 0x7FFFFFFFu;
+            lmax[i] = max(max(max(ab[i][0], ab[i][1]), max(ab[i][2], ab[i][3])),
+                          max(max(ab[i][4], ab[i][5]), max(ab[i][6], ab[i][7])));
+            gmax[i] = lmax[i];
+            F[i] = sum8_skip(v[i], -1);
+        }
+        reduce(gmax, F);
+        // an outlier needs a group where one lane alone holds values with an
+        // exponent >= e1 - 2 (one ballot); only a warp with such a group
+        // counts them exactly
+        bool cand_any = false;
+        uint32_t thr[UNR];
+#pragma unroll
+        for (uint32_t i = 0; i < UNR; ++i) {
+            const uint32_t e1 = gmax[i] >> 23;
+            thr[i] = (e1 - 2u) << 23;
+            const uint32_t g1 = (__ballot_sync(0xFFFFFFFFu, lmax[i] >= thr[i]) >> (lane & 28u)) & 0xFu;
+            outl[i] = i < ns && e1 < 255u && e1 >= 2u && __popc(g1) == 1;   // candidate so far
+            cand_any |= outl[i];
+            oslot[i] = -1;
+            gref[i] = gmax[i];
+        }
+        if (__any_sync(0xFFFFFFFFu, cand_any)) {
+            // exact test: the group's one candidate lane holds a single such value
+#pragma unroll
+            for (uint32_t i = 0; i < UNR; ++i) {
+                uint32_t c = 0;
+                int first = -1;
+#pragma unroll
+                for (int k = 7; k >= 0; --k)
+                    if (ab[i][k] >= thr[i]) {
+                        ++c;
+                        first = k;
+                    }
+                const uint32_t g2 = (__ballot_sync(0xFFFFFFFFu, c >= 2u) >> (lane & 28u)) & 0xFu;
+                outl[i] = outl[i] && g2 == 0u;
+                oslot[i] = (outl[i] && c == 1u) ? first : -1;
+                // the reductions without the outlier (a group that has none gets
+                // the same values again)
+                uint32_t m = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = max(m, k == oslot[i] ? 0u : ab[i][k]);
+                gref[i] = m;
+                F[i] = sum8_skip(v[i], oslot[i]);
+            }
+            reduce(gref, F);
+        }
+#pragma unroll
+        for (uint32_t i = 0; i < UNR; ++i) {
+            if (!(i < ns) || pc[i] >= p_total) continue;
+            const bool finite = (gmax[i] >> 23) != 255u;
+            const int E = max(static_cast<int>(gref[i] >> 23) - 127, -96);
+            const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
+            const float d21 = __int_as_float((106 + E) << 23);    // 2^(E-21)
+            const float dn = !finite ? __int_as_float(0x7FC00000) : (outl[i] ? -d21 : d21);
+            // m = rint(x * 2^(21-E)): adding 1.5 * 2^23 in one fp32 FMA rounds
+            // the exact x * 2^(21-E) to the nearest integer (ties to even); the
+            // sum's bits minus those of 1.5 * 2^23 are m.  The outlier's m is 0.
+            constexpr float kRound = 12582912.0f;
+            constexpr uint32_t kRoundBits = 0x4B400000u;
+            // (a group with a NaN or an infinity gets meaningless planes and a NaN scale)
+            uint32_t mm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mm[k] = (__float_as_uint(fmaf(v[i][k], up, kRound)) - kRoundBits) & (k == oslot[i] ? 0u : 0xFFFFFFFFu);
+            const uint32_t u = pc[i] / PU, pu = pc[i] % PU;
+            const uint32_t us = FMT == kFmtQ4K ? ((u & 1) * XH + (u >> 1)) : u;   // unit slot
+            const uint32_t j = pu >> 2;                                          // 32-column group
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // byte-plane transpose: plane k holds byte k of the four columns
+                const uint32_t t0 = __byte_perm(mm[4 * h], mm[4 * h + 1], 0x5140u);
+                const uint32_t t1 = __byte_perm(mm[4 * h + 2], mm[4 * h + 3], 0x5140u);
+                const uint32_t t2 = __byte_perm(mm[4 * h], mm[4 * h + 1], 0x7362u);
+                const uint32_t t3 = __byte_perm(mm[4 * h + 2], mm[4 * h + 3], 0x7362u);
+                const uint32_t dst = xs_addr + 16u * (us * SU + 2 * pu + h);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(__byte_perm(t0, t1, 0x5410u)),
+                             "r"(__byte_perm(t0, t1, 0x7632u)), "r"(__byte_perm(t2, t3, 0x5410u)),
+                             "r"(__byte_perm(t2, t3, 0x7632u))
+                             : "memory");
+            }
+            if ((lane & 3) == 0) {
+                xscale[us * NJ + j] = dn;
+                if constexpr (FMT == kFmtQ4K) xsum[us * 4 + j] = F[i];
+            }
+            if constexpr (FMT == kFmtQ6K)
+                if ((lane & 1) == 0) xsum[us * 8 + (pu >> 1)] = F[i];
+            if (oslot[i] >= 0) {
+                uint32_t xb = 0u;      // the outlier's bits, picked without indexing registers
+#pragma unroll
+                for (int k = 0; k < 8; ++k) xb |= __float_as_uint(v[i][k]) & (k == oslot[i] ? 0xFFFFFFFFu : 0u);
+                xout[2 * (us * NJ + j)] = __uint_as_float(xb);
+                xout[2 * (us * NJ + j) + 1] = __int_as_float(static_cast<int>(8 * (pu & 3)) + oslot[i]);
+            }
+        }
+#pragma unroll
+        for (uint32_t i = 0; i < UNR; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[i][k] = nx[i][k];
+    }
+}
+
 template <int FMT, int B, int NTH>
 __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint32_t cwarp, uint32_t lane,
                                         uint32_t xs_addr, float *xsum, float *xscale, float *xout)
 {
     constexpr uint32_t UC = FMT == kFmtQ80 ? 32 : 128;
     constexpr uint32_t G = UC / 4;          // float4 groups of a unit (a power of two)
-    constexpr uint32_t NJ = UC / 32;
     constexpr uint32_t SU = B * G + 1;
     constexpr uint32_t UNR = 4;
     static_assert(NTH % 32 == 0, "whole warps");
@@ -790,123 +976,8 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const float *x0, uint
                     }
                 }
             };
-            if constexpr (B == 1) {
-                // Per 32-column group (its 8 lanes): e1, the largest biased
-                // exponent (a shuffle-max tree), and the plain sum (Q4_K: 32
-                // columns, Q6_K: its 16-column halves).  An outlier is the
-                // only value of the group with exponent >= e1 - 2 (so it is
-                // at least 2^3 times every other value): two ballots count,
-                // per group, the lanes holding one or more such values.  Only
-                // a warp that holds an outlier redoes both reductions with it
-                // left out; the group's exponent is then that of the largest
-                // other value, and the outlier is kept exactly on the side.
-                uint32_t eb[UNR][4], e1[UNR];
-                float F[UNR];
-#pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) {
-                    eb[i][0] = (__float_as_uint(v[i].x) >> 23) & 255u;
-                    eb[i][1] = (__float_as_uint(v[i].y) >> 23) & 255u;
-                    eb[i][2] = (__float_as_uint(v[i].z) >> 23) & 255u;
-                    eb[i][3] = (__float_as_uint(v[i].w) >> 23) & 255u;
-                    e1[i] = max(max(eb[i][0], eb[i][1]), max(eb[i][2], eb[i][3]));
-                    F[i] = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-                }
-                auto reduce = [&](uint32_t (&e)[UNR], float (&f)[UNR]) {
-#pragma unroll
-                    for (int o = 1; o <= 4; o <<= 1)
-#pragma unroll
-                        for (uint32_t i = 0; i < UNR; ++i) {
-                            e[i] = max(e[i], __shfl_xor_sync(0xFFFFFFFFu, e[i], o));
-                            if (FMT == kFmtQ4K || (FMT == kFmtQ6K && o < 4))
-                                f[i] += __shfl_xor_sync(0xFFFFFFFFu, f[i], o);
-                        }
-                };
-                reduce(e1, F);
-                int oslot[UNR];                                        // this lane's outlier column, -1 none
-                bool outl[UNR], anyo = false;
-#pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) {
-                    const uint32_t t = e1[i] - 2u;                     // e1 >= 2 whenever it matters below
-                    const uint32_t c = (eb[i][0] >= t) + (eb[i][1] >= t) + (eb[i][2] >= t) + (eb[i][3] >= t);
-                    const uint32_t g1 = (__ballot_sync(0xFFFFFFFFu, c >= 1u) >> (lane & 24u)) & 0xFFu;
-                    const uint32_t g2 = (__ballot_sync(0xFFFFFFFFu, c >= 2u) >> (lane & 24u)) & 0xFFu;
-                    outl[i] = e1[i] != 255u && e1[i] >= 2u && __popc(g1) == 1 && g2 == 0u;
-                    oslot[i] = !(outl[i] && c == 1u) ? -1
-                               : (eb[i][0] >= t ? 0 : (eb[i][1] >= t ? 1 : (eb[i][2] >= t ? 2 : 3)));
-                    anyo |= outl[i];
-                }
-                uint32_t eref[UNR];
-#pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) eref[i] = e1[i];
-                if (__any_sync(0xFFFFFFFFu, anyo)) {
-                    // the same reductions without the outlier (no change for a
-                    // group that has none)
-                    float Wv[UNR];
-#pragma unroll
-                    for (uint32_t i = 0; i < UNR; ++i) {
-                        const int k = oslot[i];
-                        eref[i] = max(max(k == 0 ? 0u : eb[i][0], k == 1 ? 0u : eb[i][1]),
-                                      max(k == 2 ? 0u : eb[i][2], k == 3 ? 0u : eb[i][3]));
-                        Wv[i] = ((k == 0 ? 0.f : v[i].x) + (k == 1 ? 0.f : v[i].y)) +
-                                ((k == 2 ? 0.f : v[i].z) + (k == 3 ? 0.f : v[i].w));
-                    }
-                    reduce(eref, Wv);
-#pragma unroll
-                    for (uint32_t i = 0; i < UNR; ++i) F[i] = Wv[i];
-                }
-                uint32_t pl[UNR][4];
-                float dn[UNR];
-#pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) {
-                    const bool finite = e1[i] != 255u;                 // a NaN or infinity: planes 0, scale NaN
-                    const int E = max(static_cast<int>(eref[i]) - 127, -96);
-                    const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
-                    const float d21 = __int_as_float((106 + E) << 23);    // 2^(E-21)
-                    dn[i] = !finite ? __int_as_float(0x7FC00000) : (outl[i] ? -d21 : d21);   // sign bit: outlier
-                    if constexpr (FMT == kFmtQ4K) sum[i] = F[i];
-                    if constexpr (FMT == kFmtQ6K) sum16[i] = F[i];
-                    // m = rint(x * 2^(21-E)), |m| <= 2^22: adding 1.5 * 2^23 in one
-                    // fp32 FMA rounds the exact x * 2^(21-E) to the nearest
-                    // integer (ties to even); the sum's bits minus those of
-                    // 1.5 * 2^23 are m.  The outlier's m is 0.
-                    constexpr float kRound = 12582912.0f;
-                    constexpr uint32_t kRoundBits = 0x4B400000u;
-                    const uint32_t keep = finite ? 0xFFFFFFFFu : 0u;
-                    const int os = oslot[i];
-                    const uint32_t m0 = (__float_as_uint(fmaf(v[i].x, up, kRound)) - kRoundBits) & (os == 0 ? 0u : keep);
-                    const uint32_t m1 = (__float_as_uint(fmaf(v[i].y, up, kRound)) - kRoundBits) & (os == 1 ? 0u : keep);
-                    const uint32_t m2 = (__float_as_uint(fmaf(v[i].z, up, kRound)) - kRoundBits) & (os == 2 ? 0u : keep);
-                    const uint32_t m3 = (__float_as_uint(fmaf(v[i].w, up, kRound)) - kRoundBits) & (os == 3 ? 0u : keep);
-                    // byte-plane transpose: plane k holds byte k of the four columns
-                    const uint32_t t0 = __byte_perm(m0, m1, 0x5140u), t1 = __byte_perm(m2, m3, 0x5140u);
-                    const uint32_t t2 = __byte_perm(m0, m1, 0x7362u), t3 = __byte_perm(m2, m3, 0x7362u);
-                    pl[i][0] = __byte_perm(t0, t1, 0x5410u);
-                    pl[i][1] = __byte_perm(t0, t1, 0x7632u);
-                    pl[i][2] = __byte_perm(t2, t3, 0x5410u);
-                    pl[i][3] = __byte_perm(t2, t3, 0x7632u);
-                }
-#pragma unroll
-                for (uint32_t i = 0; i < UNR; ++i) {
-                    if (!in[i]) continue;
-                    const uint32_t grp = g[i] >> 3;                    // 32-column group of the unit
-                    if ((lane & 7) == 0) {
-                        xscale[us[i] * NJ + grp] = dn[i];
-                        if constexpr (FMT == kFmtQ4K) xsum[us[i] * 4 + grp] = sum[i];
-                    }
-                    if (oslot[i] >= 0) {
-                        // the outlier's value and its column within the group
-                        const int k = oslot[i];
-                        const float xv = k == 0 ? v[i].x : (k == 1 ? v[i].y : (k == 2 ? v[i].z : v[i].w));
-                        xout[2 * (us[i] * NJ + grp)] = xv;
-                        xout[2 * (us[i] * NJ + grp) + 1] = __int_as_float(static_cast<int>(4 * (g[i] & 7u)) + k);
-                    }
-                    if constexpr (FMT == kFmtQ6K)
-                        if ((lane & 3) == 0) xsum[us[i] * 8 + (g[i] >> 2)] = sum16[i];
-                    const uint32_t dst = xs_addr + 16u * (us[i] * SU + g[i]);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(dst), "r"(pl[i][0]), "r"(pl[i][1]), "r"(pl[i][2]), "r"(pl[i][3]) : "memory");
-                }
-            } else {
+            {
+                static_assert(B >= 2, "batch 1 is staged by stage_x1");
                 plain_sums(v);
 #pragma unroll
                 for (uint32_t i = 0; i < UNR; ++i) {
@@ -1034,6 +1105,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     const int gr = a.pair ? (a.rows_w >> 1) : a.rows_w;   // output rows per row group
     const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + gr - 1) / gr);
     const uint32_t nkc = static_cast<uint32_t>(a.nkc);
+    const uint32_t kw = static_cast<uint32_t>(a.kw);
 
     // programmatic dependent launch: the next grid in the stream may start
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1060,10 +1132,10 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
             const uint64_t pol = l2_evict_first_policy();
             bool ok = true;
             uint32_t t = 0, tm = 0, use = 0;                 // item number, its stage offset and use
-            for (uint32_t g = w; ok && g < n_groups; g += nw) {
+            for (uint32_t g = w / kw; ok && g < n_groups; g += nw / kw) {
                 const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
                 const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
-                for (uint32_t c = 0; c < nkc; ++c, ++t) {
+                for (uint32_t c = w % kw; c < nkc; c += kw, ++t) {
                     const uint32_t st = w * m + tm;
                     const uint32_t bar = bar_full + 8u * st;
                     if (*abort_flag || (use > 0 && !mbar_wait_sleep(bar_empty + 8u * st, (use - 1) & 1u, a.wait_ns))) {
@@ -1111,19 +1183,68 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     // the weights do not depend on earlier kernels, x may: with programmatic
     // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    stage_x<FMT, B, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
-                             reinterpret_cast<float *>(smem + a.off_xsum),
-                             reinterpret_cast<float *>(smem + a.off_xscale),
-                             reinterpret_cast<float *>(smem + a.off_xout));
+    if constexpr (B == 1)
+        stage_x1<FMT, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
+                               reinterpret_cast<float *>(smem + a.off_xsum),
+                               reinterpret_cast<float *>(smem + a.off_xscale),
+                               reinterpret_cast<float *>(smem + a.off_xout));
+    else
+        stage_x<FMT, B, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
+                                 reinterpret_cast<float *>(smem + a.off_xsum),
+                                 reinterpret_cast<float *>(smem + a.off_xscale),
+                                 reinterpret_cast<float *>(smem + a.off_xout));
     named_bar_sync(1, 32 * NW);
     if (cwarp >= nw) return;
 
+    // the team sums of a row group and its outputs
+    auto finish = [&](int64_t row0, int n, const float (&acc)[R][B]) {
+        // sum over the SW lanes of each team (every lane of the team gets it)
+        float v[R][B];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                float t = acc[r][b];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1)
+                    if (o < SW) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);   // SW is the same for the warp
+                v[r][b] = t;
+            }
+        if (!a.pair) {
+            // lane 0 of the team writes its rows
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const int lr = team * R + r;
+                    if (sl == 0 && lr < n) y0[b * a.ldy + row0 + lr] = v[r][b];
+                }
+        } else if (SW == 32) {
+            // one team: rows r < R/2 are gate rows, r + R/2 their up rows
+#pragma unroll
+            for (int r = 0; r < R / 2; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b)
+                    if (sl == 0 && r < n) y0[b * a.ldy + row0 + r] = silu(v[r][b]) * v[r + R / 2][b];
+        } else {
+            // teams t < T/2 hold gate rows, team t + T/2 (lanes + 16) the up rows
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const float u = __shfl_down_sync(0xFFFFFFFFu, v[r][b], 16);
+                    const int lr = team * R + r;
+                    if (lane < 16 && sl == 0 && lr < n) y0[b * a.ldy + row0 + lr] = silu(v[r][b]) * u;
+                }
+        }
+    };
+    float *part = reinterpret_cast<float *>(smem + a.off_part);
     const uintptr_t wbase = reinterpret_cast<uintptr_t>(w0);
     const int chunk_lu = SW * cpl;                 // lane units per chunk
     const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
     uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
     bool failed = false;
-    for (uint32_t g = cwarp; g < n_groups && !failed; g += nw) {
+    for (uint32_t g = cwarp / kw; g < n_groups && !failed; g += nw / kw) {
         const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
         const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
         float acc[R][B];
@@ -1131,7 +1252,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
-        for (uint32_t c = 0; c < nkc; ++c) {
+        for (uint32_t c = cwarp % kw; c < nkc; c += kw) {
             const uint32_t st = st0 + tm;
             bool ok = mbar_wait_sleep(bar_full + 8u * st, par, a.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok);   // the warp leaves together or not at all
@@ -1166,112 +1287,185 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
             }
             // lane units of this lane in this chunk: i*SW + sl (i < cpl) from
             // the chunk's start, lane unit c*chunk_lu + i*SW + sl of the row
+            // this chunk's sums, started from zero: the row's sum adds them up
+            // in chunk order (the same order when the chunks of a row group
+            // are shared by kw warps)
+            float pacc[R][B];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) pacc[r][b] = 0.f;
             const int lu0 = static_cast<int>(c) * chunk_lu + sl;
+            // batch 1: the exact terms of the outliers of this lane's groups,
+            // read from the stage before it is handed back (rare: a sign bit
+            // of a group scale), added after the unit's plane terms
+            float oterm[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) oterm[r] = 0.f;
             if constexpr (FMT == kFmtQ4K) {
+                // a lane past the row's last unit (only in a row's last chunk)
+                // works on that last unit and its sums are dropped
                 const bool valid = lu0 < a.LU;
+                const int lu = valid ? lu0 : a.LU - 1;
+                const int su = lu - static_cast<int>(c) * chunk_lu;   // the unit within the chunk
+                const bool has_hi = 2 * lu + 1 < a.U;
+                auto outliers = [&]() {
+                    const float4 s0 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
+                    const float4 s1 = *reinterpret_cast<const float4 *>(xscale + 4 * (XH + lu));
+                    const uint32_t sg = (__float_as_uint(s0.x) | __float_as_uint(s0.y) | __float_as_uint(s0.z) |
+                                         __float_as_uint(s0.w) | __float_as_uint(s1.x) | __float_as_uint(s1.y) |
+                                         __float_as_uint(s1.z) | __float_as_uint(s1.w)) >> 31;
+                    if (B == 1 && sg) {
+                        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                        for (int j = 0; j < 8; ++j)
+                            if (sv[j] < 0.f && (j < 4 || has_hi)) {
+                                const int slot = 8 * ((j < 4 ? 0 : XH) + lu) + 2 * (j & 3);
+                                const float xv = xout[slot];
+                                const int i = __float_as_int(xout[slot + 1]);
+#pragma unroll
+                                for (int r = 0; r < R; ++r)
+                                    oterm[r] += q4k_outlier_term(rowp[r] + su * UB, j, i, xv);
+                            }
+                    }
+                };
               if constexpr (B == 1 && WIDE) {
                 // one 128-column half at a time: the stage is handed back once
                 // the second half is in registers
                 uint4 hd[R], q4[R][4];
-                const int lu = lu0;
-                const bool has_hi = 2 * lu + 1 < a.U;
-                if (valid) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
+                    hd[r] = p[0];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) q4[r][i] = p[1 + i];
+                }
+                q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, pacc);
+                if (has_hi) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + sl * UB);
-                        hd[r] = p[0];
+                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) q4[r][i] = p[1 + i];
-                    }
-                    q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, xout + 8 * lu,
-                                       acc);
-                    if (has_hi) {
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + sl * UB);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) q4[r][i] = p[5 + i];
-                        }
+                        for (int i = 0; i < 4; ++i) q4[r][i] = p[5 + i];
                     }
                 }
+                outliers();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
-                if (valid && has_hi)
+                mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                if (has_hi)
                     q4k_half_dig<R, 1>(hd, q4, xs + 16 * SU * (XH + lu), xsum + 4 * (XH + lu),
-                                       xscale + 4 * (XH + lu), xout + 8 * (XH + lu), acc);
+                                       xscale + 4 * (XH + lu), pacc);
               } else {
                 uint4 hd[R], qs[R][8];
-                if (valid) {
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + sl * UB);
-                        hd[r] = p[0];
+                for (int r = 0; r < R; ++r) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
+                    hd[r] = p[0];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) qs[r][i] = p[1 + i];
-                    }
+                    for (int i = 0; i < 8; ++i) qs[r][i] = p[1 + i];
                 }
+                outliers();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
-                if (valid) {
-                    const int lu = lu0;
-                    const bool has_hi = 2 * lu + 1 < a.U;
-                    const uint8_t *xa0 = xs + 16 * SU * lu;
-                    const uint8_t *xa1 = xs + 16 * SU * (XH + lu);
-                    if constexpr (B == 1)
-                        q4k_sb_dig<R>(hd, qs, has_hi, xa0, xa1, xsum + 4 * lu, xsum + 4 * (XH + lu),
-                                      xscale + 4 * lu, xscale + 4 * (XH + lu), xout + 8 * lu,
-                                      xout + 8 * (XH + lu), acc);
-                    else
-                        q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, acc);
-                }
+                mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                const uint8_t *xa0 = xs + 16 * SU * lu;
+                const uint8_t *xa1 = xs + 16 * SU * (XH + lu);
+                if constexpr (B == 1)
+                    q4k_sb_dig<R>(hd, qs, has_hi, xa0, xa1, xsum + 4 * lu, xsum + 4 * (XH + lu),
+                                  xscale + 4 * lu, xscale + 4 * (XH + lu), pacc);
+                else if (valid)
+                    q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, pacc);
               }
+                if constexpr (B == 1) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) pacc[r][0] = valid ? pacc[r][0] + oterm[r] : 0.f;
+                }
             } else if constexpr (FMT == kFmtQ6K) {
                 // lane unit = half super-block: block li/2 of the chunk, half li%2
                 // (a chunk holds whole super-blocks: chunk_lu is even when nkc > 1)
                 Q6Half hr[R];
                 const bool valid = lu0 < a.LU;
-                if (valid) {
+                const int lu = valid ? lu0 : a.LU - 1;     // past the row's end: its last unit, sums dropped
+                const int su = lu - static_cast<int>(c) * chunk_lu;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) q6_load(rowp[r] + (sl >> 1) * 210, lu0 & 1, hr[r]);
+                for (int r = 0; r < R; ++r) q6_load(rowp[r] + (su >> 1) * 210, lu & 1, hr[r]);
+                if constexpr (B == 1) {
+                    const float4 sc4 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
+                    if ((__float_as_uint(sc4.x) | __float_as_uint(sc4.y) | __float_as_uint(sc4.z) |
+                         __float_as_uint(sc4.w)) >> 31) {
+                        const float scv[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+                        for (int t = 0; t < 4; ++t)
+                            if (scv[t] < 0.f) {
+                                const float xv = xout[8 * lu + 2 * t];
+                                const int i = __float_as_int(xout[8 * lu + 2 * t + 1]);
+#pragma unroll
+                                for (int r = 0; r < R; ++r)
+                                    oterm[r] += q6k_outlier_term(rowp[r] + (su >> 1) * 210, lu & 1, t, i, xv);
+                            }
+                    }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8u * st);   // the stage may be refilled
-                if (valid) {
-                    const uint8_t *xa = xs + 16 * SU * lu0;
-                    if constexpr (B == 1)
-                        q6k_half_dig<R>(hr, xa, xsum + 8 * lu0, xscale + 4 * lu0, xout + 8 * lu0, acc);
-                    else
-                        q6k_half_fp<B, R>(hr, xa, acc);
+                mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                const uint8_t *xa = xs + 16 * SU * lu;
+                if constexpr (B == 1) {
+                    q6k_half_dig<R>(hr, xa, xsum + 8 * lu, xscale + 4 * lu, pacc);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) pacc[r][0] = valid ? pacc[r][0] + oterm[r] : 0.f;
+                } else if (valid) {
+                    q6k_half_fp<B, R>(hr, xa, pacc);
                 }
             } else {
-                uint32_t wv[CM][R][9], off[CM][R];
+                // one block at a time (words in registers, realigned), the stage
+                // handed back once the lane's last block of the item is loaded
 #pragma unroll
                 for (int i = 0; i < CM; ++i) {
+                    if (i >= cpl) break;
                     const int lu = lu0 + i * SW;
-                    if (i < cpl && lu < a.LU) {
+                    const bool has = lu < a.LU;
+                    uint32_t wv[R][9], off[R];
+                    if (has) {
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uintptr_t ad = reinterpret_cast<uintptr_t>(rowp[r] + (i * SW + sl) * UB);
-                            off[i][r] = static_cast<uint32_t>(ad & 3u);          // 0 or 2
-                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - off[i][r]);
+                            off[r] = static_cast<uint32_t>(ad & 3u);          // 0 or 2
+                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - off[r]);
 #pragma unroll
-                            for (int k = 0; k < 9; ++k) wv[i][r][k] = wp[k];
+                            for (int k = 0; k < 9; ++k) wv[r][k] = wp[k];
+                        }
+                        if (B == 1 && xscale[lu] < 0.f) {
+                            const float xv = xout[2 * lu];
+                            const int ic = __float_as_int(xout[2 * lu + 1]);
+#pragma unroll
+                            for (int r = 0; r < R; ++r)
+                                oterm[r] += q8_outlier_term(rowp[r] + (i * SW + sl) * UB, ic, xv);
                         }
                     }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8u * st);
-#pragma unroll
-                for (int i = 0; i < CM; ++i) {
-                    const int lu = lu0 + i * SW;
-                    if (i < cpl && lu < a.LU) {
+                    if (i == cpl - 1) {
+                        __syncwarp();
+                        mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                    }
+                    if (has) {
                         const uint8_t *xa = xs + 16 * SU * lu;
                         if constexpr (B == 1)
-                            q8_blk_dig<R>(wv[i], off[i], xa, xscale[lu], xout + 2 * lu, acc);
+                            q8_blk_dig<R>(wv, off, xa, xscale[lu], pacc);
                         else
-                            q8_blk_fp<B, R>(wv[i], off[i], xa, acc);
+                            q8_blk_fp<B, R>(wv, off, xa, pacc);
                     }
                 }
+                if constexpr (B == 1) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) pacc[r][0] += oterm[r];
+                }
+            }
+            if (kw == 1) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int b = 0; b < B; ++b) acc[r][b] += pacc[r][b];
+            } else {
+                float *pp = part + ((g * nkc + c) * 32u + static_cast<uint32_t>(lane)) * (R * B);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int b = 0; b < B; ++b) pp[r * B + b] = pacc[r][b];
             }
             if (++tm == m) {
                 tm = 0;
@@ -1279,46 +1473,29 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
             }
         }
         if (failed) break;
-        // sum over the SW lanes of each team (every lane of the team gets it)
-        float v[R][B];
+        if (kw == 1) finish(row0, n, acc);
+    }
+    if (kw > 1) {
+        // the warps of a row group meet; its first warp adds the chunk sums
+        // in chunk order and writes the outputs
+        named_bar_sync(2, 32 * static_cast<int>(nw));
+        const uint32_t g = cwarp / kw;
+        if (!failed && cwarp % kw == 0 && g < n_groups) {
+            const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
+            const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
+            float acc[R][B];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int b = 0; b < B; ++b) {
-                float t = acc[r][b];
+                for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
+            for (uint32_t c = 0; c < nkc; ++c) {
+                const float *pp = part + ((g * nkc + c) * 32u + static_cast<uint32_t>(lane)) * (R * B);
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) {
-                    const float u = __shfl_xor_sync(0xFFFFFFFFu, t, o);
-                    if (o < SW) t += u;
-                }
-                v[r][b] = t;
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int b = 0; b < B; ++b) acc[r][b] += pp[r * B + b];
             }
-        if (!a.pair) {
-            // lane 0 of the team writes its rows
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    const int lr = team * R + r;
-                    if (sl == 0 && lr < n) y0[b * a.ldy + row0 + lr] = v[r][b];
-                }
-        } else if (SW == 32) {
-            // one team: rows r < R/2 are gate rows, r + R/2 their up rows
-#pragma unroll
-            for (int r = 0; r < R / 2; ++r)
-#pragma unroll
-                for (int b = 0; b < B; ++b)
-                    if (sl == 0 && r < n) y0[b * a.ldy + row0 + r] = silu(v[r][b]) * v[r + R / 2][b];
-        } else {
-            // teams t < T/2 hold gate rows, team t + T/2 (lanes + 16) the up rows
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    const float u = __shfl_down_sync(0xFFFFFFFFu, v[r][b], 16);
-                    const int lr = team * R + r;
-                    if (lane < 16 && sl == 0 && lr < n) y0[b * a.ldy + row0 + lr] = silu(v[r][b]) * u;
-                }
+            finish(row0, n, acc);
         }
     }
 }

@@ -15,6 +15,8 @@ struct GemvPlan {
     int U, LU, XU, SW, R, cpl, nkc, rows_w, chunk_bytes, row_stride;
     int nw, m, stages, stage_bytes, pair, up_stage_off, cpa;
     int wide;   // batch 1: the 16-warp form (Q4_K: a lane holds half a super-block at a time)
+    int kw;     // consumer warps sharing a row group's K chunks (1: no split)
+    int off_part;
     int off_x, off_xsum, off_xscale, off_xout, off_stage, smem, grid;
     int64_t row_bytes;
 };

@@ -374,7 +374,7 @@ def debug_skip_item(item: int) -> int:
 PLAN_FIELDS = ("SW", "R", "nkc", "rows_w", "stages", "stage_bytes", "smem", "grid", "XU", "cpl", "nw", "m")
 
 
-PLAN_FOR_FIELDS = PLAN_FIELDS + ("LU", "cpa", "off_stage", "wide")
+PLAN_FOR_FIELDS = PLAN_FIELDS + ("LU", "cpa", "off_stage", "wide", "kw")
 
 
 def debug_gemv_plan_for(fmt: str, rows: int, K: int, batch: int, sms: int, smem_optin: int,

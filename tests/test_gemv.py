@@ -314,3 +314,32 @@ def test_binding_refuses_wrong_tensors_before_launch(qk):
         qk.qmatvec_experts("q4_k", w, 2, rows // 2, K, x, 1, torch.zeros(3, dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert torch.all(y == 7.0)
+
+
+SPLIT = [("q4_k", 1, 14336), ("q4_k", 31, 14336), ("q4_k", 33, 20480), ("q4_k", 896, 4864),
+         ("q8_0", 576, 20000), ("q8_0", 1, 8192), ("q6_k", 31, 14336), ("q6_k", 33, 8192)]
+
+
+@pytest.mark.parametrize("fmt,rows,K", SPLIT)
+@pytest.mark.parametrize("batch", [1, 3])
+def test_split_k_over_warps_matches_oracle_and_unsplit_bits(qk, orc, fmt, rows, K, batch):
+    """Calls with few rows a CTA share each row's K chunks among warps; the
+    result equals the oracle and, bit for bit, the same rows of a call whose
+    CTAs split K over a different number of warps (or not at all)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    smem = getattr(torch.cuda.get_device_properties(0), "shared_memory_per_block_optin", 232448)
+    bb = batch                                      # the batch rows of one launch (the host splits larger ones)
+    while qk.debug_gemv_plan_for(fmt, rows, K, bb, sms, smem) is None:
+        bb -= 1
+    p = qk.debug_gemv_plan_for(fmt, rows, K, bb, sms, smem)
+    if p["kw"] == 1:
+        pytest.skip(f"{fmt} {rows}x{K}: batch {bb} leaves no room to split")
+    # the same rows in a larger call, split differently or not at all
+    big = next(n for n in (4000, 16000) if qk.debug_gemv_plan_for(fmt, n, K, bb, sms, smem)["kw"] != p["kw"])
+    wq = synth.weights(fmt, big, K, seed=18)
+    x = synth.activations(batch, K, seed=18)
+    y = gpu_gemv(qk, fmt, wq, 0, rows, K, x).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x, rows=np.arange(rows))
+    assert_close(y, yr, s, f"split {fmt} {rows}x{K} b{batch}")
+    y_big = gpu_gemv(qk, fmt, wq, 0, big, K, x).cpu().numpy()
+    assert np.array_equal(y, y_big[:, :rows])

@@ -71,3 +71,26 @@ def test_wide_form_for_calls_with_many_items():
     assert plan("q4_k", 28672, 4096, 1)["wide"] == 1         # 48 (gate+up)
     assert plan("q4_k", 4096, 14336, 1)["wide"] == 1         # 28 (ffn_down, 2 chunks a row)
     assert plan("q4_k", 28672, 4096, 2)["wide"] == 0
+
+
+def test_split_k_over_warps_for_few_row_groups():
+    """A CTA with fewer row groups than warps shares each group's K chunks
+    among kw warps (their sums are added in chunk order, so the row's cut and
+    its bits stay those of the unsplit plan)."""
+    p = plan("q4_k", 896, 4864, 1)                 # Qwen ffn_down: 6 rows a CTA, 3 chunks a row
+    assert p["nkc"] == 3 and p["kw"] == 3 and p["nw"] == 3
+    p = plan("q4_k", 1, 14336, 1)                  # one row, two chunks
+    assert p["nkc"] == 2 and p["kw"] == 2 and p["nw"] == 2 and p["grid"] == 1
+    p = plan("q8_0", 33, 20000, 1)
+    assert p["kw"] > 1 and p["nw"] == p["kw"]
+    assert plan("q4_k", 28672, 4096, 1)["kw"] == 1    # whole rows: nothing to split
+    assert plan("q4_k", 4096, 14336, 1)["kw"] == 1    # 28 row groups a CTA fill the warps
+    for fmt in ("q8_0", "q4_k", "q6_k"):
+        for K in KS:
+            for rows in ROWS:
+                for batch in (1, 2, 8):
+                    q = plan(fmt, rows, K, batch)
+                    if q is None:
+                        continue
+                    assert 1 <= q["kw"] <= max(1, q["nkc"])
+                    assert q["kw"] == 1 or (q["nkc"] > 1 and q["nw"] % q["kw"] == 0)
