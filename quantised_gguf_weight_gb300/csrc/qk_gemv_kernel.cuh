@@ -1244,7 +1244,32 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
     uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
     bool failed = false;
-    for (uint32_t g = cwarp / kw; g < n_groups && !failed; g += nw / kw) {
+    const uint32_t g_first = cwarp / kw, g_step = nw / kw, c_first = cwarp % kw;
+    // batch 1: bit c set when this lane's units of chunk c have a group with
+    // an outlier (a sign bit of a group scale), found once after staging
+    uint64_t omask = 0;
+    if constexpr (B == 1) {
+        for (uint32_t c = c_first; c < nkc && c < 64; c += kw) {
+            uint32_t sg = 0;
+            for (int i = 0; i < cpl; ++i) {
+                const int lu = static_cast<int>(c) * SW * cpl + i * SW + sl;
+                if (lu >= a.LU) break;
+                if constexpr (FMT == kFmtQ80) {
+                    sg |= __float_as_uint(xscale[lu]);
+                } else {
+                    const uint4 s0 = *reinterpret_cast<const uint4 *>(xscale + 4 * lu);
+                    sg |= s0.x | s0.y | s0.z | s0.w;
+                    if constexpr (FMT == kFmtQ4K) {
+                        const uint4 s1 = *reinterpret_cast<const uint4 *>(xscale + 4 * (XH + lu));
+                        sg |= s1.x | s1.y | s1.z | s1.w;
+                    }
+                }
+            }
+            if (sg >> 31) omask |= 1ull << c;
+        }
+        if (nkc > 64) omask = ~0ull;                 // (beyond 64 chunks: every chunk is checked)
+    }
+    for (uint32_t g = g_first; g < n_groups && !failed; g += g_step) {
         const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
         const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
         float acc[R][B];
@@ -1252,8 +1277,9 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
-        for (uint32_t c = cwarp % kw; c < nkc; c += kw) {
+        for (uint32_t c = c_first; c < nkc; c += kw) {
             const uint32_t st = st0 + tm;
+            const bool ochunk = B == 1 && ((omask >> (c < 64 ? c : 63)) & 1u) != 0;
             bool ok = mbar_wait_sleep(bar_full + 8u * st, par, a.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok);   // the warp leaves together or not at all
             if (!ok) {
@@ -1310,12 +1336,9 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                 const int su = lu - static_cast<int>(c) * chunk_lu;   // the unit within the chunk
                 const bool has_hi = 2 * lu + 1 < a.U;
                 auto outliers = [&]() {
-                    const float4 s0 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
-                    const float4 s1 = *reinterpret_cast<const float4 *>(xscale + 4 * (XH + lu));
-                    const uint32_t sg = (__float_as_uint(s0.x) | __float_as_uint(s0.y) | __float_as_uint(s0.z) |
-                                         __float_as_uint(s0.w) | __float_as_uint(s1.x) | __float_as_uint(s1.y) |
-                                         __float_as_uint(s1.z) | __float_as_uint(s1.w)) >> 31;
-                    if (B == 1 && sg) {
+                    if (ochunk && valid) {
+                        const float4 s0 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(xscale + 4 * (XH + lu));
                         const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
                         for (int j = 0; j < 8; ++j)
                             if (sv[j] < 0.f && (j < 4 || has_hi)) {
@@ -1388,9 +1411,8 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
 #pragma unroll
                 for (int r = 0; r < R; ++r) q6_load(rowp[r] + (su >> 1) * 210, lu & 1, hr[r]);
                 if constexpr (B == 1) {
-                    const float4 sc4 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
-                    if ((__float_as_uint(sc4.x) | __float_as_uint(sc4.y) | __float_as_uint(sc4.z) |
-                         __float_as_uint(sc4.w)) >> 31) {
+                    if (ochunk && valid) {
+                        const float4 sc4 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
                         const float scv[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
                         for (int t = 0; t < 4; ++t)
                             if (scv[t] < 0.f) {
@@ -1430,7 +1452,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
 #pragma unroll
                             for (int k = 0; k < 9; ++k) wv[r][k] = wp[k];
                         }
-                        if (B == 1 && xscale[lu] < 0.f) {
+                        if (B == 1 && ochunk && xscale[lu] < 0.f) {
                             const float xv = xout[2 * lu];
                             const int ic = __float_as_int(xout[2 * lu + 1]);
 #pragma unroll
