@@ -747,6 +747,8 @@ def run_only(args, torch, qk, synth, device):
     if fmt not in fns:
         raise SystemExit(f"--only: unknown format {fmt!r} (q8_0, q4_k or q6_k)")
     fn = fns[fmt]
+    if args.no_tc:
+        qk.debug_gemv_tc(0)            # batch 2..8: the fp32 form, for comparison
     stream = torch.cuda.Stream(device=device)
 
     def mk(w):
@@ -762,7 +764,7 @@ def run_only(args, torch, qk, synth, device):
     ms = time_calls(torch, stream, [mk(w) for w in ws] * max(1, 8 // copies), max(1, args.steps))
     b = call_bytes(rb, rows, K, batch)
     print(json.dumps({"only": args.only, "avg_us": round(ms * 1e3, 2), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
-                      "copies": copies}), flush=True)
+                      "copies": copies, "form": "fp32" if args.no_tc else "default"}), flush=True)
     return 0
 
 
@@ -792,6 +794,8 @@ def main():
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--only-gemm", default=None, help="M:N:K -- time the Q4_K prefill GEMM only")
     ap.add_argument("--only", default=None, help="FMT:ROWS:K:BATCH -- time one GEMV call only")
+    ap.add_argument("--no-tc", action="store_true",
+                    help="with --only: batch 2..8 calls take the fp32 form instead of the tensor-core form")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

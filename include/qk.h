@@ -96,11 +96,12 @@ typedef enum {
  *       |d*scale*q| + 32*|d*scale| for Q6_K.  The kernels sum a Q4_K or Q6_K
  *       weight's two terms separately, so this is sum|w*x| unless the terms
  *       of the weights nearly cancel (then S is the larger);
- *   A = 0 at batch 2..8.  Batch 1 holds each 32-column group of x as 24-bit
- *       integers that share one binary exponent: that of the group's largest
- *       magnitude or, when the largest is at least 2^3 times (in binary
- *       exponent) every other value of the group, that of the second largest,
- *       the largest value then being carried exactly on its own.  A value of
+ *   A is the term of the activation encoding, 0 where x is used as fp32:
+ *     - Batch 1 holds each 32-column group of x as 24-bit integers that
+ *       share one binary exponent: that of the group's largest magnitude
+ *       or, when the largest is at least 2^3 times (in binary exponent)
+ *       every other value of the group, that of the second largest, the
+ *       largest value then being carried exactly on its own.  A value of
  *       x is thus held within 2^-20 times the second largest magnitude of
  *       its group (the largest within 2^-22 of itself), and
  *       A = 2^-20 * sum_groups (second largest |x| of the group) *
@@ -109,7 +110,22 @@ typedef enum {
  *       nothing, and A is far inside 1e-5 * S unless a row's weights sit
  *       mostly on values much smaller than their group's second largest
  *       (for instance two values 2^20 times the rest in one group, meeting
- *       zero weights).  NaN and infinities in x give non-finite results.
+ *       zero weights).
+ *     - Batch 2..8 takes one of two forms.  Q8_0 with K a multiple of 128
+ *       (K up to 4096) and Q4_K (K up to 4864) take the tensor-core form
+ *       when the call has at least 128 rows per SM of the device (19456
+ *       rows on 152 SMs) and, for Q4_K, batch 4..8; other calls take the
+ *       fp32 form, for which A = 0.  The tensor-core form applies the same
+ *       rule for a lone outlier (carried exactly), then holds each 32-column
+ *       group of a batch row as two fp16 pieces of x scaled by the power of
+ *       two that puts the group's largest remaining magnitude M in
+ *       [2^14, 2^15) ([2^10, 2^11) for the high-nibble groups of Q4_K): a
+ *       value is held within 2^-24 of itself or within 2^-39 (2^-35) * M,
+ *       whichever is more (M taken as at least 2^-100), so
+ *       A = 2^-35 * sum_groups M * (sum |w| over the group's columns).  Each form's arithmetic for a row depends on K
+ *       only: row ranges of a tensor give the bits of the whole call when
+ *       both take the same form.
+ *   NaN and infinities in x give non-finite results.
  */
 int qmatvec_q8_0(const void *w, int64_t row_offset, int64_t rows, int64_t K,
                  const float *x, int batch, float *y, int64_t ldy, qk_stream_t stream);

@@ -24,6 +24,9 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int64_t> g_skip_item{-1};
 std::atomic<int> g_programmatic{0};
 std::atomic<int> g_gemm_skip_chunk{-1};
+// batch 2..8 on the tensor cores: 0 never, 1 where it is the faster form
+// (the default), 2 wherever the format and K allow it (tests)
+std::atomic<int> g_gemv_tc{1};
 
 // Strict-blocks mode starts on when the environment sets QK_STRICT=1.
 int strict_from_env()
@@ -67,6 +70,28 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
     if (qk::strict_blocks_reject(fmt, K)) return QK_ERR_BAD_DIM;
     if (!aligned(w, fmt == qk::kFmtQ4K ? 16 : 2) || !aligned(x, 4) || !aligned(y, 4))
         return QK_ERR_ALIGN;
+    // batch 2..8 of Q8_0 / Q4_K: the tensor-core form where the format and
+    // K allow it and it is the faster form: every SM gets at least one whole
+    // 128-row tile (the tensor cores work on 128 rows whatever their number)
+    // and, for Q4_K, the batch is 4 or more (at batch 2 and 3 the fp32 form
+    // keeps up with its 4-bit weights)
+    const int tc_mode = g_gemv_tc.load();
+    if (!pair && batch >= 2 && tc_mode != 0) {
+        qk::GemvTcPlan tp;
+        int sms = 0, smem = 0;
+        const bool faster = qk::device_limits(&sms, &smem) && rows >= 128LL * sms &&
+                            (fmt == qk::kFmtQ80 || batch >= 4);
+        if ((tc_mode == 2 || faster) && qk::gemv_tc_plan(fmt, rows, K, &tp)) {
+            if (row_offset > (INT64_MAX / tp.row_bytes) - rows) return QK_ERR_BAD_DIM;
+            int *err = error_word_ptr();
+            if (!err) return QK_ERR_CUDA;
+            const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * tp.row_bytes;
+            cudaError_t e = qk::gemv_tc_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
+                                               reinterpret_cast<cudaStream_t>(stream), tp, err, g_wait_limit_ns.load(),
+                                               g_programmatic.load() != 0);
+            return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
+        }
+    }
     // the kernel keeps a launch's activation rows in shared memory: a batch
     // whose activations do not fit is cut into launches of fewer rows (as
     // even as possible); only a single row that does not fit is refused
@@ -393,6 +418,25 @@ int qk_debug_gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, int pair
                            p.XU, p.cpl, p.nw, p.m, p.LU, p.cpa, p.off_stage, p.wide, p.kw};
     int k = 0;
     for (; k < n && k < 17; ++k) out[k] = v[k];
+    return k;
+}
+
+// Test hook, not part of the public header: the tensor-core form of later
+// batch 2..8 GEMV calls: 0 never (the fp32 form), 1 where it is the faster
+// form (the default), 2 wherever the format and K allow it.  Returns the
+// previous setting.
+int qk_debug_gemv_tc(int mode) { return g_gemv_tc.exchange(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
+
+// Test hook, not part of the public header: the tensor-core GEMV plan for an
+// explicit device, as {G, NC, row_stride, stage_bytes, NS, smem, grid,
+// off_stage, off_bop}; -1 when the format and K do not take that form.
+int qk_debug_gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin, int64_t *out, int n)
+{
+    qk::GemvTcPlan p;
+    if (!out || !qk::gemv_tc_plan_for(fmt, rows, K, sms, smem_optin, &p)) return -1;
+    const int64_t v[9] = {p.G, p.NC, p.row_stride, p.stage_bytes, p.NS, p.smem, p.grid, p.off_stage, p.off_bop};
+    int k = 0;
+    for (; k < n && k < 9; ++k) out[k] = v[k];
     return k;
 }
 

@@ -200,6 +200,15 @@ bool gemv_plan_for(int fmt, int64_t rows, int64_t K, int batch, bool pair, int64
 
 }  // namespace
 
+bool device_limits(int *sms, int *smem_optin)
+{
+    const DevInfo di = dev_info();
+    if (di.sms <= 0) return false;
+    *sms = di.sms;
+    *smem_optin = di.smem_optin;
+    return true;
+}
+
 // Launch plan of a GEMV call; returns false if it cannot fit in shared memory.
 bool gemv_plan(int fmt, int64_t rows, int64_t K, int batch, bool pair, GemvPlan *p, int64_t n_assign)
 {

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qk {
@@ -30,6 +31,28 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
                         int batch, float *y, int64_t ldy, cudaStream_t st, const GemvPlan &p,
                         int *err, uint64_t wait_ns, int64_t skip_item, bool pdl, int64_t up_rows = 0,
                         const int32_t *expid = nullptr, int64_t n_experts = 0, int xk = 1);
+
+// Plan of the batch 2..8 tensor-core GEMV (qk_gemv_tc.cu): groups of 32
+// columns, 256-column items a tile, stage ring and shared-memory layout.
+struct GemvTcPlan {
+    int G, NC, chunk_bytes, row_stride, stage_bytes, NS;
+    int off_bop, off_scale, off_xsum, off_out, off_flag, off_xch, off_stage, smem, grid;
+    int64_t row_bytes;
+};
+bool gemv_tc_plan(int fmt, int64_t rows, int64_t K, GemvTcPlan *p);
+bool gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin, GemvTcPlan *p);
+cudaError_t gemv_tc_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x, int batch,
+                           float *y, int64_t ldy, cudaStream_t st, const GemvTcPlan &p, int *err, uint64_t wait_ns,
+                           bool pdl);
+// The driver's tensor-map encoder (qk_gemm.cu), looked up once.
+namespace gemm {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+}  // namespace gemm
+// SM count and shared memory per block (opt-in) of the current device.
+bool device_limits(int *sms, int *smem_optin);
 
 // The device error word of the current device and the bound of device waits.
 int *library_error_word();

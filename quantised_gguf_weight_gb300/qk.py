@@ -97,6 +97,10 @@ def load(path: str | None = None):
         lib.qk_debug_gemv_plan.restype = I
         lib.qk_debug_gemv_plan_for.argtypes = [I, I64, I64, I, I, I64, I, I, ctypes.POINTER(ctypes.c_int64), I]
         lib.qk_debug_gemv_plan_for.restype = I
+        lib.qk_debug_gemv_tc.argtypes = [I]
+        lib.qk_debug_gemv_tc.restype = I
+        lib.qk_debug_gemv_tc_plan_for.argtypes = [I, I64, I64, I, I, ctypes.POINTER(ctypes.c_int64), I]
+        lib.qk_debug_gemv_tc_plan_for.restype = I
         _lib = lib
         return lib
 
@@ -388,6 +392,27 @@ def debug_gemv_plan_for(fmt: str, rows: int, K: int, batch: int, sms: int, smem_
     if n < 0:
         return None
     return dict(zip(PLAN_FOR_FIELDS, list(out)[:n]))
+
+
+def debug_gemv_tc(mode: int) -> int:
+    """Test hook: the tensor-core form of later batch 2..8 GEMV calls: 0 never (the
+    fp32 form), 1 where it is the faster form (the default), 2 wherever the format
+    and K allow it.  Returns the previous setting."""
+    return int(load().qk_debug_gemv_tc(int(mode)))
+
+
+TC_PLAN_FIELDS = ("G", "NC", "row_stride", "stage_bytes", "NS", "smem", "grid", "off_stage", "off_bop")
+
+
+def debug_gemv_tc_plan_for(fmt: str, rows: int, K: int, sms: int, smem_optin: int) -> dict | None:
+    """Test hook: the tensor-core GEMV plan (batch 2..8) for an explicit device, computed
+    on the host; None when the format and K do not take that form."""
+    out = (ctypes.c_int64 * len(TC_PLAN_FIELDS))()
+    n = load().qk_debug_gemv_tc_plan_for({"q8_0": 0, "q4_k": 1, "q6_k": 2}[fmt], int(rows), int(K), int(sms),
+                                         int(smem_optin), out, len(TC_PLAN_FIELDS))
+    if n < 0:
+        return None
+    return dict(zip(TC_PLAN_FIELDS, list(out)[:n]))
 
 
 def debug_gemv_plan(fmt: str, rows: int, K: int, batch: int) -> dict:

@@ -94,3 +94,54 @@ def test_split_k_over_warps_for_few_row_groups():
                         continue
                     assert 1 <= q["kw"] <= max(1, q["nkc"])
                     assert q["kw"] == 1 or (q["nkc"] > 1 and q["nw"] % q["kw"] == 0)
+
+
+# ---------------------------------------------------------------- tensor-core form (batch 2..8)
+
+def tc_plan(fmt, rows, K):
+    return qk.debug_gemv_tc_plan_for(fmt, rows, K, SMS, SMEM)
+
+
+def test_tensor_core_form_depends_on_format_and_K_only():
+    """Q8_0 takes it for K a multiple of 128 that fits, Q4_K for any K that
+    fits, Q6_K never; the plan is the same for every row count but the grid."""
+    for fmt in ("q8_0", "q4_k", "q6_k"):
+        for K in KS + [128, 640, 2048, 4864]:
+            plans = [tc_plan(fmt, rows, K) for rows in ROWS]
+            taken = {p is not None for p in plans}
+            assert len(taken) == 1, (fmt, K)
+            if fmt == "q6_k" or (fmt == "q8_0" and K % 128):
+                assert not taken.pop(), (fmt, K)
+            if plans[0] is not None:
+                same = {tuple(v for k, v in p.items() if k != "grid") for p in plans}
+                assert len(same) == 1, (fmt, K)
+                assert [p["grid"] for p in plans] == [min(r, SMS) for r in ROWS]
+    # the configurations that use it
+    assert tc_plan("q8_0", 151936, 896) is not None        # Q8_0 lm_head
+    assert tc_plan("q4_k", 28672, 4096) is not None        # Llama-8B gate+up
+    assert tc_plan("q4_k", 4096, 14336) is None            # its activations do not fit
+    assert tc_plan("q8_0", 4096, 14336) is None
+    assert tc_plan("q8_0", 1000, 4096) is not None          # Q8_0: the activations and two stages fit up to 4096
+    assert tc_plan("q8_0", 1000, 4224) is None
+    assert tc_plan("q4_k", 1000, 4864) is not None          # Q4_K: up to 4864
+    assert tc_plan("q4_k", 1000, 5120) is None
+
+
+@pytest.mark.parametrize("fmt,K", [("q8_0", 128), ("q8_0", 896), ("q8_0", 4096), ("q4_k", 256), ("q4_k", 300),
+                                   ("q4_k", 4096), ("q4_k", 4864)])
+def test_tensor_core_plan_layout(fmt, K):
+    """Groups and items cover the padded K, the B operand (32 bytes a column,
+    1024-byte aligned) and the tables precede at least two stages, and all of
+    it fits in the block's shared memory."""
+    p = tc_plan(fmt, 1000, K)
+    Kp = -(-K // 256) * 256 if fmt == "q4_k" else K
+    assert p["G"] * 32 == Kp
+    assert p["NC"] == -(-Kp // 256)
+    assert p["off_bop"] % 1024 == 0
+    assert p["off_bop"] + 32 * Kp <= p["off_stage"]
+    assert p["off_stage"] % 128 == 0
+    assert p["row_stride"] % 16 == 0 and (p["row_stride"] // 16) % 2 == 1    # conflict-free row reads
+    # Q4_K: one box of 128 rows x 144 bytes; Q8_0: four of 64 rows x 144 bytes
+    assert p["stage_bytes"] == 128 * 144 if fmt == "q4_k" else 4 * 64 * 144
+    assert 2 <= p["NS"] <= 8
+    assert p["smem"] == p["off_stage"] + p["NS"] * p["stage_bytes"] + 1024 <= SMEM
