@@ -88,7 +88,7 @@ int gemv_entry(int fmt, const void *w, int64_t row_offset, int64_t rows, int64_t
             const uint8_t *w_rows = static_cast<const uint8_t *>(w) + row_offset * tp.row_bytes;
             cudaError_t e = qk::gemv_tc_launch(fmt, w_rows, rows, K, x, batch, y, ldy,
                                                reinterpret_cast<cudaStream_t>(stream), tp, err, g_wait_limit_ns.load(),
-                                               g_programmatic.load() != 0);
+                                               g_programmatic.load() != 0, g_skip_item.load());
             return e == cudaSuccess ? QK_OK : QK_ERR_CUDA;
         }
     }
@@ -385,9 +385,9 @@ int qk_set_strict_blocks(int enable) { return g_strict_blocks.exchange(enable ? 
 int qk_version(void) { return 100; }
 
 // Test hook, not part of the public header: in CTA 0 of every later GEMV
-// launch, consumer warp 0's item number `item` is never copied (-1 restores
-// normal operation), so that warp's bounded wait runs out and the launch
-// records QK_ERR_TIMEOUT.
+// launch, consumer warp 0's item number `item` (the tensor-core form: the
+// CTA's item `item`) is never copied (-1 restores normal operation), so a
+// bounded wait runs out and the launch records QK_ERR_TIMEOUT.
 int64_t qk_debug_skip_item(int64_t item) { return g_skip_item.exchange(item); }
 
 // Test hook: the launch plan a GEMV call of this shape would use, as

@@ -73,6 +73,7 @@ struct GemvTcArgs {
     int stage_bytes, NS;
     int off_bop, off_scale, off_xsum, off_out, off_flag, off_xch, off_stage;
     int ph0, ph1;          // Q8_0: 16-byte phase of the rows of even / odd index within their boxes
+    int64_t skip_item;     // test hook: CTA 0 never loads this item (-1: off)
     uint64_t wait_ns;
     int *err;
 };
@@ -378,7 +379,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                 const int64_t row0 = r_begin + static_cast<int64_t>(t) * kTcM;
                 const uint32_t bar = sb + kBarFull + 8u * s;
                 const uint32_t dst = stage0 + static_cast<uint32_t>(s * a.stage_bytes);
-                if (FMT == kFmtQ4K) {
+                if (blockIdx.x == 0 && i == a.skip_item) {
+                    // test hook: this item is never loaded, so the converters' bounded wait runs out
+                } else if (FMT == kFmtQ4K) {
                     // 128 rows x one super-block (rows past the call read as zeros)
                     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kTcM * a.chunk_bytes));
                     tma_load_2d(dst, &tm0, c * a.chunk_bytes, static_cast<int32_t>(row0), bar, pol);
@@ -403,7 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
             }
             // the boxes issued land before the CTA leaves
             for (int i = max(0, last_issued - NS + 1); i <= last_issued; ++i)
-                mbar_wait(sb + kBarFull + 8u * (i % NS), (i / NS) & 1, a.wait_ns);
+                if (!(blockIdx.x == 0 && i == a.skip_item))
+                    mbar_wait(sb + kBarFull + 8u * (i % NS), (i / NS) & 1, a.wait_ns);
         }
         __syncwarp();
     } else if (warp == kTcIssuer) {
@@ -833,7 +837,7 @@ bool gemv_tc_plan(int fmt, int64_t rows, int64_t K, GemvTcPlan *p)
 
 cudaError_t gemv_tc_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x, int batch,
                            float *y, int64_t ldy, cudaStream_t st, const GemvTcPlan &p, int *err, uint64_t wait_ns,
-                           bool pdl)
+                           bool pdl, int64_t skip_item)
 {
     GemvTcArgs a;
     a.w = w_rows;
@@ -845,6 +849,7 @@ cudaError_t gemv_tc_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t
     a.row_bytes = p.row_bytes;
     a.G = p.G;
     a.NC = p.NC;
+    a.skip_item = skip_item;
     a.chunk_bytes = p.chunk_bytes;
     a.row_stride = p.row_stride;
     a.stage_bytes = p.stage_bytes;

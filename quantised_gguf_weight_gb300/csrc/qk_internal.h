@@ -43,7 +43,7 @@ bool gemv_tc_plan(int fmt, int64_t rows, int64_t K, GemvTcPlan *p);
 bool gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin, GemvTcPlan *p);
 cudaError_t gemv_tc_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K, const float *x, int batch,
                            float *y, int64_t ldy, cudaStream_t st, const GemvTcPlan &p, int *err, uint64_t wait_ns,
-                           bool pdl);
+                           bool pdl, int64_t skip_item = -1);
 // The driver's tensor-map encoder (qk_gemm.cu), looked up once.
 namespace gemm {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,

@@ -162,3 +162,28 @@ def test_default_form_choice(qk):
         torch.cuda.synchronize()
         assert not torch.equal(y_tc, y_32), (fmt, rows, batch)      # the two forms differ in their bits
         assert torch.equal(y_auto, y_tc if tc else y_32), (fmt, rows, batch)
+
+
+@pytest.mark.parametrize("fmt,K,item", [("q8_0", 896, 0), ("q4_k", 4096, 5)])
+def test_tensor_core_bounded_wait_times_out_and_context_survives(qk, orc, fmt, K, item):
+    """An item whose weights are never loaded (test hook, CTA 0) makes the
+    converters' bounded wait run out: the launch records QK_ERR_TIMEOUT, the
+    tensor memory is freed, and later launches work normally."""
+    rows, batch = 3000, 4
+    wq = synth.weights(fmt, rows, K, seed=47)
+    x = synth.activations(batch, K, seed=47)
+    wd, xd = torch.from_numpy(wq).cuda(), torch.from_numpy(x).cuda()
+    assert qk.device_error() == 0
+    old = qk.set_wait_limit_ns(20_000_000)
+    qk.debug_skip_item(item)
+    try:
+        _call(qk, fmt, wd, 0, rows, K, xd)
+        assert qk.device_error() == 6
+    finally:
+        qk.debug_skip_item(-1)
+        qk.set_wait_limit_ns(old)
+    assert qk.device_error() == 0
+    for _ in range(3):                      # the tensor memory of every SM is free again
+        y = _call(qk, fmt, wd, 0, rows, K, xd).cpu().numpy()
+    yr, s = orc.gemv(fmt, wq, K, x)
+    _check(y, yr, s, "after timeout")
