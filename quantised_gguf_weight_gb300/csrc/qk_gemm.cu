@@ -226,6 +226,10 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 mbar_wait(bar(kBarXFull + t % kStages), (t / kStages) & 1, a.wait_ns);
             }
         }
+        // the other lanes wait here, blocked, until lane 0 is done: the warp
+        // reaches the cluster barrier below converged, and lane 0 does not
+        // share its issue slots with lanes spinning in that barrier
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // -------------------------------------------------------- MMA issuer (even CTA)
@@ -284,6 +288,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 mbar_arrive_remote(peer0 + 8u * s);
             }
         }
+        __syncwarp();            // (as for warp 0: converged before the cluster barrier)
     } else {
         // ------------------------------------------------------------ dequantise + epilogue
         // thread -> weight row t of the tile and half `sel` of each 64-column
