@@ -257,32 +257,32 @@ __device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int
 __device__ __forceinline__ void q4k_tc_store_a(const uint4 &q0, const uint4 &q1, uint32_t taddr)
 {
     constexpr uint32_t kOne = 0x64006400u, kMinus = 0xE400E400u;   // fp16 1024 and -1024
-    uint32_t lo[16], hi[16];
 #pragma unroll
-    for (int w8 = 0; w8 < 8; ++w8) {
-        const uint4 &v = w8 < 4 ? q0 : q1;
-        const uint32_t w = (w8 & 3) == 0 ? v.x : (w8 & 3) == 1 ? v.y : (w8 & 3) == 2 ? v.z : v.w;
-        const uint32_t w1 = w >> 8;
-        lo[2 * w8] = hadd2_bits(lop3_and_or(w, 0x000F000Fu, kOne), kMinus);
-        lo[2 * w8 + 1] = hadd2_bits(lop3_and_or(w1, 0x000F000Fu, kOne), kMinus);
-        hi[2 * w8] = hadd2_bits(lop3_and_or(w, 0x00F000F0u, kOne), kMinus);
-        hi[2 * w8 + 1] = hadd2_bits(lop3_and_or(w1, 0x00F000F0u, kOne), kMinus);
+    for (int e = 0; e < 2; ++e) {                // low nibbles (sub-block 2m), then high (2m+1): one store each
+        const uint32_t mask = e ? 0x00F000F0u : 0x000F000Fu;
+        uint32_t r[16];
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) {
+            const uint4 &v = w8 < 4 ? q0 : q1;
+            const uint32_t w = (w8 & 3) == 0 ? v.x : (w8 & 3) == 1 ? v.y : (w8 & 3) == 2 ? v.z : v.w;
+            r[2 * w8] = hadd2_bits(lop3_and_or(w, mask, kOne), kMinus);
+            r[2 * w8 + 1] = hadd2_bits(lop3_and_or(w >> 8, mask, kOne), kMinus);
+        }
+        tmem_st_32x32b_x16(taddr + 16u * e, r);
     }
-    tmem_st_32x32b_x16(taddr, lo);
-    tmem_st_32x32b_x16(taddr + 16u, hi);
 }
 
-// Q8_0, kTcGPW blocks of a chunk whose first byte sits PH bytes past the
-// 16-byte boundary w0 of a row's 288-byte span (its first 144 bytes at sp0,
-// the rest at sp1): the blocks' exact fp16 q (pairs, block jj in r[jj]) and
-// their d.  Only the 16-byte words the blocks touch are read, so the last
-// word ends inside the span.  Registers only: the tensor-memory stores come
-// after the caller's branch on PH, with the warp converged.
+// Q8_0, one block whose first byte sits PH bytes past the 16-byte boundary
+// w0 of a row's 288-byte span (its first 144 bytes at sp0, the rest at sp1):
+// the block's exact fp16 q (pairs) and its d.  Only the 16-byte words the
+// block touches are read, so the last word ends inside the span.  Registers
+// only: the tensor-memory store comes after the caller's branch on PH, with
+// the warp converged.
 template <int PH>
-__device__ __forceinline__ void q80_tc_convert(const uint8_t *sp0, const uint8_t *sp1, int w0,
-                                               uint32_t (&r)[kTcGPW][16], float (&d)[kTcGPW])
+__device__ __forceinline__ void q80_tc_convert(const uint8_t *sp0, const uint8_t *sp1, int w0, uint32_t (&r)[16],
+                                               float &d)
 {
-    constexpr int NLD = (PH + 34 * kTcGPW + 15) / 16;
+    constexpr int NLD = (PH + 34 + 15) / 16;
     uint32_t wx[4 * NLD];
 #pragma unroll
     for (int i = 0; i < NLD; ++i) {
@@ -294,15 +294,11 @@ __device__ __forceinline__ void q80_tc_convert(const uint8_t *sp0, const uint8_t
         wx[4 * i + 3] = v.w ^ 0x80808080u;
     }
     constexpr uint32_t kBias = 0x64646464u, kMinus = 0xE480E480u;   // fp16 high bytes of 1024+u; -1152
+    d = half_bits_to_float(((wx[PH >> 2] >> (8 * (PH & 3))) ^ 0x8080u) & 0xFFFFu);
 #pragma unroll
-    for (int jj = 0; jj < kTcGPW; ++jj) {
-        const int bb = PH + 34 * jj;
-        d[jj] = half_bits_to_float(((wx[bb >> 2] >> (8 * (bb & 3))) ^ 0x8080u) & 0xFFFFu);
-#pragma unroll
-        for (int pi = 0; pi < 16; ++pi) {
-            const int bo = bb + 2 + 2 * pi;
-            r[jj][pi] = hadd2_bits(prmt(wx[bo >> 2], kBias, (bo & 3) ? 0x4342u : 0x4140u), kMinus);
-        }
+    for (int pi = 0; pi < 16; ++pi) {
+        const int bo = PH + 2 + 2 * pi;
+        r[pi] = hadd2_bits(prmt(wx[bo >> 2], kBias, (bo & 3) ? 0x4342u : 0x4140u), kMinus);
     }
 }
 
@@ -561,8 +557,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                     const uint8_t *sp1 = sp0 + kQ8Half;
                     const int o = par ? a.ph1 : a.ph0;
                     auto at = [&](int off) { return off < 144 ? sp0 + off : sp1 + (off - 144); };
-                    const int ph = (o + 34 * kTcGPW * h) & 15;
-                    const int w0 = o + 34 * kTcGPW * h - ph;             // window start (16-byte aligned)
                     // outliers first (the blocks' d from the stage)
 #pragma unroll
                     for (int jj = 0; jj < kTcGPW; ++jj) {
@@ -586,28 +580,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                             }
                         }
                     }
-                    float dq[kTcGPW];
-                    uint32_t r[kTcGPW][16];
-                    // the rows of a warp share one parity, so ph is the same
-                    // for all its lanes; the branch holds register work and
+                    // one block at a time (fewer registers live); the rows of a
+                    // warp share one parity, so each block's phase is the same
+                    // for all its lanes, and the branch holds register work and
                     // shared-memory reads only
-                    switch (ph) {
-                    case 0: q80_tc_convert<0>(sp0, sp1, w0, r, dq); break;
-                    case 2: q80_tc_convert<2>(sp0, sp1, w0, r, dq); break;
-                    case 4: q80_tc_convert<4>(sp0, sp1, w0, r, dq); break;
-                    case 6: q80_tc_convert<6>(sp0, sp1, w0, r, dq); break;
-                    case 8: q80_tc_convert<8>(sp0, sp1, w0, r, dq); break;
-                    case 10: q80_tc_convert<10>(sp0, sp1, w0, r, dq); break;
-                    case 12: q80_tc_convert<12>(sp0, sp1, w0, r, dq); break;
-                    default: q80_tc_convert<14>(sp0, sp1, w0, r, dq); break;
+#pragma unroll
+                    for (int jj = 0; jj < kTcGPW; ++jj) {
+                        const int bo = o + 34 * (kTcGPW * h + jj);
+                        const int ph = bo & 15;
+                        const int w0 = bo - ph;
+                        float dq = 0.f;
+                        uint32_t r[16];
+                        switch (ph) {
+                        case 0: q80_tc_convert<0>(sp0, sp1, w0, r, dq); break;
+                        case 2: q80_tc_convert<2>(sp0, sp1, w0, r, dq); break;
+                        case 4: q80_tc_convert<4>(sp0, sp1, w0, r, dq); break;
+                        case 6: q80_tc_convert<6>(sp0, sp1, w0, r, dq); break;
+                        case 8: q80_tc_convert<8>(sp0, sp1, w0, r, dq); break;
+                        case 10: q80_tc_convert<10>(sp0, sp1, w0, r, dq); break;
+                        case 12: q80_tc_convert<12>(sp0, sp1, w0, r, dq); break;
+                        default: q80_tc_convert<14>(sp0, sp1, w0, r, dq); break;
+                        }
+                        scur[jj] = dq;
+                        if (jj + 1 == kTcGPW) {
+                            __syncwarp();
+                            mbar_arrive_if(sb + kBarEmpty + 8u * s, lane == 0);   // the stage may be refilled
+                        }
+                        if (jj < nblk) tmem_st_32x32b_x16(acol + 16u * jj, r);
                     }
-                    __syncwarp();
-                    mbar_arrive_if(sb + kBarEmpty + 8u * s, lane == 0);   // the stage may be refilled
-#pragma unroll
-                    for (int jj = 0; jj < kTcGPW; ++jj)
-                        if (jj < nblk) tmem_st_32x32b_x16(acol + 16u * jj, r[jj]);
-#pragma unroll
-                    for (int jj = 0; jj < kTcGPW; ++jj) scur[jj] = dq[jj];
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -626,25 +626,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                     break;
                 }
                 tc_fence_after();
-                uint32_t dv[kTcGPW][16];
-#pragma unroll
-                for (int jj = 0; jj < kTcGPW; ++jj)
-                    if (jj < nblk) tmem_ld_32x32b_x16(tl + 256u + 128u * p + 16u * (kTcGPW * h + jj), dv[jj]);
-                tmem_ld_wait();
-                tc_fence_before();
 #pragma unroll
                 for (int jj = 0; jj < kTcGPW; ++jj) {
                     if (jj < nblk) {
-                        // batch rows in pairs (f32x2): accumulator columns b
-                        // (hi) and B + b (lo), per-row scales d*sc / dmin*m,
-                        // per-(group, batch row) scales S and sums of x
+                        // one group at a time (fewer registers live): batch
+                        // rows in pairs (f32x2), accumulator columns b (hi) and
+                        // B + b (lo), per-row scales d*sc / dmin*m, per-(group,
+                        // batch row) scales S and sums of x
+                        uint32_t dv[16];
+                        tmem_ld_32x32b_x16(tl + 256u + 128u * p + 16u * (kTcGPW * h + jj), dv);
+                        tmem_ld_wait();
                         const int g = 8 * c + kTcGPW * h + jj;
                         const uint64_t dsc2 = pack2f(sprev[jj], sprev[jj]);
                         const uint64_t ndm2 = FMT == kFmtQ4K ? pack2f(-sprev[kTcGPW + jj], -sprev[kTcGPW + jj]) : 0ull;
 #pragma unroll
                         for (int mm = 0; mm < B / 2; ++mm) {
-                            const uint64_t hi2 = pack2(dv[jj][2 * mm], dv[jj][2 * mm + 1]);
-                            const uint64_t lo2 = pack2(dv[jj][B + 2 * mm], dv[jj][B + 2 * mm + 1]);
+                            const uint64_t hi2 = pack2(dv[2 * mm], dv[2 * mm + 1]);
+                            const uint64_t lo2 = pack2(dv[B + 2 * mm], dv[B + 2 * mm + 1]);
                             const uint64_t s2 = *reinterpret_cast<const uint64_t *>(stab + 8 * g + 2 * mm);
                             uint64_t a2 = pack2f(acc[2 * mm], acc[2 * mm + 1]);
                             a2 = fma_f32x2(dsc2, mul_f32x2(add_f32x2(hi2, lo2), s2), a2);
@@ -655,7 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                             acc[2 * mm + 1] = r2.y;
                         }
                         if constexpr (B & 1) {
-                            const float tsum = (__uint_as_float(dv[jj][B - 1]) + __uint_as_float(dv[jj][2 * B - 1])) *
+                            const float tsum = (__uint_as_float(dv[B - 1]) + __uint_as_float(dv[2 * B - 1])) *
                                                stab[8 * g + B - 1];
                             acc[B - 1] = fmaf(sprev[jj], tsum, acc[B - 1]);
                             if constexpr (FMT == kFmtQ4K)
@@ -663,6 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                         }
                     }
                 }
+                tc_fence_before();
 #pragma unroll
                 for (int b = 0; b < B; ++b) acc[b] += oprev[b];
                 if (c == NC - 1) {
