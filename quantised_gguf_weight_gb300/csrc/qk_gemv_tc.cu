@@ -79,8 +79,11 @@ struct GemvTcArgs {
 };
 
 // barrier block (offsets from the 1024-aligned base)
-constexpr uint32_t kBarFull = 0, kBarEmpty = 64, kBarAFull = 128, kBarMma = 144, kBarXFull = 160,
-                   kBarXEmpty = 176, kTmemSlot = 192, kAbort = 196;
+static_assert((kTcCW & (kTcCW - 1)) == 0, "the exchange counts arrivals modulo kTcCW");
+// (kXCount: per tile parity and lane quarter, the converter warps that have
+// left their partial sums of a tile)
+constexpr uint32_t kBarFull = 0, kBarEmpty = 64, kBarAFull = 128, kBarMma = 144, kTmemSlot = 192, kAbort = 196,
+                   kXCount = 200;
 
 // One lane of the (converged) warp is elected.
 __device__ __forceinline__ bool elect_one()
@@ -137,116 +140,135 @@ __device__ __forceinline__ uint32_t bop_chunk(int k, int n)
 }
 
 // x -> B operand, per-group scales, Q4_K group sums, outliers.  Four lanes
-// take one (batch row, group) unit, eight columns each.
+// take one (batch row, group) unit, eight columns each; a warp takes 8 units
+// a round.  The loads of up to kStageBatch rounds are issued together (two
+// 16-byte loads a lane and round where x allows it) before any of them is
+// used, so a call pays about one memory latency per kStageBatch rounds.
+constexpr int kStageBatch = 4;
+
 template <int FMT, int B>
 __device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int cw, int lane)
 {
     const int q4 = lane & 3;
     const int units = B * a.G;
+    constexpr int kRound = 8 * kTcConvWarps;                 // units a round (all converter warps)
     float *stab = reinterpret_cast<float *>(sm + a.off_scale);
     float *xtab = reinterpret_cast<float *>(sm + a.off_xsum);
-    float2 *otab = reinterpret_cast<float2 *>(sm + a.off_out);
+    float *otab = reinterpret_cast<float *>(sm + a.off_out);
     uint8_t *ftab = sm + a.off_flag;
-    // the loads of a round are issued one round ahead
-    auto load = [&](int base, float (&v)[8]) {
-        const int u = base + (lane >> 2);
-        const bool act = u < units;
-        const int b = act ? u / a.G : 0;
-        const int g = act ? u - b * a.G : 0;
-        const int64_t c0 = 32LL * g + 8 * q4;
+    const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15u) == 0);
+    for (int base0 = cw * 8; base0 < units; base0 += kStageBatch * kRound) {
+        float vb[kStageBatch][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = (act && c0 + e < a.K) ? a.x[b * a.K + c0 + e] : 0.f;
-    };
-    float vn[8];
-    load(cw * 8, vn);
-    for (int base = cw * 8; base < units; base += 8 * kTcConvWarps) {
-        float v[8];
+        for (int r = 0; r < kStageBatch; ++r) {
+            const int u = base0 + r * kRound + (lane >> 2);
+            const bool act = u < units;
+            const int b = act ? u / a.G : 0;
+            const int g = act ? u - b * a.G : 0;
+            const int64_t c0 = 32LL * g + 8 * q4;
+            const float *src = a.x + b * a.K + c0;
+            if (act && vec && c0 + 8 <= a.K) {
+                const float4 lo = __ldg(reinterpret_cast<const float4 *>(src));
+                const float4 hi = __ldg(reinterpret_cast<const float4 *>(src) + 1);
+                vb[r][0] = lo.x; vb[r][1] = lo.y; vb[r][2] = lo.z; vb[r][3] = lo.w;
+                vb[r][4] = hi.x; vb[r][5] = hi.y; vb[r][6] = hi.z; vb[r][7] = hi.w;
+            } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = vn[e];
-        if (base + 8 * kTcConvWarps < units) load(base + 8 * kTcConvWarps, vn);
-        const int u = base + (lane >> 2);
-        const bool act = u < units;
-        const int b = act ? u / a.G : 0;
-        const int g = act ? u - b * a.G : 0;
-        uint32_t ab[8], lmax = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            ab[e] = __float_as_uint(v[e]) & 0x7FFFFFFFu;
-            lmax = max(lmax, ab[e]);
+                for (int e = 0; e < 8; ++e) vb[r][e] = (act && c0 + e < a.K) ? __ldg(src + e) : 0.f;
+            }
         }
-        uint32_t gmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, 1));
-        gmax = max(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 2));
-        const bool nonfinite = gmax >= 0x7F800000u;
-        // the batch-1 outlier rule: the only value whose exponent is within
-        // 2 of the group's largest is carried exactly, off the pieces
-        const int e1 = static_cast<int>(gmax >> 23);
-        const uint32_t thr = e1 >= 2 ? static_cast<uint32_t>(e1 - 2) << 23 : 0u;
-        int cnt = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) cnt += ab[e] >= thr ? 1 : 0;
-        int gcnt = cnt + __shfl_xor_sync(0xFFFFFFFFu, cnt, 1);
-        gcnt += __shfl_xor_sync(0xFFFFFFFFu, gcnt, 2);
-        const bool has_out = !nonfinite && gcnt == 1;
-        int oe = -1;
-        if (has_out && cnt == 1) {
+        for (int r = 0; r < kStageBatch; ++r) {
+            if (base0 + r * kRound >= units) break;              // the same for the warp
+            const float (&v)[8] = vb[r];
+            const int u = base0 + r * kRound + (lane >> 2);
+            const bool act = u < units;
+            const int b = act ? u / a.G : 0;
+            const int g = act ? u - b * a.G : 0;
+            uint32_t ab[8], lmax = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                ab[e] = __float_as_uint(v[e]) & 0x7FFFFFFFu;
+                lmax = max(lmax, ab[e]);
+            }
+            uint32_t gmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, 1));
+            gmax = max(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 2));
+            const bool nonfinite = gmax >= 0x7F800000u;
+            // the batch-1 outlier rule: the only value whose exponent is within
+            // 2 of the group's largest is carried exactly, off the pieces
+            const int e1 = static_cast<int>(gmax >> 23);
+            const uint32_t thr = e1 >= 2 ? static_cast<uint32_t>(e1 - 2) << 23 : 0u;
+            int cnt = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cnt += ab[e] >= thr ? 1 : 0;
+            int gcnt = cnt + __shfl_xor_sync(0xFFFFFFFFu, cnt, 1);
+            gcnt += __shfl_xor_sync(0xFFFFFFFFu, gcnt, 2);
+            const bool has_out = !nonfinite && gcnt == 1;
+            int oe = -1;
+            if (has_out && cnt == 1) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (ab[e] >= thr) oe = e;
+            }
+            uint32_t lm2 = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (ab[e] >= thr) oe = e;
-        }
-        uint32_t lm2 = 0;
+                if (e != oe) lm2 = max(lm2, ab[e]);
+            uint32_t gm2 = max(lm2, __shfl_xor_sync(0xFFFFFFFFu, lm2, 1));
+            gm2 = max(gm2, __shfl_xor_sync(0xFFFFFFFFu, gm2, 2));
+            // scale: the largest kept magnitude lands in [2^14, 2^15) (Q4_K high
+            // nibbles: [2^10, 2^11)); groups below 2^-100 keep the scale of 2^-100
+            int E = static_cast<int>(gm2 >> 23) - 127;
+            if (E < -100) E = -100;
+            const int k = 14 - E;                                  // in [-113, 114]
+            const int kx = (FMT == kFmtQ4K && (g & 1)) ? k - 4 : k;
+            const float f = __int_as_float((127 + kx) << 23);
+            float sum = 0.f;
+            uint32_t ob = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (e != oe) lm2 = max(lm2, ab[e]);
-        uint32_t gm2 = max(lm2, __shfl_xor_sync(0xFFFFFFFFu, lm2, 1));
-        gm2 = max(gm2, __shfl_xor_sync(0xFFFFFFFFu, gm2, 2));
-        // scale: the largest kept magnitude lands in [2^14, 2^15) (Q4_K high
-        // nibbles: [2^10, 2^11)); groups below 2^-100 keep the scale of 2^-100
-        int E = static_cast<int>(gm2 >> 23) - 127;
-        if (E < -100) E = -100;
-        const int k = 14 - E;                                  // in [-113, 114]
-        const int kx = (FMT == kFmtQ4K && (g & 1)) ? k - 4 : k;
-        const float f = __int_as_float((127 + kx) << 23);
-        float sum = 0.f;
-        uint32_t ob = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (e != oe) sum += v[e];
-            ob |= (e == oe) ? __float_as_uint(v[e]) : 0u;
-        }
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t hp = 0, lp = 0;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int e = tc_kperm<FMT>(2 * j + t);
-                const float xs = (e == oe || nonfinite) ? 0.f : v[e] * f;
-                const __half hh = __float2half_rn(xs);
-                const __half hl = __float2half_rn(xs - __half2float(hh));
-                hp |= static_cast<uint32_t>(__half_as_ushort(hh)) << (16 * t);
-                lp |= static_cast<uint32_t>(__half_as_ushort(hl)) << (16 * t);
+            for (int e = 0; e < 8; ++e) {
+                if (e != oe) sum += v[e];
+                ob |= (e == oe) ? __float_as_uint(v[e]) : 0u;
             }
-            hw[j] = hp;
-            lw[j] = lp;
-        }
-        if (act) {
-            // B rows: the hi pieces of batch row b in row b, its lo pieces in row B + b
-            const int kc = 32 * g + 8 * q4;
-            *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, b)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, B + b)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            if (b == 0) {
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+            uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int n = 2 * B; n < 16; ++n)
-                    *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, n)) = make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 4; ++j) {
+                uint32_t hp = 0, lp = 0;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int e = tc_kperm<FMT>(2 * j + t);
+                    const float xs = (e == oe || nonfinite) ? 0.f : v[e] * f;
+                    const __half hh = __float2half_rn(xs);
+                    const __half hl = __float2half_rn(xs - __half2float(hh));
+                    hp |= static_cast<uint32_t>(__half_as_ushort(hh)) << (16 * t);
+                    lp |= static_cast<uint32_t>(__half_as_ushort(hl)) << (16 * t);
+                }
+                hw[j] = hp;
+                lw[j] = lp;
             }
-            if (q4 == 0) {
-                stab[g * 8 + b] = nonfinite ? __int_as_float(0x7FC00000) : __int_as_float((127 - k) << 23);
-                if (FMT == kFmtQ4K) xtab[g * 8 + b] = sum;
-                ftab[g * 8 + b] = has_out ? 1 : 0;
+            if (act) {
+                // B rows: the hi pieces of batch row b in row b, its lo pieces in row B + b
+                const int kc = 32 * g + 8 * q4;
+                *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, b)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, B + b)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                if (b == 0) {
+#pragma unroll
+                    for (int n = 2 * B; n < 16; ++n)
+                        *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, n)) = make_uint4(0, 0, 0, 0);
+                }
+                if (q4 == 0) {
+                    stab[g * 8 + b] = nonfinite ? __int_as_float(0x7FC00000) : __int_as_float((127 - k) << 23);
+                    if (FMT == kFmtQ4K) xtab[g * 8 + b] = sum;
+                    if (!has_out) ftab[g * 8 + b] = 0;
+                }
+                if (oe >= 0) {
+                    // the group's one outlier: its value, and its column + 1 as the flag
+                    otab[g * 8 + b] = __uint_as_float(ob);
+                    ftab[g * 8 + b] = static_cast<uint8_t>(8 * q4 + oe + 1);
+                }
             }
-            if (oe >= 0) otab[g * 8 + b] = make_float2(__uint_as_float(ob), __int_as_float(8 * q4 + oe));
         }
     }
 }
@@ -340,8 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
             mbar_init(sb + kBarAFull + 8u * p, kTcConvWarps);
             mbar_init(sb + kBarMma + 8u * p, 1);
         }
-        mbar_init(sb + kBarXFull, 4 * (kTcCW - 1));
-        mbar_init(sb + kBarXEmpty, 4);
+        for (int q = 0; q < 8; ++q) reinterpret_cast<uint32_t *>(sm + kXCount)[q] = 0u;
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 
         const float *stab = reinterpret_cast<const float *>(sm + a.off_scale);
         const float *xtab = reinterpret_cast<const float *>(sm + a.off_xsum);
-        const float2 *otab = reinterpret_cast<const float2 *>(sm + a.off_out);
+        const float *otab = reinterpret_cast<const float *>(sm + a.off_out);
         const uint8_t *ftab = sm + a.off_flag;
         float acc[B], ocur[B], oprev[B];
         float scur[2 * kTcGPW], sprev[2 * kTcGPW];              // Q8_0: d; Q4_K: d*sc, then dmin*m
@@ -535,12 +556,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 #pragma unroll
                             for (int b = 0; b < B; ++b) {
                                 const uint32_t fw = b < 4 ? fl.x : fl.y;
-                                if ((fw >> (8 * (b & 3))) & 0xFFu) {
-                                    const float2 o = otab[g * 8 + b];
-                                    const int col = __float_as_int(o.y);
+                                const int fb = static_cast<int>((fw >> (8 * (b & 3))) & 0xFFu);
+                                if (fb) {
+                                    const int col = fb - 1;
                                     const int qv = (slot[16 + 32 * h + col] >> (4 * e)) & 15;
                                     const float wv = fmaf(scur[e], static_cast<float>(qv), -scur[2 + e]);
-                                    ocur[b] += wv * o.x;
+                                    ocur[b] += wv * otab[g * 8 + b];
                                 }
                             }
                         }
@@ -570,11 +591,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 #pragma unroll
                                 for (int b = 0; b < B; ++b) {
                                     const uint32_t fw = b < 4 ? fl.x : fl.y;
-                                    if ((fw >> (8 * (b & 3))) & 0xFFu) {
-                                        const float2 ov = otab[g * 8 + b];
-                                        const int col = __float_as_int(ov.y);
+                                    const int fb = static_cast<int>((fw >> (8 * (b & 3))) & 0xFFu);
+                                    if (fb) {
+                                        const int col = fb - 1;
                                         const float wv = dj * static_cast<float>(static_cast<int8_t>(*at(bo + 2 + col)));
-                                        ocur[b] += wv * ov.x;
+                                        ocur[b] += wv * otab[g * 8 + b];
                                     }
                                 }
                             }
@@ -665,41 +686,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 #pragma unroll
                 for (int b = 0; b < B; ++b) acc[b] += oprev[b];
                 if (c == NC - 1) {
-                    // ---------------- the tile's rows: the warps of a quarter meet
-                    // (one exchange buffer: a tile's writers first wait for the
-                    // reads of the tile before, done a whole tile earlier)
-                    float *xch = reinterpret_cast<float *>(sm + a.off_xch);
+                    // ---------------- the tile's rows: each warp of a lane quarter
+                    // leaves its partial sums; the last of the four to arrive adds
+                    // them in the order h = 0..3 and stores the rows (no warp waits).
+                    // A tile's arrivals all come before those of the tile two
+                    // later (a warp reaches that one only after every warp has
+                    // converted the item after this tile's last), so two buffers
+                    // and counters by tile parity suffice; with two or more items
+                    // a tile, before those of the next tile too (one buffer).
+                    float *xch = reinterpret_cast<float *>(sm + a.off_xch) + (NC == 1 ? (t & 1) * (kTcCW * kTcM * B) : 0);
+                    uint32_t *cnt = reinterpret_cast<uint32_t *>(sm + kXCount) + 4 * (t & 1) + qd;
                     const int64_t row0 = r_begin + static_cast<int64_t>(t) * kTcM;
                     const int n = static_cast<int>(min(static_cast<int64_t>(kTcM), r_end - row0));
-                    if (h > 0) {
-                        bool ok2 = true;
-                        if (t >= 1) ok2 = !*abort_flag && mbar_wait_sleep(sb + kBarXEmpty, (t - 1) & 1, a.wait_ns);
-                        ok2 = __all_sync(0xFFFFFFFFu, ok2);
-                        if (!ok2) {
-                            fail();
-                            break;
-                        }
 #pragma unroll
-                        for (int b = 0; b < B; ++b) xch[((h - 1) * kTcM + L) * 8 + b] = acc[b];
-                        __syncwarp();
-                        mbar_arrive_if(sb + kBarXFull, lane == 0);
-                    } else {
-                        bool ok2 = !*abort_flag && mbar_wait_sleep(sb + kBarXFull, t & 1, a.wait_ns);
-                        ok2 = __all_sync(0xFFFFFFFFu, ok2);
-                        if (!ok2) {
-                            fail();
-                            break;
-                        }
+                    for (int b = 0; b < B; ++b) xch[(h * kTcM + L) * B + b] = acc[b];
+                    __syncwarp();
+                    __threadfence_block();
+                    uint32_t prev = 0;
+                    if (lane == 0) prev = atomicAdd(cnt, 1u);
+                    prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+                    if ((prev & (kTcCW - 1)) == kTcCW - 1) {
+                        __threadfence_block();
                         float yv[B];
 #pragma unroll
                         for (int b = 0; b < B; ++b) {
-                            float v = acc[b];
+                            float v = xch[L * B + b];
 #pragma unroll
-                            for (int hh = 1; hh < kTcCW; ++hh) v += xch[((hh - 1) * kTcM + L) * 8 + b];
+                            for (int hh = 1; hh < kTcCW; ++hh) v += xch[(hh * kTcM + L) * B + b];
                             yv[b] = v;
                         }
-                        __syncwarp();
-                        mbar_arrive_if(sb + kBarXEmpty, lane == 0);
                         if (rho < n) {
 #pragma unroll
                             for (int b = 0; b < B; ++b) a.y[b * a.ldy + row0 + rho] = yv[b];
@@ -801,9 +816,11 @@ bool gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin,
     const int64_t off_scale = off_bop + 32 * Kp;
     const int64_t off_xsum = off_scale + 32LL * G;
     const int64_t off_out = off_xsum + (fmt == kFmtQ4K ? 32LL * G : 0);
-    const int64_t off_flag = off_out + 64LL * G;
+    const int64_t off_flag = off_out + 32LL * G;
     const int64_t off_xch = round_up_tc(off_flag + 8LL * G, 16);
-    const int64_t off_stage = round_up_tc(off_xch + static_cast<int64_t>(kTcCW - 1) * kTcM * 8 * 4, 128);
+    // the partial sums of a tile: 4 warps x 128 rows x up to 8 batch rows
+    // (two buffers when a tile is one item)
+    const int64_t off_stage = round_up_tc(off_xch + (NC == 1 ? 2 : 1) * static_cast<int64_t>(kTcCW) * kTcM * 8 * 4, 128);
     const int64_t budget = static_cast<int64_t>(smem_optin) - 1024;   // alignment slack of the base
     int64_t ns = (budget - off_stage) / stage_bytes;
     if (ns > kTcMaxStages) ns = kTcMaxStages;
