@@ -149,36 +149,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Eight floats from a 32-byte aligned global address in one 256-bit load
-// (read-only path).
-__device__ __forceinline__ void ldg_v8(const float *p, float (&v)[8])
-{
-    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
-                 : "l"(p));
-}
-
-// Named barrier that also returns whether any of its threads passed true.
-__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0u;
-}
-
-// A compile-time bool carried as a type (to pick one of two forms of a generic lambda).
-template <bool V>
-struct BoolTag {
-    static constexpr bool value = V;
-};
-
 // ---------------------------------------------------------------- numerics helpers
 
 // fp16 bits -> fp32 (exact), through the CUDA half conversion.

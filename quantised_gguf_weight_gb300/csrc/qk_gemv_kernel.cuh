@@ -731,10 +731,9 @@ __device__ __forceinline__ float sum8_skip(const float (&v)[8], int skip)
 // Each value becomes m = rint(x * 2^(21-E)), |m| <= 2^22, stored as three
 // byte planes (planes 0, 1 unsigned, plane 2 signed; the fourth byte of each
 // 16-byte slot unused); a group holding a NaN or an infinity gets a NaN
-// scale (its planes then do not matter).  Returns whether this thread
-// marked a group as holding an outlier.
+// scale (its planes then do not matter).
 template <int FMT, int NTH>
-__device__ __forceinline__ bool stage_x1(const GemvArgs &a, const float *x0, uint32_t cwarp, uint32_t lane,
+__device__ __forceinline__ void stage_x1(const GemvArgs &a, const float *x0, uint32_t cwarp, uint32_t lane,
                                          uint32_t xs_addr, float *xsum, float *xscale, float *xout)
 {
     constexpr uint32_t UC = FMT == kFmtQ80 ? 32 : 128;
@@ -747,11 +746,8 @@ __device__ __forceinline__ bool stage_x1(const GemvArgs &a, const float *x0, uin
     const uint32_t K = static_cast<uint32_t>(a.K);
     const uint32_t p_total = static_cast<uint32_t>(a.U) * PU;
     const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x0) & 15u) == 0);
-    const bool vec32 = (K % 8 == 0) && ((reinterpret_cast<uintptr_t>(x0) & 31u) == 0);
     // pieces base + i*NTH + lane (i < UNR) of a round; the next round's loads
-    // are issued before this round's arithmetic (a piece is one 32-byte load
-    // when x allows it: two 16-byte loads a lane would each touch twice the
-    // cache lines they use)
+    // are issued before this round's arithmetic
     auto load = [&](uint32_t base, float (&v)[UNR][8]) {
         const uint32_t ns = min(UNR, (p_total - base + NTH - 1) / NTH);
 #pragma unroll
@@ -761,9 +757,7 @@ __device__ __forceinline__ bool stage_x1(const GemvArgs &a, const float *x0, uin
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[i][k] = 0.f;
             if (i < ns && pc < p_total) {
-                if (vec32 && c0 + 7 < K) {
-                    ldg_v8(x0 + c0, v[i]);
-                } else if (vec && c0 + 7 < K) {
+                if (vec && c0 + 7 < K) {
                     const float4 lo = __ldg(reinterpret_cast<const float4 *>(x0 + c0));
                     const float4 hi = __ldg(reinterpret_cast<const float4 *>(x0 + c0) + 1);
                     v[i][0] = lo.x; v[i][1] = lo.y; v[i][2] = lo.z; v[i][3] = lo.w;
@@ -777,7 +771,6 @@ __device__ __forceinline__ bool stage_x1(const GemvArgs &a, const float *x0, uin
         }
     };
     float v[UNR][8], nx[UNR][8];
-    bool marked = false;
     if (cwarp * 32 < p_total) load(cwarp * 32, v);
     for (uint32_t base = cwarp * 32; base < p_total; base += UNR * NTH) {
         if (base + UNR * NTH < p_total) load(base + UNR * NTH, nx);   // the same for the warp
@@ -855,7 +848,6 @@ __device__ __forceinline__ bool stage_x1(const GemvArgs &a, const float *x0, uin
 #pragma unroll
         for (uint32_t i = 0; i < UNR; ++i) {
             if (!(i < ns) || pc[i] >= p_total) continue;
-            marked |= outl[i];
             const bool finite = (gmax[i] >> 23) != 255u;
             const int E = max(static_cast<int>(gref[i] >> 23) - 127, -96);
             const float up = __int_as_float((148 - E) << 23);     // 2^(21-E)
@@ -906,7 +898,6 @@ __device__ __forceinline__ bool stage_x1(const GemvArgs &a, const float *x0, uin
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[i][k] = nx[i][k];
     }
-    return marked;
 }
 
 template <int FMT, int B, int NTH>
@@ -1192,20 +1183,17 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     // the weights do not depend on earlier kernels, x may: with programmatic
     // dependent launch only this part waits for the previous grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    bool any_outl = false;     // batch 1: some group staged in this CTA has an outlier
-    if constexpr (B == 1) {
-        const bool mine = stage_x1<FMT, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
-                                                 reinterpret_cast<float *>(smem + a.off_xsum),
-                                                 reinterpret_cast<float *>(smem + a.off_xscale),
-                                                 reinterpret_cast<float *>(smem + a.off_xout));
-        any_outl = named_bar_or(1, 32 * NW, mine);
-    } else {
+    if constexpr (B == 1)
+        stage_x1<FMT, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
+                               reinterpret_cast<float *>(smem + a.off_xsum),
+                               reinterpret_cast<float *>(smem + a.off_xscale),
+                               reinterpret_cast<float *>(smem + a.off_xout));
+    else
         stage_x<FMT, B, 32 * NW>(a, x0, cwarp, static_cast<uint32_t>(lane), smem_u32(xs),
                                  reinterpret_cast<float *>(smem + a.off_xsum),
                                  reinterpret_cast<float *>(smem + a.off_xscale),
                                  reinterpret_cast<float *>(smem + a.off_xout));
-        named_bar_sync(1, 32 * NW);
-    }
+    named_bar_sync(1, 32 * NW);
     if (cwarp >= nw) return;
 
     // the team sums of a row group and its outputs
@@ -1250,42 +1238,271 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                 }
         }
     };
-    // the consumer loop, in two forms at batch 1: with the exact outlier terms
-    // (some group staged in this CTA has an outlier) and without any of that code
-    auto consume = [&](auto outl_tag) {
-        constexpr bool OUTL = decltype(outl_tag)::value;
-        float *part = reinterpret_cast<float *>(smem + a.off_part);
-        const uintptr_t wbase = reinterpret_cast<uintptr_t>(w0);
-        const int chunk_lu = SW * cpl;                 // lane units per chunk
-        const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
-        uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
-        bool failed = false;
-        const uint32_t g_first = cwarp / kw, g_step = nw / kw, c_first = cwarp % kw;
-        // batch 1: bit c set when this lane's units of chunk c have a group with
-        // an outlier (a sign bit of a group scale), found once after staging
-        uint64_t omask = 0;
-        if constexpr (OUTL) {
-            for (uint32_t c = c_first; c < nkc && c < 64; c += kw) {
-                uint32_t sg = 0;
-                for (int i = 0; i < cpl; ++i) {
-                    const int lu = static_cast<int>(c) * SW * cpl + i * SW + sl;
-                    if (lu >= a.LU) break;
-                    if constexpr (FMT == kFmtQ80) {
-                        sg |= __float_as_uint(xscale[lu]);
-                    } else {
-                        const uint4 s0 = *reinterpret_cast<const uint4 *>(xscale + 4 * lu);
-                        sg |= s0.x | s0.y | s0.z | s0.w;
-                        if constexpr (FMT == kFmtQ4K) {
-                            const uint4 s1 = *reinterpret_cast<const uint4 *>(xscale + 4 * (XH + lu));
-                            sg |= s1.x | s1.y | s1.z | s1.w;
-                        }
+    float *part = reinterpret_cast<float *>(smem + a.off_part);
+    const uintptr_t wbase = reinterpret_cast<uintptr_t>(w0);
+    const int chunk_lu = SW * cpl;                 // lane units per chunk
+    const uint32_t st0 = cwarp * m;                // this warp's stages st0 .. st0+m-1
+    uint32_t tm = 0, par = 0;                      // stage offset and parity of the next item
+    bool failed = false;
+    const uint32_t g_first = cwarp / kw, g_step = nw / kw, c_first = cwarp % kw;
+    // batch 1: bit c set when this lane's units of chunk c have a group with
+    // an outlier (a sign bit of a group scale), found once after staging
+    uint64_t omask = 0;
+    if constexpr (B == 1) {
+        for (uint32_t c = c_first; c < nkc && c < 64; c += kw) {
+            uint32_t sg = 0;
+            for (int i = 0; i < cpl; ++i) {
+                const int lu = static_cast<int>(c) * SW * cpl + i * SW + sl;
+                if (lu >= a.LU) break;
+                if constexpr (FMT == kFmtQ80) {
+                    sg |= __float_as_uint(xscale[lu]);
+                } else {
+                    const uint4 s0 = *reinterpret_cast<const uint4 *>(xscale + 4 * lu);
+                    sg |= s0.x | s0.y | s0.z | s0.w;
+                    if constexpr (FMT == kFmtQ4K) {
+                        const uint4 s1 = *reinterpret_cast<const uint4 *>(xscale + 4 * (XH + lu));
+                        sg |= s1.x | s1.y | s1.z | s1.w;
                     }
                 }
-                if (sg >> 31) omask |= 1ull << c;
             }
-            if (nkc > 64) omask = ~0ull;                 // (beyond 64 chunks: every chunk is checked)
+            if (sg >> 31) omask |= 1ull << c;
         }
-        for (uint32_t g = g_first; g < n_groups && !failed; g += g_step) {
+        if (nkc > 64) omask = ~0ull;                 // (beyond 64 chunks: every chunk is checked)
+    }
+    for (uint32_t g = g_first; g < n_groups && !failed; g += g_step) {
+        const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
+        const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
+        float acc[R][B];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
+        for (uint32_t c = c_first; c < nkc; c += kw) {
+            const uint32_t st = st0 + tm;
+            const bool ochunk = B == 1 && ((omask >> (c < 64 ? c : 63)) & 1u) != 0;
+            bool ok = mbar_wait_sleep(bar_full + 8u * st, par, a.wait_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok);   // the warp leaves together or not at all
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    record_error(a.err, kErrTimeout);
+                }
+                failed = true;
+                break;
+            }
+            const uint8_t *stage = smem + a.off_stage + st * static_cast<uint32_t>(a.stage_bytes);
+            // where this lane's rows start their chunk in the stage (rows past
+            // the group's end read its last row and are not stored)
+            // (pair mode: the item's rows lr < P are gate rows, the rest their up rows)
+            const uint8_t *rowp[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                int lr = team * R + r;
+                const bool up = a.pair && lr >= gr;
+                const int q = min(up ? lr - gr : lr, n - 1);      // output row within the group
+                const int64_t grow = row0 + q + (up ? a.up_rows : 0);   // weight row
+                if (nkc == 1) {
+                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>((row0 + (up ? a.up_rows : 0)) * a.row_bytes);
+                    rowp[r] = stage + (up ? a.up_stage_off : 0) + (gsrc & 15u) + static_cast<int64_t>(q) * a.row_bytes;
+                } else {
+                    lr = up ? gr + q : q;
+                    const uintptr_t gsrc = wbase + static_cast<uintptr_t>(grow * a.row_bytes) +
+                                           static_cast<uintptr_t>(c) * a.chunk_bytes;
+                    rowp[r] = stage + lr * a.row_stride + (gsrc & 15u);
+                }
+            }
+            // lane units of this lane in this chunk: i*SW + sl (i < cpl) from
+            // the chunk's start, lane unit c*chunk_lu + i*SW + sl of the row
+            // this chunk's sums, started from zero: the row's sum adds them up
+            // in chunk order (the same order when the chunks of a row group
+            // are shared by kw warps)
+            float pacc[R][B];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b) pacc[r][b] = 0.f;
+            const int lu0 = static_cast<int>(c) * chunk_lu + sl;
+            // batch 1: the exact terms of the outliers of this lane's groups,
+            // read from the stage before it is handed back (rare: a sign bit
+            // of a group scale), added after the unit's plane terms
+            float oterm[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) oterm[r] = 0.f;
+            if constexpr (FMT == kFmtQ4K) {
+                // a lane past the row's last unit (only in a row's last chunk)
+                // works on that last unit and its sums are dropped
+                const bool valid = lu0 < a.LU;
+                const int lu = valid ? lu0 : a.LU - 1;
+                const int su = lu - static_cast<int>(c) * chunk_lu;   // the unit within the chunk
+                const bool has_hi = 2 * lu + 1 < a.U;
+                auto outliers = [&]() {
+                    if (ochunk && valid) {
+                        const float4 s0 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(xscale + 4 * (XH + lu));
+                        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                        for (int j = 0; j < 8; ++j)
+                            if (sv[j] < 0.f && (j < 4 || has_hi)) {
+                                const int slot = 8 * ((j < 4 ? 0 : XH) + lu) + 2 * (j & 3);
+                                const float xv = xout[slot];
+                                const int i = __float_as_int(xout[slot + 1]);
+#pragma unroll
+                                for (int r = 0; r < R; ++r)
+                                    oterm[r] += q4k_outlier_term(rowp[r] + su * UB, j, i, xv);
+                            }
+                    }
+                };
+              if constexpr (B == 1 && WIDE) {
+                // one 128-column half at a time: the stage is handed back once
+                // the second half is in registers
+                uint4 hd[R], q4[R][4];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
+                    hd[r] = p[0];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) q4[r][i] = p[1 + i];
+                }
+                q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, pacc);
+                if (has_hi) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q4[r][i] = p[5 + i];
+                    }
+                }
+                outliers();
+                __syncwarp();
+                mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                if (has_hi)
+                    q4k_half_dig<R, 1>(hd, q4, xs + 16 * SU * (XH + lu), xsum + 4 * (XH + lu),
+                                       xscale + 4 * (XH + lu), pacc);
+              } else {
+                uint4 hd[R], qs[R][8];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
+                    hd[r] = p[0];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) qs[r][i] = p[1 + i];
+                }
+                outliers();
+                __syncwarp();
+                mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                const uint8_t *xa0 = xs + 16 * SU * lu;
+                const uint8_t *xa1 = xs + 16 * SU * (XH + lu);
+                if constexpr (B == 1)
+                    q4k_sb_dig<R>(hd, qs, has_hi, xa0, xa1, xsum + 4 * lu, xsum + 4 * (XH + lu),
+                                  xscale + 4 * lu, xscale + 4 * (XH + lu), pacc);
+                else if (valid)
+                    q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, pacc);
+              }
+                if constexpr (B == 1) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) pacc[r][0] = valid ? pacc[r][0] + oterm[r] : 0.f;
+                }
+            } else if constexpr (FMT == kFmtQ6K) {
+                // lane unit = half super-block: block li/2 of the chunk, half li%2
+                // (a chunk holds whole super-blocks: chunk_lu is even when nkc > 1)
+                Q6Half hr[R];
+                const bool valid = lu0 < a.LU;
+                const int lu = valid ? lu0 : a.LU - 1;     // past the row's end: its last unit, sums dropped
+                const int su = lu - static_cast<int>(c) * chunk_lu;
+#pragma unroll
+                for (int r = 0; r < R; ++r) q6_load(rowp[r] + (su >> 1) * 210, lu & 1, hr[r]);
+                if constexpr (B == 1) {
+                    if (ochunk && valid) {
+                        const float4 sc4 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
+                        const float scv[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+                        for (int t = 0; t < 4; ++t)
+                            if (scv[t] < 0.f) {
+                                const float xv = xout[8 * lu + 2 * t];
+                                const int i = __float_as_int(xout[8 * lu + 2 * t + 1]);
+#pragma unroll
+                                for (int r = 0; r < R; ++r)
+                                    oterm[r] += q6k_outlier_term(rowp[r] + (su >> 1) * 210, lu & 1, t, i, xv);
+                            }
+                    }
+                }
+                __syncwarp();
+                mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                const uint8_t *xa = xs + 16 * SU * lu;
+                if constexpr (B == 1) {
+                    q6k_half_dig<R>(hr, xa, xsum + 8 * lu, xscale + 4 * lu, pacc);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) pacc[r][0] = valid ? pacc[r][0] + oterm[r] : 0.f;
+                } else if (valid) {
+                    q6k_half_fp<B, R>(hr, xa, pacc);
+                }
+            } else {
+                // one block at a time (words in registers, realigned), the stage
+                // handed back once the lane's last block of the item is loaded
+#pragma unroll
+                for (int i = 0; i < CM; ++i) {
+                    if (i >= cpl) break;
+                    const int lu = lu0 + i * SW;
+                    const bool has = lu < a.LU;
+                    uint32_t wv[R][9], off[R];
+                    if (has) {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uintptr_t ad = reinterpret_cast<uintptr_t>(rowp[r] + (i * SW + sl) * UB);
+                            off[r] = static_cast<uint32_t>(ad & 3u);          // 0 or 2
+                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - off[r]);
+#pragma unroll
+                            for (int k = 0; k < 9; ++k) wv[r][k] = wp[k];
+                        }
+                        if (B == 1 && ochunk && xscale[lu] < 0.f) {
+                            const float xv = xout[2 * lu];
+                            const int ic = __float_as_int(xout[2 * lu + 1]);
+#pragma unroll
+                            for (int r = 0; r < R; ++r)
+                                oterm[r] += q8_outlier_term(rowp[r] + (i * SW + sl) * UB, ic, xv);
+                        }
+                    }
+                    if (i == cpl - 1) {
+                        __syncwarp();
+                        mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
+                    }
+                    if (has) {
+                        const uint8_t *xa = xs + 16 * SU * lu;
+                        if constexpr (B == 1)
+                            q8_blk_dig<R>(wv, off, xa, xscale[lu], pacc);
+                        else
+                            q8_blk_fp<B, R>(wv, off, xa, pacc);
+                    }
+                }
+                if constexpr (B == 1) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) pacc[r][0] += oterm[r];
+                }
+            }
+            if (kw == 1) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int b = 0; b < B; ++b) acc[r][b] += pacc[r][b];
+            } else {
+                float *pp = part + ((g * nkc + c) * 32u + static_cast<uint32_t>(lane)) * (R * B);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int b = 0; b < B; ++b) pp[r * B + b] = pacc[r][b];
+            }
+            if (++tm == m) {
+                tm = 0;
+                par ^= 1u;
+            }
+        }
+        if (failed) break;
+        if (kw == 1) finish(row0, n, acc);
+    }
+    if (kw > 1) {
+        // the warps of a row group meet; its first warp adds the chunk sums
+        // in chunk order and writes the outputs
+        named_bar_sync(2, 32 * static_cast<int>(nw));
+        const uint32_t g = cwarp / kw;
+        if (!failed && cwarp % kw == 0 && g < n_groups) {
             const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
             const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
             float acc[R][B];
@@ -1293,257 +1510,15 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
-            for (uint32_t c = c_first; c < nkc; c += kw) {
-                const uint32_t st = st0 + tm;
-                const bool ochunk = OUTL && ((omask >> (c < 64 ? c : 63)) & 1u) != 0;
-                bool ok = mbar_wait_sleep(bar_full + 8u * st, par, a.wait_ns);
-                ok = __all_sync(0xFFFFFFFFu, ok);   // the warp leaves together or not at all
-                if (!ok) {
-                    if (lane == 0) {
-                        *abort_flag = 1;
-                        record_error(a.err, kErrTimeout);
-                    }
-                    failed = true;
-                    break;
-                }
-                const uint8_t *stage = smem + a.off_stage + st * static_cast<uint32_t>(a.stage_bytes);
-                // where this lane's rows start their chunk in the stage (rows past
-                // the group's end read its last row and are not stored)
-                // (pair mode: the item's rows lr < P are gate rows, the rest their up rows)
-                const uint8_t *rowp[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    int lr = team * R + r;
-                    const bool up = a.pair && lr >= gr;
-                    const int q = min(up ? lr - gr : lr, n - 1);      // output row within the group
-                    const int64_t grow = row0 + q + (up ? a.up_rows : 0);   // weight row
-                    if (nkc == 1) {
-                        const uintptr_t gsrc = wbase + static_cast<uintptr_t>((row0 + (up ? a.up_rows : 0)) * a.row_bytes);
-                        rowp[r] = stage + (up ? a.up_stage_off : 0) + (gsrc & 15u) + static_cast<int64_t>(q) * a.row_bytes;
-                    } else {
-                        lr = up ? gr + q : q;
-                        const uintptr_t gsrc = wbase + static_cast<uintptr_t>(grow * a.row_bytes) +
-                                               static_cast<uintptr_t>(c) * a.chunk_bytes;
-                        rowp[r] = stage + lr * a.row_stride + (gsrc & 15u);
-                    }
-                }
-                // lane units of this lane in this chunk: i*SW + sl (i < cpl) from
-                // the chunk's start, lane unit c*chunk_lu + i*SW + sl of the row
-                // this chunk's sums, started from zero: the row's sum adds them up
-                // in chunk order (the same order when the chunks of a row group
-                // are shared by kw warps)
-                float pacc[R][B];
+            for (uint32_t c = 0; c < nkc; ++c) {
+                const float *pp = part + ((g * nkc + c) * 32u + static_cast<uint32_t>(lane)) * (R * B);
 #pragma unroll
                 for (int r = 0; r < R; ++r)
 #pragma unroll
-                    for (int b = 0; b < B; ++b) pacc[r][b] = 0.f;
-                const int lu0 = static_cast<int>(c) * chunk_lu + sl;
-                // batch 1: the exact terms of the outliers of this lane's groups,
-                // read from the stage before it is handed back (rare: a sign bit
-                // of a group scale), added after the unit's plane terms
-                float oterm[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) oterm[r] = 0.f;
-                if constexpr (FMT == kFmtQ4K) {
-                    // a lane past the row's last unit (only in a row's last chunk)
-                    // works on that last unit and its sums are dropped
-                    const bool valid = lu0 < a.LU;
-                    const int lu = valid ? lu0 : a.LU - 1;
-                    const int su = lu - static_cast<int>(c) * chunk_lu;   // the unit within the chunk
-                    const bool has_hi = 2 * lu + 1 < a.U;
-                    auto outliers = [&]() {
-                        if (ochunk && valid) {
-                            const float4 s0 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
-                            const float4 s1 = *reinterpret_cast<const float4 *>(xscale + 4 * (XH + lu));
-                            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                            for (int j = 0; j < 8; ++j)
-                                if (sv[j] < 0.f && (j < 4 || has_hi)) {
-                                    const int slot = 8 * ((j < 4 ? 0 : XH) + lu) + 2 * (j & 3);
-                                    const float xv = xout[slot];
-                                    const int i = __float_as_int(xout[slot + 1]);
-#pragma unroll
-                                    for (int r = 0; r < R; ++r)
-                                        oterm[r] += q4k_outlier_term(rowp[r] + su * UB, j, i, xv);
-                                }
-                        }
-                    };
-                  if constexpr (B == 1 && WIDE) {
-                    // one 128-column half at a time: the stage is handed back once
-                    // the second half is in registers
-                    uint4 hd[R], q4[R][4];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
-                        hd[r] = p[0];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) q4[r][i] = p[1 + i];
-                    }
-                    q4k_half_dig<R, 0>(hd, q4, xs + 16 * SU * lu, xsum + 4 * lu, xscale + 4 * lu, pacc);
-                    if (has_hi) {
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) q4[r][i] = p[5 + i];
-                        }
-                    }
-                    outliers();
-                    __syncwarp();
-                    mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
-                    if (has_hi)
-                        q4k_half_dig<R, 1>(hd, q4, xs + 16 * SU * (XH + lu), xsum + 4 * (XH + lu),
-                                           xscale + 4 * (XH + lu), pacc);
-                  } else {
-                    uint4 hd[R], qs[R][8];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint4 *p = reinterpret_cast<const uint4 *>(rowp[r] + su * UB);
-                        hd[r] = p[0];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) qs[r][i] = p[1 + i];
-                    }
-                    outliers();
-                    __syncwarp();
-                    mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
-                    const uint8_t *xa0 = xs + 16 * SU * lu;
-                    const uint8_t *xa1 = xs + 16 * SU * (XH + lu);
-                    if constexpr (B == 1)
-                        q4k_sb_dig<R>(hd, qs, has_hi, xa0, xa1, xsum + 4 * lu, xsum + 4 * (XH + lu),
-                                      xscale + 4 * lu, xscale + 4 * (XH + lu), pacc);
-                    else if (valid)
-                        q4k_sb_fp<B, R>(hd, qs, has_hi, xa0, xa1, xsum + lu, xsum + XH + lu, a.XU, pacc);
-                  }
-                    if constexpr (B == 1) {
-#pragma unroll
-                        for (int r = 0; r < R; ++r) pacc[r][0] = valid ? (OUTL ? pacc[r][0] + oterm[r] : pacc[r][0]) : 0.f;
-                    }
-                } else if constexpr (FMT == kFmtQ6K) {
-                    // lane unit = half super-block: block li/2 of the chunk, half li%2
-                    // (a chunk holds whole super-blocks: chunk_lu is even when nkc > 1)
-                    Q6Half hr[R];
-                    const bool valid = lu0 < a.LU;
-                    const int lu = valid ? lu0 : a.LU - 1;     // past the row's end: its last unit, sums dropped
-                    const int su = lu - static_cast<int>(c) * chunk_lu;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) q6_load(rowp[r] + (su >> 1) * 210, lu & 1, hr[r]);
-                    if constexpr (B == 1) {
-                        if (ochunk && valid) {
-                            const float4 sc4 = *reinterpret_cast<const float4 *>(xscale + 4 * lu);
-                            const float scv[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
-                            for (int t = 0; t < 4; ++t)
-                                if (scv[t] < 0.f) {
-                                    const float xv = xout[8 * lu + 2 * t];
-                                    const int i = __float_as_int(xout[8 * lu + 2 * t + 1]);
-#pragma unroll
-                                    for (int r = 0; r < R; ++r)
-                                        oterm[r] += q6k_outlier_term(rowp[r] + (su >> 1) * 210, lu & 1, t, i, xv);
-                                }
-                        }
-                    }
-                    __syncwarp();
-                    mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
-                    const uint8_t *xa = xs + 16 * SU * lu;
-                    if constexpr (B == 1) {
-                        q6k_half_dig<R>(hr, xa, xsum + 8 * lu, xscale + 4 * lu, pacc);
-#pragma unroll
-                        for (int r = 0; r < R; ++r) pacc[r][0] = valid ? (OUTL ? pacc[r][0] + oterm[r] : pacc[r][0]) : 0.f;
-                    } else if (valid) {
-                        q6k_half_fp<B, R>(hr, xa, pacc);
-                    }
-                } else {
-                    // one block at a time (words in registers, realigned), the stage
-                    // handed back once the lane's last block of the item is loaded
-#pragma unroll
-                    for (int i = 0; i < CM; ++i) {
-                        if (i >= cpl) break;
-                        const int lu = lu0 + i * SW;
-                        const bool has = lu < a.LU;
-                        uint32_t wv[R][9], off[R];
-                        if (has) {
-#pragma unroll
-                            for (int r = 0; r < R; ++r) {
-                                const uintptr_t ad = reinterpret_cast<uintptr_t>(rowp[r] + (i * SW + sl) * UB);
-                                off[r] = static_cast<uint32_t>(ad & 3u);          // 0 or 2
-                                const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - off[r]);
-#pragma unroll
-                                for (int k = 0; k < 9; ++k) wv[r][k] = wp[k];
-                            }
-                            if (B == 1 && ochunk && xscale[lu] < 0.f) {
-                                const float xv = xout[2 * lu];
-                                const int ic = __float_as_int(xout[2 * lu + 1]);
-#pragma unroll
-                                for (int r = 0; r < R; ++r)
-                                    oterm[r] += q8_outlier_term(rowp[r] + (i * SW + sl) * UB, ic, xv);
-                            }
-                        }
-                        if (i == cpl - 1) {
-                            __syncwarp();
-                            mbar_arrive_if(bar_empty + 8u * st, lane == 0);   // the stage may be refilled
-                        }
-                        if (has) {
-                            const uint8_t *xa = xs + 16 * SU * lu;
-                            if constexpr (B == 1)
-                                q8_blk_dig<R>(wv, off, xa, xscale[lu], pacc);
-                            else
-                                q8_blk_fp<B, R>(wv, off, xa, pacc);
-                        }
-                    }
-                    if constexpr (OUTL) {
-#pragma unroll
-                        for (int r = 0; r < R; ++r) pacc[r][0] += oterm[r];
-                    }
-                }
-                if (kw == 1) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int b = 0; b < B; ++b) acc[r][b] += pacc[r][b];
-                } else {
-                    float *pp = part + ((g * nkc + c) * 32u + static_cast<uint32_t>(lane)) * (R * B);
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int b = 0; b < B; ++b) pp[r * B + b] = pacc[r][b];
-                }
-                if (++tm == m) {
-                    tm = 0;
-                    par ^= 1u;
-                }
+                    for (int b = 0; b < B; ++b) acc[r][b] += pp[r * B + b];
             }
-            if (failed) break;
-            if (kw == 1) finish(row0, n, acc);
+            finish(row0, n, acc);
         }
-        if (kw > 1) {
-            // the warps of a row group meet; its first warp adds the chunk sums
-            // in chunk order and writes the outputs
-            named_bar_sync(2, 32 * static_cast<int>(nw));
-            const uint32_t g = cwarp / kw;
-            if (!failed && cwarp % kw == 0 && g < n_groups) {
-                const int64_t row0 = r_begin + static_cast<int64_t>(g) * gr;
-                const int n = static_cast<int>(min(static_cast<int64_t>(gr), r_end - row0));
-                float acc[R][B];
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
-                for (uint32_t c = 0; c < nkc; ++c) {
-                    const float *pp = part + ((g * nkc + c) * 32u + static_cast<uint32_t>(lane)) * (R * B);
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int b = 0; b < B; ++b) acc[r][b] += pp[r * B + b];
-                }
-                finish(row0, n, acc);
-            }
-        }
-    };
-    if constexpr (B == 1) {
-        if (any_outl)
-            consume(BoolTag<true>{});
-        else
-            consume(BoolTag<false>{});
-    } else {
-        consume(BoolTag<false>{});
     }
 }
 
