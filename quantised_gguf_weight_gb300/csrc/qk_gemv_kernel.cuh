@@ -1017,30 +1017,30 @@ __device__ __forceinline__ uint32_t span16(uintptr_t gs, uintptr_t ge)
     return static_cast<uint32_t>(((ge + 15) & ~static_cast<uintptr_t>(15)) - (gs & ~static_cast<uintptr_t>(15)));
 }
 
-__device__ __forceinline__ void copy_item(const GemvArgs &a, const uint8_t *w0, int64_t row0, int n, uint32_t c,
-                                          uint32_t dst, uint32_t bar, uint64_t pol)
+__device__ __forceinline__ void copy_item(const GemvArgs &a, bool pair, const uint8_t *w0, int64_t row0, int n,
+                                          uint32_t c, uint32_t dst, uint32_t bar, uint64_t pol)
 {
     const uint8_t *g0 = w0 + row0 * a.row_bytes;
-    const uint8_t *u0 = a.pair ? g0 + a.up_rows * a.row_bytes : nullptr;
+    const uint8_t *u0 = pair ? g0 + a.up_rows * a.row_bytes : nullptr;
     if (a.nkc == 1) {
         const uintptr_t gs = reinterpret_cast<uintptr_t>(g0), ge = gs + static_cast<uintptr_t>(n * a.row_bytes);
         uint32_t bytes = span16(gs, ge);
         uint32_t ubytes = 0;
         uintptr_t us = 0;
-        if (a.pair) {
+        if (pair) {
             us = reinterpret_cast<uintptr_t>(u0);
             ubytes = span16(us, us + static_cast<uintptr_t>(n * a.row_bytes));
         }
         mbar_arrive_expect_tx(bar, bytes + ubytes);
         bulk_g2s(dst, reinterpret_cast<const void *>(gs & ~static_cast<uintptr_t>(15)), bytes, bar, pol);
-        if (a.pair)
+        if (pair)
             bulk_g2s(dst + static_cast<uint32_t>(a.up_stage_off),
                      reinterpret_cast<const void *>(us & ~static_cast<uintptr_t>(15)), ubytes, bar, pol);
         return;
     }
     const int64_t cb = static_cast<int64_t>(c) * a.chunk_bytes;
     const int64_t cl = min(static_cast<int64_t>(a.chunk_bytes), a.row_bytes - cb);
-    const int spans = a.pair ? 2 : 1;
+    const int spans = pair ? 2 : 1;
     const int P = a.rows_w >> 1;
     uint32_t total = 0;
     for (int h = 0; h < spans; ++h)
@@ -1059,9 +1059,13 @@ __device__ __forceinline__ void copy_item(const GemvArgs &a, const uint8_t *w0, 
         }
 }
 
-template <int FMT, int B, bool WIDE = false>
+// PLAIN: a call without the SwiGLU pair and experts modes (their code is
+// left out of this instantiation, which keeps the kernel small).
+template <int FMT, int B, bool WIDE = false, bool PLAIN = false>
 __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_kernel(const GemvArgs a)
 {
+    const bool pair = !PLAIN && a.pair != 0;
+    const bool experts = !PLAIN && a.cpa > 0;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int R = gemv_rows(FMT, B);
     constexpr int NW = gemv_warps(FMT, B, WIDE);
@@ -1080,7 +1084,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     const float *x0 = a.x;
     float *y0 = a.y;
     int64_t r_begin, r_end;
-    if (a.cpa > 0) {
+    if (experts) {
         // experts mode: CTA -> (assignment, part of the expert's rows); the
         // expert id comes from an earlier kernel, so wait for it first
         const int64_t asg = blockIdx.x / a.cpa, j = blockIdx.x - asg * a.cpa;
@@ -1102,7 +1106,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
         r_begin = (a.rows * blockIdx.x) / nG;
         r_end = (a.rows * (blockIdx.x + 1)) / nG;
     }
-    const int gr = a.pair ? (a.rows_w >> 1) : a.rows_w;   // output rows per row group
+    const int gr = pair ? (a.rows_w >> 1) : a.rows_w;   // output rows per row group
     const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + gr - 1) / gr);
     const uint32_t nkc = static_cast<uint32_t>(a.nkc);
     const uint32_t kw = static_cast<uint32_t>(a.kw);
@@ -1144,7 +1148,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                     }
                     const bool skip = w == 0 && t == a.skip_item && blockIdx.x == 0;   // test hook
                     if (!skip) {
-                        copy_item(a, w0, row0, n, c, stage0 + st * static_cast<uint32_t>(a.stage_bytes), bar, pol);
+                        copy_item(a, pair, w0, row0, n, c, stage0 + st * static_cast<uint32_t>(a.stage_bytes), bar, pol);
                         issued_use[st] = static_cast<int>(use);
                     }
                     if (++tm == m) {
@@ -1210,7 +1214,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                     if (o < SW) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);   // SW is the same for the warp
                 v[r][b] = t;
             }
-        if (!a.pair) {
+        if (!pair) {
             // lane 0 of the team writes its rows
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -1298,7 +1302,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 int lr = team * R + r;
-                const bool up = a.pair && lr >= gr;
+                const bool up = pair && lr >= gr;
                 const int q = min(up ? lr - gr : lr, n - 1);      // output row within the group
                 const int64_t grow = row0 + q + (up ? a.up_rows : 0);   // weight row
                 if (nkc == 1) {
@@ -1527,10 +1531,10 @@ cudaError_t gemv_launch_q4k(int batch, bool wide, const GemvArgs &a, int grid, i
 cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q6k(int batch, bool wide, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
-template <int FMT, int B, bool WIDE = false>
+template <int FMT, int B, bool WIDE = false, bool PLAIN = false>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
-    auto kern = gemv_kernel<FMT, B, WIDE>;
+    auto kern = gemv_kernel<FMT, B, WIDE, PLAIN>;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

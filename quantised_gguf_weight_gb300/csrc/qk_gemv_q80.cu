@@ -7,7 +7,9 @@ namespace qk {
 cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
     switch (batch) {
-    case 1: return gemv_launch_one<kFmtQ80, 1>(a, grid, smem, st, pdl);
+    case 1:
+        if (!a.pair && a.cpa == 0) return gemv_launch_one<kFmtQ80, 1, false, true>(a, grid, smem, st, pdl);   // the plain form
+        return gemv_launch_one<kFmtQ80, 1>(a, grid, smem, st, pdl);
     case 2: return gemv_launch_one<kFmtQ80, 2>(a, grid, smem, st, pdl);
     case 3: return gemv_launch_one<kFmtQ80, 3>(a, grid, smem, st, pdl);
     case 4: return gemv_launch_one<kFmtQ80, 4>(a, grid, smem, st, pdl);
