@@ -1059,11 +1059,16 @@ __device__ __forceinline__ void copy_item(const GemvArgs &a, bool pair, const ui
         }
 }
 
-// PLAIN: a call without the SwiGLU pair and experts modes (their code is
-// left out of this instantiation, which keeps the kernel small).
-template <int FMT, int B, bool WIDE = false, bool PLAIN = false>
+// MODE: kModeAny, or a plain call (no SwiGLU pair, no experts mode) whose
+// row groups are split over warps (kModePlain) or not (kModePlainKw1).  The
+// code a plain instantiation does not need is left out: a smaller kernel
+// costs less instruction fetch when calls of different shapes alternate.
+constexpr int kModeAny = 0, kModePlain = 1, kModePlainKw1 = 2;
+
+template <int FMT, int B, bool WIDE = false, int MODE = kModeAny>
 __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_kernel(const GemvArgs a)
 {
+    constexpr bool PLAIN = MODE != kModeAny;
     const bool pair = !PLAIN && a.pair != 0;
     const bool experts = !PLAIN && a.cpa > 0;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1109,7 +1114,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
     const int gr = pair ? (a.rows_w >> 1) : a.rows_w;   // output rows per row group
     const uint32_t n_groups = static_cast<uint32_t>((r_end - r_begin + gr - 1) / gr);
     const uint32_t nkc = static_cast<uint32_t>(a.nkc);
-    const uint32_t kw = static_cast<uint32_t>(a.kw);
+    const uint32_t kw = MODE == kModePlainKw1 ? 1u : static_cast<uint32_t>(a.kw);
 
     // programmatic dependent launch: the next grid in the stream may start
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1531,10 +1536,10 @@ cudaError_t gemv_launch_q4k(int batch, bool wide, const GemvArgs &a, int grid, i
 cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 cudaError_t gemv_launch_q6k(int batch, bool wide, const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl);
 
-template <int FMT, int B, bool WIDE = false, bool PLAIN = false>
+template <int FMT, int B, bool WIDE = false, int MODE = kModeAny>
 cudaError_t gemv_launch_one(const GemvArgs &a, int grid, int smem, cudaStream_t st, bool pdl)
 {
-    auto kern = gemv_kernel<FMT, B, WIDE, PLAIN>;
+    auto kern = gemv_kernel<FMT, B, WIDE, MODE>;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

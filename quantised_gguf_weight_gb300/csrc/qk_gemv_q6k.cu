@@ -8,9 +8,12 @@ cudaError_t gemv_launch_q6k(int batch, bool wide, const GemvArgs &a, int grid, i
 {
     switch (batch) {
     case 1:
-        if (!a.pair && a.cpa == 0)   // the plain form (no pair or experts code)
-            return wide ? gemv_launch_one<kFmtQ6K, 1, true, true>(a, grid, smem, st, pdl)
-                        : gemv_launch_one<kFmtQ6K, 1, false, true>(a, grid, smem, st, pdl);
+        if (!a.pair && a.cpa == 0 && a.kw == 1)   // the plain forms (no pair or experts code)
+            return wide ? gemv_launch_one<kFmtQ6K, 1, true, kModePlainKw1>(a, grid, smem, st, pdl)
+                        : gemv_launch_one<kFmtQ6K, 1, false, kModePlainKw1>(a, grid, smem, st, pdl);
+        if (!a.pair && a.cpa == 0)
+            return wide ? gemv_launch_one<kFmtQ6K, 1, true, kModePlain>(a, grid, smem, st, pdl)
+                        : gemv_launch_one<kFmtQ6K, 1, false, kModePlain>(a, grid, smem, st, pdl);
         return wide ? gemv_launch_one<kFmtQ6K, 1, true>(a, grid, smem, st, pdl)
                     : gemv_launch_one<kFmtQ6K, 1>(a, grid, smem, st, pdl);
     case 2: return gemv_launch_one<kFmtQ6K, 2>(a, grid, smem, st, pdl);

@@ -8,7 +8,9 @@ cudaError_t gemv_launch_q80(int batch, const GemvArgs &a, int grid, int smem, cu
 {
     switch (batch) {
     case 1:
-        if (!a.pair && a.cpa == 0) return gemv_launch_one<kFmtQ80, 1, false, true>(a, grid, smem, st, pdl);   // the plain form
+        // the plain forms (no pair or experts code)
+        if (!a.pair && a.cpa == 0 && a.kw == 1) return gemv_launch_one<kFmtQ80, 1, false, kModePlainKw1>(a, grid, smem, st, pdl);
+        if (!a.pair && a.cpa == 0) return gemv_launch_one<kFmtQ80, 1, false, kModePlain>(a, grid, smem, st, pdl);
         return gemv_launch_one<kFmtQ80, 1>(a, grid, smem, st, pdl);
     case 2: return gemv_launch_one<kFmtQ80, 2>(a, grid, smem, st, pdl);
     case 3: return gemv_launch_one<kFmtQ80, 3>(a, grid, smem, st, pdl);
