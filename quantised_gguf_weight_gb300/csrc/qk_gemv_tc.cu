@@ -13,7 +13,7 @@
 //     hi pieces of batch row b, row B + b its lo pieces (MMA N = 16).
 //   W (the A operand, tensor memory): each thread of the 16 converter warps
 //     (4 per tensor-memory lane quarter, each taking 2 of an item's 8
-//     groups) decodes its part of one weight row of a 128-row tile into
+//     groups, or 1 of a Q8_0 row's last half item) decodes its part of one weight row of a 128-row tile into
 //     exact fp16 integers (Q8_0: q; Q4_K: q, or 16q for the high nibbles,
 //     whose x pieces are scaled down by 16 to match) and stores them into
 //     its tensor-memory lane.
@@ -517,7 +517,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                 const int64_t row0 = r_begin + static_cast<int64_t>(t) * kTcM;
                 const int n = static_cast<int>(min(static_cast<int64_t>(kTcM), r_end - row0));
                 const bool valid = rho < n;
-                const int nblk = max(0, min(kTcGPW, a.G - 8 * c - kTcGPW * h));   // this warp's groups
+                // this warp's groups gi0, gi0 + 1, ... (nblk of them): kTcGPW a
+                // part, or one a part when the item holds four groups or fewer
+                // (a Q8_0 row's last half item), so that all parts share it
+                const int ngi = min(8, a.G - 8 * c);
+                const int gi0 = ngi <= 4 ? h : kTcGPW * h;
+                const int nblk = ngi <= 4 ? (h < ngi ? 1 : 0) : max(0, min(kTcGPW, ngi - kTcGPW * h));
                 bool ok = !*abort_flag && mbar_wait_sleep(sb + kBarFull + 8u * s, use & 1, a.wait_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) {
@@ -525,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                     break;
                 }
                 const uint8_t *stg = sm + a.off_stage + s * a.stage_bytes;
-                const uint32_t acol = tl + 128u * p + static_cast<uint32_t>(16 * kTcGPW * h);
+                const uint32_t acol = tl + 128u * p + static_cast<uint32_t>(16 * gi0);
 #pragma unroll
                 for (int b = 0; b < B; ++b) ocur[b] = 0.f;
                 if constexpr (FMT == kFmtQ4K) {
@@ -581,11 +586,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                     // outliers first (the blocks' d from the stage)
 #pragma unroll
                     for (int jj = 0; jj < kTcGPW; ++jj) {
-                        const int g = 8 * c + kTcGPW * h + jj;
+                        const int g = 8 * c + gi0 + jj;
                         if (jj < nblk) {
                             const uint2 fl = *reinterpret_cast<const uint2 *>(ftab + 8 * g);
                             if ((fl.x | fl.y) != 0u && valid) {
-                                const int bo = o + 34 * (kTcGPW * h + jj);
+                                const int bo = o + 34 * (gi0 + jj);
                                 const float dj = half_bits_to_float(static_cast<uint32_t>(*at(bo)) |
                                                                     (static_cast<uint32_t>(*at(bo + 1)) << 8));
 #pragma unroll
@@ -607,20 +612,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                     // shared-memory reads only
 #pragma unroll
                     for (int jj = 0; jj < kTcGPW; ++jj) {
-                        const int bo = o + 34 * (kTcGPW * h + jj);
-                        const int ph = bo & 15;
-                        const int w0 = bo - ph;
                         float dq = 0.f;
                         uint32_t r[16];
-                        switch (ph) {
-                        case 0: q80_tc_convert<0>(sp0, sp1, w0, r, dq); break;
-                        case 2: q80_tc_convert<2>(sp0, sp1, w0, r, dq); break;
-                        case 4: q80_tc_convert<4>(sp0, sp1, w0, r, dq); break;
-                        case 6: q80_tc_convert<6>(sp0, sp1, w0, r, dq); break;
-                        case 8: q80_tc_convert<8>(sp0, sp1, w0, r, dq); break;
-                        case 10: q80_tc_convert<10>(sp0, sp1, w0, r, dq); break;
-                        case 12: q80_tc_convert<12>(sp0, sp1, w0, r, dq); break;
-                        default: q80_tc_convert<14>(sp0, sp1, w0, r, dq); break;
+                        if (jj < nblk) {                         // the same for the warp
+                            const int bo = o + 34 * (gi0 + jj);
+                            const int ph = bo & 15;
+                            const int w0 = bo - ph;
+                            switch (ph) {
+                            case 0: q80_tc_convert<0>(sp0, sp1, w0, r, dq); break;
+                            case 2: q80_tc_convert<2>(sp0, sp1, w0, r, dq); break;
+                            case 4: q80_tc_convert<4>(sp0, sp1, w0, r, dq); break;
+                            case 6: q80_tc_convert<6>(sp0, sp1, w0, r, dq); break;
+                            case 8: q80_tc_convert<8>(sp0, sp1, w0, r, dq); break;
+                            case 10: q80_tc_convert<10>(sp0, sp1, w0, r, dq); break;
+                            case 12: q80_tc_convert<12>(sp0, sp1, w0, r, dq); break;
+                            default: q80_tc_convert<14>(sp0, sp1, w0, r, dq); break;
+                            }
                         }
                         scur[jj] = dq;
                         if (jj + 1 == kTcGPW) {
@@ -639,7 +646,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                 // ---------------- epilogue of item j = i - 1
                 const int j = i - 1, p = j & 1;
                 const int t = tj, c = cj;
-                const int nblk = max(0, min(kTcGPW, a.G - 8 * c - kTcGPW * h));
+                const int ngi = min(8, a.G - 8 * c);
+                const int gi0 = ngi <= 4 ? h : kTcGPW * h;
+                const int nblk = ngi <= 4 ? (h < ngi ? 1 : 0) : max(0, min(kTcGPW, ngi - kTcGPW * h));
                 bool ok = !*abort_flag && mbar_wait_sleep(sb + kBarMma + 8u * p, (j >> 1) & 1, a.wait_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) {
@@ -655,9 +664,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                         // B + b (lo), per-row scales d*sc / dmin*m, per-(group,
                         // batch row) scales S and sums of x
                         uint32_t dv[16];
-                        tmem_ld_32x32b_x16(tl + 256u + 128u * p + 16u * (kTcGPW * h + jj), dv);
+                        tmem_ld_32x32b_x16(tl + 256u + 128u * p + 16u * (gi0 + jj), dv);
                         tmem_ld_wait();
-                        const int g = 8 * c + kTcGPW * h + jj;
+                        const int g = 8 * c + gi0 + jj;
                         const uint64_t dsc2 = pack2f(sprev[jj], sprev[jj]);
                         const uint64_t ndm2 = FMT == kFmtQ4K ? pack2f(-sprev[kTcGPW + jj], -sprev[kTcGPW + jj]) : 0ull;
 #pragma unroll
