@@ -85,11 +85,13 @@ struct Shape {
 };
 
 // barrier slots (8 bytes each) after the barrier offset, four per stage kind:
-// XFull (this CTA's copies of the stage landed: activations and Q4_K bytes),
-// AFull (this CTA's dequantising warps wrote the stage; implies XFull),
-// Empty (the pair's MMAs of the stage completed), Peer (even CTA: the odd
-// CTA's stage is complete)
-constexpr int kBarXFull = 0, kBarAFull = 4, kBarEmpty = 8, kBarPeer = 12, kBarAcc = 16, kBarDone = 17;
+// XFull (this CTA's activation copies of the stage landed), AFull (this
+// CTA's dequantising warps wrote the stage's weights; they have read its raw
+// bytes), Empty (the pair's MMAs of the stage completed), Peer (even CTA: the
+// odd CTA's stage is complete), RFull (this CTA's raw weight bytes of the
+// stage landed: Q4_K, and Q8_0 by TMA)
+constexpr int kBarXFull = 0, kBarAFull = 4, kBarEmpty = 8, kBarPeer = 12, kBarAcc = 16, kBarDone = 17,
+              kBarRFull = 18;
 constexpr int kOffTmemSlot = 184, kOffAbort = 188;
 
 struct Args {
@@ -150,6 +152,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarXFull + s), 1);
+            mbar_init(bar(kBarRFull + s), 1);
             mbar_init(bar(kBarAFull + s), kDeq / 32);   // one arrival per dequantising warp
             mbar_init(bar(kBarEmpty + s), 1);
             mbar_init(bar(kBarPeer + s), 1);
@@ -193,38 +196,71 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             };
-            // the weights do not depend on the kernel before this one: the
-            // first stages' weight copies go out before the wait for it (their
-            // bytes are announced without an arrival), the activations after
-            const int pre = nk < kStages ? nk : kStages;
-            if (L::raw_stage > 0)
-                for (int kc = 0; kc < pre; ++kc) {
-                    mbar_expect_tx(bar(kBarXFull + kc), static_cast<uint32_t>(L::raw_stage));
-                    raw_copies(kc, kc, bar(kBarXFull + kc));
+            // Two cursors.  Raw weight bytes of chunk kr go into raw slot
+            // kr % kStages once the dequantising warps have read the chunk
+            // kStages back (its AFull); they do not depend on the kernel
+            // before this one, so the first kStages go out before the wait for
+            // it.  The activations of chunk kb go into stage kb % kStages once
+            // the pair's MMAs of the chunk kStages back completed (Empty).  So
+            // a chunk's raw bytes are in place well before its stage frees, and
+            // the dequantisation overlaps the activation copy.  No cycle: raw
+            // kr needs the dequantisation of kr - kStages, which needs raw
+            // kr - kStages and the MMAs of kr - 2 kStages, whose activations
+            // (kb > kr - kStages) are out already.
+            int kr = 0, kb = 0;
+            if constexpr (L::raw_stage > 0) {
+                for (; kr < nk && kr < kStages; ++kr) {
+                    mbar_arrive_expect_tx(bar(kBarRFull + kr), static_cast<uint32_t>(L::raw_stage));
+                    raw_copies(kr, kr, bar(kBarRFull + kr));
                 }
+            } else {
+                kr = nk;
+            }
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            int issued = 0;
-            for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
-                const int s = kc % kStages;
-                if (kc >= kStages && !wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns,
-                                                    abort_flag, a.err, true))
-                    break;
-                if (!(kc == a.skip_chunk && blockIdx.x == 0)) {
-                    const uint32_t full = bar(kBarXFull + s);
-                    const bool early = kc < pre;           // weights already on their way
-                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(nh * L::b_half + (early ? 0 : L::raw_stage)));
-                    for (int h = 0; h < nh; ++h)
-                        tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kc * kBK,
-                                    m0 + h * kBN + static_cast<int>(rank) * kBNc, full, pol_x);
-                    if (!early) raw_copies(kc, s, full);
+            uint64_t idle_since = 0;
+            while ((kb < nk || kr < nk) && !*abort_flag) {
+                bool did = false;
+                if (kb < nk && (kb < kStages || mbar_test(bar(kBarEmpty + kb % kStages), ((kb / kStages) - 1) & 1))) {
+                    const int s = kb % kStages;
+                    if (!(kb == a.skip_chunk && blockIdx.x == 0)) {
+                        const uint32_t full = bar(kBarXFull + s);
+                        mbar_arrive_expect_tx(full, static_cast<uint32_t>(nh * L::b_half));
+                        for (int h = 0; h < nh; ++h)
+                            tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kb * kBK,
+                                        m0 + h * kBN + static_cast<int>(rank) * kBNc, full, pol_x);
+                    }
+                    ++kb;
+                    did = true;
                 }
-                ++issued;
+                if (kr < nk && kr < kb + kStages &&
+                    mbar_test(bar(kBarAFull + kr % kStages), ((kr / kStages) - 1) & 1)) {
+                    const int s = kr % kStages;
+                    mbar_arrive_expect_tx(bar(kBarRFull + s), static_cast<uint32_t>(L::raw_stage));
+                    raw_copies(kr, s, bar(kBarRFull + s));
+                    ++kr;
+                    did = true;
+                }
+                if (did) {
+                    idle_since = 0;
+                } else {
+                    // bounded: no progress for the wait limit aborts the CTA
+                    const uint64_t now = globaltimer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > a.wait_ns) {
+                        *abort_flag = 1;
+                        record_error(a.err, kErrTimeout);
+                    }
+                }
             }
             // let every copy issued land before the CTA can exit
-            for (int t = issued - kStages; t < issued; ++t) {
+            for (int t = kb - kStages; t < kb; ++t) {
                 if (t < 0 || (t == a.skip_chunk && blockIdx.x == 0)) continue;
                 mbar_wait(bar(kBarXFull + t % kStages), (t / kStages) & 1, a.wait_ns);
             }
+            if constexpr (L::raw_stage > 0)
+                for (int t = kr - kStages; t < kr; ++t)
+                    if (t >= 0) mbar_wait(bar(kBarRFull + t % kStages), (t / kStages) & 1, a.wait_ns);
         }
         // the other lanes wait here, blocked, until lane 0 is done: the warp
         // reaches the cluster barrier below converged, and lane 0 does not
@@ -241,6 +277,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 // polled: the issuing thread must not sleep past the phase
                 if (!ready) {
                     if (!wait_or_abort(bar(kBarAFull + s), par, a.wait_ns, abort_flag, a.err, true)) break;
+                    if (!wait_or_abort(bar(kBarXFull + s), par, a.wait_ns, abort_flag, a.err, true)) break;
                     if (!wait_or_abort(bar(kBarPeer + s), par, a.wait_ns, abort_flag, a.err, true)) break;
                 }
                 ready = false;
@@ -264,7 +301,8 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         // complete already?  Then its MMAs follow without a gap
                         const int s1 = (kc + 1) % kStages;
                         const uint32_t par1 = ((kc + 1) / kStages) & 1;
-                        ready = mbar_test(bar(kBarAFull + s1), par1) && mbar_test(bar(kBarPeer + s1), par1);
+                        ready = mbar_test(bar(kBarAFull + s1), par1) && mbar_test(bar(kBarXFull + s1), par1) &&
+                                mbar_test(bar(kBarPeer + s1), par1);
                     }
                 }
                 any = true;
@@ -279,12 +317,13 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
         } else if (lane == 0) {
             // -------------------------------------------------------- stage-ready forwarder (odd CTA)
-            // AFull of a stage implies its copies landed (the dequantising
-            // warps waited for them)
+            // the stage is complete when its weights are written (AFull) and
+            // its activation copy landed (XFull)
             const uint32_t peer0 = mapa_shared(bar(kBarPeer), 0);
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
                 if (!wait_or_abort(bar(kBarAFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err, true)) break;
+                if (!wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err, true)) break;
                 mbar_arrive_remote(peer0 + 8u * s);
             }
         }
@@ -300,9 +339,11 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
                 const int c = kc & 3;
-                // the stage's copies landed (which also means its MMAs of
-                // kStages chunks back completed: the producer waited for that)
-                const bool ok = wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                // the chunk's raw bytes landed, and the stage's weights of
+                // kStages chunks back are no longer read (their MMAs completed)
+                bool ok = wait_or_abort(bar(kBarRFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                if (ok && kc >= kStages)
+                    ok = wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
 #pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
@@ -375,7 +416,10 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // words around it are realigned as in the direct path
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
-                const bool ok = wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                // raw bytes landed; the stage's weights of kStages chunks back no longer read
+                bool ok = wait_or_abort(bar(kBarRFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                if (ok && kc >= kStages)
+                    ok = wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
                 const uint32_t pos = static_cast<uint32_t>((68 * kc) & 15) + 34u * static_cast<uint32_t>(sel);
                 const uint32_t off = pos & 3u;                  // 0 or 2
@@ -450,9 +494,11 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int k = 0; k < 9; ++k) cur[i][k] = nxt[i][k];
                 }
                 if (kc + 1 < nk) fetch(kc + 1, nxt, nof);
-                // the stage's activation copy landed, so its MMAs of kStages chunks
-                // back completed (the producer waited for that)
-                const bool ok = wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
+                // the stage's weights of kStages chunks back are no longer read
+                // (their MMAs completed)
+                bool ok = true;
+                if (kc >= kStages)
+                    ok = wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
 #pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
