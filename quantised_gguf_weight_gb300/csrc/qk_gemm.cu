@@ -223,11 +223,21 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (kb < nk && (kb < kStages || mbar_test(bar(kBarEmpty + kb % kStages), ((kb / kStages) - 1) & 1))) {
                     const int s = kb % kStages;
                     if (!(kb == a.skip_chunk && blockIdx.x == 0)) {
+                        // both CTAs' activation copies are counted on the even
+                        // CTA's XFull (the odd CTA's through the pair form of the
+                        // load), so the issuer sees them without a forwarded signal
                         const uint32_t full = bar(kBarXFull + s);
-                        mbar_arrive_expect_tx(full, static_cast<uint32_t>(nh * L::b_half));
-                        for (int h = 0; h < nh; ++h)
-                            tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kb * kBK,
-                                        m0 + h * kBN + static_cast<int>(rank) * kBNc, full, pol_x);
+                        if (rank == 0) {
+                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(2 * nh * L::b_half));
+                            for (int h = 0; h < nh; ++h)
+                                tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kb * kBK,
+                                            m0 + h * kBN, full, pol_x);
+                        } else {
+                            const uint32_t full0 = mapa_shared(full, 0);
+                            for (int h = 0; h < nh; ++h)
+                                tma_load_2d_peer(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kb * kBK,
+                                                 m0 + h * kBN + kBNc, full0, pol_x);
+                        }
                     }
                     ++kb;
                     did = true;
@@ -253,11 +263,14 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             }
-            // let every copy issued land before the CTA can exit
-            for (int t = kb - kStages; t < kb; ++t) {
-                if (t < 0 || (t == a.skip_chunk && blockIdx.x == 0)) continue;
-                mbar_wait(bar(kBarXFull + t % kStages), (t / kStages) & 1, a.wait_ns);
-            }
+            // let every copy issued land before the CTA can exit (the even
+            // CTA's XFull counts the odd CTA's activation copies too, and the
+            // odd CTA leaves only after the closing cluster barrier)
+            if (rank == 0)
+                for (int t = kb - kStages; t < kb; ++t) {
+                    if (t < 0 || (t == a.skip_chunk && blockIdx.x == 0)) continue;
+                    mbar_wait(bar(kBarXFull + t % kStages), (t / kStages) & 1, a.wait_ns);
+                }
             if constexpr (L::raw_stage > 0)
                 for (int t = kr - kStages; t < kr; ++t)
                     if (t >= 0) mbar_wait(bar(kBarRFull + t % kStages), (t / kStages) & 1, a.wait_ns);
@@ -317,13 +330,12 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
         } else if (lane == 0) {
             // -------------------------------------------------------- stage-ready forwarder (odd CTA)
-            // the stage is complete when its weights are written (AFull) and
-            // its activation copy landed (XFull)
+            // the stage's weights are written (AFull); its activation copy
+            // is counted on the even CTA's XFull directly
             const uint32_t peer0 = mapa_shared(bar(kBarPeer), 0);
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
                 if (!wait_or_abort(bar(kBarAFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err, true)) break;
-                if (!wait_or_abort(bar(kBarXFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err, true)) break;
                 mbar_arrive_remote(peer0 + 8u * s);
             }
         }

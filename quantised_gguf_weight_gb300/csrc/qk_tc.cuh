@@ -274,6 +274,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// The same load by a CTA of a pair whose completion is counted on an
+// mbarrier of the other CTA of the pair (`bar` a shared::cluster address
+// from mapa); the box lands in this CTA's shared memory at `dst`.
+__device__ __forceinline__ void tma_load_2d_peer(uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y,
+                                                 uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled store (or f32 add-reduce) of a shared-memory box to global
 // through the tensor map; completion tracked by the thread's bulk groups.
 // Elements of the box outside the tensor are not written.
