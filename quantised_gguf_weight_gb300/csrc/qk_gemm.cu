@@ -148,6 +148,13 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int m0 = m_block * (kBN * kHalves);
     const int nh = (kHalves == 2 && (a.M - m0) > kBN) ? 2 : 1;   // token blocks of kBN used in this pass
     const int nk = a.nk;
+    // The pair takes its K chunks in the order k0, k0 + 1, ... (mod nk), k0
+    // set by its weight tile: pairs running at the same time read different
+    // activation chunks instead of all the same lines of L2 at once.  The
+    // order depends on the tile only, so the same rows in the same tile
+    // position give the same bits in every mode.
+    const int k0 = static_cast<int>((static_cast<int64_t>(n_tile) * 37) % nk);
+    auto phys = [&](int k) { const int p = k + k0; return p >= nk ? p - nk : p; };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -211,7 +218,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if constexpr (L::raw_stage > 0) {
                 for (; kr < nk && kr < kStages; ++kr) {
                     mbar_arrive_expect_tx(bar(kBarRFull + kr), static_cast<uint32_t>(L::raw_stage));
-                    raw_copies(kr, kr, bar(kBarRFull + kr));
+                    raw_copies(phys(kr), kr, bar(kBarRFull + kr));
                 }
             } else {
                 kr = nk;
@@ -230,12 +237,12 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         if (rank == 0) {
                             mbar_arrive_expect_tx(full, static_cast<uint32_t>(2 * nh * L::b_half));
                             for (int h = 0; h < nh; ++h)
-                                tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kb * kBK,
+                                tma_load_2d(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, phys(kb) * kBK,
                                             m0 + h * kBN, full, pol_x);
                         } else {
                             const uint32_t full0 = mapa_shared(full, 0);
                             for (int h = 0; h < nh; ++h)
-                                tma_load_2d_peer(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, kb * kBK,
+                                tma_load_2d_peer(base_u32 + kOffB + s * kBStage + h * L::b_half, &tm_x, phys(kb) * kBK,
                                                  m0 + h * kBN + kBNc, full0, pol_x);
                         }
                     }
@@ -246,7 +253,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     mbar_test(bar(kBarAFull + kr % kStages), ((kr / kStages) - 1) & 1)) {
                     const int s = kr % kStages;
                     mbar_arrive_expect_tx(bar(kBarRFull + s), static_cast<uint32_t>(L::raw_stage));
-                    raw_copies(kr, s, bar(kBarRFull + s));
+                    raw_copies(phys(kr), s, bar(kBarRFull + s));
                     ++kr;
                     did = true;
                 }
@@ -350,7 +357,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if constexpr (!kQ8 && !kQ8T) {
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
-                const int c = kc & 3;
+                const int c = phys(kc) & 3;
                 // the chunk's raw bytes landed, and the stage's weights of
                 // kStages chunks back are no longer read (their MMAs completed)
                 bool ok = wait_or_abort(bar(kBarRFull + s), (kc / kStages) & 1, a.wait_ns, abort_flag, a.err);
@@ -433,7 +440,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (ok && kc >= kStages)
                     ok = wait_or_abort(bar(kBarEmpty + s), ((kc / kStages) - 1) & 1, a.wait_ns, abort_flag, a.err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;       // the warp goes on together or not at all
-                const uint32_t pos = static_cast<uint32_t>((68 * kc) & 15) + 34u * static_cast<uint32_t>(sel);
+                const uint32_t pos = static_cast<uint32_t>((68 * phys(kc)) & 15) + 34u * static_cast<uint32_t>(sel);
                 const uint32_t off = pos & 3u;                  // 0 or 2
 #pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
@@ -495,7 +502,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             };
-            fetch(0, nxt, nof);
+            fetch(phys(0), nxt, nof);
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kStages;
                 uint32_t cur[kTiles][9], cof[kTiles];
@@ -505,7 +512,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                     for (int k = 0; k < 9; ++k) cur[i][k] = nxt[i][k];
                 }
-                if (kc + 1 < nk) fetch(kc + 1, nxt, nof);
+                if (kc + 1 < nk) fetch(phys(kc + 1), nxt, nof);
                 // the stage's weights of kStages chunks back are no longer read
                 // (their MMAs completed)
                 bool ok = true;
