@@ -62,13 +62,14 @@ constexpr int kThreads = 64 + kDeq;
 constexpr uint32_t kTmemCols = 512;
 
 // Modes: Y = X W^T (store), Y += X W^T (acc), or H = silu(X Wg^T) * (X Wu^T)
-// (swiglu: a gate tile and an up tile per CTA, half the tokens).
+// (swiglu: a CTA's 128-row weight tile holds the gate rows of 64 outputs in
+// rows 0..63 and their up rows in rows 64..127).
 constexpr int kStore = 0, kAcc = 1, kSwiglu = 2;
 
 template <int FMT, int MODE>
 struct Shape {
-    static constexpr int halves = MODE == kSwiglu ? 1 : 2;   // token blocks of kBN per CTA pass
-    static constexpr int tiles = MODE == kSwiglu ? 2 : 1;    // weight tiles per K chunk
+    static constexpr int halves = 2;                          // token blocks of kBN per CTA pass
+    static constexpr int tiles = 1;                           // weight tiles per K chunk
     static constexpr int b_half = kBNc * kBK * 2;            // 16 KB: a CTA's slice of one token block
     static constexpr int b_stage = halves * b_half;
     static constexpr int a_tile = kBM * kBK * 2;             // 16 KB
@@ -76,12 +77,12 @@ struct Shape {
     // raw weight bytes of a chunk (Q8_0 from a row stride that is not a
     // multiple of 16 bytes: none, the dequantising threads read them directly)
     static constexpr int raw_stage = FMT == kFmtQ80 ? 0 : tiles * (FMT == kFmtQ80T ? kBM * kQ8Box : kRawChunk);
-    static constexpr int stages = FMT == kFmtQ80 ? 4 : (FMT == kFmtQ80T || MODE == kSwiglu ? 3 : 4);
+    static constexpr int stages = FMT == kFmtQ80T ? 3 : 4;
     static constexpr int off_b = 0;
     static constexpr int off_a = off_b + stages * b_stage;
     static constexpr int off_raw = off_a + stages * a_stage;
     static constexpr int off_bar = off_raw + stages * raw_stage;
-    static constexpr int smem = off_bar + 256 + 1024;        // + alignment slack
+    static constexpr int smem = off_bar + (MODE == kSwiglu ? 512 : 256) + 1024;   // + alignment slack
 };
 
 // barrier slots (8 bytes each) after the barrier offset, four per stage kind:
@@ -93,6 +94,9 @@ struct Shape {
 constexpr int kBarXFull = 0, kBarAFull = 4, kBarEmpty = 8, kBarPeer = 12, kBarAcc = 16, kBarDone = 17,
               kBarRFull = 18;
 constexpr int kOffTmemSlot = 184, kOffAbort = 188;
+// swiglu epilogue: per exchange pair p (0..3) the full and empty barriers of
+// its two streams, slots kBarXch + 4p + {0: A full, 1: A empty, 2: B full, 3: B empty}
+constexpr int kBarXch = 24;
 
 struct Args {
     float *y;
@@ -101,7 +105,7 @@ struct Args {
     const uint8_t *wq8[2];  // Q8_0: first byte of output row 0 of each weight tile (read directly)
     int64_t row_bytes;      // Q8_0: bytes of one weight row
     int nb;                 // Q8_0: blocks of 32 per row
-    int n_tiles;            // pair tiles of 2*kBM weight rows
+    int n_tiles;            // pair tiles (2*kBM output rows; swiglu: kBM)
     int nk;            // number of 64-column K chunks
     int skip_chunk;    // test hook: CTA 0 never loads the activations of this chunk (-1: none)
     int tma_y;         // 1: the output is written through the tensor map of Y (16-byte aligned rows)
@@ -144,16 +148,18 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int pair = blockIdx.x >> 1;
     const int n_tile = pair % a.n_tiles;
     const int m_block = pair / a.n_tiles;
-    const int n0 = n_tile * (2 * kBM) + static_cast<int>(rank) * kBM;   // this CTA's first weight row
+    // this CTA's first output row (swiglu: its 64 rows' gate rows, then their up rows)
+    constexpr int kRowsCta = MODE == kSwiglu ? kBM / 2 : kBM;
+    const int n0 = n_tile * (2 * kRowsCta) + static_cast<int>(rank) * kRowsCta;
     const int m0 = m_block * (kBN * kHalves);
     const int nh = (kHalves == 2 && (a.M - m0) > kBN) ? 2 : 1;   // token blocks of kBN used in this pass
     const int nk = a.nk;
     // The pair takes its K chunks in the order k0, k0 + 1, ... (mod nk), k0
     // set by its weight tile: pairs running at the same time read different
     // activation chunks instead of all the same lines of L2 at once.  The
-    // order depends on the tile only, so the same rows in the same tile
-    // position give the same bits in every mode.
-    const int k0 = static_cast<int>((static_cast<int64_t>(n_tile) * 37) % nk);
+    // order depends on the output rows' 256-row block only (a swiglu pair
+    // covers half of one), so the same rows give the same bits in every mode.
+    const int k0 = static_cast<int>((static_cast<int64_t>(MODE == kSwiglu ? n_tile >> 1 : n_tile) * 37) % nk);
     auto phys = [&](int k) { const int p = k + k0; return p >= nk ? p - nk : p; };
 
     if (tid == 0) {
@@ -166,6 +172,8 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
         mbar_init(bar(kBarAcc), 1);
         mbar_init(bar(kBarDone), 1);
+        if (MODE == kSwiglu)
+            for (int i = 0; i < 16; ++i) mbar_init(bar(kBarXch + i), 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
@@ -189,17 +197,20 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint64_t pol_w = l2_evict_first_policy();
             const uint64_t pol_x = l2_evict_last_policy();
             auto raw_copies = [&](int kc, int s, uint32_t full) {
+                // (swiglu: two boxes of 64 rows, the gate rows then the up rows)
+                constexpr int kParts = MODE == kSwiglu ? 2 : 1;
                 if constexpr (kQ8T) {
                     // blocks 2kc, 2kc+1 span bytes 68kc .. 68kc+67 of a row
-                    for (int i = 0; i < kTiles; ++i)
-                        tma_load_2d(base_u32 + kOffRaw + s * kRawStage + i * (kBM * kQ8Box), &tm_w,
+                    for (int i = 0; i < kParts; ++i)
+                        tma_load_2d(base_u32 + kOffRaw + s * kRawStage + i * (kRowsCta * kQ8Box), &tm_w,
                                     (68 * kc) & ~15, a.row0[i] + n0, full, pol_w);
                 } else if constexpr (!kQ8) {
                     const int kb = kc >> 2, c = kc & 3;
-                    for (int i = 0; i < kTiles; ++i) {
-                        const uint32_t raw = base_u32 + kOffRaw + s * kRawStage + i * kRawChunk;
-                        tma_load_2d(raw, &tm_w, kb * 144, a.row0[i] + n0, full, pol_w);
-                        tma_load_2d(raw + kRawHdr, &tm_q, kb * 144 + 16 + 32 * c, a.row0[i] + n0, full, pol_w);
+                    const uint32_t raw = base_u32 + kOffRaw + s * kRawStage;
+                    for (int i = 0; i < kParts; ++i) {
+                        tma_load_2d(raw + i * (kRowsCta * 16), &tm_w, kb * 144, a.row0[i] + n0, full, pol_w);
+                        tma_load_2d(raw + kRawHdr + i * (kRowsCta * 32), &tm_q, kb * 144 + 16 + 32 * c,
+                                    a.row0[i] + n0, full, pol_w);
                     }
                 }
             };
@@ -483,14 +494,17 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // Q8_0: block 2kc + sel of this thread's row of each tile (rows past N
             // repeat the last row, unstored), read as the nine aligned words
             // around the 34-byte block, one chunk ahead
-            const int64_t nr = min(static_cast<int64_t>(n0 + t), a.N - 1);
+            // (swiglu: rows 0..63 of the tile are gate rows, 64..127 their up rows)
+            const int tr = MODE == kSwiglu ? (t & (kRowsCta - 1)) : t;
+            const uint8_t *wrow = (MODE == kSwiglu && t >= kRowsCta) ? a.wq8[1] : a.wq8[0];
+            const int64_t nr = min(static_cast<int64_t>(n0 + tr), a.N - 1);
             uint32_t nxt[kTiles][9], nof[kTiles];
             auto fetch = [&](int kc, uint32_t (&wv)[kTiles][9], uint32_t (&of)[kTiles]) {
                 const int j = 2 * kc + sel;
 #pragma unroll
                 for (int i = 0; i < kTiles; ++i) {
                     if (j < a.nb) {
-                        const uintptr_t ad = reinterpret_cast<uintptr_t>(a.wq8[i] + nr * a.row_bytes + 34 * j);
+                        const uintptr_t ad = reinterpret_cast<uintptr_t>(wrow + nr * a.row_bytes + 34 * j);
                         const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad & ~static_cast<uintptr_t>(3));
 #pragma unroll
                         for (int k = 0; k < 9; ++k) wv[i][k] = __ldg(wp + k);
@@ -560,11 +574,99 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // warp w may read TMEM lanes 32*(w%4) ..; the two warps of each lane
             // quarter take one half of the accumulator columns each
             const int q = warp & 3;
-            const int n = n0 + 32 * q + lane;
             const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * q) << 16);
             const int cols = nh * kBN;
             const int part = (warp - 2) >> 2;
-            if (a.tma_y) {
+            if constexpr (MODE == kSwiglu) {
+                // The gate rows of outputs n0 + 32 fq .. n0 + 32 fq + 31 sit in
+                // lane quarter fq, their up rows in quarter fq + 2.  The two
+                // warps of a part and an fq swap alternate 32-token chunks through
+                // shared memory (the up warp sends the even chunks on stream A,
+                // the gate warp the odd ones on stream B, one 4 KB buffer each
+                // with a full and an empty barrier), and each warp finishes the
+                // chunks it receives: silu(g) * u, stored.
+                const int fq = q & 1;
+                const bool upw = q >= 2;
+                const int px = 2 * part + fq;
+                const uint32_t xbuf = base_u32 + 65536u + static_cast<uint32_t>(px) * 8192u;   // A, then B
+                const uint32_t xbar = bar(kBarXch + 4 * px);    // A full, A empty, B full, B empty
+                const int n = n0 + 32 * fq + lane;
+                const int jbeg = part * (cols / 2);
+                const uint32_t buf0 = base_u32 + static_cast<uint32_t>(warp - 2) * 8192u;   // as below
+                int nv = 0;                                     // chunks of this part with tokens below M
+                if (n0 + 32 * fq < a.N)
+                    for (int j0 = jbeg; j0 < jbeg + cols / 2 && m0 + j0 < a.M; j0 += 32) ++nv;
+                uint32_t nb = 0;
+                for (int c2 = 0; c2 < nv; c2 += 2) {
+                    const uint32_t ph = static_cast<uint32_t>(c2 >> 1);
+                    const int cs = upw ? c2 : c2 + 1;           // the chunk this warp sends
+                    if (cs < nv) {
+                        const uint32_t sfull = xbar + (upw ? 0u : 16u), sbuf = xbuf + (upw ? 0u : 4096u);
+                        bool ok = true;
+                        if (ph > 0) ok = wait_or_abort(sfull + 8u, (ph - 1) & 1u, a.wait_ns, abort_flag, a.err);
+                        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(jbeg + 32 * cs), v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbuf + static_cast<uint32_t>(i * 32 + lane) * 4u),
+                                         "r"(v[i])
+                                         : "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sfull);
+                    }
+                    const int cr = upw ? c2 + 1 : c2;           // the chunk this warp finishes
+                    if (cr < nv) {
+                        const uint32_t rfull = xbar + (upw ? 16u : 0u), rbuf = xbuf + (upw ? 4096u : 0u);
+                        const bool ok = wait_or_abort(rfull, ph & 1u, a.wait_ns, abort_flag, a.err);
+                        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                        uint32_t v[32], o[32];
+                        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(jbeg + 32 * cr), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            asm volatile("ld.shared.b32 %0, [%1];"
+                                         : "=r"(o[i])
+                                         : "r"(rbuf + static_cast<uint32_t>(i * 32 + lane) * 4u)
+                                         : "memory");
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float g = __uint_as_float(upw ? o[i] : v[i]);
+                            const float u = __uint_as_float(upw ? v[i] : o[i]);
+                            v[i] = __float_as_uint(g / (1.0f + expf(-g)) * u);
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rfull + 8u);   // the buffer may be refilled
+                        const int j0 = jbeg + 32 * cr;
+                        if (a.tma_y) {
+                            if (lane == 0) bulk_wait_group_read<1>();   // this tile's buffer is read out
+                            __syncwarp();
+                            const uint32_t buf = buf0 + nb * 4096u;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + static_cast<uint32_t>(i * 32 + lane) * 4u),
+                                             "r"(v[i])
+                                             : "memory");
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d<false>(&tm_y, buf, n0 + 32 * fq, m0 + j0);
+                                bulk_commit_group();
+                            }
+                            nb ^= 1u;
+                        } else if (n < a.N) {
+                            // rows not 16-byte aligned: direct stores
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int64_t m = m0 + j0 + i;
+                                if (m < a.M) a.y[m * a.ldy + n] = __uint_as_float(v[i]);
+                            }
+                        }
+                    }
+                }
+                if (a.tma_y && lane == 0) bulk_wait_group_all();
+            } else if (a.tma_y) {
                 // each 32 rows x 32 tokens go through a 4 KB shared-memory tile
                 // ([token][row], two per warp, the stages' space is free now)
                 // and one TMA store (acc: f32 add-reduce) of the tile
@@ -575,18 +677,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     if (!rows_in || m0 + j0 >= a.M) break;        // warp-uniform
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
-                    if constexpr (MODE == kSwiglu) {
-                        uint32_t u[32];                            // the up tile's accumulators
-                        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kBN + j0), u);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float g = __uint_as_float(v[i]);
-                            v[i] = __float_as_uint(g / (1.0f + expf(-g)) * __uint_as_float(u[i]));
-                        }
-                    } else {
-                        tmem_ld_wait();
-                    }
+                    tmem_ld_wait();
                     if (lane == 0) bulk_wait_group_read<1>();     // this tile's buffer is read out
                     __syncwarp();
                     const uint32_t buf = buf0 + nb * 4096u;
@@ -607,31 +698,18 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             } else {
                 // rows not 16-byte aligned: direct stores, one token of 32 rows
                 // a warp instruction
+                const int n = n0 + 32 * q + lane;
                 for (int j0 = part * (cols / 2); j0 < (part + 1) * (cols / 2); j0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
-                    if constexpr (MODE == kSwiglu) {
-                        uint32_t u[32];                            // the up tile's accumulators
-                        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kBN + j0), u);
-                        tmem_ld_wait();
-                        if (n < a.N) {
+                    tmem_ld_wait();
+                    if (n < a.N) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int64_t m = m0 + j0 + i;
-                                const float g = __uint_as_float(v[i]);
-                                if (m < a.M) a.y[m * a.ldy + n] = g / (1.0f + expf(-g)) * __uint_as_float(u[i]);
-                            }
-                        }
-                    } else {
-                        tmem_ld_wait();
-                        if (n < a.N) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int64_t m = m0 + j0 + i;
-                                if (m < a.M) {
-                                    float *yp = a.y + m * a.ldy + n;
-                                    *yp = MODE == kAcc ? *yp + __uint_as_float(v[i]) : __uint_as_float(v[i]);
-                                }
+                        for (int i = 0; i < 32; ++i) {
+                            const int64_t m = m0 + j0 + i;
+                            if (m < a.M) {
+                                float *yp = a.y + m * a.ldy + n;
+                                *yp = MODE == kAcc ? *yp + __uint_as_float(v[i]) : __uint_as_float(v[i]);
                             }
                         }
                     }
@@ -768,18 +846,20 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     const int64_t lo = mode == kSwiglu ? std::min<int64_t>(0, up_rows) : 0;
     const int64_t hi = mode == kSwiglu ? std::max<int64_t>(N, up_rows + N) : N;
     // two maps over the Q4_K rows: the 16-byte headers and the 32 quant
-    // bytes of one 64-column chunk, 128 rows a box (x offsets are multiples
+    // bytes of one 64-column chunk, 128 rows a box (swiglu: 64, the gate
+    // and the up rows of a tile come as two boxes; x offsets are multiples
     // of 16 bytes: 144 kb and 144 kb + 16 + 32 c)
+    const int box_rows = mode == kSwiglu ? kBM / 2 : kBM;
     CUtensorMap tm_q;
     // Q8_0 rows of a multiple of 16 bytes (K a multiple of 256) from a
-    // 16-byte aligned tensor come by TMA, 128 rows x 80 bytes a box; other
-    // Q8_0 rows are read directly
+    // 16-byte aligned tensor come by TMA, 128 rows (swiglu: 64) x 80 bytes a
+    // box; other Q8_0 rows are read directly
     const bool q8_tma = q8 && row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(w_rows + lo * row_bytes) & 15u) == 0;
     if (q8_tma) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(hi - lo)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
         const cuuint32_t estr[2] = {1, 1};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQ8Box), static_cast<cuuint32_t>(kBM)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQ8Box), static_cast<cuuint32_t>(box_rows)};
         if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows + lo * row_bytes), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
@@ -795,7 +875,7 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
         const cuuint32_t estr[2] = {1, 1};
         for (int m = 0; m < 2; ++m) {
-            const cuuint32_t box[2] = {m ? 32u : 16u, static_cast<cuuint32_t>(kBM)};
+            const cuuint32_t box[2] = {m ? 32u : 16u, static_cast<cuuint32_t>(box_rows)};
             if (enc(m ? &tm_q : &tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w_rows + lo * row_bytes),
                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
@@ -831,12 +911,13 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     a.wq8[1] = w_rows + up_rows * row_bytes;
     a.row_bytes = row_bytes;
     a.nb = static_cast<int>((K + 31) / 32);
-    a.n_tiles = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));
+    const int64_t rows_pair = mode == kSwiglu ? kBM : 2 * kBM;   // output rows of a CTA pair
+    a.n_tiles = static_cast<int>((N + rows_pair - 1) / rows_pair);
     a.nk = static_cast<int>((K8 + kBK - 1) / kBK);
     a.skip_chunk = skip_chunk;
     a.wait_ns = wait_ns;
     a.err = err;
-    const int64_t per_cta = mode == kSwiglu ? kBN : 2 * kBN;   // tokens per CTA pass
+    const int64_t per_cta = 2 * kBN;                          // tokens per CTA pass
     const int64_t m_blocks = (M + per_cta - 1) / per_cta;
     const int64_t grid = 2 * a.n_tiles * m_blocks;          // CTA pairs
     if (q8_tma) {
