@@ -169,7 +169,9 @@ int qmatvec_q6_k(const void *w, int64_t row_offset, int64_t rows, int64_t K,
  *   x            device fp32 [batch][K];  h  device fp32 [batch][ldh], ldh == 0
  *                means ldh = F; only h[b*ldh + p] for p < F is written.
  * g and u are computed exactly as the plain GEMV's rows (each within the
- * plain GEMV's accuracy bound, see qmatvec_q8_0); silu uses CUDA's expf.  Errors: as the plain
+ * plain GEMV's accuracy bound, see qmatvec_q8_0); silu uses CUDA's expf and its
+ * fast division (within 2 ulp; a denominator past 2^126 gives a zero of z's
+ * sign, the limit).  Errors: as the plain
  * GEMV; a negative up_offset is QK_ERR_BAD_DIM.
  */
 int qmatvec_swiglu_q8_0(const void *w, int64_t gate_offset, int64_t up_offset, int64_t F, int64_t K,
@@ -244,7 +246,7 @@ int qgemm_q4_k_acc(const void *w, int64_t row_offset, int64_t N, int64_t K, cons
  * m < M and p < F
  *   g = sum_k bf16(W[gate_offset + p][k]) * bf16(x[m*K + k])
  *   u = sum_k bf16(W[up_offset + p][k])   * bf16(x[m*K + k])
- *   h[m*ldh + p] = silu(g) * u,   silu(z) = z / (1 + e^-z)  (CUDA expf),
+ *   h[m*ldh + p] = silu(g) * u,   silu(z) = z / (1 + e^-z)  (CUDA expf, fast division as above),
  * g and u accumulated in fp32 on the tensor cores exactly as qgemm_q4_k's
  * outputs.  Gate and up are row ranges of one Q4_K tensor (or of one
  * allocation holding both); gate_offset, up_offset >= 0.  Workspace and

@@ -157,6 +157,18 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h16)
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h16 & 0xFFFFu)));
 }
 
+// SwiGLU's gate: silu(z) = z / (1 + e^-z), with CUDA's expf and its fast
+// division (within 2 ulp of the correctly rounded quotient).  Gate sums of a
+// few hundred are common, where e^-z overflows; the IEEE division by
+// infinity leaves its fast path, at a cost that showed in whole kernels, so a
+// denominator beyond the fast division's range (2^126) gives the limit, a
+// zero of z's sign.
+__device__ __forceinline__ float silu(float z)
+{
+    const float den = 1.0f + expf(-z);
+    return den < 8.5e37f ? __fdividef(z, den) : 0.0f * z;
+}
+
 constexpr uint32_t kMagic = 0x4B000000u;   // 2^23 as an fp32 bit pattern
 constexpr float kTwo23 = 8388608.0f;
 

@@ -123,18 +123,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     return false;
 }
 
-// silu(g) = g / (1 + e^-g) with CUDA's expf and its fast division (within
-// 2 ulp of the correctly rounded quotient).  Gate sums of a few hundred are
-// common, where e^-g overflows: the IEEE division by infinity then leaves
-// its fast path, at a cost that showed in the whole epilogue, so a
-// denominator beyond the fast division's range gives the limit, a zero of
-// g's sign.
-__device__ __forceinline__ float silu_fast(float g)
-{
-    const float den = 1.0f + expf(-g);
-    return den < 8.5e37f ? __fdividef(g, den) : 0.0f * g;
-}
-
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -646,7 +634,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         for (int i = 0; i < 32; ++i) {
                             const float g = __uint_as_float(upw ? o[i] : v[i]);
                             const float u = __uint_as_float(upw ? v[i] : o[i]);
-                            v[i] = __float_as_uint(silu_fast(g) * u);
+                            v[i] = __float_as_uint(silu(g) * u);
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(rfull + 8u);   // the buffer may be refilled

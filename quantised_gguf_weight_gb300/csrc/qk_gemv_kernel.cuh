@@ -77,8 +77,6 @@ __device__ __forceinline__ int q4k_nibble_shift(int c)
 // magnitude; small integers and other values with few significant bits are
 // represented exactly.
 
-// SwiGLU's gate: silu(z) = z / (1 + e^-z), with CUDA's expf.
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // sum(q*m) of one group from its three plane sums, as a float.
 __device__ __forceinline__ float planes_to_float(int s0, int s1, int s2)

@@ -7,8 +7,8 @@ u like the plain GEMV, each within e_g = 1e-5 * S_g + 1e-6 (S = sum|w*x|), so
 
 because |silu'| <= 1.0998 everywhere (the first two terms carry the matvec
 errors through silu(g) * u), and the fp32 evaluation of silu (CUDA's expf,
-one division) and of the product adds a few units in the last place of h,
-covered by the relative term.
+its fast division: within 2 ulp) and of the product adds a few units in the
+last place of h, covered by the relative term.
 """
 import numpy as np
 import pytest
