@@ -792,7 +792,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other GEMV configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--only-gemm", default=None, help="M:N:K -- time the Q4_K prefill GEMM only")
+    ap.add_argument("--only-gemm", default=None,
+                    help="M:N:K or MODE:FMT:M:N:K (store|swiglu, q4_k|q8_0) -- time one prefill GEMM only")
     ap.add_argument("--only", default=None, help="FMT:ROWS:K:BATCH -- time one GEMV call only")
     ap.add_argument("--no-tc", action="store_true",
                     help="with --only: batch 2..8 calls take the fp32 form instead of the tensor-core form")
@@ -817,22 +818,38 @@ def main():
     if args.only:
         return run_only(args, torch, qk, synth, device)
     if args.only_gemm:
-        M, N, K = (int(v) for v in args.only_gemm.split(":"))
-        wq = torch.from_numpy(synth.weights("q4_k", N, K, seed=4)).to(device)
+        # M:N:K (the Q4_K store GEMM) or MODE:FMT:M:N:K (MODE store or swiglu,
+        # FMT q4_k or q8_0; swiglu: N gate rows and N up rows, h = silu(g) * u)
+        parts = args.only_gemm.split(":")
+        mode, fmt = ("store", "q4_k") if len(parts) == 3 else (parts[0], parts[1])
+        if mode not in ("store", "swiglu") or fmt not in ("q4_k", "q8_0"):
+            raise SystemExit(f"--only-gemm: unknown mode or format in {args.only_gemm!r}")
+        M, N, K = (int(v) for v in parts[-3:])
+        wrows = 2 * N if mode == "swiglu" else N
+        wq = torch.from_numpy(synth.weights(fmt, wrows, K, seed=4)).to(device)
         x = torch.from_numpy(synth.activations(M, K, seed=4)).to(device)
         y = torch.empty((M, N), device=device)
         wsp = torch.empty(qk.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=device)
         stream = torch.cuda.Stream(device=device)
-        for _ in range(args.warmup):
-            qk.qgemm_q4_k(wq, 0, N, K, x, y=y, ldy=N, workspace=wsp, stream=stream)
         lib = qk.load()
+        fn = {("store", "q4_k"): lib.qgemm_q4_k, ("store", "q8_0"): lib.qgemm_q8_0,
+              ("swiglu", "q4_k"): lib.qgemm_swiglu_q4_k, ("swiglu", "q8_0"): lib.qgemm_swiglu_q8_0}[(mode, fmt)]
 
         def f(sh):
-            assert lib.qgemm_q4_k(wq.data_ptr(), 0, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(),
-                                  wsp.numel(), sh) == 0
+            if mode == "swiglu":
+                st = fn(wq.data_ptr(), 0, N, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(), wsp.numel(), sh)
+            else:
+                st = fn(wq.data_ptr(), 0, N, K, x.data_ptr(), M, y.data_ptr(), N, wsp.data_ptr(), wsp.numel(), sh)
+            assert st == 0
+        # eager warm-up launches (also the launches an ncu capture skips)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                f(stream.cuda_stream)
+        torch.cuda.synchronize()
         ms = time_calls(torch, stream, [f] * 4, max(1, args.steps))
+        flops = 2.0 * M * wrows * K
         print(json.dumps({"only_gemm": args.only_gemm, "avg_us": round(ms * 1e3, 2),
-                          "TFLOP/s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}), flush=True)
+                          "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}), flush=True)
         return 0
     r = measure_ours(args, torch, qk, synth, device, rank, ws)
     cpu = None

@@ -577,6 +577,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * q) << 16);
             const int cols = nh * kBN;
             const int part = (warp - 2) >> 2;
+            const int n = n0 + 32 * q + lane;             // store, acc: this lane's output row
             if constexpr (MODE == kSwiglu) {
                 // The gate rows of outputs n0 + 32 fq .. n0 + 32 fq + 31 sit in
                 // lane quarter fq, their up rows in quarter fq + 2.  The two
@@ -590,7 +591,7 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const int px = 2 * part + fq;
                 const uint32_t xbuf = base_u32 + 65536u + static_cast<uint32_t>(px) * 8192u;   // A, then B
                 const uint32_t xbar = bar(kBarXch + 4 * px);    // A full, A empty, B full, B empty
-                const int n = n0 + 32 * fq + lane;
+                const int nsw = n0 + 32 * fq + lane;            // this lane's output row
                 const int jbeg = part * (cols / 2);
                 const uint32_t buf0 = base_u32 + static_cast<uint32_t>(warp - 2) * 8192u;   // as below
                 int nv = 0;                                     // chunks of this part with tokens below M
@@ -655,12 +656,12 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                 bulk_commit_group();
                             }
                             nb ^= 1u;
-                        } else if (n < a.N) {
+                        } else if (nsw < a.N) {
                             // rows not 16-byte aligned: direct stores
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 const int64_t m = m0 + j0 + i;
-                                if (m < a.M) a.y[m * a.ldy + n] = __uint_as_float(v[i]);
+                                if (m < a.M) a.y[m * a.ldy + nsw] = __uint_as_float(v[i]);
                             }
                         }
                     }
@@ -698,7 +699,6 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             } else {
                 // rows not 16-byte aligned: direct stores, one token of 32 rows
                 // a warp instruction
-                const int n = n0 + 32 * q + lane;
                 for (int j0 = part * (cols / 2); j0 < (part + 1) * (cols / 2); j0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j0), v);
