@@ -429,14 +429,14 @@ int qk_debug_gemv_tc(int mode) { return g_gemv_tc.exchange(mode < 0 ? 0 : (mode 
 
 // Test hook, not part of the public header: the tensor-core GEMV plan for an
 // explicit device, as {G, NC, row_stride, stage_bytes, NS, smem, grid,
-// off_stage, off_bop}; -1 when the format and K do not take that form.
+// off_stage, off_bop, ks}; -1 when the format and K do not take that form.
 int qk_debug_gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin, int64_t *out, int n)
 {
     qk::GemvTcPlan p;
     if (!out || !qk::gemv_tc_plan_for(fmt, rows, K, sms, smem_optin, &p)) return -1;
-    const int64_t v[9] = {p.G, p.NC, p.row_stride, p.stage_bytes, p.NS, p.smem, p.grid, p.off_stage, p.off_bop};
+    const int64_t v[10] = {p.G, p.NC, p.row_stride, p.stage_bytes, p.NS, p.smem, p.grid, p.off_stage, p.off_bop, p.ks};
     int k = 0;
-    for (; k < n && k < 9; ++k) out[k] = v[k];
+    for (; k < n && k < 10; ++k) out[k] = v[k];
     return k;
 }
 

@@ -72,6 +72,9 @@ struct GemvTcArgs {
     int row_stride;        // bytes a row takes in a stage
     int stage_bytes, NS;
     int off_bop, off_scale, off_xsum, off_out, off_flag, off_xch, off_stage;
+    int ks;                // 1: K split over a cluster of two CTAs (the odd CTA takes the items
+                           // c >= NC/2 of every tile and hands its row sums to the even one)
+    int off_ksx;           // ks: the odd CTA's row sums of a tile [2 buffers][128 rows][8], in the even CTA
     int ph0, ph1;          // Q8_0: 16-byte phase of the rows of even / odd index within their boxes
     int64_t skip_item;     // test hook: CTA 0 never loads this item (-1: off)
     uint64_t wait_ns;
@@ -82,8 +85,10 @@ struct GemvTcArgs {
 static_assert((kTcCW & (kTcCW - 1)) == 0, "the exchange counts arrivals modulo kTcCW");
 // (kXCount: per tile parity and lane quarter, the converter warps that have
 // left their partial sums of a tile)
-constexpr uint32_t kBarFull = 0, kBarEmpty = 64, kBarAFull = 128, kBarMma = 144, kTmemSlot = 192, kAbort = 196,
-                   kXCount = 200;
+// (kKsFull, kKsEmpty: K split over a cluster, per buffer of the odd CTA's row
+// sums: written (in the even CTA), and read (in the odd CTA))
+constexpr uint32_t kBarFull = 0, kBarEmpty = 64, kBarAFull = 128, kBarMma = 144, kKsFull = 160, kKsEmpty = 176,
+                   kTmemSlot = 192, kAbort = 196, kXCount = 200;
 
 // One lane of the (converged) warp is elected.
 __device__ __forceinline__ bool elect_one()
@@ -147,10 +152,12 @@ __device__ __forceinline__ uint32_t bop_chunk(int k, int n)
 constexpr int kStageBatch = 4;
 
 template <int FMT, int B>
-__device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int cw, int lane)
+__device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int cw, int lane, int g_lo, int g_hi)
 {
+    // the groups g_lo .. g_hi - 1 (the CTA's part of K)
     const int q4 = lane & 3;
-    const int units = B * a.G;
+    const int Gh = g_hi - g_lo;
+    const int units = B * Gh;
     constexpr int kRound = 8 * kTcConvWarps;                 // units a round (all converter warps)
     float *stab = reinterpret_cast<float *>(sm + a.off_scale);
     float *xtab = reinterpret_cast<float *>(sm + a.off_xsum);
@@ -163,8 +170,8 @@ __device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int
         for (int r = 0; r < kStageBatch; ++r) {
             const int u = base0 + r * kRound + (lane >> 2);
             const bool act = u < units;
-            const int b = act ? u / a.G : 0;
-            const int g = act ? u - b * a.G : 0;
+            const int b = act ? u / Gh : 0;
+            const int g = g_lo + (act ? u - b * Gh : 0);
             const int64_t c0 = 32LL * g + 8 * q4;
             const float *src = a.x + b * a.K + c0;
             if (act && vec && c0 + 8 <= a.K) {
@@ -183,8 +190,8 @@ __device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int
             const float (&v)[8] = vb[r];
             const int u = base0 + r * kRound + (lane >> 2);
             const bool act = u < units;
-            const int b = act ? u / a.G : 0;
-            const int g = act ? u - b * a.G : 0;
+            const int b = act ? u / Gh : 0;
+            const int g = g_lo + (act ? u - b * Gh : 0);
             uint32_t ab[8], lmax = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -249,8 +256,9 @@ __device__ __forceinline__ void tc_stage_x(const GemvTcArgs &a, uint8_t *sm, int
                 lw[j] = lp;
             }
             if (act) {
-                // B rows: the hi pieces of batch row b in row b, its lo pieces in row B + b
-                const int kc = 32 * g + 8 * q4;
+                // B rows: the hi pieces of batch row b in row b, its lo pieces in
+                // row B + b (columns counted from the CTA's first staged one)
+                const int kc = 32 * (g - g_lo) + 8 * q4;
                 *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, b)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4 *>(sm + a.off_bop + bop_chunk(kc, B + b)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 if (b == 0) {
@@ -336,21 +344,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kAbort);
 
-    // this CTA's rows; Q8_0 tiles start on a row of even index (the even and
-    // odd rows come from two tensor maps, 64 rows of each a tile)
-    const int64_t nG = gridDim.x;
+    // this CTA's rows (K split: the rows of its cluster); Q8_0 tiles start on
+    // a row of even index (the even and odd rows come from two tensor maps,
+    // 64 rows of each a tile)
+    const bool ks = a.ks != 0;
+    const uint32_t rank = ks ? cluster_ctarank() : 0u;
+    const int64_t nG = ks ? gridDim.x / 2 : gridDim.x;
+    const int64_t gid = ks ? blockIdx.x / 2 : blockIdx.x;
     int64_t r_begin, r_end;
     if (FMT == kFmtQ80) {
         const int64_t pairs = (a.rows + 1) / 2;
-        r_begin = min(a.rows, 2 * ((pairs * blockIdx.x) / nG));
-        r_end = min(a.rows, 2 * ((pairs * (blockIdx.x + 1)) / nG));
+        r_begin = min(a.rows, 2 * ((pairs * gid) / nG));
+        r_end = min(a.rows, 2 * ((pairs * (gid + 1)) / nG));
     } else {
-        r_begin = (a.rows * blockIdx.x) / nG;
-        r_end = (a.rows * (blockIdx.x + 1)) / nG;
+        r_begin = (a.rows * gid) / nG;
+        r_end = (a.rows * (gid + 1)) / nG;
     }
     const int T = static_cast<int>((r_end - r_begin + kTcM - 1) / kTcM);
     const int NC = a.NC, NS = a.NS;
-    const int items = T * NC;
+    // the items c_lo .. c_hi - 1 of every tile (K split: one half each)
+    const int c_lo = ks && rank ? NC / 2 : 0, c_hi = ks && !rank ? NC / 2 : NC;
+    const int items = T * (c_hi - c_lo);
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
@@ -361,6 +375,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         for (int p = 0; p < 2; ++p) {
             mbar_init(sb + kBarAFull + 8u * p, kTcConvWarps);
             mbar_init(sb + kBarMma + 8u * p, 1);
+            mbar_init(sb + kKsFull + 8u * p, 4);                   // the odd CTA's four lane quarters
+            mbar_init(sb + kKsEmpty + 8u * p, 4);                  // the even CTA's four lane quarters
         }
         for (int q = 0; q < 8; ++q) reinterpret_cast<uint32_t *>(sm + kXCount)[q] = 0u;
         *abort_flag = 0;
@@ -371,7 +387,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         tmem_relinquish_1();
     }
     tc_fence_before();
-    __syncthreads();
+    if (ks)
+        cluster_sync();      // both CTAs' barriers are initialised before either signals the other
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + kTmemSlot);
     int last_issued = -1;                                        // producer: its last item
@@ -387,7 +406,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
             const uint64_t pol = l2_evict_first_policy();
             const uint32_t stage0 = sb + static_cast<uint32_t>(a.off_stage);
             bool ok = true;
-            int s = 0, use = 0, t = 0, c = 0;                    // stage and its use; tile and chunk of item i
+            int s = 0, use = 0, t = 0, c = c_lo;                 // stage and its use; tile and chunk of item i
             for (int i = 0; i < items; ++i) {
                 if (use > 0 && (*abort_flag || !mbar_wait_sleep(sb + kBarEmpty + 8u * s, (use - 1) & 1, a.wait_ns))) {
                     ok = false;
@@ -415,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                 }
                 last_issued = i;
                 if (++s == NS) { s = 0; ++use; }
-                if (++c == NC) { c = 0; ++t; }
+                if (++c == c_hi) { c = c_lo; ++t; }
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -438,8 +457,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         const uint64_t bdesc0 = smem_desc_sw128_kmajor(sb + static_cast<uint32_t>(a.off_bop));
         int last = -1;
         bool ok = true;
-        int c = 0;                                               // chunk of item i
-        for (int i = 0; i < items; ++i, c = (c + 1 == NC) ? 0 : c + 1) {
+        int c = c_lo;                                            // chunk of item i
+        for (int i = 0; i < items; ++i, c = (c + 1 == c_hi) ? c_lo : c + 1) {
             const int p = i & 1;
             bool w_ok = !*abort_flag && mbar_wait_sleep(sb + kBarAFull + 8u * p, (i >> 1) & 1, a.wait_ns);
             if (!__all_sync(0xFFFFFFFFu, w_ok)) {
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
             }
             tc_fence_after();
             const int ng = min(8, a.G - 8 * c);
-            const uint64_t bd_item = bdesc0 + static_cast<uint64_t>(c * (4 * 2048 / 16));
+            const uint64_t bd_item = bdesc0 + static_cast<uint64_t>((c - c_lo) * (4 * 2048 / 16));
             const uint32_t d0 = tmem + 256u + 128u * p, a0 = tmem + 128u * p;
             if (elect_one()) {
 #pragma unroll
@@ -485,7 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 
         // x may be written by the previous kernel in the stream
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        tc_stage_x<FMT, B>(a, sm, cw, lane);
+        tc_stage_x<FMT, B>(a, sm, cw, lane, 8 * c_lo, min(a.G, 8 * c_hi));
         fence_proxy_async_smem();                                // the B operand, for the tensor cores
         named_bar_sync(1, 32 * kTcConvWarps);                   // the tables, for every converter
 
@@ -508,8 +527,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
             failed = true;
         };
 
-        int s = 0, use = 0, t = 0, c = 0;                        // item i: stage and its use, tile and chunk
-        int tj = 0, cj = 0;                                      // item i - 1: tile and chunk
+        int s = 0, use = 0, t = 0, c = c_lo;                     // item i: stage and its use, tile and chunk
+        int tj = 0, cj = c_lo;                                   // item i - 1: tile and chunk
         for (int i = 0; i <= items && !failed; ++i) {
             if (i < items) {
                 // ---------------- convert item i into A[i & 1]
@@ -694,7 +713,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                 tc_fence_before();
 #pragma unroll
                 for (int b = 0; b < B; ++b) acc[b] += oprev[b];
-                if (c == NC - 1) {
+                if (c == c_hi - 1) {
                     // ---------------- the tile's rows: each warp of a lane quarter
                     // leaves its partial sums; the last of the four to arrive adds
                     // them in the order h = 0..3 and stores the rows (no warp waits).
@@ -724,9 +743,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                             for (int hh = 1; hh < kTcCW; ++hh) v += xch[(hh * kTcM + L) * B + b];
                             yv[b] = v;
                         }
-                        if (rho < n) {
+                        if (ks && rank) {
+                            // K split, odd CTA: its row sums of the tile go to buffer
+                            // t & 1 of the even CTA (once the even CTA has read the
+                            // tile two before out of it)
+                            const uint32_t kb = static_cast<uint32_t>(t & 1);
+                            bool ok = t < 2 || mbar_wait_poll(sb + kKsEmpty + 8u * kb, ((t >> 1) - 1) & 1, a.wait_ns);
+                            ok = __all_sync(0xFFFFFFFFu, ok);
+                            if (!ok) {
+                                fail();
+                            } else {
+                                const uint32_t dst = mapa_shared(
+                                    sb + static_cast<uint32_t>(a.off_ksx) + ((kb * kTcM + rho) * 8u) * 4u, 0);
 #pragma unroll
-                            for (int b = 0; b < B; ++b) a.y[b * a.ldy + row0 + rho] = yv[b];
+                                for (int b = 0; b < B; ++b)
+                                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4u * b), "f"(yv[b])
+                                                 : "memory");
+                                __syncwarp();
+                                if (lane == 0) {
+                                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                                    mbar_arrive_remote(mapa_shared(sb + kKsFull + 8u * kb, 0));
+                                }
+                            }
+                        } else {
+                            bool ok = true;
+                            if (ks) {
+                                // K split, even CTA: add the odd CTA's sums of the second
+                                // half of K, then free the buffer
+                                const uint32_t kb = static_cast<uint32_t>(t & 1);
+                                ok = mbar_wait_poll(sb + kKsFull + 8u * kb, (t >> 1) & 1, a.wait_ns);
+                                ok = __all_sync(0xFFFFFFFFu, ok);
+                                if (!ok) {
+                                    fail();
+                                } else {
+                                    const float *src =
+                                        reinterpret_cast<const float *>(sm + a.off_ksx) + (kb * kTcM + rho) * 8;
+#pragma unroll
+                                    for (int b = 0; b < B; ++b) yv[b] += src[b];
+                                    __syncwarp();
+                                    if (lane == 0) mbar_arrive_remote(mapa_shared(sb + kKsEmpty + 8u * kb, 1));
+                                }
+                            }
+                            if (ok && rho < n) {
+#pragma unroll
+                                for (int b = 0; b < B; ++b) a.y[b * a.ldy + row0 + rho] = yv[b];
+                            }
                         }
                     }
 #pragma unroll
@@ -740,13 +801,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
             tj = t;
             cj = c;
             if (++s == NS) { s = 0; ++use; }
-            if (++c == NC) { c = 0; ++t; }
+            if (++c == c_hi) { c = c_lo; ++t; }
         }
     }
 
-    // every tensor-memory access of the CTA is done before it is freed
+    // every tensor-memory access of the CTA is done before it is freed (K
+    // split: and neither CTA leaves while the other may still write to it)
     tc_fence_before();
-    __syncthreads();
+    if (ks)
+        cluster_sync();
+    else
+        __syncthreads();
     if (warp == kTcIssuer) {
         tc_fence_after();
         tmem_dealloc_1(tmem, kTcCols);
@@ -773,11 +838,22 @@ cudaError_t gemv_tc_launch_one(const CUtensorMap &tm0, const CUtensorMap &tm1, c
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.ks) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;     // K split: CTA pairs
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, tm0, tm1, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -821,15 +897,23 @@ bool gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin,
     const int chunk_bytes = fmt == kFmtQ4K ? 144 : 272;
     const int row_stride = 144;                                    // 16-byte units odd: conflict-free row reads
     const int stage_bytes = fmt == kFmtQ4K ? kTcM * 144 : 4 * kQ8Half;
+    // K split over a cluster of two CTAs when a tile has an even number of
+    // items, 8 or more: each CTA then converts half of every tile of the
+    // cluster's rows and stages its half of x (the B operand holds that
+    // half).  It depends on K only, so the order of a row's additions (the
+    // two halves' sums, then their sum) does too.
+    const int ks = (NC % 2 == 0 && NC >= 8) ? 1 : 0;
     const int64_t off_bop = kTcBarBytes;
-    const int64_t off_scale = off_bop + 32 * Kp;
+    const int64_t off_scale = off_bop + 32 * (ks ? Kp / 2 : Kp);
     const int64_t off_xsum = off_scale + 32LL * G;
     const int64_t off_out = off_xsum + (fmt == kFmtQ4K ? 32LL * G : 0);
     const int64_t off_flag = off_out + 32LL * G;
     const int64_t off_xch = round_up_tc(off_flag + 8LL * G, 16);
     // the partial sums of a tile: 4 warps x 128 rows x up to 8 batch rows
     // (two buffers when a tile is one item)
-    const int64_t off_stage = round_up_tc(off_xch + (NC == 1 ? 2 : 1) * static_cast<int64_t>(kTcCW) * kTcM * 8 * 4, 128);
+    // (K split: the odd CTA's row sums of a tile, 2 buffers x 128 rows x 8)
+    const int64_t off_ksx = round_up_tc(off_xch + (NC == 1 ? 2 : 1) * static_cast<int64_t>(kTcCW) * kTcM * 8 * 4, 16);
+    const int64_t off_stage = round_up_tc(off_ksx + (ks ? 2LL * kTcM * 8 * 4 : 0), 128);
     const int64_t budget = static_cast<int64_t>(smem_optin) - 1024;   // alignment slack of the base
     int64_t ns = (budget - off_stage) / stage_bytes;
     if (ns > kTcMaxStages) ns = kTcMaxStages;
@@ -847,8 +931,11 @@ bool gemv_tc_plan_for(int fmt, int64_t rows, int64_t K, int sms, int smem_optin,
     p->off_flag = static_cast<int>(off_flag);
     p->off_xch = static_cast<int>(off_xch);
     p->off_stage = static_cast<int>(off_stage);
+    p->off_ksx = static_cast<int>(off_ksx);
+    p->ks = ks;
     p->smem = static_cast<int>(off_stage + ns * stage_bytes + 1024);
-    p->grid = static_cast<int>(rows < sms ? rows : sms);
+    // (K split: one CTA pair for every 2 SMs, never more pairs than rows)
+    p->grid = ks ? 2 * static_cast<int>(rows < sms / 2 ? rows : sms / 2) : static_cast<int>(rows < sms ? rows : sms);
     p->row_bytes = fmt == kFmtQ4K ? (Kp / 256) * 144 : (K / 32) * 34;
     return true;
 }
@@ -886,6 +973,8 @@ cudaError_t gemv_tc_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t
     a.off_flag = p.off_flag;
     a.off_xch = p.off_xch;
     a.off_stage = p.off_stage;
+    a.ks = p.ks;
+    a.off_ksx = p.off_ksx;
     a.wait_ns = wait_ns;
     a.err = err;
     // The rows come by TMA.  Q4_K: one map over the call's rows (144-byte

@@ -37,6 +37,7 @@ cudaError_t gemv_launch(int fmt, const uint8_t *w_rows, int64_t rows, int64_t K,
 struct GemvTcPlan {
     int G, NC, chunk_bytes, row_stride, stage_bytes, NS;
     int off_bop, off_scale, off_xsum, off_out, off_flag, off_xch, off_stage, smem, grid;
+    int ks, off_ksx;       // K split over CTA pairs (clusters of two), and its exchange buffers
     int64_t row_bytes;
 };
 bool gemv_tc_plan(int fmt, int64_t rows, int64_t K, GemvTcPlan *p);

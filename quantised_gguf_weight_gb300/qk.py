@@ -401,7 +401,7 @@ def debug_gemv_tc(mode: int) -> int:
     return int(load().qk_debug_gemv_tc(int(mode)))
 
 
-TC_PLAN_FIELDS = ("G", "NC", "row_stride", "stage_bytes", "NS", "smem", "grid", "off_stage", "off_bop")
+TC_PLAN_FIELDS = ("G", "NC", "row_stride", "stage_bytes", "NS", "smem", "grid", "off_stage", "off_bop", "ks")
 
 
 def debug_gemv_tc_plan_for(fmt: str, rows: int, K: int, sms: int, smem_optin: int) -> dict | None:

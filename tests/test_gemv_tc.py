@@ -49,11 +49,14 @@ def _sm():
 
 SHAPES = [
     # fmt, rows, K, batch: ragged tiles (1, 127, 129 rows), a short last item
-    # (K = 640, 896: 128 columns), padded Q4_K super-blocks (K = 300, 896)
+    # (K = 640, 896: 128 columns), padded Q4_K super-blocks (K = 300, 896);
+    # K split over CTA pairs (K = 2048, 4096: 8 and 16 items a tile) with one
+    # row a pair (1 row), one tile a pair, and 4 or 5 tiles a pair (the odd
+    # CTA's row sums reuse their two buffers)
     ("q8_0", 1, 128, 2), ("q8_0", 127, 896, 8), ("q8_0", 129, 896, 3), ("q8_0", 1000, 896, 5),
-    ("q8_0", 300, 2048, 4), ("q8_0", 999, 640, 7), ("q8_0", 5000, 3840, 2),
+    ("q8_0", 300, 2048, 4), ("q8_0", 999, 640, 7), ("q8_0", 5000, 3840, 2), ("q8_0", 30000, 2048, 6),
     ("q4_k", 1, 256, 2), ("q4_k", 200, 300, 6), ("q4_k", 1000, 4096, 4), ("q4_k", 257, 896, 8),
-    ("q4_k", 600, 4864, 3), ("q4_k", 20000, 1024, 5),
+    ("q4_k", 600, 4864, 3), ("q4_k", 20000, 1024, 5), ("q4_k", 1, 2048, 7), ("q4_k", 48640, 2048, 3),
 ]
 
 

@@ -104,7 +104,8 @@ def tc_plan(fmt, rows, K):
 
 def test_tensor_core_form_depends_on_format_and_K_only():
     """Q8_0 takes it for K a multiple of 128 that fits, Q4_K for any K that
-    fits, Q6_K never; the plan is the same for every row count but the grid."""
+    fits, Q6_K never; the plan is the same for every row count but the grid
+    (K split over CTA pairs: one pair a row at most, 76 pairs on 152 SMs)."""
     for fmt in ("q8_0", "q4_k", "q6_k"):
         for K in KS + [128, 640, 2048, 4864]:
             plans = [tc_plan(fmt, rows, K) for rows in ROWS]
@@ -115,30 +116,38 @@ def test_tensor_core_form_depends_on_format_and_K_only():
             if plans[0] is not None:
                 same = {tuple(v for k, v in p.items() if k != "grid") for p in plans}
                 assert len(same) == 1, (fmt, K)
-                assert [p["grid"] for p in plans] == [min(r, SMS) for r in ROWS]
+                assert [p["grid"] for p in plans] == [2 * min(r, SMS // 2) if p["ks"] else min(r, SMS)
+                                                      for r, p in zip(ROWS, plans)]
     # the configurations that use it
     assert tc_plan("q8_0", 151936, 896) is not None        # Q8_0 lm_head
     assert tc_plan("q4_k", 28672, 4096) is not None        # Llama-8B gate+up
     assert tc_plan("q4_k", 4096, 14336) is None            # its activations do not fit
     assert tc_plan("q8_0", 4096, 14336) is None
-    assert tc_plan("q8_0", 1000, 4096) is not None          # Q8_0: the activations and two stages fit up to 4096
-    assert tc_plan("q8_0", 1000, 4224) is None
-    assert tc_plan("q4_k", 1000, 4864) is not None          # Q4_K: up to 4864
-    assert tc_plan("q4_k", 1000, 5120) is None
+    # K split over CTA pairs from 8 items a tile when their number is even
+    # (each CTA then holds half of x): the activations and two stages fit
+    assert tc_plan("q8_0", 1000, 896)["ks"] == 0
+    assert tc_plan("q8_0", 1000, 4096)["ks"] == 1
+    assert tc_plan("q8_0", 1000, 4224) is None              # 17 items: not split, does not fit
+    assert tc_plan("q8_0", 1000, 7168)["ks"] == 1           # split: up to 7168
+    assert tc_plan("q8_0", 1000, 7680) is None
+    assert tc_plan("q4_k", 1000, 4864)["ks"] == 0           # Q4_K, 19 items: not split, up to 4864
+    assert tc_plan("q4_k", 1000, 8704)["ks"] == 1           # split: up to 8704
+    assert tc_plan("q4_k", 1000, 8960) is None
 
 
 @pytest.mark.parametrize("fmt,K", [("q8_0", 128), ("q8_0", 896), ("q8_0", 4096), ("q4_k", 256), ("q4_k", 300),
                                    ("q4_k", 4096), ("q4_k", 4864)])
 def test_tensor_core_plan_layout(fmt, K):
-    """Groups and items cover the padded K, the B operand (32 bytes a column,
-    1024-byte aligned) and the tables precede at least two stages, and all of
-    it fits in the block's shared memory."""
+    """Groups and items cover the padded K, the B operand (32 bytes a column
+    of the CTA's part of K, 1024-byte aligned) and the tables precede at
+    least two stages, and all of it fits in the block's shared memory."""
     p = tc_plan(fmt, 1000, K)
     Kp = -(-K // 256) * 256 if fmt == "q4_k" else K
     assert p["G"] * 32 == Kp
     assert p["NC"] == -(-Kp // 256)
+    assert p["ks"] == (1 if p["NC"] % 2 == 0 and p["NC"] >= 8 else 0)
     assert p["off_bop"] % 1024 == 0
-    assert p["off_bop"] + 32 * Kp <= p["off_stage"]
+    assert p["off_bop"] + 32 * (Kp // 2 if p["ks"] else Kp) <= p["off_stage"]
     assert p["off_stage"] % 128 == 0
     assert p["row_stride"] % 16 == 0 and (p["row_stride"] // 16) % 2 == 1    # conflict-free row reads
     # Q4_K: one box of 128 rows x 144 bytes; Q8_0: four of 64 rows x 144 bytes
