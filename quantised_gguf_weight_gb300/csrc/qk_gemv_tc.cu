@@ -332,7 +332,7 @@ __device__ __forceinline__ void q80_tc_convert(const uint8_t *sp0, const uint8_t
     }
 }
 
-template <int FMT, int B>
+template <int FMT, int B, bool KS>
 __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm0,
                                                                  const __grid_constant__ CUtensorMap tm1,
                                                                  const GemvTcArgs a)
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // this CTA's rows (K split: the rows of its cluster); Q8_0 tiles start on
     // a row of even index (the even and odd rows come from two tensor maps,
     // 64 rows of each a tile)
-    const bool ks = a.ks != 0;
+    constexpr bool ks = KS;                                  // (a.ks: the plan's choice, launched as KS)
     const uint32_t rank = ks ? cluster_ctarank() : 0u;
     const int64_t nG = ks ? gridDim.x / 2 : gridDim.x;
     const int64_t gid = ks ? blockIdx.x / 2 : blockIdx.x;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         tmem_relinquish_1();
     }
     tc_fence_before();
-    if (ks)
+    if constexpr (ks)
         cluster_sync();      // both CTAs' barriers are initialised before either signals the other
     else
         __syncthreads();
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // every tensor-memory access of the CTA is done before it is freed (K
     // split: and neither CTA leaves while the other may still write to it)
     tc_fence_before();
-    if (ks)
+    if constexpr (ks)
         cluster_sync();
     else
         __syncthreads();
@@ -818,11 +818,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     }
 }
 
-template <int FMT, int B>
-cudaError_t gemv_tc_launch_one(const CUtensorMap &tm0, const CUtensorMap &tm1, const GemvTcArgs &a, int grid,
-                               int smem, cudaStream_t st, bool pdl)
+template <int FMT, int B, bool KS>
+cudaError_t gemv_tc_launch_ks(const CUtensorMap &tm0, const CUtensorMap &tm1, const GemvTcArgs &a, int grid,
+                              int smem, cudaStream_t st, bool pdl)
 {
-    auto kern = gemv_tc_kernel<FMT, B>;
+    auto kern = gemv_tc_kernel<FMT, B, KS>;
     static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -840,7 +840,7 @@ cudaError_t gemv_tc_launch_one(const CUtensorMap &tm0, const CUtensorMap &tm1, c
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (a.ks) {
+    if (KS) {
         attr[na].id = cudaLaunchAttributeClusterDimension;     // K split: CTA pairs
         attr[na].val.clusterDim.x = 2;
         attr[na].val.clusterDim.y = 1;
@@ -857,6 +857,14 @@ cudaError_t gemv_tc_launch_one(const CUtensorMap &tm0, const CUtensorMap &tm1, c
     e = cudaLaunchKernelEx(&cfg, kern, tm0, tm1, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int FMT, int B>
+cudaError_t gemv_tc_launch_one(const CUtensorMap &tm0, const CUtensorMap &tm1, const GemvTcArgs &a, int grid,
+                               int smem, cudaStream_t st, bool pdl)
+{
+    return a.ks ? gemv_tc_launch_ks<FMT, B, true>(tm0, tm1, a, grid, smem, st, pdl)
+                : gemv_tc_launch_ks<FMT, B, false>(tm0, tm1, a, grid, smem, st, pdl);
 }
 
 template <int FMT>
