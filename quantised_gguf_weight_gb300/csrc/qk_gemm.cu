@@ -106,6 +106,7 @@ struct Args {
     int64_t row_bytes;      // Q8_0: bytes of one weight row
     int nb;                 // Q8_0: blocks of 32 per row
     int n_tiles;            // pair tiles (2*kBM output rows; swiglu: kBM)
+    int tok_pass;           // tokens a pair takes in one pass: 2*kBN, or kBN (one block)
     int nk;            // number of 64-column K chunks
     int skip_chunk;    // test hook: CTA 0 never loads the activations of this chunk (-1: none)
     int tma_y;         // 1: the output is written through the tensor map of Y (16-byte aligned rows)
@@ -151,8 +152,11 @@ gemm_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     // this CTA's first output row (swiglu: its 64 rows' gate rows, then their up rows)
     constexpr int kRowsCta = MODE == kSwiglu ? kBM / 2 : kBM;
     const int n0 = n_tile * (2 * kRowsCta) + static_cast<int>(rank) * kRowsCta;
-    const int m0 = m_block * (kBN * kHalves);
-    const int nh = (kHalves == 2 && (a.M - m0) > kBN) ? 2 : 1;   // token blocks of kBN used in this pass
+    // (written so, the store GEMM at N = 14336 keeps the speed it had before
+    // the one-block pass existed; m_block * tok_pass measured 2% slower)
+    const bool one_block = a.tok_pass == kBN;
+    const int m0 = m_block * (kBN * kHalves) / (one_block ? 2 : 1);
+    const int nh = (kHalves == 2 && !one_block && (a.M - m0) > kBN) ? 2 : 1;   // token blocks of kBN in this pass
     const int nk = a.nk;
     // The pair takes its K chunks in the order k0, k0 + 1, ... (mod nk), k0
     // set by its weight tile: pairs running at the same time read different
@@ -917,8 +921,15 @@ cudaError_t gemm_launch(int fmt, const uint8_t *w_rows, int64_t N, int64_t K, co
     a.skip_chunk = skip_chunk;
     a.wait_ns = wait_ns;
     a.err = err;
-    const int64_t per_cta = 2 * kBN;                          // tokens per CTA pass
-    const int64_t m_blocks = (M + per_cta - 1) / per_cta;
+    // Tokens a pair takes in one pass: 2 kBN; or one block of kBN when the
+    // weight tiles are few, so that twice the pairs (each tile's weights
+    // dequantised once per token block) still run at once, one pair to two
+    // SMs.  Every output sums its K chunks in the same order either way.
+    int sms = 0, smem_optin = 0;
+    const bool have_sms = device_limits(&sms, &smem_optin);
+    const int64_t m_half = (M + kBN - 1) / kBN;
+    a.tok_pass = (have_sms && M > kBN && a.n_tiles * m_half <= sms / 2) ? kBN : 2 * kBN;
+    const int64_t m_blocks = (M + a.tok_pass - 1) / a.tok_pass;
     const int64_t grid = 2 * a.n_tiles * m_blocks;          // CTA pairs
     if (q8_tma) {
         if (mode == kSwiglu) return launch_mode<kFmtQ80T, kSwiglu>(tm_x, tm_w, tm_q, tm_y, a, grid, st);
