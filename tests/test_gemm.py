@@ -129,3 +129,19 @@ def test_gemm_bounded_wait_times_out(qk, orc):
         qk.set_wait_limit_ns(old)
     y = run_gemm(qk, wq, 0, N, K, x)
     check(y, orc, wq, K, x, np.arange(N), "after timeout")
+
+
+def test_gemm_token_pass_does_not_change_bits(qk):
+    """A call with few weight tiles lets each CTA pair take one 256-token
+    block a pass instead of two; every output still sums its K chunks in
+    the same order, so rows 0..511 of a 14336-row call (two blocks a pass)
+    equal a 512-row call over the same rows (one block a pass) bit for bit."""
+    M, K = 512, 2048
+    wq = synth.weights("q4_k", 14336, K, seed=9)
+    x = synth.activations(M, K, seed=9)
+    wd = torch.from_numpy(wq).cuda()
+    xd = torch.from_numpy(x).cuda()
+    y_big = qk.qgemm_q4_k(wd, 0, 14336, K, xd)
+    y_small = qk.qgemm_q4_k(wd, 0, 512, K, xd)
+    torch.cuda.synchronize()
+    assert torch.equal(y_big[:, :512], y_small)
