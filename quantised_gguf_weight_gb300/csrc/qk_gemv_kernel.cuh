@@ -495,9 +495,11 @@ __device__ __forceinline__ void q8_blk_fp(const uint32_t (&wv)[R][9], const uint
 template <int N>
 __device__ __forceinline__ void lds_realign(const uint8_t *p, uint32_t (&out)[N])
 {
-    const uintptr_t ad = reinterpret_cast<uintptr_t>(p);
-    const uint32_t o = static_cast<uint32_t>(ad & 3u);
-    const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - o);
+    // (the aligned word address is formed in the shared window, so that the
+    // loads are shared-memory loads, not generic ones)
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    const uint32_t o = sa & 3u;
+    const uint32_t *wp = static_cast<const uint32_t *>(__cvta_shared_to_generic(sa - o));
     const uint32_t sel = o ? 0x5432u : 0x3210u;
     uint32_t prev = wp[0];
 #pragma unroll
@@ -1472,9 +1474,11 @@ __global__ void __launch_bounds__(32 * (gemv_warps(FMT, B, WIDE) + 1), 1) gemv_k
                     if (has) {
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            const uintptr_t ad = reinterpret_cast<uintptr_t>(rowp[r] + (i * SW + sl) * UB);
-                            off[r] = static_cast<uint32_t>(ad & 3u);          // 0 or 2
-                            const uint32_t *wp = reinterpret_cast<const uint32_t *>(ad - off[r]);
+                            const uint32_t sa = static_cast<uint32_t>(
+                                __cvta_generic_to_shared(rowp[r] + (i * SW + sl) * UB));
+                            off[r] = sa & 3u;          // 0 or 2
+                            // (formed in the shared window: shared-memory loads, not generic ones)
+                            const uint32_t *wp = static_cast<const uint32_t *>(__cvta_shared_to_generic(sa - off[r]));
 #pragma unroll
                             for (int k = 0; k < 9; ++k) wv[r][k] = wp[k];
                         }
